@@ -1,0 +1,189 @@
+"""DASH task orders and the critical path of the compute/reduce DAG (test infrastructure).
+
+Only the test suite may use this module. It shares no code with the C++ schedule
+builder and simulator inside the CUDA library; the tests compare the two.
+
+The model (Pith review of "DASH: Deterministic Attention Scheduling for High-throughput
+Reproducible LLM Training", sections "Core claim", "What carries the argument" and the
+"Axiom & Free-Parameter Ledger"):
+
+* Work is a grid of tasks (KV_i, Q_j). Each task is a chain: a compute phase C(i, j) of
+  cost c, then a reduction phase R(i, j) of cost r that adds the task's partial dQ_j into
+  the dQ_j accumulator.
+* All tasks of one KV tile run back to back on one SM (dK/dV stay resident there).
+* The reductions into one dQ_j block run one at a time, in a fixed order; zero-weight
+  edges between consecutive reductions encode that order.
+* The objective is the critical path (longest path) of the resulting DAG.
+
+Causal masks keep task (i, j) only when j >= i (query tile j sees key tile i); the KV_i
+chain then has n - i tasks (referee report, major comment 2).
+
+Schedules (the abstract; the Figure 3, 4, 6 and 7 captions; "What carries the argument"):
+
+* ascending   -- the FlashAttention-3 baseline: KV_i visits Q tiles in increasing order.
+* descending  -- Descending Q-Tile Iteration: KV_i visits Q tiles in decreasing order.
+* shift       -- Shift Scheduling (full mask): at step t, KV_i works on Q_((i + t) mod n),
+                 so no two SMs reduce into the same dQ block at the same step.
+* symmetric_shift -- Symmetric Shift (causal mask, n even): one SM slot p < n/2 takes the
+                 longest chain KV_p and the shortest chain KV_(n-1-p). Phase 1 covers
+                 the dense lower-left rectangle (KV_0..KV_(n/2-1) x Q_(n/2)..Q_(n-1)) by a
+                 cyclic shift; phase 2 runs the folded triangles from the diagonal,
+                 the upper-left triangle first, then the lower-right one, keeping each
+                 KV tile contiguous (Figure 7 caption).
+
+Readings where the pages are silent (listed in the design notes as well):
+
+* The fixed dQ order of ascending and descending is ascending KV index.
+* Shift's cyclic index runs over Q tiles for a fixed KV tile (a KV tile must stay on
+  one SM); its dQ_j order, like symmetric shift's, is the step at which each
+  contribution arrives in the lock-step model.
+* Symmetric shift, phase 2: KV_p visits Q_p..Q_(n/2-1) upwards from the diagonal, then
+  KV_(n-1-p) visits Q_(n-1) down to Q_(n-1-p).
+* m heads are spread over P SMs by dealing the units (head, chain slot) round robin in
+  head-major order; each SM runs its units in dealing order.
+"""
+
+from __future__ import annotations
+
+from collections import deque
+
+__all__ = [
+    "SCHEDULES",
+    "chains",
+    "reduction_order",
+    "schedule_dag",
+    "longest_path",
+    "simulate",
+]
+
+SCHEDULES = ("ascending", "descending", "shift", "symmetric_shift")
+
+
+def _keys(mask: str, i: int, n: int) -> list[int]:
+    """Q tiles that KV tile i contributes to, in increasing order."""
+    return list(range(n)) if mask == "full" else list(range(i, n))
+
+
+def chains(mask: str, sched: str, n: int) -> list[list[tuple[int, int]]]:
+    """Task chains, one per SM slot, each a list of (kv_tile, q_tile) in execution order."""
+    if mask not in ("full", "causal"):
+        raise ValueError(mask)
+    if sched == "ascending":
+        return [[(i, j) for j in _keys(mask, i, n)] for i in range(n)]
+    if sched == "descending":
+        return [[(i, j) for j in reversed(_keys(mask, i, n))] for i in range(n)]
+    if sched == "shift":
+        if mask != "full":
+            raise ValueError("shift scheduling is defined for the full mask")
+        return [[(i, (i + t) % n) for t in range(n)] for i in range(n)]
+    if sched == "symmetric_shift":
+        if mask != "causal" or n % 2:
+            raise ValueError("symmetric shift is defined for the causal mask with even n")
+        half = n // 2
+        out = []
+        for p in range(half):
+            phase1 = [(p, half + (p + t) % half) for t in range(half)]
+            upper_left = [(p, p + u) for u in range(half - p)]
+            lower_right = [(n - 1 - p, n - 1 - u) for u in range(p + 1)]
+            out.append(phase1 + upper_left + lower_right)
+        return out
+    raise ValueError(sched)
+
+
+def reduction_order(mask: str, sched: str, n: int) -> dict[int, list[int]]:
+    """For each dQ block j, the KV tiles that reduce into it, in the fixed order."""
+    ch = chains(mask, sched, n)
+    contrib: dict[int, list[tuple[int, int]]] = {j: [] for j in range(n)}
+    for chain in ch:
+        for step, (i, j) in enumerate(chain):
+            contrib[j].append((step, i))
+    order = {}
+    for j, lst in contrib.items():
+        if sched in ("ascending", "descending"):
+            order[j] = sorted(i for _, i in lst)
+        else:
+            steps = [st for st, _ in lst]
+            if len(set(steps)) != len(steps):
+                raise AssertionError(f"two contributions to dQ_{j} arrive at the same step")
+            order[j] = [i for _, i in sorted(lst)]
+    return order
+
+
+def longest_path(n_vertices: int, edges: list[tuple[int, int, float]]):
+    """Earliest start time of every vertex (longest path from any source, sources at 0).
+
+    Returns None when the graph has a cycle.
+    """
+    succ: list[list[tuple[int, float]]] = [[] for _ in range(n_vertices)]
+    indeg = [0] * n_vertices
+    for u, v, w in edges:
+        succ[u].append((v, w))
+        indeg[v] += 1
+    depth = [0.0] * n_vertices
+    ready = deque(v for v in range(n_vertices) if indeg[v] == 0)
+    seen = 0
+    while ready:
+        u = ready.popleft()
+        seen += 1
+        for v, w in succ[u]:
+            depth[v] = max(depth[v], depth[u] + w)
+            indeg[v] -= 1
+            if indeg[v] == 0:
+                ready.append(v)
+    return depth if seen == n_vertices else None
+
+
+def schedule_dag(mask: str, sched: str, n: int, m: int, num_sms: int, c: float, r: float):
+    """Build the explicit DAG of m heads' tasks dealt onto ``num_sms`` SMs.
+
+    Every task (head, i, j) owns four vertices: compute start/end and reduce start/end.
+    Returns (n_vertices, edges, tasks, sm_of_task) where tasks[k] = (head, i, j) and task k
+    owns vertices 4k..4k+3.
+    """
+    ch = chains(mask, sched, n)
+    order = reduction_order(mask, sched, n)
+    units = [(h, slot) for h in range(m) for slot in range(len(ch))]   # head-major deal
+    per_sm: list[list[int]] = [[] for _ in range(num_sms)]
+    tasks: list[tuple[int, int, int]] = []
+    sm_of_task: list[int] = []
+    index: dict[tuple[int, int, int], int] = {}
+    for u, (h, slot) in enumerate(units):
+        sm = u % num_sms
+        for (i, j) in ch[slot]:
+            k = len(tasks)
+            tasks.append((h, i, j))
+            sm_of_task.append(sm)
+            index[(h, i, j)] = k
+            per_sm[sm].append(k)
+    edges: list[tuple[int, int, float]] = []
+    for k in range(len(tasks)):
+        cs, ce, rs, re = 4 * k, 4 * k + 1, 4 * k + 2, 4 * k + 3
+        edges += [(cs, ce, c), (ce, rs, 0.0), (rs, re, r)]
+    for lst in per_sm:                               # one SM runs its tasks back to back
+        for a, b in zip(lst, lst[1:]):
+            edges.append((4 * a + 3, 4 * b, 0.0))
+    for h in range(m):                               # fixed dQ reduction order
+        for j, kv in order.items():
+            for a, b in zip(kv, kv[1:]):
+                edges.append((4 * index[(h, a, j)] + 3, 4 * index[(h, b, j)] + 2, 0.0))
+    return 4 * len(tasks), edges, tasks, sm_of_task
+
+
+def simulate(mask: str, sched: str, n: int, m: int, num_sms: int, c: float, r: float):
+    """Critical path of the schedule DAG.
+
+    Returns a dict with ``makespan`` (None on a cycle, i.e. a deadlock), ``sm_end`` (finish
+    time per SM) and ``sm_idle`` (finish time minus busy time per SM).
+    """
+    nv, edges, tasks, sm_of_task = schedule_dag(mask, sched, n, m, num_sms, c, r)
+    depth = longest_path(nv, edges)
+    if depth is None:
+        return {"makespan": None, "sm_end": None, "sm_idle": None}
+    sm_end = [0.0] * num_sms
+    sm_busy = [0.0] * num_sms
+    for k, sm in enumerate(sm_of_task):
+        sm_end[sm] = max(sm_end[sm], depth[4 * k + 3])       # reduce-end vertex
+        sm_busy[sm] += c + r
+    makespan = max(sm_end) if tasks else 0.0
+    return {"makespan": makespan, "sm_end": sm_end,
+            "sm_idle": [e - b for e, b in zip(sm_end, sm_busy)]}

@@ -1,0 +1,187 @@
+"""Pins for the DAG oracle (oracle/dag.py) against what the pages and the model fix.
+
+* the closed-form makespans of tests/golden/dag_closed_forms.txt (pages' formulas and
+  ones derived from the chain recurrence), evaluated here from the formula text;
+* the referee's worked counterexample (n = 2, m = 1, causal);
+* Lemma 1 by brute force on random parallel isomorphic chains;
+* coverage, per-KV contiguity and conflict-freedom of the task orders;
+* a textbook longest-path example and cycle detection.
+"""
+
+import itertools
+import os
+import random
+
+import pytest
+
+from oracle.dag import SCHEDULES, chains, longest_path, reduction_order, simulate
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "dag_closed_forms.txt")
+
+
+def _golden_rows():
+    rows = []
+    with open(GOLDEN) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#") or line.startswith("EXAMPLE"):
+                continue
+            mask, sched, _p, m, formula, src = (x.strip() for x in line.split("|"))
+            rows.append((mask, sched, m, formula, src))
+    return rows
+
+
+def _valid(mask, sched, n):
+    if sched == "shift" and mask != "full":
+        return False
+    if sched == "symmetric_shift" and (mask != "causal" or n % 2):
+        return False
+    return True
+
+
+def test_longest_path_textbook():
+    # a -> b (3), a -> c (2), b -> d (4), c -> d (6), d -> e (1): longest to e = 9 via a-c-d-e
+    depth = longest_path(5, [(0, 1, 3), (0, 2, 2), (1, 3, 4), (2, 3, 6), (3, 4, 1)])
+    assert depth == [0, 3, 2, 8, 9]
+    assert longest_path(3, [(0, 1, 1), (1, 2, 1), (2, 0, 1)]) is None
+
+
+@pytest.mark.parametrize("row", _golden_rows(), ids=lambda r: f"{r[0]}-{r[1]}-m{r[2]}")
+@pytest.mark.parametrize("c,r", [(3, 1), (5, 2), (1, 4)])
+def test_closed_forms(row, c, r):
+    mask, sched, m_spec, formula, _src = row
+    for n in range(1, 17):
+        if not _valid(mask, sched, n):
+            continue
+        for m in ([1] if m_spec == "1" else [1, 2, 3, 4]):
+            got = simulate(mask, sched, n, m, n, c, r)["makespan"]
+            want = eval(formula, {}, {"n": n, "m": m, "c": c, "r": r})
+            assert got == want, (mask, sched, n, m, c, r, got, want)
+
+
+@pytest.mark.parametrize("c,r", [(3, 1), (1, 1)])
+def test_referee_counterexample(c, r):
+    # n = 2, m = 1, causal: every schedule >= 2(c + r) > 1.5(c + r).
+    for sched in ("ascending", "descending", "symmetric_shift"):
+        for sms in (1, 2):
+            t = simulate("causal", sched, 2, 1, sms, c, r)["makespan"]
+            assert t >= 2 * (c + r) > 1.5 * (c + r)
+    assert simulate("causal", "symmetric_shift", 2, 1, 2, c, r)["makespan"] == 3 * (c + r)
+
+
+@pytest.mark.parametrize("sched", SCHEDULES)
+@pytest.mark.parametrize("mask", ["full", "causal"])
+def test_coverage_contiguity_conflicts(mask, sched):
+    for n in list(range(1, 17)) + [64, 128]:
+        if not _valid(mask, sched, n):
+            continue
+        ch = chains(mask, sched, n)
+        tasks = [t for c in ch for t in c]
+        want = {(i, j) for i in range(n) for j in range(n) if mask == "full" or j >= i}
+        assert len(tasks) == len(want) and set(tasks) == want
+        for c in ch:                       # each KV tile's tasks are contiguous in its chain
+            kvs = [i for i, _ in c]
+            runs = [k for k, _ in itertools.groupby(kvs)]
+            assert len(runs) == len(set(runs))
+        assert {i for c in ch for i, _ in c} == set(range(n))
+        order = reduction_order(mask, sched, n)
+        for j in range(n):
+            assert sorted(order[j]) == sorted(i for i, jj in tasks if jj == j)
+        if sched in ("shift", "symmetric_shift"):
+            for step in range(max(len(c) for c in ch)):
+                js = [c[step][1] for c in ch if step < len(c)]
+                assert len(js) == len(set(js)), "two SMs reduce into one dQ block at one step"
+
+
+def test_bounds_hold_everywhere():
+    # makespan >= longest chain of one KV tile and >= total work / P
+    for mask, sched in itertools.product(["full", "causal"], SCHEDULES):
+        for n in (2, 4, 6, 8):
+            if not _valid(mask, sched, n):
+                continue
+            for m, sms in ((1, n), (3, n), (2, 3), (5, 4), (4, 2 * n + 1)):
+                c, r = 3, 1
+                t = simulate(mask, sched, n, m, sms, c, r)["makespan"]
+                slots = len(chains(mask, sched, n))
+                if t is None:
+                    # a deadlock needs a head whose chains are not all co-resident
+                    assert sched in ("shift", "symmetric_shift") and sms < 2 * slots
+                    continue
+                work = m * sum(len(ch) for ch in chains(mask, sched, n)) * (c + r)
+                assert t >= work / sms
+                assert t >= n * (c + r)           # KV_0 owns n tasks under both masks
+
+
+def test_ascending_descending_never_deadlock():
+    # Their dQ order is ascending KV index, which is also the dealing order.
+    for mask, sched in itertools.product(["full", "causal"], ["ascending", "descending"]):
+        for n in (1, 2, 3, 5, 8):
+            for m in (1, 2, 3):
+                for sms in (1, 2, 3, 7):
+                    assert simulate(mask, sched, n, m, sms, 2, 1)["makespan"] is not None
+
+
+def test_shift_deadlocks_when_a_head_is_split_behind_itself():
+    # n = 4 on 3 SMs: KV_3 of head 0 is queued behind KV_0 on SM 0, but KV_0's last task
+    # (j = 3, arrival step 3) must wait for KV_3's first reduction into dQ_3 (step 0).
+    assert simulate("full", "shift", 4, 1, 3, 3, 1)["makespan"] is None
+    assert simulate("full", "shift", 4, 1, 4, 3, 1)["makespan"] == 4 * 4
+
+
+def _chain_graph(n_chains, weights):
+    """n parallel isomorphic chains between one source (0) and one sink (1)."""
+    k = len(weights)
+    edges = []
+    vid = lambda a, p: 2 + a * (k + 1) + p          # vertex p (0..k) of chain a
+    for a in range(n_chains):
+        edges.append((0, vid(a, 0), 0.0))
+        for p, w in enumerate(weights):
+            edges.append((vid(a, p), vid(a, p + 1), float(w)))
+        edges.append((vid(a, k), 1, 0.0))
+    return 2 + n_chains * (k + 1), edges, vid
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_lemma1_brute_force(seed):
+    # Lemma 1: on parallel isomorphic chains with one source and one sink, a zero-weight
+    # edge (u, v) keeps the critical path iff depth(u) <= depth(v).
+    rng = random.Random(seed)
+    n_chains = rng.randint(2, 4)
+    weights = [rng.choice([1, 2, 3, 5]) for _ in range(rng.randint(2, 6))]
+    nv, edges, vid = _chain_graph(n_chains, weights)
+    base = longest_path(nv, edges)
+    cp = base[1]
+    k = len(weights)
+    for _ in range(30):
+        a, b = rng.sample(range(n_chains), 2)
+        u, v = vid(a, rng.randint(0, k)), vid(b, rng.randint(0, k))
+        new = longest_path(nv, edges + [(u, v, 0.0)])
+        assert new is not None
+        assert (new[1] == cp) == (base[u] <= base[v])
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_lemma1_sufficient_direction_general_dag(seed):
+    # On any DAG, a zero-weight edge with depth(u) <= depth(v) changes no depth at all.
+    rng = random.Random(1000 + seed)
+    nv = rng.randint(4, 12)
+    edges = [(u, v, float(rng.randint(0, 4))) for u in range(nv) for v in range(u + 1, nv)
+             if rng.random() < 0.35]
+    base = longest_path(nv, edges)
+    for u in range(nv):
+        for v in range(nv):
+            if u != v and base[u] <= base[v] and u < v:
+                assert longest_path(nv, edges + [(u, v, 0.0)]) == base
+
+
+def test_deadlock_detected_when_order_contradicts_program_order():
+    # Two KV chains on ONE SM in a fixed order whose dQ order is reversed -> a cycle.
+    # Ascending on a single SM works (its dQ order follows the deal order) ...
+    assert simulate("full", "ascending", 3, 1, 1, 3, 1)["makespan"] == 9 * 4
+    # ... and the explicit graph with a reversed reduction edge has a cycle.
+    from oracle.dag import schedule_dag
+    nv, edges, tasks, _ = schedule_dag("full", "ascending", 2, 1, 1, 3, 1)
+    idx = {t: k for k, t in enumerate(tasks)}
+    # force R(1, 0) before R(0, 0): KV_1 runs after KV_0 on the only SM
+    edges = edges + [(4 * idx[(0, 1, 0)] + 3, 4 * idx[(0, 0, 0)] + 2, 0.0)]
+    assert longest_path(nv, edges) is None
