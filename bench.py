@@ -1,0 +1,442 @@
+#!/usr/bin/env python
+"""Benchmark of the deterministic attention backward (DASH schedules) on one GB300.
+
+One step = one whole backward through the C ABI: preprocess (D = rowsum(dO*O)), the main
+kernel (compute + ordered dQ reduction) and, for the non-deterministic variant, the dQ
+convert. Default workload: full mask, batch 2, 16 heads, seqlen 8192, headdim 128, BF16
+N(0,1) inputs, Shift Scheduling (the best DASH order for a full mask). Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--schedule NAME]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU (replicas: the
+path has no exchange between heads); value = total FLOPs of all ranks / max time.
+--impl reference times the fp64 CPU oracle on the host cores instead.
+"""
+
+import os
+
+# BLAS threads for the CPU oracle legs: all cores this process may use (set before numpy).
+_CORES = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+os.environ.setdefault("OPENBLAS_NUM_THREADS", str(_CORES))
+os.environ.setdefault("OMP_NUM_THREADS", str(_CORES))
+
+import argparse  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import math  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "deterministic attn-bwd TFLOPS (BF16, 1×GB300) and % of tensor peak vs non-det"
+
+WORKLOADS = {
+    "full-1x256x1x64": dict(mask="full", B=1, S=256, H=1, D=64),
+    "causal-4x2048x16x64": dict(mask="causal", B=4, S=2048, H=16, D=64),
+    "full-2x8192x16x128": dict(mask="full", B=2, S=8192, H=16, D=128),
+    "causal-1x16384x32x128": dict(mask="causal", B=1, S=16384, H=32, D=128),
+}
+DEFAULT_WORKLOAD = "full-2x8192x16x128"
+BEST_DASH = {"full": "shift", "causal": "symmetric_shift"}
+L2_BYTES = 129 * 1024 * 1024
+
+
+def bwd_flops(w) -> float:
+    """Algorithmic backward FLOPs: 10*B*H*S^2*D (5 GEMM-shaped products), halved when causal."""
+    f = 10.0 * w["B"] * w["H"] * w["S"] ** 2 * w["D"]
+    return f / 2 if w["mask"] == "causal" else f
+
+
+def slice_flops(w) -> float:
+    return bwd_flops(w) / (w["B"] * w["H"])
+
+
+def input_bytes(w) -> int:
+    t = w["B"] * w["S"] * w["H"] * w["D"] * 2
+    return 5 * t + w["B"] * w["H"] * w["S"] * 4
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p["hbm_gbs"]), "measured"
+    return 1900.0, 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            cmd += ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            pass
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------
+# the fp64 CPU oracle (reported baseline / reference arm)
+# ---------------------------------------------------------------------------------------
+def oracle_slices(w, budget_s: float, max_slices: int, seed: int = 0):
+    """Time the oracle backward on (b, h) slices of the workload until budget_s is used.
+
+    Returns (seconds per slice, slices timed). Inputs are the workload's own seeded bf16
+    tensors; O and LSE come from the oracle forward (untimed)."""
+    from oracle.attention import attn_bwd_slice, attn_fwd_slice
+    from reproducible_deterministic_attn_gb300.inputs import make_inputs
+
+    x = make_inputs(w["B"], w["S"], w["H"], w["D"], seed)
+    f = lambda t, b, h: t[b, :, h].float().double().numpy()
+    causal = w["mask"] == "causal"
+    scale = 1.0 / math.sqrt(w["D"])
+    times = []
+    for idx in range(min(max_slices, w["B"] * w["H"])):
+        b, h = divmod(idx, w["H"])
+        q, k, v, do = (f(x[n], b, h) for n in ("q", "k", "v", "do"))
+        o, lse = attn_fwd_slice(q, k, v, scale, causal, row_block=1024)
+        t0 = time.perf_counter()
+        attn_bwd_slice(q, k, v, o, do, lse, scale, causal, row_block=1024)
+        times.append(time.perf_counter() - t0)
+        if sum(times) >= budget_s:
+            break
+    return statistics.median(times), len(times)
+
+
+def cpu_baseline(w, budget_s=12.0):
+    per_slice, n = oracle_slices(w, budget_s, max_slices=64)
+    tflops = slice_flops(w) / per_slice / 1e12
+    return {"value": tflops, "unit": "TFLOPS", "cores": int(os.environ["OPENBLAS_NUM_THREADS"]),
+            "kind": "oracle",
+            "sample": f"{n} (batch, head) slice(s) of the workload (seqlen {w['S']}, headdim "
+                      f"{w['D']}, {w['mask']} mask), fp64 NumPy/OpenBLAS, median time per slice "
+                      f"scaled to the slice's FLOPs"}
+
+
+def run_reference(args, w, rank):
+    if rank != 0:
+        return
+    per = []
+    steps = args.steps if args.steps else 3
+    warm = args.warmup if args.warmup is not None else 1
+    # each step: one (b, h) slice of the backward (bounded sample of the workload)
+    from oracle.attention import attn_bwd_slice, attn_fwd_slice
+    from reproducible_deterministic_attn_gb300.inputs import make_inputs
+
+    x = make_inputs(1, w["S"], 1, w["D"], 0)
+    f = lambda t: t[0, :, 0].float().double().numpy()
+    q, k, v, do = (f(x[n]) for n in ("q", "k", "v", "do"))
+    causal = w["mask"] == "causal"
+    scale = 1.0 / math.sqrt(w["D"])
+    o, lse = attn_fwd_slice(q, k, v, scale, causal, row_block=1024)
+    for it in range(warm + steps):
+        t0 = time.perf_counter()
+        attn_bwd_slice(q, k, v, o, do, lse, scale, causal, row_block=1024)
+        dt = time.perf_counter() - t0
+        if it >= warm:
+            per.append(dt)
+    ms = statistics.median(per) * 1e3
+    value = slice_flops(w) / (ms / 1e3) / 1e12
+    cores = int(os.environ["OPENBLAS_NUM_THREADS"])
+    sample = (f"one (batch, head) slice per step (seqlen {w['S']}, headdim {w['D']}, "
+              f"{w['mask']} mask), fp64 NumPy/OpenBLAS oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
+        "n_gpus": args.gpus, "steps": steps, "warmup": warm, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(args, w),
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(args, w):
+    return {"workload": args.workload, "mask": w["mask"], "batch": w["B"], "heads": w["H"],
+            "seqlen": w["S"], "headdim": w["D"], "schedule": args.schedule,
+            "deterministic": True,
+            "l2": ("inputs larger than L2 (%.0f MB read per step vs 129 MB L2)"
+                   % (input_bytes(w) / 2**20)) if input_bytes(w) > L2_BYTES else
+                  "L2 flushed between steps (256 MB write)"}
+
+
+# ---------------------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------------------
+def traffic_from_profile(w, sched):
+    """Per-launch DRAM bytes of the main kernel from the committed ncu summary, if it was
+    taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "bwd_main_traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("source_hash") != kernel_source_hash():
+        return None
+    key = f"{w['mask']}-{w['B']}x{w['S']}x{w['H']}x{w['D']}-{sched}"
+    ent = rec.get("per_launch_bytes", {}).get(key)
+    return float(ent) if ent is not None else None
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "reproducible_deterministic_attn_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def run_gpu(args, w, rank, world, local_rank):
+    import torch.distributed as dist
+
+    import reproducible_deterministic_attn_gb300 as da
+    from reproducible_deterministic_attn_gb300 import build as _build
+    from reproducible_deterministic_attn_gb300.inputs import make_inputs
+
+    _build.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    B, S, H, D = w["B"], w["S"], w["H"], w["D"]
+    causal = w["mask"] == "causal"
+    mask = da.MASK_CAUSAL if causal else da.MASK_FULL
+    scale = 1.0 / math.sqrt(D)
+    sched = da.SCHEDULES[args.schedule]
+
+    x = make_inputs(B, S, H, D, seed=rank)
+    q, k, v, do = (x[nm].to(dev) for nm in ("q", "k", "v", "do"))
+    o, lse = da.attn_forward(q, k, v, scale, causal)
+    ws = da.new_workspace(B, S, H, D, dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    flush = None
+    if input_bytes(w) <= L2_BYTES:
+        flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
+
+    def step(det=1, s=sched):
+        if flush is not None:
+            flush.fill_(1)
+        da.dash_attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, scale, mask, s, det)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+
+    def timed(n_steps, det=1, s=sched, profile=False):
+        barrier()
+        if profile:
+            da.dash_profile_enable(True)
+            da.dash_profile_read()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n_steps):
+            step(det, s)
+        e1.record()
+        barrier()
+        ms = e0.elapsed_time(e1)
+        main = None
+        if profile:
+            tot, cnt = da.dash_profile_read()
+            da.dash_profile_enable(False)
+            main = tot / max(cnt, 1)
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms / n_steps, main
+
+    warm = args.warmup if args.warmup is not None else 3
+    for _ in range(warm):
+        step()
+    st = da.dash_attn_get_status(ws)
+    if st != da.DASH_OK:
+        raise da.DashError(st, "warm-up backward")
+    if args.steps:
+        steps = args.steps
+    else:
+        t0 = time.perf_counter()
+        step()
+        torch.cuda.synchronize()
+        one = time.perf_counter() - t0
+        steps = int(min(500, max(10, math.ceil(2.0 / max(one, 1e-4)))))
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    ms_step, main_ms = timed(steps, profile=True)
+    clocks = sampler.stop() if sampler else None
+    st = da.dash_attn_get_status(ws)
+    if st != da.DASH_OK:
+        raise da.DashError(st, "timed backward")
+
+    total_flops = bwd_flops(w) * world
+    value = total_flops / (ms_step / 1e3) / 1e12
+    peak_tf, _, peak_kind = load_peaks()
+
+    # the other variants of the same run: non-deterministic (speed reference) and the
+    # FA3-baseline ascending order
+    side = {}
+    n_side = max(3, steps // 4)
+    for name, det, s in (("nondet", 0, da.SCHED_ASCENDING), ("ascending", 1, da.SCHED_ASCENDING),
+                         ("descending", 1, da.SCHED_DESCENDING)):
+        if name == args.schedule:
+            continue
+        for _ in range(2):
+            step(det, s)
+        ms_s, _ = timed(n_side, det, s)
+        side[name] = bwd_flops(w) * world / (ms_s / 1e3) / 1e12
+
+    # end to end through the public API with host buffers: pinned H2D of this step's
+    # inputs, the backward, D2H of dQ/dK/dV, every step
+    host = {nm: t.cpu().pin_memory() for nm, t in
+            (("q", q), ("k", k), ("v", v), ("o", o), ("do", do), ("lse", lse))}
+    outs = {nm: torch.empty(q.shape, dtype=q.dtype).pin_memory() for nm in ("dq", "dk", "dv")}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs.values())
+    n_e2e = max(3, steps // 4)
+
+    def e2e_step():
+        q.copy_(host["q"], non_blocking=True)
+        k.copy_(host["k"], non_blocking=True)
+        v.copy_(host["v"], non_blocking=True)
+        o.copy_(host["o"], non_blocking=True)
+        do.copy_(host["do"], non_blocking=True)
+        lse.copy_(host["lse"], non_blocking=True)
+        da.dash_attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, scale, mask, sched, 1)
+        outs["dq"].copy_(dq, non_blocking=True)
+        outs["dk"].copy_(dk, non_blocking=True)
+        outs["dv"].copy_(dv, non_blocking=True)
+
+    e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w)
+    achieved = bwd_flops(w) / (main_ms / 1e3) / 1e12 if main_ms else None
+    launches_per_step = 2          # preprocess + main (deterministic path)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": steps,
+        "warmup": warm, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(args, w),
+        "pct_of_peak": 100.0 * value / world / peak_tf,
+        "nondet_tflops": side.get("nondet"),
+        "det_vs_nondet": value / side["nondet"] if side.get("nondet") else None,
+        "schedules": {args.schedule: value, **{kk: vv for kk, vv in side.items() if kk != "nondet"}},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf,
+                     "unit": "TFLOP/s", "frac": (achieved / peak_tf) if achieved else None,
+                     "traffic": traffic_from_profile(w, args.schedule),
+                     "kernel": "bwd main (compute + ordered dQ reduction)",
+                     "peak_kind": f"{peak_kind} bf16 dense (burst)"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": bwd_flops(w) * world / (e2e_ms / 1e3) / 1e12, "unit": "TFLOPS",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=0)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--schedule", default=None,
+                    choices=["ascending", "descending", "shift", "symmetric_shift"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = WORKLOADS[args.workload]
+    if args.schedule is None:
+        args.schedule = BEST_DASH[w["mask"]]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, w, rank)
+        return
+    if world > 1:
+        import torch.distributed as dist
+
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", rank=rank, world_size=world)
+    try:
+        run_gpu(args, w, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,187 @@
+/*
+ * dash_attn.h -- C ABI of the deterministic attention backward with DASH schedules.
+ *
+ * Source of the method: "DASH: Deterministic Attention Scheduling for High-throughput
+ * Reproducible LLM Training" (ICLR 2026; arXiv 2601.21824), as summarised on its research
+ * map page (sections "Problem" and "Approach") and in its Pith review ("The pith",
+ * "Core claim", "What carries the argument", the referee report and Figures 1-7).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Tensors Q, K, V, O, dO, dQ, dK, dV are bf16, contiguous, BSHD: element (b, s, h, d)
+ *   sits at index ((b * S + s) * H + h) * D + d. LSE is fp32 [B, H, S], natural log of
+ *   the sum of exp(scale * q.k) over the keys a query may see.
+ * - Supported: D in {64, 128}; S a positive multiple of 128; B, H >= 1;
+ *   B * H * S * D < 2^31. Anything else returns DASH_ERR_UNSUPPORTED.
+ * - The causal mask is top-left aligned (query i sees keys 0..i).
+ * - All device pointers are owned by the caller and must stay valid until the work
+ *   queued on `stream` has finished. The library allocates nothing per call; it keeps a
+ *   small cache of schedule tables per device (released by dash_attn_shutdown).
+ * - Calls are asynchronous on `stream`. Argument errors are returned synchronously and
+ *   queue no work. Device-side failures (a reduction wait that timed out) are recorded
+ *   in the workspace and reported by dash_attn_get_status.
+ * - Pointers must be 16-byte aligned.
+ */
+#ifndef DASH_ATTN_H
+#define DASH_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Attention mask. */
+typedef enum { DASH_MASK_FULL = 0, DASH_MASK_CAUSAL = 1 } dash_mask_t;
+
+/*
+ * Task orders (research map page, "Approach"; Pith review, "What carries the argument";
+ * Figure 3, 4, 6 and 7 captions). KV tile i always runs all of its tasks on one SM.
+ * - ASCENDING: the FlashAttention-3 baseline; KV_i visits Q tiles upwards.
+ * - DESCENDING: Descending Q-Tile Iteration; KV_i visits Q tiles downwards.
+ * - SHIFT: Shift Scheduling (full mask only); at step t KV_i works on Q_((i+t) mod n).
+ * - SYMMETRIC_SHIFT: Symmetric Shift (causal mask only, n even); one SM slot takes
+ *   KV_p and KV_(n-1-p): phase 1 shifts over the dense lower-left rectangle, phase 2
+ *   runs the folded triangles from the diagonal, upper-left first.
+ * The dQ_j reduction order is ascending KV index for ASCENDING and DESCENDING, and the
+ * arrival step for SHIFT and SYMMETRIC_SHIFT.
+ */
+typedef enum {
+  DASH_SCHED_ASCENDING = 0,
+  DASH_SCHED_DESCENDING = 1,
+  DASH_SCHED_SHIFT = 2,
+  DASH_SCHED_SYMMETRIC_SHIFT = 3
+} dash_sched_t;
+
+typedef enum {
+  DASH_OK = 0,
+  DASH_ERR_INVALID_ARG = 1,         /* null pointer, negative size, bad enum value */
+  DASH_ERR_UNSUPPORTED = 2,         /* valid but not implemented (head dim, mask/schedule pair) */
+  DASH_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < dash_attn_bwd_workspace_size() */
+  DASH_ERR_CUDA = 4,                /* a CUDA runtime call failed; see dash_last_error() */
+  DASH_ERR_SYNC_TIMEOUT = 5,        /* a dQ reduction wait exceeded its time limit */
+  DASH_ERR_DEADLOCK_RISK = 6        /* the schedule's waits form a cycle on this grid */
+} dash_status_t;
+
+/*
+ * Forward pass: O = softmax(scale * Q K^T [+ causal mask]) V and LSE per query row.
+ * Produces the two inputs the backward recomputes P from (FlashAttention-3's forward,
+ * named on the research map page under "Builds on").
+ *   q, k, v : [B, S, H, D] bf16 (read)      o : [B, S, H, D] bf16 (written)
+ *   lse     : [B, H, S] fp32 (written)      mask : dash_mask_t
+ * Returns DASH_OK or an argument/CUDA error; nothing is queued on error.
+ */
+dash_status_t dash_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int S, int H, int D, float scale, int mask,
+                            cudaStream_t stream);
+
+/*
+ * Bytes of scratch dash_attn_bwd needs for this shape: a status header, D = rowsum(dO*O)
+ * (fp32 [B,H,S]), the fp32 dQ accumulator [B,H,S,D] and one int32 semaphore per dQ block
+ * [B,H,S/128]. Returns 0 for an unsupported shape.
+ */
+size_t dash_attn_bwd_workspace_size(int B, int S, int H, int D);
+
+/*
+ * Backward pass (the DASH problem statement: research map page "Problem"; Pith review
+ * "Core claim"). Recomputes P from Q, K and LSE, then forms dV, dP, dS, dK and dQ. Each
+ * KV tile's dK/dV accumulates on one SM. Each dQ block is the sum of one partial per KV
+ * tile that sees it:
+ *   deterministic = 1: the partials are added in the fixed order `schedule` defines,
+ *                      serialised through one semaphore per dQ block. The result is
+ *                      bitwise identical for identical inputs, shape and schedule on the
+ *                      same GPU model and build. Different schedules may differ in the
+ *                      last bits (their dQ orders differ).
+ *   deterministic = 0: the partials are added atomically in arrival order (the speed
+ *                      reference; results vary in the last bits run to run).
+ *   q, k, v, o, dO : [B, S, H, D] bf16 (read);  lse : [B, H, S] fp32 (read)
+ *   dq, dk, dv     : [B, S, H, D] bf16 (written; must not alias the inputs)
+ *   workspace      : device scratch of at least dash_attn_bwd_workspace_size() bytes,
+ *                    256-byte aligned, not shared with work running concurrently.
+ *   schedule       : dash_sched_t. SHIFT needs the full mask, SYMMETRIC_SHIFT the causal
+ *                    mask; other pairs return DASH_ERR_UNSUPPORTED.
+ * Returns DASH_ERR_DEADLOCK_RISK (nothing queued) if the schedule's reduction waits would
+ * form a cycle on the persistent grid this GPU can hold.
+ */
+dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                            const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                            void* workspace, size_t workspace_bytes,
+                            int B, int S, int H, int D, float scale, int mask, int schedule,
+                            int deterministic, cudaStream_t stream);
+
+/*
+ * Synchronises `stream` and reads the status header of `workspace` written by the last
+ * dash_attn_bwd on it: DASH_OK, or DASH_ERR_SYNC_TIMEOUT when a reduction wait ran out
+ * (the kernel then abandons its remaining work; outputs are undefined). Also returns
+ * DASH_ERR_CUDA if the stream reports an error.
+ */
+dash_status_t dash_attn_get_status(const void* workspace, cudaStream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* dash_status_string(int status);
+
+/* Text of the last CUDA error seen by this thread inside the library ("" if none). */
+const char* dash_last_error(void);
+
+/* Frees the cached schedule tables on every device. Safe to call more than once. */
+void dash_attn_shutdown(void);
+
+/*
+ * Testing hook for the failure path of the ordered dQ reduction. Sets, for later
+ * dash_attn_bwd calls in this process, the time limit of one semaphore wait
+ * (timeout_ns <= 0 restores the default of 10 s) and a skew added to every awaited
+ * ordinal. With a skew > 0 no wait can ever be satisfied: each one runs out its limit,
+ * the kernel records DASH_ERR_SYNC_TIMEOUT in the workspace and returns, and the CUDA
+ * context stays usable. Not thread-safe against concurrent dash_attn_bwd calls.
+ */
+void dash_debug_set_sync(long long timeout_ns, int ordinal_skew);
+
+/*
+ * Profiling hook. With on != 0, every later dash_attn_bwd records a pair of CUDA events
+ * on its stream, immediately before and after its main (compute + dQ reduction) kernel,
+ * up to 1024 pairs. dash_profile_read waits for the recorded events, writes the summed
+ * main-kernel milliseconds and the number of launches, and forgets them. on = 0 stops
+ * recording. Returns a dash_status_t.
+ */
+dash_status_t dash_profile_enable(int on);
+dash_status_t dash_profile_read(double* total_ms, int* launches);
+
+/* ---- Schedule model (host only; no GPU needed) ------------------------------------ */
+
+/*
+ * Number of chains ("SM slots") per head for (mask, schedule) over n KV tiles:
+ * n for ASCENDING/DESCENDING/SHIFT, n/2 for SYMMETRIC_SHIFT. Negative dash_status_t
+ * value on an unsupported pair or n < 1 (or odd n for SYMMETRIC_SHIFT).
+ */
+int dash_sched_num_slots(int mask, int schedule, int n);
+
+/*
+ * Copies the task table the kernel follows.
+ *   slot_offsets : int32[num_slots + 1]; chain p is tasks[slot_offsets[p] .. slot_offsets[p+1])
+ *   tasks        : int32[cap]; each entry packs (kv_tile << 16) | q_tile, in execution order
+ *   ordinals     : int32[n * n]; ordinals[i * n + j] = position of KV_i's partial in the dQ_j
+ *                  reduction order, or -1 where the mask removes task (i, j)
+ * Returns the number of tasks, or a negative dash_status_t value (cap too small:
+ * -DASH_ERR_INVALID_ARG).
+ */
+int dash_sched_table(int mask, int schedule, int n, int32_t* slot_offsets, int32_t* tasks,
+                     int cap, int32_t* ordinals);
+
+/*
+ * Critical path of the compute/reduce DAG (Pith review, "What carries the argument"):
+ * every task is a compute phase of cost c then a reduce phase of cost r; one SM runs its
+ * tasks back to back; reductions into one dQ block follow the schedule's order. `heads`
+ * heads' chains are dealt round robin, head-major, onto `num_sms` SMs (the kernel's own
+ * dealing). Writes the makespan and, if sm_end is not NULL, each SM's finish time
+ * (double[num_sms]). Returns DASH_ERR_DEADLOCK_RISK when the waits form a cycle.
+ */
+dash_status_t dash_sched_simulate(int mask, int schedule, int n, int heads, int num_sms,
+                                  double c, double r, double* makespan, double* sm_end);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DASH_ATTN_H */

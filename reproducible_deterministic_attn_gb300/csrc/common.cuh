@@ -1,0 +1,113 @@
+// Shared device helpers: parameter blocks, bf16 conversion, the bounded semaphore wait.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+namespace dash {
+
+constexpr int kTile = 128;             // KV tile rows = Q tile rows (square task grid)
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Workspace header (int32 words). The header occupies the first 256 bytes.
+enum : int {
+  WS_STATUS = 0,      // 0 = ok, DASH_ERR_SYNC_TIMEOUT on a timed-out wait
+  WS_BH = 1,          // (batch * H + head) of the first failing wait
+  WS_QTILE = 2,       // dQ block of the first failing wait
+  WS_EXPECT = 3,      // ordinal it waited for
+  WS_SEEN = 4,        // semaphore value it last saw
+};
+constexpr size_t kWsHeaderBytes = 256;
+constexpr int kStatusSyncTimeout = 5;
+
+struct FwdParams {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  __nv_bfloat16* o;
+  float* lse;
+  int B, S, H, D;
+  float scale;
+  int causal;
+};
+
+struct BwdParams {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  const __nv_bfloat16* o;
+  const __nv_bfloat16* dO;
+  const float* lse;          // [B, H, S]
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int* ws_header;            // status words
+  float* Dsum;               // [B, H, S] rowsum(dO * O)
+  float* dq_acc;             // [B, H, S, D] fp32
+  int* sems;                 // [B, H, n]
+  const int32_t* slot_off;   // schedule: chain offsets
+  const int32_t* tasks;      // schedule: (kv << 16) | q
+  const int32_t* ord;        // schedule: n * n ordinals
+  const int32_t* cnt;        // schedule: contributors per dQ block
+  int B, S, H, D;
+  int n;                     // tiles per head
+  int num_slots;             // chains per head
+  int num_units;             // B * H * num_slots
+  float scale;
+  float scale_log2;          // scale * log2(e)
+  int causal;
+  int deterministic;
+  long long timeout_ns;      // bound on one semaphore wait
+  int ordinal_skew;          // testing hook: added to every awaited ordinal
+};
+
+__device__ __forceinline__ long long global_timer_ns() {
+  long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ int ld_relaxed_gpu(const int* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Spin (one thread) until *sem == target. Gives up when another CTA has already
+// reported a failure, or after timeout_ns, recording the first failure in the
+// workspace header. Returns true when it is this CTA's turn.
+__device__ __noinline__ bool wait_turn(const int* sem, int target, int* ws, long long timeout_ns,
+                                       int bh, int qtile) {
+  int seen = ld_acquire_gpu(sem);
+  if (seen == target) return true;
+  const long long t0 = global_timer_ns();
+  // iteration cap as a second bound, independent of the timer
+  const long long max_iter = timeout_ns / 16 + (1ll << 20);
+  for (long long it = 0; it < max_iter; ++it) {
+    __nanosleep(40);
+    seen = ld_acquire_gpu(sem);
+    if (seen == target) return true;
+    if (ld_relaxed_gpu(ws + WS_STATUS) != 0) return false;
+    if (global_timer_ns() - t0 > timeout_ns) break;
+  }
+  if (atomicCAS(ws + WS_STATUS, 0, kStatusSyncTimeout) == 0) {
+    ws[WS_BH] = bh;
+    ws[WS_QTILE] = qtile;
+    ws[WS_EXPECT] = target;
+    ws[WS_SEEN] = seen;
+    __threadfence();
+  }
+  return false;
+}
+
+}  // namespace dash

@@ -1,0 +1,389 @@
+// C ABI entry points of libdash_attn: argument checks, schedule-table cache, the
+// deadlock check of the persistent grid, and the kernel launches.
+#include "../../include/dash_attn.h"
+
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "common.cuh"
+#include "kernels_simt.cuh"
+#include "sched.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+// Testing hooks (dash_debug_set_sync): bound on one semaphore wait and a skew added to
+// every awaited ordinal (a skew > 0 makes every wait time out).
+long long g_timeout_ns = 10ll * 1000 * 1000 * 1000;
+int g_ordinal_skew = 0;
+
+dash_status_t cuda_fail(cudaError_t e, const char* what) {
+  g_last_error = std::string(what) + ": " + cudaGetErrorString(e);
+  return DASH_ERR_CUDA;
+}
+
+#define DASH_CUDA(call)                                   \
+  do {                                                    \
+    cudaError_t e_ = (call);                              \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call);   \
+  } while (0)
+
+struct DeviceTables {
+  int32_t* slot_off = nullptr;
+  int32_t* tasks = nullptr;
+  int32_t* ord = nullptr;
+  int32_t* cnt = nullptr;
+  int num_slots = 0;
+};
+
+std::mutex g_mu;
+std::map<std::tuple<int, int, int, int>, DeviceTables> g_tables;        // (dev, mask, sched, n)
+std::map<std::tuple<int, int, int, int, int>, bool> g_deadlock_free;    // (mask, sched, n, heads, grid)
+
+dash_status_t get_tables(int dev, int mask, int sched, int n, DeviceTables* out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto key = std::make_tuple(dev, mask, sched, n);
+  auto it = g_tables.find(key);
+  if (it != g_tables.end()) {
+    *out = it->second;
+    return DASH_OK;
+  }
+  dash::Schedule sc;
+  int rc = dash::build_schedule(mask, sched, n, &sc);
+  if (rc) return (dash_status_t)rc;
+  DeviceTables t;
+  t.num_slots = sc.num_slots;
+  auto upload = [](const std::vector<int32_t>& v, int32_t** dst) -> cudaError_t {
+    cudaError_t e = cudaMalloc(dst, v.size() * sizeof(int32_t));
+    if (e != cudaSuccess) return e;
+    return cudaMemcpy(*dst, v.data(), v.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
+  };
+  DASH_CUDA(upload(sc.slot_off, &t.slot_off));
+  DASH_CUDA(upload(sc.tasks, &t.tasks));
+  DASH_CUDA(upload(sc.ord, &t.ord));
+  DASH_CUDA(upload(sc.cnt, &t.cnt));
+  g_tables[key] = t;
+  *out = t;
+  return DASH_OK;
+}
+
+// True when the schedule's waits are acyclic for `heads` heads on `grid` persistent CTAs.
+bool deadlock_free(int mask, int sched, int n, int heads, int grid) {
+  auto key = std::make_tuple(mask, sched, n, heads, grid);
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_deadlock_free.find(key);
+    if (it != g_deadlock_free.end()) return it->second;
+  }
+  bool ok = true;
+  if (sched == dash::SCHED_SHIFT || sched == dash::SCHED_SYMMETRIC_SHIFT) {
+    // Ascending/descending wait only on lower KV indices, which are dealt earlier.
+    dash::Schedule sc;
+    if (dash::build_schedule(mask, sched, n, &sc) != 0) return false;
+    double mk = 0;
+    ok = dash::simulate(sc, heads, grid, 1.0, 0.1, &mk, nullptr);
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_deadlock_free[key] = ok;
+  return ok;
+}
+
+bool shape_ok(int B, int S, int H, int D) {
+  if (B < 1 || S < 1 || H < 1) return false;
+  if (D != 64 && D != 128) return false;
+  if (S % dash::kTile) return false;
+  if (S / dash::kTile > 32767) return false;
+  if ((long long)B * S * H * D >= (1ll << 31)) return false;
+  return true;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Profiling hook state: a pool of event pairs recorded around the main kernel.
+constexpr int kProfPairs = 1024;
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+int g_prof_used = 0;
+std::vector<cudaEvent_t> g_prof_ev;   // 2 * kProfPairs
+
+cudaEvent_t prof_event(bool stop) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!g_prof_on || g_prof_used >= kProfPairs) return nullptr;
+  cudaEvent_t e = g_prof_ev[2 * g_prof_used + (stop ? 1 : 0)];
+  if (stop) ++g_prof_used;
+  return e;
+}
+
+struct WsLayout {
+  size_t dsum, dq_acc, sems, total;
+};
+
+WsLayout ws_layout(int B, int S, int H, int D) {
+  WsLayout w;
+  const size_t rows = (size_t)B * H * S;
+  w.dsum = dash::kWsHeaderBytes;
+  w.dq_acc = round_up(w.dsum + rows * sizeof(float), 256);
+  w.sems = round_up(w.dq_acc + rows * D * sizeof(float), 256);
+  w.total = round_up(w.sems + (size_t)B * H * (S / dash::kTile) * sizeof(int), 256);
+  return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dash_status_string(int status) {
+  switch (status) {
+    case DASH_OK: return "DASH_OK";
+    case DASH_ERR_INVALID_ARG: return "DASH_ERR_INVALID_ARG";
+    case DASH_ERR_UNSUPPORTED: return "DASH_ERR_UNSUPPORTED";
+    case DASH_ERR_WORKSPACE_TOO_SMALL: return "DASH_ERR_WORKSPACE_TOO_SMALL";
+    case DASH_ERR_CUDA: return "DASH_ERR_CUDA";
+    case DASH_ERR_SYNC_TIMEOUT: return "DASH_ERR_SYNC_TIMEOUT";
+    case DASH_ERR_DEADLOCK_RISK: return "DASH_ERR_DEADLOCK_RISK";
+    default: return "DASH_ERR_UNKNOWN";
+  }
+}
+
+const char* dash_last_error(void) { return g_last_error.c_str(); }
+
+void dash_debug_set_sync(long long timeout_ns, int ordinal_skew) {
+  g_timeout_ns = timeout_ns > 0 ? timeout_ns : 10ll * 1000 * 1000 * 1000;
+  g_ordinal_skew = ordinal_skew;
+}
+
+void dash_attn_shutdown(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int cur = -1;
+  cudaGetDevice(&cur);
+  for (auto& kv : g_tables) {
+    cudaSetDevice(std::get<0>(kv.first));
+    cudaFree(kv.second.slot_off);
+    cudaFree(kv.second.tasks);
+    cudaFree(kv.second.ord);
+    cudaFree(kv.second.cnt);
+  }
+  if (cur >= 0) cudaSetDevice(cur);
+  g_tables.clear();
+  g_deadlock_free.clear();
+}
+
+size_t dash_attn_bwd_workspace_size(int B, int S, int H, int D) {
+  if (!shape_ok(B, S, H, D)) return 0;
+  return ws_layout(B, S, H, D).total;
+}
+
+dash_status_t dash_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int S, int H, int D, float scale, int mask,
+                            cudaStream_t stream) {
+  if (!q || !k || !v || !o || !lse) return DASH_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || H < 1 || D < 1) return DASH_ERR_INVALID_ARG;
+  if (mask != DASH_MASK_FULL && mask != DASH_MASK_CAUSAL) return DASH_ERR_INVALID_ARG;
+  if (!(scale > 0.f)) return DASH_ERR_INVALID_ARG;
+  if (!shape_ok(B, S, H, D)) return DASH_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return DASH_ERR_INVALID_ARG;
+  dash::FwdParams p{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v,
+                    (__nv_bfloat16*)o, lse, B, S, H, D, scale, mask == DASH_MASK_CAUSAL};
+  dim3 grid(S / 64, B * H);
+  const size_t smem = (size_t)(64 * D + 2 * 64 * D + 64 * 65 + 3 * 64) * sizeof(float);
+  if (D == 64) {
+    DASH_CUDA(cudaFuncSetAttribute(dash::fwd_simt_kernel<64>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    dash::fwd_simt_kernel<64><<<grid, 256, smem, stream>>>(p);
+  } else {
+    DASH_CUDA(cudaFuncSetAttribute(dash::fwd_simt_kernel<128>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    dash::fwd_simt_kernel<128><<<grid, 256, smem, stream>>>(p);
+  }
+  DASH_CUDA(cudaGetLastError());
+  return DASH_OK;
+}
+
+dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                            const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                            void* workspace, size_t workspace_bytes,
+                            int B, int S, int H, int D, float scale, int mask, int schedule,
+                            int deterministic, cudaStream_t stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || !workspace)
+    return DASH_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || H < 1 || D < 1) return DASH_ERR_INVALID_ARG;
+  if (mask != DASH_MASK_FULL && mask != DASH_MASK_CAUSAL) return DASH_ERR_INVALID_ARG;
+  if (schedule < DASH_SCHED_ASCENDING || schedule > DASH_SCHED_SYMMETRIC_SHIFT)
+    return DASH_ERR_INVALID_ARG;
+  if (deterministic != 0 && deterministic != 1) return DASH_ERR_INVALID_ARG;
+  if (!(scale > 0.f)) return DASH_ERR_INVALID_ARG;
+  if (!shape_ok(B, S, H, D)) return DASH_ERR_UNSUPPORTED;
+  for (const void* ptr : {q, k, v, o, dO, (const void*)lse, (const void*)dq, (const void*)dk,
+                          (const void*)dv})
+    if (!aligned16(ptr)) return DASH_ERR_INVALID_ARG;
+  if (((uintptr_t)workspace & 255u) != 0) return DASH_ERR_INVALID_ARG;
+  const WsLayout wl = ws_layout(B, S, H, D);
+  if (workspace_bytes < wl.total) return DASH_ERR_WORKSPACE_TOO_SMALL;
+  const int n = S / dash::kTile;
+  {
+    dash::Schedule probe;
+    int rc = dash::build_schedule(mask, schedule, n, &probe);
+    if (rc) return (dash_status_t)rc;
+  }
+  int dev = 0;
+  DASH_CUDA(cudaGetDevice(&dev));
+  DeviceTables tb;
+  dash_status_t st = get_tables(dev, mask, schedule, n, &tb);
+  if (st != DASH_OK) return st;
+
+  char* ws = (char*)workspace;
+  dash::BwdParams p;
+  p.q = (const __nv_bfloat16*)q;
+  p.k = (const __nv_bfloat16*)k;
+  p.v = (const __nv_bfloat16*)v;
+  p.o = (const __nv_bfloat16*)o;
+  p.dO = (const __nv_bfloat16*)dO;
+  p.lse = lse;
+  p.dq = (__nv_bfloat16*)dq;
+  p.dk = (__nv_bfloat16*)dk;
+  p.dv = (__nv_bfloat16*)dv;
+  p.ws_header = (int*)ws;
+  p.Dsum = (float*)(ws + wl.dsum);
+  p.dq_acc = (float*)(ws + wl.dq_acc);
+  p.sems = (int*)(ws + wl.sems);
+  p.slot_off = tb.slot_off;
+  p.tasks = tb.tasks;
+  p.ord = tb.ord;
+  p.cnt = tb.cnt;
+  p.B = B;
+  p.S = S;
+  p.H = H;
+  p.D = D;
+  p.n = n;
+  p.num_slots = tb.num_slots;
+  p.num_units = B * H * tb.num_slots;
+  p.scale = scale;
+  p.scale_log2 = scale * dash::kLog2e;
+  p.causal = mask == DASH_MASK_CAUSAL;
+  p.deterministic = deterministic;
+  p.timeout_ns = g_timeout_ns;
+  p.ordinal_skew = g_ordinal_skew;
+
+  // Persistent grid: every CTA must be resident at once (the ordered reduction waits on
+  // other CTAs), so the grid is the occupancy limit and the launch is cooperative.
+  const int threads = 512;
+  const size_t smem = (size_t)2 * dash::kTile * D * 2 + (size_t)2 * 32 * D * 2 +
+                      (size_t)2 * 32 * (dash::kTile + 1) * 4 + (size_t)dash::kTile * D * 4 +
+                      2 * 32 * 4;
+  void* kfn = D == 64 ? (void*)dash::bwd_simt_kernel<64> : (void*)dash::bwd_simt_kernel<128>;
+  DASH_CUDA(cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  int per_sm = 0, sms = 0;
+  DASH_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, threads, smem));
+  DASH_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  if (per_sm < 1) {
+    g_last_error = "backward kernel does not fit on one SM";
+    return DASH_ERR_CUDA;
+  }
+  int grid = per_sm * sms;
+  if (grid > p.num_units) grid = p.num_units;
+  if (deterministic && !deadlock_free(mask, schedule, n, B * H, grid))
+    return DASH_ERR_DEADLOCK_RISK;
+
+  dash::bwd_preprocess_kernel<<<sms * 4, 256, 0, stream>>>(p);
+  DASH_CUDA(cudaGetLastError());
+  void* args[] = {&p};
+  cudaEvent_t ev0 = prof_event(false);
+  if (ev0) DASH_CUDA(cudaEventRecord(ev0, stream));
+  if (deterministic) {
+    DASH_CUDA(cudaLaunchCooperativeKernel(kfn, dim3(grid), dim3(threads), args, smem, stream));
+  } else {
+    DASH_CUDA(cudaLaunchKernel(kfn, dim3(grid), dim3(threads), args, smem, stream));
+  }
+  if (ev0) DASH_CUDA(cudaEventRecord(prof_event(true), stream));
+  if (!deterministic) {
+    dash::dq_convert_kernel<<<sms * 4, 256, 0, stream>>>(p);
+    DASH_CUDA(cudaGetLastError());
+  }
+  return DASH_OK;
+}
+
+dash_status_t dash_attn_get_status(const void* workspace, cudaStream_t stream) {
+  if (!workspace) return DASH_ERR_INVALID_ARG;
+  DASH_CUDA(cudaStreamSynchronize(stream));
+  int words[8];
+  DASH_CUDA(cudaMemcpy(words, workspace, sizeof(words), cudaMemcpyDeviceToHost));
+  if (words[dash::WS_STATUS] == dash::kStatusSyncTimeout) {
+    char buf[160];
+    snprintf(buf, sizeof(buf), "dQ reduction wait timed out: bh=%d q_tile=%d expected=%d seen=%d",
+             words[dash::WS_BH], words[dash::WS_QTILE], words[dash::WS_EXPECT],
+             words[dash::WS_SEEN]);
+    g_last_error = buf;
+    return DASH_ERR_SYNC_TIMEOUT;
+  }
+  return DASH_OK;
+}
+
+dash_status_t dash_profile_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (on && g_prof_ev.empty()) {
+    g_prof_ev.resize(2 * kProfPairs);
+    for (auto& e : g_prof_ev) DASH_CUDA(cudaEventCreate(&e));
+  }
+  g_prof_on = on != 0;
+  return DASH_OK;
+}
+
+dash_status_t dash_profile_read(double* total_ms, int* launches) {
+  if (!total_ms || !launches) return DASH_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  double sum = 0.0;
+  for (int k = 0; k < g_prof_used; ++k) {
+    DASH_CUDA(cudaEventSynchronize(g_prof_ev[2 * k + 1]));
+    float ms = 0.f;
+    DASH_CUDA(cudaEventElapsedTime(&ms, g_prof_ev[2 * k], g_prof_ev[2 * k + 1]));
+    sum += ms;
+  }
+  *total_ms = sum;
+  *launches = g_prof_used;
+  g_prof_used = 0;
+  return DASH_OK;
+}
+
+int dash_sched_num_slots(int mask, int schedule, int n) {
+  dash::Schedule sc;
+  int rc = dash::build_schedule(mask, schedule, n, &sc);
+  return rc ? -rc : sc.num_slots;
+}
+
+int dash_sched_table(int mask, int schedule, int n, int32_t* slot_offsets, int32_t* tasks,
+                     int cap, int32_t* ordinals) {
+  dash::Schedule sc;
+  int rc = dash::build_schedule(mask, schedule, n, &sc);
+  if (rc) return -rc;
+  if (!slot_offsets || !tasks || !ordinals || cap < (int)sc.tasks.size())
+    return -DASH_ERR_INVALID_ARG;
+  std::memcpy(slot_offsets, sc.slot_off.data(), sc.slot_off.size() * sizeof(int32_t));
+  std::memcpy(tasks, sc.tasks.data(), sc.tasks.size() * sizeof(int32_t));
+  std::memcpy(ordinals, sc.ord.data(), sc.ord.size() * sizeof(int32_t));
+  return (int)sc.tasks.size();
+}
+
+dash_status_t dash_sched_simulate(int mask, int schedule, int n, int heads, int num_sms,
+                                  double c, double r, double* makespan, double* sm_end) {
+  if (heads < 1 || num_sms < 1 || !makespan || !(c >= 0) || !(r >= 0)) return DASH_ERR_INVALID_ARG;
+  dash::Schedule sc;
+  int rc = dash::build_schedule(mask, schedule, n, &sc);
+  if (rc) return (dash_status_t)rc;
+  std::vector<double> ends;
+  if (!dash::simulate(sc, heads, num_sms, c, r, makespan, &ends)) return DASH_ERR_DEADLOCK_RISK;
+  if (sm_end) std::memcpy(sm_end, ends.data(), ends.size() * sizeof(double));
+  return DASH_OK;
+}
+
+}  // extern "C"

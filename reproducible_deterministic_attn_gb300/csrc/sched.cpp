@@ -1,0 +1,157 @@
+// Host-side DASH schedule tables and the compute/reduce DAG simulator.
+//
+// Task orders ("DASH: Deterministic Attention Scheduling for High-throughput Reproducible
+// LLM Training": abstract; Pith review "What carries the argument"; Figure 3, 4, 6, 7):
+//   ascending        KV_i visits its Q tiles upwards (FlashAttention-3 baseline)
+//   descending       KV_i visits its Q tiles downwards (Descending Q-Tile Iteration)
+//   shift            full mask: step t of KV_i works on Q_((i+t) mod n)
+//   symmetric shift  causal, n even: slot p runs KV_p over the lower-left rectangle with
+//                    a cyclic shift, then KV_p's upper-left triangle upwards from the
+//                    diagonal, then KV_(n-1-p)'s lower-right triangle downwards.
+// dQ_j reduction order: ascending KV index for ascending/descending; the arrival step
+// (position in the chain) for shift and symmetric shift, which never puts two chains
+// on one dQ block at the same step.
+#include "sched.h"
+
+#include <algorithm>
+
+namespace dash {
+
+namespace {
+inline int32_t pack(int kv, int q) { return (int32_t)((kv << 16) | q); }
+}  // namespace
+
+int build_schedule(int mask, int sched, int n, Schedule* out) {
+  if (n < 1 || n > 32767) return 1;                         // DASH_ERR_INVALID_ARG
+  if (mask != MASK_FULL && mask != MASK_CAUSAL) return 1;
+  if (sched < SCHED_ASCENDING || sched > SCHED_SYMMETRIC_SHIFT) return 1;
+  if (sched == SCHED_SHIFT && mask != MASK_FULL) return 2;  // DASH_ERR_UNSUPPORTED
+  if (sched == SCHED_SYMMETRIC_SHIFT && (mask != MASK_CAUSAL || (n & 1))) return 2;
+
+  Schedule s;
+  s.mask = mask;
+  s.sched = sched;
+  s.n = n;
+  const bool causal = mask == MASK_CAUSAL;
+  std::vector<std::vector<int32_t>> chains;
+  if (sched == SCHED_SYMMETRIC_SHIFT) {
+    const int half = n / 2;
+    for (int p = 0; p < half; ++p) {
+      std::vector<int32_t> ch;
+      for (int t = 0; t < half; ++t) ch.push_back(pack(p, half + (p + t) % half));
+      for (int u = 0; u < half - p; ++u) ch.push_back(pack(p, p + u));
+      for (int u = 0; u <= p; ++u) ch.push_back(pack(n - 1 - p, n - 1 - u));
+      chains.push_back(std::move(ch));
+    }
+  } else {
+    for (int i = 0; i < n; ++i) {
+      std::vector<int32_t> ch;
+      const int lo = causal ? i : 0;
+      const int len = n - lo;
+      for (int t = 0; t < len; ++t) {
+        int q;
+        if (sched == SCHED_ASCENDING) q = lo + t;
+        else if (sched == SCHED_DESCENDING) q = n - 1 - t;
+        else q = (i + t) % n;                                  // shift (full only)
+        ch.push_back(pack(i, q));
+      }
+      chains.push_back(std::move(ch));
+    }
+  }
+  s.num_slots = (int)chains.size();
+  s.slot_off.assign(s.num_slots + 1, 0);
+  for (int p = 0; p < s.num_slots; ++p) {
+    s.slot_off[p + 1] = s.slot_off[p] + (int32_t)chains[p].size();
+    s.max_chain = std::max(s.max_chain, (int)chains[p].size());
+    s.tasks.insert(s.tasks.end(), chains[p].begin(), chains[p].end());
+  }
+
+  // Reduction order per dQ block.
+  s.ord.assign((size_t)n * n, -1);
+  s.cnt.assign(n, 0);
+  if (sched == SCHED_ASCENDING || sched == SCHED_DESCENDING) {
+    for (int j = 0; j < n; ++j) {
+      int k = 0;
+      for (int i = 0; i < n; ++i)
+        if (!causal || j >= i) s.ord[(size_t)i * n + j] = k++;
+      s.cnt[j] = k;
+    }
+  } else {
+    // arrival step; no two chains share (step, q tile) -- checked here
+    std::vector<std::vector<std::pair<int, int>>> arrivals(n);  // (step, kv)
+    for (int p = 0; p < s.num_slots; ++p)
+      for (int t = 0; t < (int)chains[p].size(); ++t) {
+        const int kv = chains[p][t] >> 16, q = chains[p][t] & 0xffff;
+        arrivals[q].push_back({t, kv});
+      }
+    for (int j = 0; j < n; ++j) {
+      auto& a = arrivals[j];
+      std::sort(a.begin(), a.end());
+      for (size_t k = 0; k < a.size(); ++k) {
+        if (k && a[k].first == a[k - 1].first) return 2;        // conflicting step
+        s.ord[(size_t)a[k].second * n + j] = (int32_t)k;
+      }
+      s.cnt[j] = (int)a.size();
+    }
+  }
+  *out = std::move(s);
+  return 0;
+}
+
+bool simulate(const Schedule& sc, int heads, int num_sms, double c, double r,
+              double* makespan, std::vector<double>* sm_end) {
+  const int n = sc.n;
+  const long long units = (long long)heads * sc.num_slots;
+  // who reduces at position k of dQ_j: inv[j * n + k] = kv tile
+  std::vector<int32_t> inv((size_t)n * n, -1);
+  for (int i = 0; i < n; ++i)
+    for (int j = 0; j < n; ++j)
+      if (sc.ord[(size_t)i * n + j] >= 0) inv[(size_t)j * n + sc.ord[(size_t)i * n + j]] = i;
+
+  // per SM: the list of units in dealing order; progress = (unit index, task index)
+  std::vector<std::vector<long long>> sm_units(num_sms);
+  for (long long u = 0; u < units; ++u) sm_units[u % num_sms].push_back(u);
+  std::vector<size_t> unit_pos(num_sms, 0), task_pos(num_sms, 0);
+  std::vector<double> t_sm(num_sms, 0.0);
+  // reduce-end time of (head, kv, q); NaN-free sentinel -1 = not yet done
+  std::vector<double> rend((size_t)heads * n * n, -1.0);
+
+  long long remaining = (long long)heads * (long long)sc.tasks.size();
+  while (remaining > 0) {
+    bool progress = false;
+    for (int sm = 0; sm < num_sms; ++sm) {
+      while (unit_pos[sm] < sm_units[sm].size()) {
+        const long long u = sm_units[sm][unit_pos[sm]];
+        const int head = (int)(u / sc.num_slots), slot = (int)(u % sc.num_slots);
+        const int beg = sc.slot_off[slot], len = sc.slot_off[slot + 1] - beg;
+        const int32_t tk = sc.tasks[beg + task_pos[sm]];
+        const int i = tk >> 16, j = tk & 0xffff;
+        const int o = sc.ord[(size_t)i * n + j];
+        double pred_end = 0.0;
+        if (o > 0) {
+          const int ip = inv[(size_t)j * n + o - 1];
+          pred_end = rend[((size_t)head * n + ip) * n + j];
+          if (pred_end < 0) break;                              // predecessor not done
+        }
+        const double c_end = t_sm[sm] + c;
+        const double r_end = std::max(c_end, pred_end) + r;
+        rend[((size_t)head * n + i) * n + j] = r_end;
+        t_sm[sm] = r_end;
+        --remaining;
+        progress = true;
+        if (++task_pos[sm] == (size_t)len) {
+          task_pos[sm] = 0;
+          ++unit_pos[sm];
+        }
+      }
+    }
+    if (!progress) return false;
+  }
+  double mk = 0.0;
+  for (double t : t_sm) mk = std::max(mk, t);
+  if (makespan) *makespan = mk;
+  if (sm_end) *sm_end = t_sm;
+  return true;
+}
+
+}  // namespace dash

@@ -1,0 +1,34 @@
+// Host-side DASH schedule tables and the compute/reduce DAG simulator.
+//
+// Model: "DASH: Deterministic Attention Scheduling for High-throughput Reproducible LLM
+// Training", Pith review, sections "Core claim" and "What carries the argument"; task
+// orders from the abstract and the Figure 3, 4, 6 and 7 captions.
+#pragma once
+
+#include <cstdint>
+#include <vector>
+
+namespace dash {
+
+enum { MASK_FULL = 0, MASK_CAUSAL = 1 };
+enum { SCHED_ASCENDING = 0, SCHED_DESCENDING = 1, SCHED_SHIFT = 2, SCHED_SYMMETRIC_SHIFT = 3 };
+
+struct Schedule {
+  int mask = 0, sched = 0, n = 0;
+  int num_slots = 0;                 // chains per head
+  int max_chain = 0;                 // longest chain
+  std::vector<int32_t> slot_off;     // num_slots + 1
+  std::vector<int32_t> tasks;        // (kv << 16) | q, execution order per chain
+  std::vector<int32_t> ord;          // n * n; position of KV_i in the dQ_j order, -1 if masked
+  std::vector<int32_t> cnt;          // n; contributors per dQ block
+};
+
+// Returns 0 and fills `out`, or a positive dash_status_t code.
+int build_schedule(int mask, int sched, int n, Schedule* out);
+
+// Event-driven critical path of `heads` heads dealt round robin (head-major) onto
+// `num_sms` SMs. Returns false on a cycle (deadlock). sm_end may be null.
+bool simulate(const Schedule& sc, int heads, int num_sms, double c, double r,
+              double* makespan, std::vector<double>* sm_end);
+
+}  // namespace dash

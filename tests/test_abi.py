@@ -1,0 +1,84 @@
+"""The C ABI library loads, exports every function include/*.h declares, and rejects bad
+arguments synchronously (no GPU needed: nothing reaches the device)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import reproducible_deterministic_attn_gb300 as da
+from tests._lib import ensure_built
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^[A-Za-z_][\w \*]*?\b(dash_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ensure_built()
+    return da.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 11
+    raw = ctypes.CDLL(da.dash_attn.LIB_PATH)
+    for name in names:
+        assert hasattr(raw, name), name
+
+
+def test_status_strings(lib):
+    assert da.dash_status_string(0) == "DASH_OK"
+    assert da.dash_status_string(5) == "DASH_ERR_SYNC_TIMEOUT"
+    assert da.dash_status_string(6) == "DASH_ERR_DEADLOCK_RISK"
+    assert da.dash_status_string(99) == "DASH_ERR_UNKNOWN"
+
+
+def test_workspace_size(lib):
+    B, S, H, D = 2, 256, 3, 64
+    ws = da.dash_attn_bwd_workspace_size(B, S, H, D)
+    need = 256 + B * H * S * 4 + B * H * S * D * 4 + B * H * (S // 128) * 4
+    assert need <= ws <= need + 4 * 256 and ws % 256 == 0
+    assert da.dash_attn_bwd_workspace_size(1, 100, 1, 64) == 0      # S not a multiple of 128
+    assert da.dash_attn_bwd_workspace_size(1, 128, 1, 96) == 0      # unsupported head dim
+
+
+def _bwd(lib, **kw):
+    a = dict(q=16, k=16, v=16, o=16, dO=16, lse=16, dq=16, dk=16, dv=16, ws=256, wsb=1 << 30,
+             B=1, S=256, H=1, D=64, scale=0.125, mask=0, sched=0, det=1)
+    a.update(kw)
+    return lib.dash_attn_bwd(a["q"], a["k"], a["v"], a["o"], a["dO"], a["lse"], a["dq"],
+                             a["dk"], a["dv"], a["ws"], a["wsb"], a["B"], a["S"], a["H"],
+                             a["D"], a["scale"], a["mask"], a["sched"], a["det"], None)
+
+
+def test_bwd_rejects_bad_arguments_without_touching_the_device(lib):
+    assert _bwd(lib, q=None) == da.DASH_ERR_INVALID_ARG
+    assert _bwd(lib, B=0) == da.DASH_ERR_INVALID_ARG
+    assert _bwd(lib, mask=2) == da.DASH_ERR_INVALID_ARG
+    assert _bwd(lib, sched=4) == da.DASH_ERR_INVALID_ARG
+    assert _bwd(lib, det=2) == da.DASH_ERR_INVALID_ARG
+    assert _bwd(lib, scale=0.0) == da.DASH_ERR_INVALID_ARG
+    assert _bwd(lib, D=96) == da.DASH_ERR_UNSUPPORTED
+    assert _bwd(lib, S=200) == da.DASH_ERR_UNSUPPORTED
+    assert _bwd(lib, q=17) == da.DASH_ERR_INVALID_ARG              # misaligned
+    assert _bwd(lib, ws=128) == da.DASH_ERR_INVALID_ARG            # workspace not 256-aligned
+    assert _bwd(lib, wsb=100) == da.DASH_ERR_WORKSPACE_TOO_SMALL
+    assert _bwd(lib, sched=2, mask=1) == da.DASH_ERR_UNSUPPORTED   # shift needs the full mask
+    assert _bwd(lib, sched=3, mask=0) == da.DASH_ERR_UNSUPPORTED   # symmetric shift: causal
+
+
+def test_fwd_rejects_bad_arguments(lib):
+    f = lib.dash_attn_fwd
+    assert f(None, 16, 16, 16, 16, 1, 128, 1, 64, 0.1, 0, None) == da.DASH_ERR_INVALID_ARG
+    assert f(16, 16, 16, 16, 16, 1, 128, 1, 32, 0.1, 0, None) == da.DASH_ERR_UNSUPPORTED
+    assert f(16, 16, 16, 16, 16, 1, 128, 1, 64, 0.1, 7, None) == da.DASH_ERR_INVALID_ARG

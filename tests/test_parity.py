@@ -1,0 +1,77 @@
+"""GPU parity: the CUDA forward/backward against the fp64 oracle, element by element.
+
+Small shapes run every (b, h) slice through the oracle; the full benchmark shapes use
+sampled slices. Tolerance: max |gpu - ref| <= 2e-2 * max |ref| per tensor; LSE 1e-3 abs.
+"""
+import pytest
+import torch
+
+from tests._lib import ensure_built, has_gpu
+from tests.gpu_common import assert_within, check_against_oracle, run_case
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not has_gpu(), reason="needs a CUDA GPU")]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+SMALL = [
+    # (B, S, H, D): single tile, several tiles, odd tile counts and head counts
+    (1, 128, 1, 64),
+    (1, 256, 1, 64),
+    (2, 384, 3, 64),
+    (1, 640, 2, 128),
+    (3, 256, 1, 128),
+]
+
+PAIRS = [("full", "ascending"), ("full", "descending"), ("full", "shift"),
+         ("causal", "ascending"), ("causal", "descending"), ("causal", "symmetric_shift")]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("mask,sched", PAIRS, ids=lambda x: x)
+@pytest.mark.parametrize("det", [1, 0])
+def test_small_shapes(shape, mask, sched, det):
+    B, S, H, D = shape
+    n = S // 128
+    if sched == "symmetric_shift" and n % 2:
+        pytest.skip("symmetric shift needs an even tile count")
+    causal = mask == "causal"
+    res = run_case(B, S, H, D, causal, sched, det, seed=1)
+    assert_within(check_against_oracle(res, causal))
+
+
+def test_config1_full_256_d64():
+    res = run_case(1, 256, 1, 64, False, "shift", 1)
+    assert_within(check_against_oracle(res, False))
+
+
+@pytest.mark.parametrize("sched", ["ascending", "descending", "symmetric_shift"])
+def test_config2_causal_4x2048x16x64(sched):
+    res = run_case(4, 2048, 16, 64, True, sched, 1)
+    assert_within(check_against_oracle(res, True, heads=[(0, 0), (1, 7), (3, 15)]))
+
+
+@pytest.mark.parametrize("sched,det", [("ascending", 1), ("shift", 1), ("ascending", 0)])
+def test_config3_full_2x8192x16x128_sampled(sched, det):
+    res = run_case(2, 8192, 16, 128, False, sched, det)
+    assert_within(check_against_oracle(res, False, heads=[(0, 3), (1, 15)]))
+    del res
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("sched", ["descending", "symmetric_shift"])
+def test_config4_causal_1x16384x32x128_sampled(sched):
+    res = run_case(1, 16384, 32, 128, True, sched, 1)
+    assert_within(check_against_oracle(res, True, heads=[(0, 31)]))
+    del res
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("S,D", [(1024, 64), (4096, 128)])
+def test_config5_token_sweep_sampled(S, D):
+    res = run_case(16384 // S, S, 32, D, True, "symmetric_shift", 1)
+    assert_within(check_against_oracle(res, True, heads=[(0, 0), (16384 // S - 1, 31)]))

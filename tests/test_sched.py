@@ -1,0 +1,77 @@
+"""The library's schedule tables and DAG simulator (host C++) against the oracle."""
+import itertools
+import random
+
+import pytest
+
+import reproducible_deterministic_attn_gb300 as da
+from oracle import dag
+from tests._lib import ensure_built
+
+NAMES = {0: "ascending", 1: "descending", 2: "shift", 3: "symmetric_shift"}
+MASKS = {0: "full", 1: "causal"}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+def _valid(mask, sched, n):
+    if sched == 2 and mask != 0:
+        return False
+    if sched == 3 and (mask != 1 or n % 2):
+        return False
+    return True
+
+
+@pytest.mark.parametrize("mask,sched", list(itertools.product([0, 1], [0, 1, 2, 3])))
+def test_tables_match_oracle(mask, sched):
+    for n in list(range(1, 17)) + [64, 128]:
+        if not _valid(mask, sched, n):
+            assert da.dash_sched_num_slots(mask, sched, n) == -da.DASH_ERR_UNSUPPORTED
+            continue
+        off, tasks, ords = da.dash_sched_table(mask, sched, n)
+        chains = dag.chains(MASKS[mask], NAMES[sched], n)
+        assert len(off) == len(chains) + 1
+        got = [tasks[off[p]:off[p + 1]] for p in range(len(chains))]
+        assert got == [list(c) for c in chains]
+        order = dag.reduction_order(MASKS[mask], NAMES[sched], n)
+        for j in range(n):
+            for pos, i in enumerate(order[j]):
+                assert ords[i][j] == pos
+        masked = sum(1 for i in range(n) for j in range(n) if ords[i][j] < 0)
+        assert masked == (0 if mask == 0 else n * (n - 1) // 2)
+
+
+def test_invalid_n():
+    assert da.dash_sched_num_slots(0, 0, 0) == -da.DASH_ERR_INVALID_ARG
+    assert da.dash_sched_num_slots(0, 0, 40000) == -da.DASH_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_simulator_matches_oracle(seed):
+    rng = random.Random(seed)
+    for _ in range(25):
+        mask, sched = rng.choice([(0, 0), (0, 1), (0, 2), (1, 0), (1, 1), (1, 3)])
+        n = rng.choice([1, 2, 3, 4, 6, 8, 10]) if sched != 3 else rng.choice([2, 4, 6, 8])
+        m = rng.randint(1, 5)
+        sms = rng.randint(1, 2 * n + 2)
+        c, r = rng.choice([(3.0, 1.0), (1.0, 0.25), (2.0, 2.0), (0.5, 1.5)])
+        want = dag.simulate(MASKS[mask], NAMES[sched], n, m, sms, c, r)
+        mk, ends = da.dash_sched_simulate(mask, sched, n, m, sms, c, r)
+        if want["makespan"] is None:
+            assert mk is None, (mask, sched, n, m, sms)
+        else:
+            assert mk == pytest.approx(want["makespan"], abs=1e-9), (mask, sched, n, m, sms)
+            assert ends == pytest.approx(want["sm_end"], abs=1e-9)
+
+
+def test_simulator_closed_forms_large_n():
+    # the pages' full-mask bound (shift) and the symmetric-shift form at the kernel's sizes
+    for n in (64, 128):
+        for m in (1, 2, 4):
+            mk, _ = da.dash_sched_simulate(0, 2, n, m, n, 3.0, 1.0)
+            assert mk == m * n * 4.0
+            mk, _ = da.dash_sched_simulate(1, 3, n, m, n, 3.0, 1.0)
+            assert mk == ((m + 1) // 2) * (n + 1) * 4.0
