@@ -43,6 +43,8 @@ WORKLOADS = {
     "causal-4x2048x16x64": dict(mask="causal", B=4, S=2048, H=16, D=64),
     "full-2x8192x16x128": dict(mask="full", B=2, S=8192, H=16, D=128),
     "causal-1x16384x32x128": dict(mask="causal", B=1, S=16384, H=32, D=128),
+    # smaller full-mask case for kernel profiles (inputs still larger than L2)
+    "full-2x4096x16x128": dict(mask="full", B=2, S=4096, H=16, D=128),
 }
 DEFAULT_WORKLOAD = "full-2x8192x16x128"
 BEST_DASH = {"full": "shift", "causal": "symmetric_shift"}

@@ -44,7 +44,8 @@ struct BwdParams {
   int* ws_header;            // status words
   float* Dsum;               // [B, H, S] rowsum(dO * O)
   float* dq_acc;             // [B, H, S, D] fp32
-  int* sems;                 // [B, H, n]
+  int* sems;                 // [B, H, S / 64]: one per 64-row dQ sub-block
+  int num_sems;
   const int32_t* slot_off;   // schedule: chain offsets
   const int32_t* tasks;      // schedule: (kv << 16) | q
   const int32_t* ord;        // schedule: n * n ordinals

@@ -2,6 +2,7 @@
 // deadlock check of the persistent grid, and the kernel launches.
 #include "../../include/dash_attn.h"
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -13,7 +14,9 @@
 #include <vector>
 
 #include "common.cuh"
-#include "kernels_simt.cuh"
+#include "bwd_aux.cuh"
+#include "fwd_simt.cuh"
+#include "kernels_tc.cuh"
 #include "sched.h"
 
 namespace {
@@ -124,6 +127,51 @@ cudaEvent_t prof_event(bool stop) {
   return e;
 }
 
+// cuTensorMapEncodeTiled from the driver, fetched through the runtime (no -lcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)f;
+  });
+  return fn;
+}
+
+// 3D view [B*S][H][D] of a BSHD bf16 tensor; box = 64 columns x 1 head x `rows` rows,
+// 128-byte swizzle (the layout the tensor-core descriptors expect).
+bool map_bshd(CUtensorMap* m, const void* ptr, int B, int S, int H, int D, int rows) {
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)B * S};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+  const cuuint32_t box[3] = {64, 1, (cuuint32_t)rows};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return encoder()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2D view [B*H*S][D] of the fp32 dQ accumulator; box = 32 columns x `rows` rows.
+bool map_acc(CUtensorMap* m, float* ptr, long long rows_total, int D, int rows) {
+  const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows_total};
+  const cuuint64_t strides[1] = {(cuuint64_t)D * 4};
+  const cuuint32_t box[2] = {32, (cuuint32_t)rows};
+  const cuuint32_t es[2] = {1, 1};
+  return encoder()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 struct WsLayout {
   size_t dsum, dq_acc, sems, total;
 };
@@ -134,7 +182,7 @@ WsLayout ws_layout(int B, int S, int H, int D) {
   w.dsum = dash::kWsHeaderBytes;
   w.dq_acc = round_up(w.dsum + rows * sizeof(float), 256);
   w.sems = round_up(w.dq_acc + rows * D * sizeof(float), 256);
-  w.total = round_up(w.sems + (size_t)B * H * (S / dash::kTile) * sizeof(int), 256);
+  w.total = round_up(w.sems + (size_t)B * H * (S / 64) * sizeof(int), 256);
   return w;
 }
 
@@ -275,13 +323,26 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
   p.timeout_ns = g_timeout_ns;
   p.ordinal_skew = g_ordinal_skew;
 
-  // Persistent grid: every CTA must be resident at once (the ordered reduction waits on
-  // other CTAs), so the grid is the occupancy limit and the launch is cooperative.
-  const int threads = 512;
-  const size_t smem = (size_t)2 * dash::kTile * D * 2 + (size_t)2 * 32 * D * 2 +
-                      (size_t)2 * 32 * (dash::kTile + 1) * 4 + (size_t)dash::kTile * D * 4 +
-                      2 * 32 * 4;
-  void* kfn = D == 64 ? (void*)dash::bwd_simt_kernel<64> : (void*)dash::bwd_simt_kernel<128>;
+  p.num_sems = B * H * (S / 64);
+
+  // Persistent grid, one CTA per SM: every CTA must be resident at once (the ordered
+  // reduction waits on other CTAs), so the launch is cooperative.
+  if (!encoder()) {
+    g_last_error = "cuTensorMapEncodeTiled is not available from the driver";
+    return DASH_ERR_CUDA;
+  }
+  dash::tc::TmaMaps maps;
+  const int br = D == 64 ? dash::tc::Cfg<64>::BR : dash::tc::Cfg<128>::BR;
+  if (!map_bshd(&maps.q, q, B, S, H, D, br) || !map_bshd(&maps.dO, dO, B, S, H, D, br) ||
+      !map_bshd(&maps.k, k, B, S, H, D, dash::kTile) ||
+      !map_bshd(&maps.v, v, B, S, H, D, dash::kTile) ||
+      !map_acc(&maps.acc, p.dq_acc, (long long)B * H * S, D, br)) {
+    g_last_error = "cuTensorMapEncodeTiled rejected a tensor";
+    return DASH_ERR_CUDA;
+  }
+  const int threads = dash::tc::kThreads;
+  const size_t smem = D == 64 ? dash::tc::Smem<64>::ALLOC : dash::tc::Smem<128>::ALLOC;
+  void* kfn = D == 64 ? (void*)dash::tc::bwd_tc_kernel<64> : (void*)dash::tc::bwd_tc_kernel<128>;
   DASH_CUDA(cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   int per_sm = 0, sms = 0;
   DASH_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, threads, smem));
@@ -290,14 +351,14 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
     g_last_error = "backward kernel does not fit on one SM";
     return DASH_ERR_CUDA;
   }
-  int grid = per_sm * sms;
+  int grid = sms;                      // one CTA per SM (512 TMEM columns each)
   if (grid > p.num_units) grid = p.num_units;
   if (deterministic && !deadlock_free(mask, schedule, n, B * H, grid))
     return DASH_ERR_DEADLOCK_RISK;
 
   dash::bwd_preprocess_kernel<<<sms * 4, 256, 0, stream>>>(p);
   DASH_CUDA(cudaGetLastError());
-  void* args[] = {&p};
+  void* args[] = {&p, &maps};
   cudaEvent_t ev0 = prof_event(false);
   if (ev0) DASH_CUDA(cudaEventRecord(ev0, stream));
   if (deterministic) {
@@ -306,10 +367,8 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
     DASH_CUDA(cudaLaunchKernel(kfn, dim3(grid), dim3(threads), args, smem, stream));
   }
   if (ev0) DASH_CUDA(cudaEventRecord(prof_event(true), stream));
-  if (!deterministic) {
-    dash::dq_convert_kernel<<<sms * 4, 256, 0, stream>>>(p);
-    DASH_CUDA(cudaGetLastError());
-  }
+  dash::dq_convert_kernel<<<sms * 4, 256, 0, stream>>>(p);
+  DASH_CUDA(cudaGetLastError());
   return DASH_OK;
 }
 
