@@ -139,6 +139,16 @@ void dash_attn_shutdown(void);
 void dash_debug_set_sync(long long timeout_ns, int ordinal_skew);
 
 /*
+ * Tracing hook. When device_counters is not NULL, later dash_attn_bwd main kernels add,
+ * per CTA, the clock cycles spent in each of their waits into
+ * device_counters[cta * 24 + site] (uint64; the sites are listed in the library's
+ * sources: producer, MMA, softmax-gradient and dQ waits, the dQ semaphore wait, the
+ * reduce, and the CTA's total cycles at index 19). The buffer must hold 24 counters per
+ * SM of the device, zeroed by the caller. NULL turns tracing off.
+ */
+void dash_debug_set_trace(void* device_counters);
+
+/*
  * Profiling hook. With on != 0, every later dash_attn_bwd records a pair of CUDA events
  * on its stream, immediately before and after its main (compute + dQ reduction) kernel,
  * up to 1024 pairs. dash_profile_read waits for the recorded events, writes the summed

@@ -27,6 +27,7 @@ thread_local std::string g_last_error;
 // every awaited ordinal (a skew > 0 makes every wait time out).
 long long g_timeout_ns = 10ll * 1000 * 1000 * 1000;
 int g_ordinal_skew = 0;
+unsigned long long* g_trace = nullptr;   // dash_debug_set_trace
 
 dash_status_t cuda_fail(cudaError_t e, const char* what) {
   g_last_error = std::string(what) + ": " + cudaGetErrorString(e);
@@ -322,6 +323,7 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
   p.deterministic = deterministic;
   p.timeout_ns = g_timeout_ns;
   p.ordinal_skew = g_ordinal_skew;
+  p.trace = g_trace;
 
   p.num_sems = B * H * (S / 64);
 
@@ -386,6 +388,10 @@ dash_status_t dash_attn_get_status(const void* workspace, cudaStream_t stream) {
     return DASH_ERR_SYNC_TIMEOUT;
   }
   return DASH_OK;
+}
+
+void dash_debug_set_trace(void* device_counters) {
+  g_trace = (unsigned long long*)device_counters;
 }
 
 dash_status_t dash_profile_enable(int on) {

@@ -71,7 +71,8 @@ struct Smem {
   static constexpr int STG_OFF = DS_OFF + PT_BYTES;          // dQ staging (fp32)
   static constexpr int STG_BYTES = BR * D * 4;
   static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
-  static constexpr int TOTAL = BAR_OFF + 256;                // barriers + flags
+  static constexpr int TRACE_OFF = BAR_OFF + 256;
+  static constexpr int TOTAL = TRACE_OFF + 8 * TR_SITES;     // barriers, flags, trace
   static constexpr int ALLOC = TOTAL + 1024;                 // slack for 1024 alignment
 };
 
@@ -120,6 +121,47 @@ struct Walk {
   }
 };
 
+// Optional wait-cycle trace: one writer per site, counters in shared memory, copied to
+// p.trace[cta * TR_SITES + site] at exit.
+struct Trace {
+  unsigned long long* c;   // shared counters, null when tracing is off
+  __device__ __forceinline__ long long t0() const { return c ? clock64() : 0; }
+  __device__ __forceinline__ void add(int site, long long start) const {
+    if (c) c[site] += (unsigned long long)(clock64() - start);
+  }
+};
+
+// One step of the flat sub-tile sequence (SUB sub-tiles per schedule task).
+struct Sub {
+  int i, j, hs, it, tile;
+  bool first, last;   // first / last sub-tile of its KV tile
+};
+
+template <int SUB>
+struct SubWalk {
+  Walk w;
+  int hs = SUB - 1, it = -1, tile = -1;
+  __device__ SubWalk(const BwdParams& p) : w(p) {}
+  __device__ bool next(Sub& s) {
+    if (hs + 1 < SUB) {
+      ++hs;
+    } else {
+      if (!w.next()) return false;
+      hs = 0;
+      if (w.first_of_tile) ++tile;
+    }
+    ++it;
+    s.i = w.i;
+    s.j = w.j;
+    s.hs = hs;
+    s.it = it;
+    s.tile = tile;
+    s.first = w.first_of_tile && hs == 0;
+    s.last = w.last_of_tile && hs == SUB - 1;
+    return true;
+  }
+};
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ TmaMaps maps) {
@@ -157,54 +199,61 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
+  unsigned long long* trace_s = (unsigned long long*)(sm + L::TRACE_OFF);
+  if (threadIdx.x < TR_SITES) trace_s[threadIdx.x] = 0;
+  const long long t_start = clock64();
   if (warp == 1) ptx::tmem_alloc(tmem_slot, kTmemCols);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const size_t rs = (size_t)p.H * D;   // BSHD row stride (elements)
+  const Trace tr{p.trace ? trace_s : nullptr};
+  const Trace tr_none{nullptr};
 
   if (warp == 0) {
     // ===================================== TMA producer =====================================
     if (lane == 0) {
-      Walk w(p);
+      SubWalk<SUB> sw(p);
+      Sub x;
       int it = 0, tl = 0;
-      while (w.next()) {
-        const int b = w.bh / p.H, h = w.bh % p.H;
-        if (w.first_of_tile) {
+      while (sw.next(x)) {
+        const int bh = sw.w.bh, b = bh / p.H, h = bh % p.H;
+        const int s = it % kStages;
+        const int q0 = x.j * kTile + x.hs * BR;
+        // Q, dO, LSE and Dsum of this sub-tile into stage s
+        long long t0 = tr.t0();
+        if (it >= kStages &&
+            !ptx::mbar_wait(bars + B_STAGE_EMPTY + s, ((it / kStages) - 1) & 1, abort_flag, tmo))
+          break;
+        tr.add(TR_PROD_STAGE_EMPTY, t0);
+        uint8_t* st = sm + L::STAGE_OFF + s * L::STAGE_BYTES;
+        ptx::mbar_expect_tx(bars + B_STAGE_FULL + s, 2 * L::QT_BYTES + 2 * BR * 4);
+        for (int cb = 0; cb < D / 64; ++cb) {
+          ptx::tma_load_3d(st + L::Q_IN_STAGE + cb * BR * 128, &maps.q, cb * 64, h, b * p.S + q0,
+                           bars + B_STAGE_FULL + s);
+          ptx::tma_load_3d(st + L::DO_IN_STAGE + cb * BR * 128, &maps.dO, cb * 64, h, b * p.S + q0,
+                           bars + B_STAGE_FULL + s);
+        }
+        ptx::bulk_load(st + L::LSE_IN_STAGE, p.lse + (size_t)bh * p.S + q0, BR * 4,
+                       bars + B_STAGE_FULL + s);
+        ptx::bulk_load(st + L::DSUM_IN_STAGE, p.Dsum + (size_t)bh * p.S + q0, BR * 4,
+                       bars + B_STAGE_FULL + s);
+        ++it;
+        // a new KV tile: K and V once the previous tile's MMAs are done with the buffer
+        if (x.first) {
+          t0 = tr.t0();
           if (tl > 0 && !ptx::mbar_wait(bars + B_KV_EMPTY, (tl - 1) & 1, abort_flag, tmo)) break;
+          tr.add(TR_PROD_KV_EMPTY, t0);
           ptx::mbar_expect_tx(bars + B_KV_FULL, 2 * L::KV_BYTES);
           for (int cb = 0; cb < D / 64; ++cb) {
             ptx::tma_load_3d(sm + L::K_OFF + cb * kTile * 128, &maps.k, cb * 64, h,
-                             b * p.S + w.i * kTile, bars + B_KV_FULL);
+                             b * p.S + x.i * kTile, bars + B_KV_FULL);
             ptx::tma_load_3d(sm + L::V_OFF + cb * kTile * 128, &maps.v, cb * 64, h,
-                             b * p.S + w.i * kTile, bars + B_KV_FULL);
+                             b * p.S + x.i * kTile, bars + B_KV_FULL);
           }
           ++tl;
         }
-        bool ok = true;
-        for (int hs = 0; hs < SUB; ++hs, ++it) {
-          const int s = it % kStages;
-          const int q0 = w.j * kTile + hs * BR;
-          if (it >= kStages &&
-              !ptx::mbar_wait(bars + B_STAGE_EMPTY + s, ((it / kStages) - 1) & 1, abort_flag, tmo)) {
-            ok = false;
-            break;
-          }
-          uint8_t* st = sm + L::STAGE_OFF + s * L::STAGE_BYTES;
-          ptx::mbar_expect_tx(bars + B_STAGE_FULL + s, 2 * L::QT_BYTES + 2 * BR * 4);
-          for (int cb = 0; cb < D / 64; ++cb) {
-            ptx::tma_load_3d(st + L::Q_IN_STAGE + cb * BR * 128, &maps.q, cb * 64, h, b * p.S + q0,
-                             bars + B_STAGE_FULL + s);
-            ptx::tma_load_3d(st + L::DO_IN_STAGE + cb * BR * 128, &maps.dO, cb * 64, h,
-                             b * p.S + q0, bars + B_STAGE_FULL + s);
-          }
-          ptx::bulk_load(st + L::LSE_IN_STAGE, p.lse + (size_t)w.bh * p.S + q0, BR * 4,
-                         bars + B_STAGE_FULL + s);
-          ptx::bulk_load(st + L::DSUM_IN_STAGE, p.Dsum + (size_t)w.bh * p.S + q0, BR * 4,
-                         bars + B_STAGE_FULL + s);
-        }
-        if (!ok) break;
       }
       // drain: every issued load has landed before the CTA may exit
       for (int k = (it > kStages ? it - kStages : 0); k < it; ++k)
@@ -213,94 +262,133 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ===================================== MMA issuer =======================================
+    // Software-pipelined issue order per sub-tile t:
+    //   dV(t), S(t+1), dK(t), dQ(t), dP(t+1)
+    // so the softmax-gradient warps compute P(t+1) while dK(t)/dQ(t) run. At a KV-tile
+    // boundary S(t+1) waits for the new K/V tile instead.
     if (lane == 0) {
       const uint32_t sK = ptx::smem_u32(sm + L::K_OFF), sV = ptx::smem_u32(sm + L::V_OFF);
       const uint32_t sP = ptx::smem_u32(sm + L::P_OFF), sdS = ptx::smem_u32(sm + L::DS_OFF);
       constexpr uint32_t ID_S = ptx::idesc_bf16(128, BR, 0, 0);     // S^T, dP^T
       constexpr uint32_t ID_ACC = ptx::idesc_bf16(128, D, 0, 1);    // dV, dK
       constexpr uint32_t ID_DQ = ptx::idesc_bf16(128, 64, 1, 1);    // dQ (D=64) / dQ^T (D=128)
-      Walk w(p);
-      int it = 0, tl = 0;
+      auto stage_addr = [&](const Sub& x) {
+        return ptx::smem_u32(sm + L::STAGE_OFF + (x.it % kStages) * L::STAGE_BYTES);
+      };
+      auto issue_S = [&](const Sub& x) -> bool {
+        long long t0 = tr.t0();
+        if (x.first && !ptx::mbar_wait(bars + B_KV_FULL, x.tile & 1, abort_flag, tmo)) return false;
+        tr.add(TR_MMA_KV_FULL, t0);
+        t0 = tr.t0();
+        if (!ptx::mbar_wait(bars + B_STAGE_FULL + x.it % kStages, (x.it / kStages) & 1, abort_flag,
+                            tmo))
+          return false;
+        tr.add(TR_MMA_STAGE_FULL, t0);
+        t0 = tr.t0();
+        if (x.it > 0 && !ptx::mbar_wait(bars + B_S_EMPTY, (x.it - 1) & 1, abort_flag, tmo))
+          return false;
+        tr.add(TR_MMA_S_EMPTY, t0);
+        ptx::tc_fence_after();
+        const uint32_t sQ = stage_addr(x) + L::Q_IN_STAGE;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t ao = (ks / 4) * (kTile * 128) + (ks % 4) * 32;
+          const uint32_t bo = (ks / 4) * (BR * 128) + (ks % 4) * 32;
+          ptx::mma_bf16(tmem + C::T_S, ptx::sdesc(sK + ao, 16, 1024), ptx::sdesc(sQ + bo, 16, 1024),
+                        ID_S, ks > 0);
+        }
+        ptx::mma_commit(bars + B_S_FULL);
+        return true;
+      };
+      auto issue_dP = [&](const Sub& x) -> bool {
+        const long long t0 = tr.t0();
+        if (x.it > 0 && !ptx::mbar_wait(bars + B_DP_EMPTY, (x.it - 1) & 1, abort_flag, tmo))
+          return false;
+        tr.add(TR_MMA_DP_EMPTY, t0);
+        ptx::tc_fence_after();
+        const uint32_t sdO = stage_addr(x) + L::DO_IN_STAGE;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t ao = (ks / 4) * (kTile * 128) + (ks % 4) * 32;
+          const uint32_t bo = (ks / 4) * (BR * 128) + (ks % 4) * 32;
+          ptx::mma_bf16(tmem + C::T_DP, ptx::sdesc(sV + ao, 16, 1024),
+                        ptx::sdesc(sdO + bo, 16, 1024), ID_S, ks > 0);
+        }
+        ptx::mma_commit(bars + B_DP_FULL);
+        return true;
+      };
+      SubWalk<SUB> sw(p);
+      Sub cur, nxt;
+      bool have = sw.next(cur);
       bool ok = true;
-      while (ok && w.next()) {
-        if (w.first_of_tile) {
-          ok = ptx::mbar_wait(bars + B_KV_FULL, tl & 1, abort_flag, tmo);
-          if (ok && tl > 0) ok = ptx::mbar_wait(bars + B_ACC_EMPTY, (tl - 1) & 1, abort_flag, tmo);
-          if (!ok) break;
+      if (have) ok = issue_S(cur) && issue_dP(cur);
+      while (ok && have) {
+        const bool have_n = sw.next(nxt);
+        const bool same_tile = have_n && !nxt.first;
+        const uint32_t st = stage_addr(cur);
+        const uint32_t sQ = st + L::Q_IN_STAGE, sdO = st + L::DO_IN_STAGE;
+        // dV += P^T dO: A = P^T (K-major, 128 kv rows x BR), B = dO (MN-major over D).
+        // The first sub-tile of a KV tile overwrites the accumulators, which the previous
+        // tile's epilogue must have read out.
+        long long t0 = tr.t0();
+        ok = ptx::mbar_wait(bars + B_P_FULL, cur.it & 1, abort_flag, tmo);
+        tr.add(TR_MMA_P_FULL, t0);
+        t0 = tr.t0();
+        if (ok && cur.first && cur.tile > 0)
+          ok = ptx::mbar_wait(bars + B_ACC_EMPTY, (cur.tile - 1) & 1, abort_flag, tmo);
+        tr.add(TR_MMA_ACC_EMPTY, t0);
+        if (!ok) break;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < BR / 16; ++ks) {
+          const uint32_t ao = (ks / 4) * (kTile * 128) + (ks % 4) * 32;
+          ptx::mma_bf16(tmem + C::T_DV, ptx::sdesc(sP + ao, 16, 1024),
+                        ptx::sdesc(sdO + ks * 2048, BR * 128, 1024), ID_ACC,
+                        !(cur.first && ks == 0));
         }
-        for (int hs = 0; hs < SUB && ok; ++hs, ++it) {
-          const int s = it % kStages;
-          const uint32_t st = ptx::smem_u32(sm + L::STAGE_OFF + s * L::STAGE_BYTES);
-          const uint32_t sQ = st + L::Q_IN_STAGE, sdO = st + L::DO_IN_STAGE;
-          ok = ptx::mbar_wait(bars + B_STAGE_FULL + s, (it / kStages) & 1, abort_flag, tmo);
-          if (ok && it > 0) ok = ptx::mbar_wait(bars + B_S_EMPTY, (it - 1) & 1, abort_flag, tmo);
-          if (!ok) break;
-          ptx::tc_fence_after();
-          // S^T = K Q^T and dP^T = V dO^T: K-major A (128 kv rows), K-major B (BR rows)
+        ptx::mma_commit(bars + B_P_EMPTY);
+        if (same_tile && !(ok = issue_S(nxt))) break;
+        // dK += dS^T Q, then the dQ partial over the 128 kv rows
+        t0 = tr.t0();
+        ok = ptx::mbar_wait(bars + B_DS_FULL, cur.it & 1, abort_flag, tmo);
+        tr.add(TR_MMA_DS_FULL, t0);
+        t0 = tr.t0();
+        if (ok && cur.it > 0) ok = ptx::mbar_wait(bars + B_DQ_EMPTY, (cur.it - 1) & 1, abort_flag, tmo);
+        tr.add(TR_MMA_DQ_EMPTY, t0);
+        if (!ok) break;
+        ptx::tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t ao = (ks / 4) * (kTile * 128) + (ks % 4) * 32;
-            const uint32_t bo = (ks / 4) * (BR * 128) + (ks % 4) * 32;
-            ptx::mma_bf16(tmem + C::T_S, ptx::sdesc(sK + ao, 16, 1024),
-                          ptx::sdesc(sQ + bo, 16, 1024), ID_S, ks > 0);
-          }
-          ptx::mma_commit(bars + B_S_FULL);
-          if (it > 0) ok = ptx::mbar_wait(bars + B_DP_EMPTY, (it - 1) & 1, abort_flag, tmo);
-          if (!ok) break;
-          ptx::tc_fence_after();
+        for (int ks = 0; ks < BR / 16; ++ks) {
+          const uint32_t ao = (ks / 4) * (kTile * 128) + (ks % 4) * 32;
+          ptx::mma_bf16(tmem + C::T_DK, ptx::sdesc(sdS + ao, 16, 1024),
+                        ptx::sdesc(sQ + ks * 2048, BR * 128, 1024), ID_ACC,
+                        !(cur.first && ks == 0));
+        }
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t ao = (ks / 4) * (kTile * 128) + (ks % 4) * 32;
-            const uint32_t bo = (ks / 4) * (BR * 128) + (ks % 4) * 32;
-            ptx::mma_bf16(tmem + C::T_DP, ptx::sdesc(sV + ao, 16, 1024),
-                          ptx::sdesc(sdO + bo, 16, 1024), ID_S, ks > 0);
-          }
-          ptx::mma_commit(bars + B_DP_FULL);
-          // dV += P^T dO: A = P^T (K-major, 128 kv rows x BR), B = dO (MN-major over D)
-          const bool first = w.first_of_tile && hs == 0;
-          ok = ptx::mbar_wait(bars + B_P_FULL, it & 1, abort_flag, tmo);
-          if (!ok) break;
-          ptx::tc_fence_after();
-#pragma unroll
-          for (int ks = 0; ks < BR / 16; ++ks) {
-            const uint32_t ao = (ks / 4) * (kTile * 128) + (ks % 4) * 32;
-            ptx::mma_bf16(tmem + C::T_DV, ptx::sdesc(sP + ao, 16, 1024),
-                          ptx::sdesc(sdO + ks * 2048, BR * 128, 1024), ID_ACC, !(first && ks == 0));
-          }
-          ptx::mma_commit(bars + B_P_EMPTY);
-          // dK += dS^T Q
-          ok = ptx::mbar_wait(bars + B_DS_FULL, it & 1, abort_flag, tmo);
-          if (ok && it > 0) ok = ptx::mbar_wait(bars + B_DQ_EMPTY, (it - 1) & 1, abort_flag, tmo);
-          if (!ok) break;
-          ptx::tc_fence_after();
-#pragma unroll
-          for (int ks = 0; ks < BR / 16; ++ks) {
-            const uint32_t ao = (ks / 4) * (kTile * 128) + (ks % 4) * 32;
-            ptx::mma_bf16(tmem + C::T_DK, ptx::sdesc(sdS + ao, 16, 1024),
-                          ptx::sdesc(sQ + ks * 2048, BR * 128, 1024), ID_ACC, !(first && ks == 0));
-          }
-          // dQ partial over the 128 kv rows (K = 128 in steps of 16 kv rows)
-#pragma unroll
-          for (int ks = 0; ks < kTile / 16; ++ks) {
-            if (D == 64) {
-              // dQ = dS K: A = dS (MN-major view of the dS^T tile), B = K (MN-major, 64 d)
-              ptx::mma_bf16(tmem + C::T_DQ, ptx::sdesc(sdS + ks * 2048, kTile * 128, 1024),
-                            ptx::sdesc(sK + ks * 2048, kTile * 128, 1024), ID_DQ, ks > 0);
-            } else {
-              // dQ^T = K^T dS^T: A = K^T (MN-major over 128 d), B = dS^T (MN-major, 64 q)
-              ptx::mma_bf16(tmem + C::T_DQ, ptx::sdesc(sK + ks * 2048, kTile * 128, 1024),
-                            ptx::sdesc(sdS + ks * 2048, kTile * 128, 1024), ID_DQ, ks > 0);
-            }
-          }
-          ptx::mma_commit(bars + B_DS_EMPTY);
-          ptx::mma_commit(bars + B_DQ_FULL);
-          ptx::mma_commit(bars + B_STAGE_EMPTY + s);
-          if (w.last_of_tile && hs == SUB - 1) {
-            ptx::mma_commit(bars + B_ACC_FULL);
-            ptx::mma_commit(bars + B_KV_EMPTY);
-            ++tl;
+        for (int ks = 0; ks < kTile / 16; ++ks) {
+          if (D == 64) {
+            // dQ = dS K: A = dS (MN-major view of the dS^T tile), B = K (MN-major, 64 d)
+            ptx::mma_bf16(tmem + C::T_DQ, ptx::sdesc(sdS + ks * 2048, kTile * 128, 1024),
+                          ptx::sdesc(sK + ks * 2048, kTile * 128, 1024), ID_DQ, ks > 0);
+          } else {
+            // dQ^T = K^T dS^T: A = K^T (MN-major over 128 d), B = dS^T (MN-major, 64 q)
+            ptx::mma_bf16(tmem + C::T_DQ, ptx::sdesc(sK + ks * 2048, kTile * 128, 1024),
+                          ptx::sdesc(sdS + ks * 2048, kTile * 128, 1024), ID_DQ, ks > 0);
           }
         }
+        ptx::mma_commit(bars + B_DS_EMPTY);
+        ptx::mma_commit(bars + B_DQ_FULL);
+        ptx::mma_commit(bars + B_STAGE_EMPTY + cur.it % kStages);
+        if (cur.last) {
+          ptx::mma_commit(bars + B_ACC_FULL);
+          ptx::mma_commit(bars + B_KV_EMPTY);
+        }
+        if (have_n) {
+          if (!same_tile && !(ok = issue_S(nxt))) break;
+          if (!(ok = issue_dP(nxt))) break;
+        }
+        cur = nxt;
+        have = have_n;
       }
       // drain: no MMA may be in flight when TMEM is released
       ptx::mma_commit(bars + B_DRAIN);
@@ -314,6 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int col0 = half * NC;
     const uint32_t lane_addr = ((uint32_t)(quarter * 32) << 16);
     const uint32_t sP = ptx::smem_u32(sm + L::P_OFF), sdS = ptx::smem_u32(sm + L::DS_OFF);
+    const Trace& trs = (warp == 4 && lane == 0) ? tr : tr_none;
     Walk w(p);
     int it = 0;
     bool ok = true;
@@ -325,8 +414,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* dsum_s = (const float*)(sm + L::STAGE_OFF + s * L::STAGE_BYTES + L::DSUM_IN_STAGE);
         const bool diag = p.causal && (w.i == w.j);
         const int kv_g = w.i * kTile + r;
+        long long t0 = trs.t0();
         ok = ptx::warp_wait(bars + B_STAGE_FULL + s, (it / kStages) & 1, abort_flag, tmo);
         if (ok) ok = ptx::warp_wait(bars + B_S_FULL, it & 1, abort_flag, tmo);
+        trs.add(TR_SG_S_FULL, t0);
         if (!ok) break;
         ptx::tc_fence_after();
         float pv[NC];
@@ -346,7 +437,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float e = ptx::ex2(fmaf(pv[c], p.scale_log2, -lse_s[qc] * kLog2e));
           pv[c] = (diag && kv_g > q0 + qc) ? 0.f : e;
         }
+        t0 = trs.t0();
         if (it > 0) ok = ptx::warp_wait(bars + B_P_EMPTY, (it - 1) & 1, abort_flag, tmo);
+        trs.add(TR_SG_P_EMPTY, t0);
         if (!ok) break;
 #pragma unroll
         for (int k = 0; k < NC / 8; ++k) {
@@ -359,7 +452,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bars + B_P_FULL);
+        t0 = trs.t0();
         ok = ptx::warp_wait(bars + B_DP_FULL, it & 1, abort_flag, tmo);
+        trs.add(TR_SG_DP_FULL, t0);
         if (!ok) break;
         ptx::tc_fence_after();
 #pragma unroll
@@ -372,7 +467,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bars + B_DP_EMPTY);
+        t0 = trs.t0();
         if (it > 0) ok = ptx::warp_wait(bars + B_DS_EMPTY, (it - 1) & 1, abort_flag, tmo);
+        trs.add(TR_SG_DS_EMPTY, t0);
         if (!ok) break;
 #pragma unroll
         for (int k = 0; k < NC / 8; ++k) {
@@ -398,6 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = ((uint32_t)(quarter * 32) << 16);
     const uint32_t stg = ptx::smem_u32(sm + L::STG_OFF);
     const bool leader = (warp == 12 && lane == 0);
+    const Trace& trq = leader ? tr : tr_none;
     __shared__ int go_flag;
     __shared__ int wg_ok[4];
     auto agree = [&](bool mine) -> bool {
@@ -414,8 +512,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int b = w.bh / p.H, h = w.bh % p.H;
       for (int hs = 0; hs < SUB && ok; ++hs, ++it) {
         const int q0 = w.j * kTile + hs * BR;
+        long long t0 = trq.t0();
         ok = agree(ptx::warp_wait(bars + B_DQ_FULL, it & 1, abort_flag, tmo));
+        trq.add(TR_DQ_FULL, t0);
         if (!ok) break;
+        t0 = trq.t0();
         ptx::tc_fence_after();
         float v[64];
         {
@@ -454,10 +555,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::fence_proxy_async_smem();
         ptx::named_bar(1, 128);
+        trq.add(TR_DQ_STAGE, t0);
         if (leader) {
           int go = 1;
           const int sem_idx = (w.bh * p.n + w.j) * SUB + hs;
           const int o = p.ord[w.i * p.n + w.j];
+          t0 = trq.t0();
           if (p.deterministic) {
             go = wait_turn(p.sems + sem_idx, o + p.ordinal_skew, p.ws_header, p.timeout_ns,
                            w.bh, w.j)
@@ -465,6 +568,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                      : 0;
             ptx::fence_proxy_async_global();
           }
+          trq.add(TR_DQ_SEM, t0);
+          t0 = trq.t0();
           if (go) {
 #pragma unroll
             for (int bx = 0; bx < D / 32; ++bx)
@@ -482,6 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             *abort_flag = 1;
           }
+          trq.add(TR_DQ_REDUCE, t0);
           go_flag = go;
         }
         ptx::named_bar(1, 128);
@@ -491,7 +597,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // ---- dK/dV epilogue after the tile's last sub-task ----
         if (w.last_of_tile && hs == SUB - 1) {
+          t0 = trq.t0();
           ok = agree(ptx::warp_wait(bars + B_ACC_FULL, tl & 1, abort_flag, tmo));
+          trq.add(TR_DQ_ACC_FULL, t0);
           if (!ok) break;
           ptx::tc_fence_after();
           const int row = quarter * 32 + lane;        // kv row
@@ -532,6 +640,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+  if (p.trace) {
+    if (threadIdx.x == 0) trace_s[TR_TOTAL] = (unsigned long long)(clock64() - t_start);
+    __syncthreads();
+    if (threadIdx.x < TR_SITES) p.trace[(size_t)blockIdx.x * TR_SITES + threadIdx.x] = trace_s[threadIdx.x];
   }
 }
 

@@ -48,6 +48,7 @@ _SIGNATURES = {
     "dash_last_error": (ctypes.c_char_p, []),
     "dash_attn_shutdown": (None, []),
     "dash_debug_set_sync": (None, [ctypes.c_longlong, _c_int]),
+    "dash_debug_set_trace": (None, [_vp]),
     "dash_profile_enable": (_c_int, [_c_int]),
     "dash_profile_read": (_c_int, [_dblp, ctypes.POINTER(_c_int)]),
     "dash_sched_num_slots": (_c_int, [_c_int, _c_int, _c_int]),
@@ -141,6 +142,11 @@ def dash_attn_shutdown() -> None:
 
 def dash_debug_set_sync(timeout_ns: int, ordinal_skew: int) -> None:
     load().dash_debug_set_sync(int(timeout_ns), int(ordinal_skew))
+
+
+def dash_debug_set_trace(counters) -> None:
+    """counters: a zeroed uint64 CUDA tensor of 24 * SM-count entries, or None to stop."""
+    load().dash_debug_set_trace(None if counters is None else counters.data_ptr())
 
 
 def dash_profile_enable(on: bool) -> None:
