@@ -61,7 +61,7 @@ typedef enum {
   DASH_ERR_UNSUPPORTED = 2,         /* valid but not implemented (head dim, mask/schedule pair) */
   DASH_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < dash_attn_bwd_workspace_size() */
   DASH_ERR_CUDA = 4,                /* a CUDA runtime call failed; see dash_last_error() */
-  DASH_ERR_SYNC_TIMEOUT = 5,        /* a dQ reduction wait exceeded its time limit */
+  DASH_ERR_SYNC_TIMEOUT = 5,        /* a wait (dQ semaphore or in-kernel pipeline) hit its limit */
   DASH_ERR_DEADLOCK_RISK = 6        /* the schedule's waits form a cycle on this grid */
 } dash_status_t;
 
@@ -113,9 +113,10 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
 
 /*
  * Synchronises `stream` and reads the status header of `workspace` written by the last
- * dash_attn_bwd on it: DASH_OK, or DASH_ERR_SYNC_TIMEOUT when a reduction wait ran out
- * (the kernel then abandons its remaining work; outputs are undefined). Also returns
- * DASH_ERR_CUDA if the stream reports an error.
+ * dash_attn_bwd on it: DASH_OK, or DASH_ERR_SYNC_TIMEOUT when a wait ran out -- a dQ
+ * semaphore wait, or a hand-off between the warps of one CTA -- after which the kernel
+ * abandons its remaining work and the outputs are undefined (dash_last_error() says
+ * which). Also returns DASH_ERR_CUDA if the stream reports an error.
  */
 dash_status_t dash_attn_get_status(const void* workspace, cudaStream_t stream);
 

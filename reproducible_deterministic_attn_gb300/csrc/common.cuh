@@ -44,7 +44,7 @@ struct BwdParams {
   int* ws_header;            // status words
   float* Dsum;               // [B, H, S] rowsum(dO * O)
   float* dq_acc;             // [B, H, S, D] fp32
-  int* sems;                 // [B, H, S / 64]: one per 64-row dQ sub-block
+  int* sems;                 // [B, H, n]: one per 128-row dQ block
   int num_sems;
   const int32_t* slot_off;   // schedule: chain offsets
   const int32_t* tasks;      // schedule: (kv << 16) | q

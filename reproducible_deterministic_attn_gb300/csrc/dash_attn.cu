@@ -1,6 +1,6 @@
 // C ABI entry points of libdash_attn: argument checks, schedule-table cache, the
 // deadlock check of the persistent grid, and the kernel launches.
-#include "../../include/dash_attn.h"
+#include "dash_attn.h"
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -183,7 +183,7 @@ WsLayout ws_layout(int B, int S, int H, int D) {
   w.dsum = dash::kWsHeaderBytes;
   w.dq_acc = round_up(w.dsum + rows * sizeof(float), 256);
   w.sems = round_up(w.dq_acc + rows * D * sizeof(float), 256);
-  w.total = round_up(w.sems + (size_t)B * H * (S / 64) * sizeof(int), 256);
+  w.total = round_up(w.sems + (size_t)B * H * (S / dash::kTile) * sizeof(int), 256);
   return w;
 }
 
@@ -325,7 +325,7 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
   p.ordinal_skew = g_ordinal_skew;
   p.trace = g_trace;
 
-  p.num_sems = B * H * (S / 64);
+  p.num_sems = B * H * n;
 
   // Persistent grid, one CTA per SM: every CTA must be resident at once (the ordered
   // reduction waits on other CTAs), so the launch is cooperative.
@@ -379,6 +379,12 @@ dash_status_t dash_attn_get_status(const void* workspace, cudaStream_t stream) {
   DASH_CUDA(cudaStreamSynchronize(stream));
   int words[8];
   DASH_CUDA(cudaMemcpy(words, workspace, sizeof(words), cudaMemcpyDeviceToHost));
+  if (words[dash::WS_STATUS] == dash::kStatusSyncTimeout && words[dash::WS_BH] < 0) {
+    char buf[160];
+    snprintf(buf, sizeof(buf), "a pipeline wait inside CTA %d timed out", words[dash::WS_QTILE]);
+    g_last_error = buf;
+    return DASH_ERR_SYNC_TIMEOUT;
+  }
   if (words[dash::WS_STATUS] == dash::kStatusSyncTimeout) {
     char buf[160];
     snprintf(buf, sizeof(buf), "dQ reduction wait timed out: bh=%d q_tile=%d expected=%d seen=%d",

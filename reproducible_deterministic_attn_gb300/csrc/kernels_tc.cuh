@@ -19,9 +19,10 @@
 //   ordinal first and releases ordinal + 1 after the add has completed (the pages' fixed
 //   serial reduction order); non-deterministic mode adds as soon as it can.
 //
-// Warp roles (512 threads): warp 0 = TMA producer, warp 1 = MMA issuer, warps 4..11 =
-// softmax-gradient (two warpgroups, each half of the BR columns), warps 12..15 = dQ
-// reduction and dK/dV epilogue. Warps 2..3 idle. TMEM: 512 columns.
+// Warp roles (512 threads): warp 0 = TMA producer, warp 1 = S^T/dP^T MMA issuer, warp 3 =
+// dV/dK/dQ MMA issuer, warp 2 = dQ reducer (semaphore waits, TMA reduce-adds, releases),
+// warps 4..11 = softmax-gradient (two warpgroups, each half of the BR columns), warps
+// 12..15 = dQ read-out into the staging buffer and the dK/dV epilogue. TMEM: 512 columns.
 #pragma once
 
 #include "common.cuh"
@@ -37,6 +38,7 @@ template <>
 struct Cfg<64> {
   static constexpr int BR = 128;  // query rows per sub-tile
   static constexpr int SUB = 1;   // sub-tiles per 128-row schedule task
+  static constexpr int STAGES = 2;  // Q/dO pipeline depth
   static constexpr int T_S = 0, T_DP = 128, T_DV = 256, T_DK = 320, T_DQ = 384;
 };
 
@@ -44,45 +46,51 @@ template <>
 struct Cfg<128> {
   static constexpr int BR = 64;
   static constexpr int SUB = 2;
+  static constexpr int STAGES = 3;
   static constexpr int T_S = 0, T_DP = 64, T_DV = 128, T_DK = 256, T_DQ = 384;
 };
 
 constexpr int kThreads = 512;
-constexpr int kStages = 2;
+constexpr int kMaxStages = 3;
 constexpr int kTmemCols = 512;
 
-// Shared-memory carve-up (byte offsets from a 1024-aligned base).
+// Shared-memory carve-up (byte offsets from a 1024-aligned base). A stage holds one
+// sub-tile's Q and dO (TMA destinations, 1024-aligned); the stages' LSE and Dsum rows sit
+// together after the dQ staging buffer.
 template <int D>
 struct Smem {
   static constexpr int BR = Cfg<D>::BR;
+  static constexpr int STAGES = Cfg<D>::STAGES;
   static constexpr int KV_BYTES = kTile * D * 2;             // one of K or V
   static constexpr int QT_BYTES = BR * D * 2;                // one of Q or dO (per stage)
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = K_OFF + KV_BYTES;
   static constexpr int STAGE_OFF = V_OFF + KV_BYTES;
-  static constexpr int STAGE_BYTES = ((2 * QT_BYTES + 2 * BR * 4) + 1023) / 1024 * 1024;
+  static constexpr int STAGE_BYTES = 2 * QT_BYTES;
   static constexpr int Q_IN_STAGE = 0;
   static constexpr int DO_IN_STAGE = QT_BYTES;
-  static constexpr int LSE_IN_STAGE = 2 * QT_BYTES;
-  static constexpr int DSUM_IN_STAGE = 2 * QT_BYTES + BR * 4;
-  static constexpr int P_OFF = STAGE_OFF + kStages * STAGE_BYTES;
+  static constexpr int P_OFF = STAGE_OFF + STAGES * STAGE_BYTES;
   static constexpr int PT_BYTES = kTile * BR * 2;            // P^T or dS^T tile
   static constexpr int DS_OFF = P_OFF + PT_BYTES;
   static constexpr int STG_OFF = DS_OFF + PT_BYTES;          // dQ staging (fp32)
   static constexpr int STG_BYTES = BR * D * 4;
-  static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
+  static constexpr int LD_OFF = STG_OFF + STG_BYTES;         // per stage: LSE[BR], Dsum[BR]
+  static constexpr int LD_STAGE_BYTES = 2 * BR * 4;
+  static constexpr int BAR_OFF = LD_OFF + STAGES * LD_STAGE_BYTES;
   static constexpr int TRACE_OFF = BAR_OFF + 256;
   static constexpr int TOTAL = TRACE_OFF + 8 * TR_SITES;     // barriers, flags, trace
   static constexpr int ALLOC = TOTAL + 1024;                 // slack for 1024 alignment
+  static_assert(ALLOC <= 232448, "shared memory budget");
 };
 
 // Barrier indices.
 enum {
   B_KV_FULL = 0, B_KV_EMPTY, B_S_FULL, B_S_EMPTY, B_DP_FULL, B_DP_EMPTY, B_P_FULL, B_P_EMPTY,
   B_DS_FULL, B_DS_EMPTY, B_DQ_FULL, B_DQ_EMPTY, B_ACC_FULL, B_ACC_EMPTY, B_DRAIN,
+  B_STG_FULL, B_STG_EMPTY, B_DRAIN2,
   B_STAGE_FULL,                     // + stage
-  B_STAGE_EMPTY = B_STAGE_FULL + kStages,
-  B_COUNT = B_STAGE_EMPTY + kStages
+  B_STAGE_EMPTY = B_STAGE_FULL + kMaxStages,
+  B_COUNT = B_STAGE_EMPTY + kMaxStages
 };
 
 struct TmaMaps {
@@ -96,27 +104,42 @@ __device__ __forceinline__ uint32_t sw_chunk(int row, int chunk, int rows) {
   return (uint32_t)((chunk >> 3) * rows * 128 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
 }
 
-// Iterates this CTA's (unit, task) sequence; every role walks the same sequence.
+// Iterates this CTA's (unit, task) sequence; every role walks the same sequence. The
+// task table is read two entries ahead so its load latency hides behind the work.
 struct Walk {
   const BwdParams& p;
   int u, t, t_end, bh, i, j;
+  int32_t prev_tk, cur_tk, nxt_tk, nxt2_tk;
   bool first_of_tile, last_of_tile;
-  __device__ Walk(const BwdParams& pp) : p(pp), u((int)blockIdx.x - (int)gridDim.x), t(0), t_end(0) {}
+  __device__ Walk(const BwdParams& pp)
+      : p(pp), u((int)blockIdx.x - (int)gridDim.x), t(0), t_end(0) {}
+  __device__ __forceinline__ int32_t task_at(int k) const {
+    return k < t_end ? __ldg(p.tasks + k) : -1;
+  }
   __device__ bool next() {
     ++t;
-    while (t >= t_end) {
-      u += gridDim.x;
-      if (u >= p.num_units) return false;
-      const int slot = u % p.num_slots;
-      bh = u / p.num_slots;
-      t = p.slot_off[slot];
-      t_end = p.slot_off[slot + 1];
+    if (t >= t_end) {
+      do {
+        u += gridDim.x;
+        if (u >= p.num_units) return false;
+        const int slot = u % p.num_slots;
+        bh = u / p.num_slots;
+        t = __ldg(p.slot_off + slot);
+        t_end = __ldg(p.slot_off + slot + 1);
+      } while (t >= t_end);
+      prev_tk = -1;
+      cur_tk = task_at(t);
+      nxt_tk = task_at(t + 1);
+    } else {
+      prev_tk = cur_tk;
+      cur_tk = nxt_tk;
+      nxt_tk = nxt2_tk;
     }
-    const int32_t tk = __ldg(p.tasks + t);
-    i = tk >> 16;
-    j = tk & 0xffff;
-    first_of_tile = (t == p.slot_off[u % p.num_slots]) || ((__ldg(p.tasks + t - 1) >> 16) != i);
-    last_of_tile = (t + 1 == t_end) || ((__ldg(p.tasks + t + 1) >> 16) != i);
+    nxt2_tk = task_at(t + 2);
+    i = cur_tk >> 16;
+    j = cur_tk & 0xffff;
+    first_of_tile = prev_tk < 0 || (prev_tk >> 16) != i;
+    last_of_tile = nxt_tk < 0 || (nxt_tk >> 16) != i;
     return true;
   }
 };
@@ -167,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ TmaMaps maps) {
   using C = Cfg<D>;
   using L = Smem<D>;
-  constexpr int BR = C::BR, SUB = C::SUB;
+  constexpr int BR = C::BR, SUB = C::SUB, kStages = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(sm + L::BAR_OFF);
@@ -192,6 +215,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(bars + B_ACC_FULL, 1);
     ptx::mbar_init(bars + B_ACC_EMPTY, 4);
     ptx::mbar_init(bars + B_DRAIN, 1);
+    ptx::mbar_init(bars + B_STG_FULL, 4);
+    ptx::mbar_init(bars + B_STG_EMPTY, 1);
+    ptx::mbar_init(bars + B_DRAIN2, 1);
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(bars + B_STAGE_FULL + s, 1);
       ptx::mbar_init(bars + B_STAGE_EMPTY + s, 1 + 8);
@@ -228,16 +254,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         tr.add(TR_PROD_STAGE_EMPTY, t0);
         uint8_t* st = sm + L::STAGE_OFF + s * L::STAGE_BYTES;
-        ptx::mbar_expect_tx(bars + B_STAGE_FULL + s, 2 * L::QT_BYTES + 2 * BR * 4);
+        ptx::mbar_expect_tx(bars + B_STAGE_FULL + s, 2 * L::QT_BYTES + L::LD_STAGE_BYTES);
         for (int cb = 0; cb < D / 64; ++cb) {
           ptx::tma_load_3d(st + L::Q_IN_STAGE + cb * BR * 128, &maps.q, cb * 64, h, b * p.S + q0,
                            bars + B_STAGE_FULL + s);
           ptx::tma_load_3d(st + L::DO_IN_STAGE + cb * BR * 128, &maps.dO, cb * 64, h, b * p.S + q0,
                            bars + B_STAGE_FULL + s);
         }
-        ptx::bulk_load(st + L::LSE_IN_STAGE, p.lse + (size_t)bh * p.S + q0, BR * 4,
-                       bars + B_STAGE_FULL + s);
-        ptx::bulk_load(st + L::DSUM_IN_STAGE, p.Dsum + (size_t)bh * p.S + q0, BR * 4,
+        uint8_t* ld = sm + L::LD_OFF + s * L::LD_STAGE_BYTES;
+        ptx::bulk_load(ld, p.lse + (size_t)bh * p.S + q0, BR * 4, bars + B_STAGE_FULL + s);
+        ptx::bulk_load(ld + BR * 4, p.Dsum + (size_t)bh * p.S + q0, BR * 4,
                        bars + B_STAGE_FULL + s);
         ++it;
         // a new KV tile: K and V once the previous tile's MMAs are done with the buffer
@@ -260,139 +286,130 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_drain(bars + B_STAGE_FULL + k % kStages, (k / kStages) & 1, 100000000ll);
       if (tl > 0) ptx::mbar_drain(bars + B_KV_FULL, (tl - 1) & 1, 100000000ll);
     }
-  } else if (warp == 1) {
-    // ===================================== MMA issuer =======================================
-    // Software-pipelined issue order per sub-tile t:
-    //   dV(t), S(t+1), dK(t), dQ(t), dP(t+1)
-    // so the softmax-gradient warps compute P(t+1) while dK(t)/dQ(t) run. At a KV-tile
-    // boundary S(t+1) waits for the new K/V tile instead.
+  } else if (warp == 1 || warp == 3) {
+    // ===================================== MMA issuers ======================================
+    // Two issuing threads keep the tensor pipe fed while either one waits on a barrier:
+    // warp 1 issues S^T and dP^T, warp 3 issues dV, dK and the dQ partial. Their TMEM
+    // regions are disjoint; the softmax-gradient hand-offs order them.
     if (lane == 0) {
+      // Descriptor low words of every operand buffer; each K step adds a compile-time
+      // offset (in 16-byte units) to them.
       const uint32_t sK = ptx::smem_u32(sm + L::K_OFF), sV = ptx::smem_u32(sm + L::V_OFF);
       const uint32_t sP = ptx::smem_u32(sm + L::P_OFF), sdS = ptx::smem_u32(sm + L::DS_OFF);
+      const uint32_t dK_k = ptx::sdesc_lo(sK, 16);                  // K, K-major
+      const uint32_t dK_mn = ptx::sdesc_lo(sK, kTile * 128);        // K, MN-major
+      const uint32_t dV_k = ptx::sdesc_lo(sV, 16);
+      const uint32_t dP_k = ptx::sdesc_lo(sP, 16);
+      const uint32_t dS_k = ptx::sdesc_lo(sdS, 16);
+      const uint32_t dS_mn = ptx::sdesc_lo(sdS, kTile * 128);
+      const uint32_t st0 = ptx::smem_u32(sm + L::STAGE_OFF);
       constexpr uint32_t ID_S = ptx::idesc_bf16(128, BR, 0, 0);     // S^T, dP^T
       constexpr uint32_t ID_ACC = ptx::idesc_bf16(128, D, 0, 1);    // dV, dK
       constexpr uint32_t ID_DQ = ptx::idesc_bf16(128, 64, 1, 1);    // dQ (D=64) / dQ^T (D=128)
-      auto stage_addr = [&](const Sub& x) {
-        return ptx::smem_u32(sm + L::STAGE_OFF + (x.it % kStages) * L::STAGE_BYTES);
+      // K-major step ks of a [rows][D] tile in 64-column blocks: 32 bytes per step inside a
+      // 128-byte row, a new block every 4 steps; MN-major step ks: 16 rows of 128 bytes.
+      auto kstep = [](int ks, int rows) -> uint32_t {
+        return ((ks >> 2) * rows * 128 + (ks & 3) * 32) >> 4;
       };
-      auto issue_S = [&](const Sub& x) -> bool {
-        long long t0 = tr.t0();
-        if (x.first && !ptx::mbar_wait(bars + B_KV_FULL, x.tile & 1, abort_flag, tmo)) return false;
-        tr.add(TR_MMA_KV_FULL, t0);
-        t0 = tr.t0();
-        if (!ptx::mbar_wait(bars + B_STAGE_FULL + x.it % kStages, (x.it / kStages) & 1, abort_flag,
-                            tmo))
-          return false;
-        tr.add(TR_MMA_STAGE_FULL, t0);
-        t0 = tr.t0();
-        if (x.it > 0 && !ptx::mbar_wait(bars + B_S_EMPTY, (x.it - 1) & 1, abort_flag, tmo))
-          return false;
-        tr.add(TR_MMA_S_EMPTY, t0);
-        ptx::tc_fence_after();
-        const uint32_t sQ = stage_addr(x) + L::Q_IN_STAGE;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t ao = (ks / 4) * (kTile * 128) + (ks % 4) * 32;
-          const uint32_t bo = (ks / 4) * (BR * 128) + (ks % 4) * 32;
-          ptx::mma_bf16(tmem + C::T_S, ptx::sdesc(sK + ao, 16, 1024), ptx::sdesc(sQ + bo, 16, 1024),
-                        ID_S, ks > 0);
-        }
-        ptx::mma_commit(bars + B_S_FULL);
-        return true;
-      };
-      auto issue_dP = [&](const Sub& x) -> bool {
-        const long long t0 = tr.t0();
-        if (x.it > 0 && !ptx::mbar_wait(bars + B_DP_EMPTY, (x.it - 1) & 1, abort_flag, tmo))
-          return false;
-        tr.add(TR_MMA_DP_EMPTY, t0);
-        ptx::tc_fence_after();
-        const uint32_t sdO = stage_addr(x) + L::DO_IN_STAGE;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t ao = (ks / 4) * (kTile * 128) + (ks % 4) * 32;
-          const uint32_t bo = (ks / 4) * (BR * 128) + (ks % 4) * 32;
-          ptx::mma_bf16(tmem + C::T_DP, ptx::sdesc(sV + ao, 16, 1024),
-                        ptx::sdesc(sdO + bo, 16, 1024), ID_S, ks > 0);
-        }
-        ptx::mma_commit(bars + B_DP_FULL);
-        return true;
+      constexpr uint32_t MN_STEP = 2048 >> 4;
+      auto stage_lo = [&](const Sub& x, int off, uint32_t lbo) {
+        return ptx::sdesc_lo(st0 + (x.it % kStages) * L::STAGE_BYTES + off, lbo);
       };
       SubWalk<SUB> sw(p);
-      Sub cur, nxt;
-      bool have = sw.next(cur);
+      Sub x;
       bool ok = true;
-      if (have) ok = issue_S(cur) && issue_dP(cur);
-      while (ok && have) {
-        const bool have_n = sw.next(nxt);
-        const bool same_tile = have_n && !nxt.first;
-        const uint32_t st = stage_addr(cur);
-        const uint32_t sQ = st + L::Q_IN_STAGE, sdO = st + L::DO_IN_STAGE;
-        // dV += P^T dO: A = P^T (K-major, 128 kv rows x BR), B = dO (MN-major over D).
-        // The first sub-tile of a KV tile overwrites the accumulators, which the previous
-        // tile's epilogue must have read out.
-        long long t0 = tr.t0();
-        ok = ptx::mbar_wait(bars + B_P_FULL, cur.it & 1, abort_flag, tmo);
-        tr.add(TR_MMA_P_FULL, t0);
-        t0 = tr.t0();
-        if (ok && cur.first && cur.tile > 0)
-          ok = ptx::mbar_wait(bars + B_ACC_EMPTY, (cur.tile - 1) & 1, abort_flag, tmo);
-        tr.add(TR_MMA_ACC_EMPTY, t0);
-        if (!ok) break;
-        ptx::tc_fence_after();
+      if (warp == 1) {
+        while (ok && sw.next(x)) {
+          long long t0 = tr.t0();
+          if (x.first && !(ok = ptx::mbar_wait(bars + B_KV_FULL, x.tile & 1, abort_flag, tmo))) break;
+          tr.add(TR_MMA_KV_FULL, t0);
+          t0 = tr.t0();
+          ok = ptx::mbar_wait(bars + B_STAGE_FULL + x.it % kStages, (x.it / kStages) & 1,
+                              abort_flag, tmo);
+          tr.add(TR_MMA_STAGE_FULL, t0);
+          t0 = tr.t0();
+          if (ok && x.it > 0) ok = ptx::mbar_wait(bars + B_S_EMPTY, (x.it - 1) & 1, abort_flag, tmo);
+          tr.add(TR_MMA_S_EMPTY, t0);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          const uint32_t dQ_k = stage_lo(x, L::Q_IN_STAGE, 16);
+          const uint32_t ddO_k = stage_lo(x, L::DO_IN_STAGE, 16);
+          // S^T = K Q^T: K-major A (128 kv rows), K-major B (BR rows)
 #pragma unroll
-        for (int ks = 0; ks < BR / 16; ++ks) {
-          const uint32_t ao = (ks / 4) * (kTile * 128) + (ks % 4) * 32;
-          ptx::mma_bf16(tmem + C::T_DV, ptx::sdesc(sP + ao, 16, 1024),
-                        ptx::sdesc(sdO + ks * 2048, BR * 128, 1024), ID_ACC,
-                        !(cur.first && ks == 0));
+          for (int ks = 0; ks < D / 16; ++ks)
+            ptx::mma_lo(tmem + C::T_S, dK_k + kstep(ks, kTile), dQ_k + kstep(ks, BR), ID_S, ks > 0);
+          ptx::mma_commit(bars + B_S_FULL);
+          t0 = tr.t0();
+          if (x.it > 0) ok = ptx::mbar_wait(bars + B_DP_EMPTY, (x.it - 1) & 1, abort_flag, tmo);
+          tr.add(TR_MMA_DP_EMPTY, t0);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          // dP^T = V dO^T
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)
+            ptx::mma_lo(tmem + C::T_DP, dV_k + kstep(ks, kTile), ddO_k + kstep(ks, BR), ID_S, ks > 0);
+          ptx::mma_commit(bars + B_DP_FULL);
         }
-        ptx::mma_commit(bars + B_P_EMPTY);
-        if (same_tile && !(ok = issue_S(nxt))) break;
-        // dK += dS^T Q, then the dQ partial over the 128 kv rows
-        t0 = tr.t0();
-        ok = ptx::mbar_wait(bars + B_DS_FULL, cur.it & 1, abort_flag, tmo);
-        tr.add(TR_MMA_DS_FULL, t0);
-        t0 = tr.t0();
-        if (ok && cur.it > 0) ok = ptx::mbar_wait(bars + B_DQ_EMPTY, (cur.it - 1) & 1, abort_flag, tmo);
-        tr.add(TR_MMA_DQ_EMPTY, t0);
-        if (!ok) break;
-        ptx::tc_fence_after();
+      } else {
+        while (ok && sw.next(x)) {
+          const uint32_t dQ_mn = stage_lo(x, L::Q_IN_STAGE, BR * 128);
+          const uint32_t ddO_mn = stage_lo(x, L::DO_IN_STAGE, BR * 128);
+          // dV += P^T dO: A = P^T (K-major, 128 kv rows x BR), B = dO (MN-major over D).
+          // The first sub-tile of a KV tile overwrites the accumulators, which the
+          // previous tile's epilogue must have read out.
+          long long t0 = tr.t0();
+          ok = ptx::mbar_wait(bars + B_P_FULL, x.it & 1, abort_flag, tmo);
+          tr.add(TR_MMA_P_FULL, t0);
+          t0 = tr.t0();
+          if (ok && x.first && x.tile > 0)
+            ok = ptx::mbar_wait(bars + B_ACC_EMPTY, (x.tile - 1) & 1, abort_flag, tmo);
+          tr.add(TR_MMA_ACC_EMPTY, t0);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          const uint32_t acc0 = x.first ? 0u : 1u;
 #pragma unroll
-        for (int ks = 0; ks < BR / 16; ++ks) {
-          const uint32_t ao = (ks / 4) * (kTile * 128) + (ks % 4) * 32;
-          ptx::mma_bf16(tmem + C::T_DK, ptx::sdesc(sdS + ao, 16, 1024),
-                        ptx::sdesc(sQ + ks * 2048, BR * 128, 1024), ID_ACC,
-                        !(cur.first && ks == 0));
-        }
+          for (int ks = 0; ks < BR / 16; ++ks)
+            ptx::mma_lo(tmem + C::T_DV, dP_k + kstep(ks, kTile), ddO_mn + ks * MN_STEP, ID_ACC,
+                        ks > 0 ? 1u : acc0);
+          ptx::mma_commit(bars + B_P_EMPTY);
+          // dK += dS^T Q, then the dQ partial over the 128 kv rows
+          t0 = tr.t0();
+          ok = ptx::mbar_wait(bars + B_DS_FULL, x.it & 1, abort_flag, tmo);
+          tr.add(TR_MMA_DS_FULL, t0);
+          t0 = tr.t0();
+          if (ok && x.it > 0) ok = ptx::mbar_wait(bars + B_DQ_EMPTY, (x.it - 1) & 1, abort_flag, tmo);
+          tr.add(TR_MMA_DQ_EMPTY, t0);
+          if (!ok) break;
+          ptx::tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < kTile / 16; ++ks) {
-          if (D == 64) {
-            // dQ = dS K: A = dS (MN-major view of the dS^T tile), B = K (MN-major, 64 d)
-            ptx::mma_bf16(tmem + C::T_DQ, ptx::sdesc(sdS + ks * 2048, kTile * 128, 1024),
-                          ptx::sdesc(sK + ks * 2048, kTile * 128, 1024), ID_DQ, ks > 0);
-          } else {
-            // dQ^T = K^T dS^T: A = K^T (MN-major over 128 d), B = dS^T (MN-major, 64 q)
-            ptx::mma_bf16(tmem + C::T_DQ, ptx::sdesc(sK + ks * 2048, kTile * 128, 1024),
-                          ptx::sdesc(sdS + ks * 2048, kTile * 128, 1024), ID_DQ, ks > 0);
+          for (int ks = 0; ks < BR / 16; ++ks)
+            ptx::mma_lo(tmem + C::T_DK, dS_k + kstep(ks, kTile), dQ_mn + ks * MN_STEP, ID_ACC,
+                        ks > 0 ? 1u : acc0);
+#pragma unroll
+          for (int ks = 0; ks < kTile / 16; ++ks) {
+            if (D == 64) {
+              // dQ = dS K: A = dS (MN-major view of the dS^T tile), B = K (MN-major, 64 d)
+              ptx::mma_lo(tmem + C::T_DQ, dS_mn + ks * MN_STEP, dK_mn + ks * MN_STEP, ID_DQ, ks > 0);
+            } else {
+              // dQ^T = K^T dS^T: A = K^T (MN-major over 128 d), B = dS^T (MN-major, 64 q)
+              ptx::mma_lo(tmem + C::T_DQ, dK_mn + ks * MN_STEP, dS_mn + ks * MN_STEP, ID_DQ, ks > 0);
+            }
+          }
+          ptx::mma_commit(bars + B_DS_EMPTY);
+          ptx::mma_commit(bars + B_DQ_FULL);
+          // the stage's Q/dO were last read by dK/dV here; the S^T/dP^T reads of this stage
+          // finished before the softmax-gradient warps released P and dS
+          ptx::mma_commit(bars + B_STAGE_EMPTY + x.it % kStages);
+          if (x.last) {
+            ptx::mma_commit(bars + B_ACC_FULL);
+            ptx::mma_commit(bars + B_KV_EMPTY);
           }
         }
-        ptx::mma_commit(bars + B_DS_EMPTY);
-        ptx::mma_commit(bars + B_DQ_FULL);
-        ptx::mma_commit(bars + B_STAGE_EMPTY + cur.it % kStages);
-        if (cur.last) {
-          ptx::mma_commit(bars + B_ACC_FULL);
-          ptx::mma_commit(bars + B_KV_EMPTY);
-        }
-        if (have_n) {
-          if (!same_tile && !(ok = issue_S(nxt))) break;
-          if (!(ok = issue_dP(nxt))) break;
-        }
-        cur = nxt;
-        have = have_n;
       }
       // drain: no MMA may be in flight when TMEM is released
-      ptx::mma_commit(bars + B_DRAIN);
-      ptx::mbar_drain(bars + B_DRAIN, 0, 1000000000ll);
+      uint64_t* drain = bars + (warp == 1 ? B_DRAIN : B_DRAIN2);
+      ptx::mma_commit(drain);
+      ptx::mbar_drain(drain, 0, 1000000000ll);
     }
   } else if (warp >= 4 && warp < 12) {
     // =============================== softmax-gradient warps =================================
@@ -410,8 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int hs = 0; hs < SUB && ok; ++hs, ++it) {
         const int s = it % kStages;
         const int q0 = w.j * kTile + hs * BR;
-        const float* lse_s = (const float*)(sm + L::STAGE_OFF + s * L::STAGE_BYTES + L::LSE_IN_STAGE);
-        const float* dsum_s = (const float*)(sm + L::STAGE_OFF + s * L::STAGE_BYTES + L::DSUM_IN_STAGE);
+        const float* lse_s = (const float*)(sm + L::LD_OFF + s * L::LD_STAGE_BYTES);
+        const float* dsum_s = lse_s + BR;
         const bool diag = p.causal && (w.i == w.j);
         const int kv_g = w.i * kTile + r;
         long long t0 = trs.t0();
@@ -487,53 +504,90 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+  } else if (warp == 2) {
+    // ===================================== dQ reducer =======================================
+    // Adds each staged dQ partial into the fp32 accumulator with a TMA bulk reduce-add.
+    // Deterministic mode takes the 128-row block's turn (semaphore == ordinal) before its
+    // first sub-tile and hands it on (ordinal + 1) once the block's reduces have
+    // completed -- always before this thread waits for its next turn. (Taking the next
+    // turn first would let every CTA of a shift ring hold a release while waiting for its
+    // neighbour's: a cycle.) The staging buffer is handed back as soon as it has been read.
+    if (lane == 0) {
+      Walk w(p);
+      int it = 0;
+      bool ok = true;
+      while (ok && w.next()) {
+        for (int hs = 0; hs < SUB && ok; ++hs, ++it) {
+          const int q0 = w.j * kTile + hs * BR;
+          long long t0 = tr.t0();
+          ok = ptx::mbar_wait(bars + B_STG_FULL, it & 1, abort_flag, tmo);
+          tr.add(TR_DQ_FULL, t0);
+          if (!ok) break;
+          const int sem_idx = w.bh * p.n + w.j;
+          const int o = p.ord[w.i * p.n + w.j];
+          if (p.deterministic && hs == 0) {
+            t0 = tr.t0();
+            ok = wait_turn(p.sems + sem_idx, o + p.ordinal_skew, p.ws_header, p.timeout_ns,
+                           w.bh, w.j);
+            tr.add(TR_DQ_SEM, t0);
+            if (!ok) {
+              *abort_flag = 1;
+              break;
+            }
+            ptx::fence_proxy_async_global();
+          }
+          t0 = tr.t0();
+#pragma unroll
+          for (int bx = 0; bx < D / 32; ++bx)
+            ptx::tma_reduce_add_2d(&maps.acc, sm + L::STG_OFF + bx * (BR * 128), bx * 32,
+                                   w.bh * p.S + q0);
+          ptx::bulk_commit();
+          ptx::bulk_wait_read_all();
+          ptx::mbar_arrive(bars + B_STG_EMPTY);
+          if (p.deterministic && hs == SUB - 1) {
+            ptx::bulk_wait_all();
+            ptx::fence_proxy_async_global();
+            __threadfence();
+            st_release_gpu(p.sems + sem_idx, o + 1 + p.ordinal_skew);
+          }
+          tr.add(TR_DQ_REDUCE, t0);
+        }
+      }
+      ptx::bulk_wait_all();
+    }
   } else if (warp >= 12) {
-    // ============================ dQ reduction + dK/dV epilogue ============================
-    // Every named barrier below is reached by all four warps unconditionally; a failed
-    // wait is agreed on through wg_ok before anyone leaves the loop.
+    // ================== dQ read-out into the staging buffer + dK/dV epilogue =================
     const int quarter = warp & 3;
     const uint32_t lane_addr = ((uint32_t)(quarter * 32) << 16);
     const uint32_t stg = ptx::smem_u32(sm + L::STG_OFF);
-    const bool leader = (warp == 12 && lane == 0);
-    const Trace& trq = leader ? tr : tr_none;
-    __shared__ int go_flag;
-    __shared__ int wg_ok[4];
-    auto agree = [&](bool mine) -> bool {
-      if (lane == 0) wg_ok[quarter] = mine ? 1 : 0;
-      ptx::named_bar(1, 128);
-      const bool all = wg_ok[0] && wg_ok[1] && wg_ok[2] && wg_ok[3];
-      ptx::named_bar(1, 128);
-      return all;
-    };
+    const Trace& trq = (warp == 12 && lane == 0) ? tr : tr_none;
     Walk w(p);
     int it = 0, tl = 0;
     bool ok = true;
     while (ok && w.next()) {
       const int b = w.bh / p.H, h = w.bh % p.H;
       for (int hs = 0; hs < SUB && ok; ++hs, ++it) {
-        const int q0 = w.j * kTile + hs * BR;
-        long long t0 = trq.t0();
-        ok = agree(ptx::warp_wait(bars + B_DQ_FULL, it & 1, abort_flag, tmo));
-        trq.add(TR_DQ_FULL, t0);
+        ok = ptx::warp_wait(bars + B_DQ_FULL, it & 1, abort_flag, tmo);
         if (!ok) break;
-        t0 = trq.t0();
         ptx::tc_fence_after();
         float v[64];
         {
-          float t0[32], t1[32];
-          ptx::tmem_ld32(tmem + lane_addr + C::T_DQ, t0);
-          ptx::tmem_ld32(tmem + lane_addr + C::T_DQ + 32, t1);
+          float t0v[32], t1v[32];
+          ptx::tmem_ld32(tmem + lane_addr + C::T_DQ, t0v);
+          ptx::tmem_ld32(tmem + lane_addr + C::T_DQ + 32, t1v);
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            v[c] = t0[c];
-            v[32 + c] = t1[c];
+            v[c] = t0v[c];
+            v[32 + c] = t1v[c];
           }
         }
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bars + B_DQ_EMPTY);
-        // the staging buffer is free: the previous reduce finished reading it before the
-        // leader reached the last barrier of the previous iteration
+        long long t0 = trq.t0();
+        if (it > 0) ok = ptx::warp_wait(bars + B_STG_EMPTY, (it - 1) & 1, abort_flag, tmo);
+        trq.add(TR_DQ_STAGE, t0);
+        if (!ok) break;
         if (D == 64) {
           // lanes = q rows; 64 d values; boxes of 32 fp32 columns x BR rows
           const int row = quarter * 32 + lane;
@@ -554,51 +608,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         ptx::fence_proxy_async_smem();
-        ptx::named_bar(1, 128);
-        trq.add(TR_DQ_STAGE, t0);
-        if (leader) {
-          int go = 1;
-          const int sem_idx = (w.bh * p.n + w.j) * SUB + hs;
-          const int o = p.ord[w.i * p.n + w.j];
-          t0 = trq.t0();
-          if (p.deterministic) {
-            go = wait_turn(p.sems + sem_idx, o + p.ordinal_skew, p.ws_header, p.timeout_ns,
-                           w.bh, w.j)
-                     ? 1
-                     : 0;
-            ptx::fence_proxy_async_global();
-          }
-          trq.add(TR_DQ_SEM, t0);
-          t0 = trq.t0();
-          if (go) {
-#pragma unroll
-            for (int bx = 0; bx < D / 32; ++bx)
-              ptx::tma_reduce_add_2d(&maps.acc, sm + L::STG_OFF + bx * (BR * 128), bx * 32,
-                                     w.bh * p.S + q0);
-            ptx::bulk_commit();
-            if (p.deterministic) {
-              ptx::bulk_wait_all();
-              ptx::fence_proxy_async_global();
-              __threadfence();
-              st_release_gpu(p.sems + sem_idx, o + 1 + p.ordinal_skew);
-            } else {
-              ptx::bulk_wait_read_all();
-            }
-          } else {
-            *abort_flag = 1;
-          }
-          trq.add(TR_DQ_REDUCE, t0);
-          go_flag = go;
-        }
-        ptx::named_bar(1, 128);
-        if (!go_flag) {
-          ok = false;
-          break;
-        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bars + B_STG_FULL);
         // ---- dK/dV epilogue after the tile's last sub-task ----
         if (w.last_of_tile && hs == SUB - 1) {
           t0 = trq.t0();
-          ok = agree(ptx::warp_wait(bars + B_ACC_FULL, tl & 1, abort_flag, tmo));
+          ok = ptx::warp_wait(bars + B_ACC_FULL, tl & 1, abort_flag, tmo);
           trq.add(TR_DQ_ACC_FULL, t0);
           if (!ok) break;
           ptx::tc_fence_after();
@@ -632,7 +647,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (leader) ptx::bulk_wait_all();
   }
 
   ptx::tc_fence_before();
@@ -640,6 +654,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+  // A CTA that gave up on any wait reports it, so an aborted run never reads as success.
+  if (threadIdx.x == 0 && *abort_flag) {
+    if (atomicCAS(p.ws_header + WS_STATUS, 0, kStatusSyncTimeout) == 0) {
+      p.ws_header[WS_BH] = -1;          // -1: an in-CTA pipeline wait, not a dQ semaphore
+      p.ws_header[WS_QTILE] = blockIdx.x;
+      __threadfence();
+    }
   }
   if (p.trace) {
     if (threadIdx.x == 0) trace_s[TR_TOTAL] = (unsigned long long)(clock64() - t_start);

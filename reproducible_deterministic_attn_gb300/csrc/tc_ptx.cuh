@@ -40,20 +40,30 @@ __device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps in hardware until the phase
+// completes or hint_ns passes, instead of polling the barrier.
+__device__ __forceinline__ bool mbar_try_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
 // Waits for completion `parity` of the barrier. Gives up (returns false) when *abort is
 // set by another role, or after timeout_ns, in which case it sets *abort itself.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           long long timeout_ns) {
   if (mbar_try(bar, parity)) return true;
   const long long t0 = global_timer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try(bar, parity)) return true;
-    if ((it & 15) == 0) {
-      if (*abort) return false;
-      if (global_timer_ns() - t0 > timeout_ns) {
-        *abort = 1;
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_sleep(bar, parity, 20000u)) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > timeout_ns) {
+      *abort = 1;
+      return false;
     }
   }
 }
@@ -127,6 +137,11 @@ __device__ __forceinline__ void bulk_commit() {
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
+// Waits until at most N of this thread's bulk groups are still pending.
+template <int N>
+__device__ __forceinline__ void bulk_wait_allow() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
 __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
@@ -154,6 +169,15 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
          ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+// The same descriptor split in 32-bit halves, for issue loops that advance only the
+// start address. hi: sbo = 1024 bytes, version 1, 128-byte swizzle -- identical for
+// every operand here. lo: start address >> 4 in bits 0..13 (shared-memory addresses stay
+// below 2^18, so adding whole 16-byte steps never carries into the lbo field above it).
+constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr >> 4) & 0x3FFF) | (((lbo >> 4) & 0x3FFF) << 16);
+}
+
 // Instruction descriptor of kind::f16: bf16 A and B, fp32 accumulator, M x N tile;
 // a_mn / b_mn select MN-major (transposed) operands.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
@@ -167,6 +191,16 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b
       "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(
           d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// MMA with descriptors given as low words (high word kDescHi for both operands).
+__device__ __forceinline__ void mma_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; .reg .b64 da, db; setp.ne.b32 p, %4, 0; mov.b64 da, {%1, %5}; "
+      "mov.b64 db, {%2, %5}; tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p; }" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kDescHi)
       : "memory");
 }
 
