@@ -112,6 +112,35 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
                             int deterministic, cudaStream_t stream);
 
 /*
+ * Backward pass that allocates no device memory. The DASH paper has no counterpart to
+ * this call; it exists for callers that cannot allocate device memory when they run the
+ * backward -- for example a framework that reserves all device memory up front for its
+ * own pool, or code that must not enter the CUDA allocator at that point. It computes
+ * the same result as dash_attn_bwd (same kernels, same schedule, same reduction order).
+ *
+ * Instead of a caller-supplied workspace it uses a fixed 64 MiB array that is part of the
+ * library's device image: every GPU that loads the library holds it until the process
+ * exits. Shapes whose scratch (dash_attn_bwd_workspace_size() plus the schedule tables)
+ * does not fit return DASH_ERR_WORKSPACE_TOO_SMALL with the sizes in dash_last_error();
+ * use dash_attn_bwd for those.
+ *   q .. dv, B .. stream : as for dash_attn_bwd.
+ *   status_out : optional device int (may be NULL); after the kernels it receives the
+ *                status word that dash_attn_get_status would report (0 = ok).
+ * The first call on a device looks up the array's device address (with that device
+ * current); make that first call before any stream capture. Every call on a device
+ * shares the one array and leaves its contents behind (the kernels clear what has to
+ * start at zero), so calls whose work overlaps on the GPU -- on different streams or
+ * from different threads -- race with each other and must be serialised by the caller.
+ * No cudaMalloc, cudaFree or other allocating routine is called; the schedule tables
+ * are built in host memory and copied into the array with cudaMemcpyAsync on `stream`.
+ */
+dash_status_t dash_attn_bwd_static(const void* q, const void* k, const void* v, const void* o,
+                                   const void* dO, const float* lse, void* dq, void* dk,
+                                   void* dv, int* status_out, int B, int S, int H, int D,
+                                   float scale, int mask, int schedule, int deterministic,
+                                   cudaStream_t stream);
+
+/*
  * Synchronises `stream` and reads the status header of `workspace` written by the last
  * dash_attn_bwd on it: DASH_OK, or DASH_ERR_SYNC_TIMEOUT when a wait ran out -- a dQ
  * semaphore wait, or a hand-off between the warps of one CTA -- after which the kernel

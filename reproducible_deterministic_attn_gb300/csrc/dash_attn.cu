@@ -458,3 +458,173 @@ dash_status_t dash_sched_simulate(int mask, int schedule, int n, int heads, int 
 }
 
 }  // extern "C"
+
+// =====================================================================================
+// Backward without device allocation (dash_attn_bwd_static).
+//
+// For callers that cannot allocate device memory at the time they run the backward --
+// for example a runtime whose memory is fully reserved up front by its own pool, or code
+// that must not enter the CUDA allocator at all -- this entry point takes its scratch
+// from a fixed array that is part of the library's device image. Inputs and outputs are
+// still the caller's buffers. The array is reserved on every GPU that loads the library
+// and stays there until the process exits.
+// =====================================================================================
+namespace {
+
+constexpr size_t kStaticScratchBytes = 64ull << 20;   // 64 MiB per device
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+unsigned char* g_static_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on `dev` (the current device). Looked up once per
+// device with that device current; later calls reuse it.
+dash_status_t static_scratch(int dev, unsigned char** out) {
+  if (dev < 0 || dev >= kMaxDevices) {
+    g_last_error = "dash_attn_bwd_static: device index out of range";
+    return DASH_ERR_UNSUPPORTED;
+  }
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+    g_static_ptr[dev] = (unsigned char*)ptr;
+  }
+  *out = g_static_ptr[dev];
+  return DASH_OK;
+}
+
+__global__ void copy_status_kernel(const int* header, int* out) { *out = header[dash::WS_STATUS]; }
+
+}  // namespace
+
+extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, const void* v,
+                                              const void* o, const void* dO, const float* lse,
+                                              void* dq, void* dk, void* dv, int* status_out,
+                                              int B, int S, int H, int D, float scale, int mask,
+                                              int schedule, int deterministic,
+                                              cudaStream_t stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return DASH_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || H < 1 || D < 1) return DASH_ERR_INVALID_ARG;
+  if (mask != DASH_MASK_FULL && mask != DASH_MASK_CAUSAL) return DASH_ERR_INVALID_ARG;
+  if (schedule < DASH_SCHED_ASCENDING || schedule > DASH_SCHED_SYMMETRIC_SHIFT)
+    return DASH_ERR_INVALID_ARG;
+  if (deterministic != 0 && deterministic != 1) return DASH_ERR_INVALID_ARG;
+  if (!(scale > 0.f)) return DASH_ERR_INVALID_ARG;
+  if (!shape_ok(B, S, H, D)) return DASH_ERR_UNSUPPORTED;
+  for (const void* ptr : {q, k, v, o, dO, (const void*)lse, (const void*)dq, (const void*)dk,
+                          (const void*)dv})
+    if (!aligned16(ptr)) return DASH_ERR_INVALID_ARG;
+  const int n = S / dash::kTile;
+  dash::Schedule sc;
+  int rc = dash::build_schedule(mask, schedule, n, &sc);
+  if (rc) return (dash_status_t)rc;
+
+  // scratch layout: the backward workspace, then the schedule tables
+  const WsLayout wl = ws_layout(B, S, H, D);
+  const size_t t_off = wl.total;
+  const size_t t_task = round_up(t_off + sc.slot_off.size() * 4, 256);
+  const size_t t_ord = round_up(t_task + sc.tasks.size() * 4, 256);
+  const size_t t_cnt = round_up(t_ord + sc.ord.size() * 4, 256);
+  const size_t need = round_up(t_cnt + sc.cnt.size() * 4, 256);
+  if (need > kStaticScratchBytes) {
+    char buf[200];
+    snprintf(buf, sizeof(buf),
+             "dash_attn_bwd_static: this shape needs %zu bytes of scratch, more than the "
+             "%zu-byte static scratch; use dash_attn_bwd with a caller-allocated workspace",
+             need, kStaticScratchBytes);
+    g_last_error = buf;
+    return DASH_ERR_WORKSPACE_TOO_SMALL;
+  }
+  int dev = 0;
+  DASH_CUDA(cudaGetDevice(&dev));
+  unsigned char* ws = nullptr;
+  dash_status_t st = static_scratch(dev, &ws);
+  if (st != DASH_OK) return st;
+
+  // Tables are written for every call: the array keeps whatever the last call left.
+  DASH_CUDA(cudaMemcpyAsync(ws + t_off, sc.slot_off.data(), sc.slot_off.size() * 4,
+                            cudaMemcpyHostToDevice, stream));
+  DASH_CUDA(cudaMemcpyAsync(ws + t_task, sc.tasks.data(), sc.tasks.size() * 4,
+                            cudaMemcpyHostToDevice, stream));
+  DASH_CUDA(cudaMemcpyAsync(ws + t_ord, sc.ord.data(), sc.ord.size() * 4,
+                            cudaMemcpyHostToDevice, stream));
+  DASH_CUDA(cudaMemcpyAsync(ws + t_cnt, sc.cnt.data(), sc.cnt.size() * 4,
+                            cudaMemcpyHostToDevice, stream));
+
+  dash::BwdParams p;
+  p.q = (const __nv_bfloat16*)q;
+  p.k = (const __nv_bfloat16*)k;
+  p.v = (const __nv_bfloat16*)v;
+  p.o = (const __nv_bfloat16*)o;
+  p.dO = (const __nv_bfloat16*)dO;
+  p.lse = lse;
+  p.dq = (__nv_bfloat16*)dq;
+  p.dk = (__nv_bfloat16*)dk;
+  p.dv = (__nv_bfloat16*)dv;
+  p.ws_header = (int*)ws;
+  p.Dsum = (float*)(ws + wl.dsum);
+  p.dq_acc = (float*)(ws + wl.dq_acc);
+  p.sems = (int*)(ws + wl.sems);
+  p.slot_off = (const int32_t*)(ws + t_off);
+  p.tasks = (const int32_t*)(ws + t_task);
+  p.ord = (const int32_t*)(ws + t_ord);
+  p.cnt = (const int32_t*)(ws + t_cnt);
+  p.B = B;
+  p.S = S;
+  p.H = H;
+  p.D = D;
+  p.n = n;
+  p.num_slots = sc.num_slots;
+  p.num_units = B * H * sc.num_slots;
+  p.scale = scale;
+  p.scale_log2 = scale * dash::kLog2e;
+  p.causal = mask == DASH_MASK_CAUSAL;
+  p.deterministic = deterministic;
+  p.timeout_ns = g_timeout_ns;
+  p.ordinal_skew = g_ordinal_skew;
+  p.trace = nullptr;
+  p.num_sems = B * H * n;
+
+  if (!encoder()) {
+    g_last_error = "cuTensorMapEncodeTiled is not available from the driver";
+    return DASH_ERR_CUDA;
+  }
+  dash::tc::TmaMaps maps;
+  const int br = D == 64 ? dash::tc::Cfg<64>::BR : dash::tc::Cfg<128>::BR;
+  if (!map_bshd(&maps.q, q, B, S, H, D, br) || !map_bshd(&maps.dO, dO, B, S, H, D, br) ||
+      !map_bshd(&maps.k, k, B, S, H, D, dash::kTile) ||
+      !map_bshd(&maps.v, v, B, S, H, D, dash::kTile) ||
+      !map_acc(&maps.acc, p.dq_acc, (long long)B * H * S, D, br)) {
+    g_last_error = "cuTensorMapEncodeTiled rejected a tensor";
+    return DASH_ERR_CUDA;
+  }
+  const int threads = dash::tc::kThreads;
+  const size_t smem = D == 64 ? dash::tc::Smem<64>::ALLOC : dash::tc::Smem<128>::ALLOC;
+  void* kfn = D == 64 ? (void*)dash::tc::bwd_tc_kernel<64> : (void*)dash::tc::bwd_tc_kernel<128>;
+  DASH_CUDA(cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  int sms = 0;
+  DASH_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  int grid = sms;
+  if (grid > p.num_units) grid = p.num_units;
+  if (deterministic && !deadlock_free(mask, schedule, n, B * H, grid))
+    return DASH_ERR_DEADLOCK_RISK;
+
+  dash::bwd_preprocess_kernel<<<sms * 4, 256, 0, stream>>>(p);
+  DASH_CUDA(cudaGetLastError());
+  void* args[] = {&p, &maps};
+  if (deterministic) {
+    DASH_CUDA(cudaLaunchCooperativeKernel(kfn, dim3(grid), dim3(threads), args, smem, stream));
+  } else {
+    DASH_CUDA(cudaLaunchKernel(kfn, dim3(grid), dim3(threads), args, smem, stream));
+  }
+  dash::dq_convert_kernel<<<sms * 4, 256, 0, stream>>>(p);
+  DASH_CUDA(cudaGetLastError());
+  if (status_out) {
+    copy_status_kernel<<<1, 1, 0, stream>>>(p.ws_header, status_out);
+    DASH_CUDA(cudaGetLastError());
+  }
+  return DASH_OK;
+}

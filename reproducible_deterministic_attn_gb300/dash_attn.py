@@ -43,6 +43,9 @@ _SIGNATURES = {
     "dash_attn_bwd": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_size,
                                _c_int, _c_int, _c_int, _c_int, _c_float, _c_int, _c_int, _c_int,
                                _vp]),
+    "dash_attn_bwd_static": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                      _c_int, _c_int, _c_int, _c_int, _c_float, _c_int, _c_int,
+                                      _c_int, _vp]),
     "dash_attn_get_status": (_c_int, [_vp, _vp]),
     "dash_status_string": (ctypes.c_char_p, [_c_int]),
     "dash_last_error": (ctypes.c_char_p, []),
@@ -121,6 +124,20 @@ def dash_attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, workspace, scale: float, mask
                                 dv.data_ptr(), workspace.data_ptr(), workspace.numel(),
                                 B, S, H, D, float(scale), int(mask), int(schedule),
                                 int(deterministic), _stream(q, stream)), "dash_attn_bwd")
+
+
+def dash_attn_bwd_static(q, k, v, o, dO, lse, dq, dk, dv, scale: float, mask: int,
+                         schedule: int, deterministic: int, status_out=None, stream=None) -> None:
+    """dash_attn_bwd without a workspace: the scratch is the library's static device array
+    (no device allocation). status_out: optional int32 CUDA tensor for the status word."""
+    B, S, H, D = _shape(q)
+    _check(load().dash_attn_bwd_static(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                       dO.data_ptr(), lse.data_ptr(), dq.data_ptr(),
+                                       dk.data_ptr(), dv.data_ptr(),
+                                       None if status_out is None else status_out.data_ptr(),
+                                       B, S, H, D, float(scale), int(mask), int(schedule),
+                                       int(deterministic), _stream(q, stream)),
+           "dash_attn_bwd_static")
 
 
 def dash_attn_get_status(workspace, stream=None) -> int:
