@@ -66,6 +66,22 @@ def input_bytes(w) -> int:
     return 5 * t + w["B"] * w["H"] * w["S"] * 4
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest of every rank's value (the timing rule: max over ranks)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: the FLOPs of all ranks over the slowest rank's step time."""
+    return flops_per_rank * world / (ms_per_step / 1e3) / 1e12
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -97,6 +113,15 @@ class ClockSampler:
                                          text=True)
         except Exception:
             self.proc = None
+        self.first = ""
+        if self.proc is not None:
+            # nvidia-smi's start-up must not overlap the timed region: wait for its first
+            # sample (it is kept and counted with the rest)
+            import select
+
+            ready, _, _ = select.select([self.proc.stdout], [], [], 10.0)
+            if ready:
+                self.first = self.proc.stdout.readline()
 
     def stop(self):
         if self.proc is None:
@@ -107,6 +132,7 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
             out = ""
+        out = self.first + out
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.strip().splitlines():
@@ -295,12 +321,9 @@ def run_gpu(args, w, rank, world, local_rank):
             tot, cnt = da.dash_profile_read()
             da.dash_profile_enable(False)
             main = tot / max(cnt, 1)
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms / n_steps, main
+        return max_over_ranks(ms, world, dev) / n_steps, main
 
+    sampler = ClockSampler(local_rank) if rank == 0 else None
     warm = args.warmup if args.warmup is not None else 3
     for _ in range(warm):
         step()
@@ -316,15 +339,13 @@ def run_gpu(args, w, rank, world, local_rank):
         one = time.perf_counter() - t0
         steps = int(min(500, max(10, math.ceil(2.0 / max(one, 1e-4)))))
 
-    sampler = ClockSampler(local_rank) if rank == 0 else None
     ms_step, main_ms = timed(steps, profile=True)
     clocks = sampler.stop() if sampler else None
     st = da.dash_attn_get_status(ws)
     if st != da.DASH_OK:
         raise da.DashError(st, "timed backward")
 
-    total_flops = bwd_flops(w) * world
-    value = total_flops / (ms_step / 1e3) / 1e12
+    value = job_tflops(bwd_flops(w), world, ms_step)
     peak_tf, _, peak_kind = load_peaks()
 
     # the other variants of the same run: non-deterministic (speed reference) and the
@@ -338,7 +359,7 @@ def run_gpu(args, w, rank, world, local_rank):
         for _ in range(2):
             step(det, s)
         ms_s, _ = timed(n_side, det, s)
-        side[name] = bwd_flops(w) * world / (ms_s / 1e3) / 1e12
+        side[name] = job_tflops(bwd_flops(w), world, ms_s)
 
     # end to end through the public API with host buffers: pinned H2D of this step's
     # inputs, the backward, D2H of dQ/dK/dV, every step
@@ -369,11 +390,7 @@ def run_gpu(args, w, rank, world, local_rank):
         e2e_step()
     e1.record()
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / n_e2e
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world, dev)
 
     if rank != 0:
         return
@@ -397,7 +414,7 @@ def run_gpu(args, w, rank, world, local_rank):
                      "kernel": "bwd main (compute + ordered dQ reduction)",
                      "peak_kind": f"{peak_kind} bf16 dense (burst)"},
         "cpu_baseline": cpu,
-        "e2e": {"value": bwd_flops(w) * world / (e2e_ms / 1e3) / 1e12, "unit": "TFLOPS",
+        "e2e": {"value": job_tflops(bwd_flops(w), world, e2e_ms), "unit": "TFLOPS",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * steps,
         "clocks": clocks,
