@@ -68,7 +68,8 @@ enum : int {
   TR_PROD_STAGE_EMPTY = 0, TR_PROD_KV_EMPTY, TR_MMA_KV_FULL, TR_MMA_STAGE_FULL, TR_MMA_S_EMPTY,
   TR_MMA_DP_EMPTY, TR_MMA_P_FULL, TR_MMA_ACC_EMPTY, TR_MMA_DS_FULL, TR_MMA_DQ_EMPTY,
   TR_SG_S_FULL, TR_SG_P_EMPTY, TR_SG_DP_FULL, TR_SG_DS_EMPTY, TR_DQ_FULL, TR_DQ_SEM,
-  TR_DQ_REDUCE, TR_DQ_ACC_FULL, TR_DQ_STAGE, TR_TOTAL, TR_SITES = 24
+  TR_DQ_REDUCE, TR_DQ_ACC_FULL, TR_DQ_STAGE, TR_TOTAL, TR_ISSUE_S, TR_ISSUE_DP, TR_ISSUE_DV,
+  TR_ISSUE_DKDQ, TR_SITES = 24
 };
 
 __device__ __forceinline__ long long global_timer_ns() {

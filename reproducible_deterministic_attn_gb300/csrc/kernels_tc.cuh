@@ -85,8 +85,8 @@ struct Smem {
 
 // Barrier indices.
 enum {
-  B_KV_FULL = 0, B_KV_EMPTY, B_S_FULL, B_S_EMPTY, B_DP_FULL, B_DP_EMPTY, B_P_FULL, B_P_EMPTY,
-  B_DS_FULL, B_DS_EMPTY, B_DQ_FULL, B_DQ_EMPTY, B_ACC_FULL, B_ACC_EMPTY, B_DRAIN,
+  B_KV_FULL = 0, B_KV_EMPTY, B_S_FULL, B_S_EMPTY, B_DP_FULL, B_DP_EMPTY, B_P_EMPTY,
+  B_DS_FULL, B_DS_EMPTY, B_DQ_FULL, B_ACC_FULL, B_ACC_EMPTY, B_DRAIN,
   B_STG_FULL, B_STG_EMPTY, B_DRAIN2,
   B_STAGE_FULL,                     // + stage
   B_STAGE_EMPTY = B_STAGE_FULL + kMaxStages,
@@ -206,12 +206,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(bars + B_S_EMPTY, 8);
     ptx::mbar_init(bars + B_DP_FULL, 1);
     ptx::mbar_init(bars + B_DP_EMPTY, 8);
-    ptx::mbar_init(bars + B_P_FULL, 8);
     ptx::mbar_init(bars + B_P_EMPTY, 1);
-    ptx::mbar_init(bars + B_DS_FULL, 8);
+    ptx::mbar_init(bars + B_DS_FULL, 8 + 4);   // 8 softmax-gradient warps + 4 dQ warps
     ptx::mbar_init(bars + B_DS_EMPTY, 1);
     ptx::mbar_init(bars + B_DQ_FULL, 1);
-    ptx::mbar_init(bars + B_DQ_EMPTY, 4);
     ptx::mbar_init(bars + B_ACC_FULL, 1);
     ptx::mbar_init(bars + B_ACC_EMPTY, 4);
     ptx::mbar_init(bars + B_DRAIN, 1);
@@ -335,52 +333,55 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t dQ_k = stage_lo(x, L::Q_IN_STAGE, 16);
           const uint32_t ddO_k = stage_lo(x, L::DO_IN_STAGE, 16);
           // S^T = K Q^T: K-major A (128 kv rows), K-major B (BR rows)
+          t0 = tr.t0();
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks)
             ptx::mma_lo(tmem + C::T_S, dK_k + kstep(ks, kTile), dQ_k + kstep(ks, BR), ID_S, ks > 0);
           ptx::mma_commit(bars + B_S_FULL);
+          tr.add(TR_ISSUE_S, t0);
           t0 = tr.t0();
           if (x.it > 0) ok = ptx::mbar_wait(bars + B_DP_EMPTY, (x.it - 1) & 1, abort_flag, tmo);
           tr.add(TR_MMA_DP_EMPTY, t0);
           if (!ok) break;
           ptx::tc_fence_after();
           // dP^T = V dO^T
+          t0 = tr.t0();
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks)
             ptx::mma_lo(tmem + C::T_DP, dV_k + kstep(ks, kTile), ddO_k + kstep(ks, BR), ID_S, ks > 0);
           ptx::mma_commit(bars + B_DP_FULL);
+          tr.add(TR_ISSUE_DP, t0);
         }
       } else {
         while (ok && sw.next(x)) {
           const uint32_t dQ_mn = stage_lo(x, L::Q_IN_STAGE, BR * 128);
           const uint32_t ddO_mn = stage_lo(x, L::DO_IN_STAGE, BR * 128);
-          // dV += P^T dO: A = P^T (K-major, 128 kv rows x BR), B = dO (MN-major over D).
-          // The first sub-tile of a KV tile overwrites the accumulators, which the
-          // previous tile's epilogue must have read out.
+          // One check covers the whole group (the tensor pipe queues about one MMA, so every
+          // check on this thread idles it): a completed dS(t) phase means every
+          // softmax-gradient warp has also published P(t) (P is written first), and the dQ
+          // warps' arrivals on the same barrier mean dQ(t-1) has left TMEM.
           long long t0 = tr.t0();
-          ok = ptx::mbar_wait(bars + B_P_FULL, x.it & 1, abort_flag, tmo);
-          tr.add(TR_MMA_P_FULL, t0);
+          ok = ptx::mbar_wait(bars + B_DS_FULL, x.it & 1, abort_flag, tmo);
+          tr.add(TR_MMA_DS_FULL, t0);
           t0 = tr.t0();
+          // The first sub-tile of a KV tile overwrites the dV/dK accumulators, which the
+          // previous tile's epilogue must have read out.
           if (ok && x.first && x.tile > 0)
             ok = ptx::mbar_wait(bars + B_ACC_EMPTY, (x.tile - 1) & 1, abort_flag, tmo);
           tr.add(TR_MMA_ACC_EMPTY, t0);
           if (!ok) break;
           ptx::tc_fence_after();
           const uint32_t acc0 = x.first ? 0u : 1u;
+          // dV += P^T dO: A = P^T (K-major, 128 kv rows x BR), B = dO (MN-major over D)
+          t0 = tr.t0();
 #pragma unroll
           for (int ks = 0; ks < BR / 16; ++ks)
             ptx::mma_lo(tmem + C::T_DV, dP_k + kstep(ks, kTile), ddO_mn + ks * MN_STEP, ID_ACC,
                         ks > 0 ? 1u : acc0);
           ptx::mma_commit(bars + B_P_EMPTY);
+          tr.add(TR_ISSUE_DV, t0);
           // dK += dS^T Q, then the dQ partial over the 128 kv rows
           t0 = tr.t0();
-          ok = ptx::mbar_wait(bars + B_DS_FULL, x.it & 1, abort_flag, tmo);
-          tr.add(TR_MMA_DS_FULL, t0);
-          t0 = tr.t0();
-          if (ok && x.it > 0) ok = ptx::mbar_wait(bars + B_DQ_EMPTY, (x.it - 1) & 1, abort_flag, tmo);
-          tr.add(TR_MMA_DQ_EMPTY, t0);
-          if (!ok) break;
-          ptx::tc_fence_after();
 #pragma unroll
           for (int ks = 0; ks < BR / 16; ++ks)
             ptx::mma_lo(tmem + C::T_DK, dS_k + kstep(ks, kTile), dQ_mn + ks * MN_STEP, ID_ACC,
@@ -397,6 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ptx::mma_commit(bars + B_DS_EMPTY);
           ptx::mma_commit(bars + B_DQ_FULL);
+          tr.add(TR_ISSUE_DKDQ, t0);
           // the stage's Q/dO were last read by dK/dV here; the S^T/dP^T reads of this stage
           // finished before the softmax-gradient warps released P and dS
           ptx::mma_commit(bars + B_STAGE_EMPTY + x.it % kStages);
@@ -466,9 +468,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ptx::pack_bf16(pv[8 * k + 4], pv[8 * k + 5]),
                             ptx::pack_bf16(pv[8 * k + 6], pv[8 * k + 7]));
         }
+        // (P is published together with dS below: the dV/dK/dQ issuer waits for both)
         ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bars + B_P_FULL);
         t0 = trs.t0();
         ok = ptx::warp_wait(bars + B_DP_FULL, it & 1, abort_flag, tmo);
         trs.add(TR_SG_DP_FULL, t0);
@@ -561,6 +562,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = ((uint32_t)(quarter * 32) << 16);
     const uint32_t stg = ptx::smem_u32(sm + L::STG_OFF);
     const Trace& trq = (warp == 12 && lane == 0) ? tr : tr_none;
+    // nothing to read out before the first sub-tile: pre-arm its dS/dQ hand-off
+    if (lane == 0) ptx::mbar_arrive(bars + B_DS_FULL);
     Walk w(p);
     int it = 0, tl = 0;
     bool ok = true;
@@ -583,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bars + B_DQ_EMPTY);
+        if (lane == 0) ptx::mbar_arrive(bars + B_DS_FULL);   // dQ(it) has left TMEM
         long long t0 = trq.t0();
         if (it > 0) ok = ptx::warp_wait(bars + B_STG_EMPTY, (it - 1) & 1, abort_flag, tmo);
         trq.add(TR_DQ_STAGE, t0);
