@@ -19,6 +19,7 @@ enum : int {
 };
 constexpr size_t kWsHeaderBytes = 256;
 constexpr int kStatusSyncTimeout = 5;
+constexpr int kStatusSmemLayout = 4;   // reported as DASH_ERR_CUDA: unusable shared-memory base
 
 struct FwdParams {
   const __nv_bfloat16* q;

@@ -17,6 +17,7 @@
 #include "bwd_aux.cuh"
 #include "fwd_simt.cuh"
 #include "kernels_tc.cuh"
+#include "kernels_tc128.cuh"
 #include "sched.h"
 
 namespace {
@@ -77,6 +78,30 @@ dash_status_t get_tables(int dev, int mask, int sched, int n, DeviceTables* out)
   g_tables[key] = t;
   *out = t;
   return DASH_OK;
+}
+
+// The backward main kernel for a head dimension: D = 64 runs the general kernel with
+// 128-row Q tiles; D = 128 runs the kernel that keeps P in TMEM (whole 128 x 128 tasks).
+struct MainKernel {
+  void* fn;
+  size_t smem;
+  int br;   // Q/dO rows per TMA box and dQ accumulator box height
+};
+MainKernel main_kernel(int D) {
+  if (D == 64)
+    return {(void*)dash::tc::bwd_tc_kernel<64>, (size_t)dash::tc::Smem<64>::ALLOC,
+            dash::tc::Cfg<64>::BR};
+  return {(void*)dash::tc::bwd_tc128_kernel, (size_t)dash::tc::L128::ALLOC, dash::kTile};
+}
+
+// The D = 128 kernel moves registers between warpgroups (setmaxnreg); its split adds up to
+// exactly the per-thread count it is launched with, so any other count is refused here
+// (a larger request than the pool holds would never be granted).
+bool launch_regs_ok(const MainKernel& mk) {
+  if (mk.fn != (void*)dash::tc::bwd_tc128_kernel) return true;
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, mk.fn) != cudaSuccess) return false;
+  return fa.numRegs == dash::tc::L128::REGS_LAUNCH;
 }
 
 // True when the schedule's waits are acyclic for `heads` heads on `grid` persistent CTAs.
@@ -334,7 +359,8 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
     return DASH_ERR_CUDA;
   }
   dash::tc::TmaMaps maps;
-  const int br = D == 64 ? dash::tc::Cfg<64>::BR : dash::tc::Cfg<128>::BR;
+  const MainKernel mk = main_kernel(D);
+  const int br = mk.br;
   if (!map_bshd(&maps.q, q, B, S, H, D, br) || !map_bshd(&maps.dO, dO, B, S, H, D, br) ||
       !map_bshd(&maps.k, k, B, S, H, D, dash::kTile) ||
       !map_bshd(&maps.v, v, B, S, H, D, dash::kTile) ||
@@ -343,8 +369,12 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
     return DASH_ERR_CUDA;
   }
   const int threads = dash::tc::kThreads;
-  const size_t smem = D == 64 ? dash::tc::Smem<64>::ALLOC : dash::tc::Smem<128>::ALLOC;
-  void* kfn = D == 64 ? (void*)dash::tc::bwd_tc_kernel<64> : (void*)dash::tc::bwd_tc_kernel<128>;
+  const size_t smem = mk.smem;
+  void* kfn = mk.fn;
+  if (!launch_regs_ok(mk)) {
+    g_last_error = "backward kernel was not built with the register count its warp roles share";
+    return DASH_ERR_CUDA;
+  }
   DASH_CUDA(cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   int per_sm = 0, sms = 0;
   DASH_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, threads, smem));
@@ -379,6 +409,10 @@ dash_status_t dash_attn_get_status(const void* workspace, cudaStream_t stream) {
   DASH_CUDA(cudaStreamSynchronize(stream));
   int words[8];
   DASH_CUDA(cudaMemcpy(words, workspace, sizeof(words), cudaMemcpyDeviceToHost));
+  if (words[dash::WS_STATUS] == dash::kStatusSmemLayout) {
+    g_last_error = "the backward kernel found its shared-memory base off a 1024-byte boundary";
+    return DASH_ERR_CUDA;
+  }
   if (words[dash::WS_STATUS] == dash::kStatusSyncTimeout && words[dash::WS_BH] < 0) {
     char buf[160];
     snprintf(buf, sizeof(buf), "a pipeline wait inside CTA %d timed out", words[dash::WS_QTILE]);
@@ -593,7 +627,8 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
     return DASH_ERR_CUDA;
   }
   dash::tc::TmaMaps maps;
-  const int br = D == 64 ? dash::tc::Cfg<64>::BR : dash::tc::Cfg<128>::BR;
+  const MainKernel mk = main_kernel(D);
+  const int br = mk.br;
   if (!map_bshd(&maps.q, q, B, S, H, D, br) || !map_bshd(&maps.dO, dO, B, S, H, D, br) ||
       !map_bshd(&maps.k, k, B, S, H, D, dash::kTile) ||
       !map_bshd(&maps.v, v, B, S, H, D, dash::kTile) ||
@@ -602,8 +637,12 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
     return DASH_ERR_CUDA;
   }
   const int threads = dash::tc::kThreads;
-  const size_t smem = D == 64 ? dash::tc::Smem<64>::ALLOC : dash::tc::Smem<128>::ALLOC;
-  void* kfn = D == 64 ? (void*)dash::tc::bwd_tc_kernel<64> : (void*)dash::tc::bwd_tc_kernel<128>;
+  const size_t smem = mk.smem;
+  void* kfn = mk.fn;
+  if (!launch_regs_ok(mk)) {
+    g_last_error = "backward kernel was not built with the register count its warp roles share";
+    return DASH_ERR_CUDA;
+  }
   DASH_CUDA(cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   int sms = 0;
   DASH_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));

@@ -24,8 +24,9 @@ def _built():
     ensure_built()
 
 
-def test_sync_timeout_is_reported_and_context_survives():
-    B, S, H, D = 1, 512, 2, 64
+@pytest.mark.parametrize("D", [64, 128])
+def test_sync_timeout_is_reported_and_context_survives(D):
+    B, S, H = 1, 512, 2
     x = make_inputs(B, S, H, D, 3)
     q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
     scale = 1 / math.sqrt(D)
