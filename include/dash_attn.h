@@ -79,8 +79,8 @@ dash_status_t dash_attn_fwd(const void* q, const void* k, const void* v, void* o
 
 /*
  * Bytes of scratch dash_attn_bwd needs for this shape: a status header, D = rowsum(dO*O)
- * (fp32 [B,H,S]), the fp32 dQ accumulator [B,H,S,D] and one int32 semaphore per dQ block
- * [B,H,S/128]. Returns 0 for an unsupported shape.
+ * and -LSE*log2(e) (two fp32 [B,H,S] arrays), the fp32 dQ accumulator [B,H,S,D] and one
+ * int32 semaphore per dQ block [B,H,S/128]. Returns 0 for an unsupported shape.
  */
 size_t dash_attn_bwd_workspace_size(int B, int S, int H, int D);
 

@@ -9,8 +9,8 @@
 namespace dash {
 
 // ---------------------------------------------------------------------------------
-// Preprocess: D = rowsum(dO * O) (one warp per row, fixed shuffle tree), clear the
-// semaphores, the status header and the fp32 dQ accumulator.
+// Preprocess: D = rowsum(dO * O) (one warp per row, fixed shuffle tree) and -LSE*log2(e)
+// per row, clear the semaphores, the status header and the fp32 dQ accumulator.
 // ---------------------------------------------------------------------------------
 __global__ void bwd_preprocess_kernel(BwdParams p) {
   const int lane = threadIdx.x & 31;
@@ -27,7 +27,10 @@ __global__ void bwd_preprocess_kernel(BwdParams p) {
     for (int c = lane; c < p.D; c += 32) acc += bf(p.dO[off + c]) * bf(p.o[off + c]);
 #pragma unroll
     for (int w = 16; w >= 1; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
-    if (lane == 0) p.Dsum[r] = acc;
+    if (lane == 0) {
+      p.Dsum[r] = acc;
+      p.nlse2[r] = -p.lse[r] * kLog2e;
+    }
   }
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long nth = (long long)gridDim.x * blockDim.x;

@@ -44,6 +44,7 @@ struct BwdParams {
   __nv_bfloat16* dv;
   int* ws_header;            // status words
   float* Dsum;               // [B, H, S] rowsum(dO * O)
+  float* nlse2;              // [B, H, S] -LSE * log2(e) (the exponent offset of P in base 2)
   float* dq_acc;             // [B, H, S, D] fp32
   int* sems;                 // [B, H, n]: one per 128-row dQ block
   int num_sems;
@@ -103,14 +104,18 @@ __device__ __noinline__ bool wait_turn(const int* sem, int target, int* ws, long
   int seen = ld_acquire_gpu(sem);
   if (seen == target) return true;
   const long long t0 = global_timer_ns();
-  // iteration cap as a second bound, independent of the timer
+  // The hand-off latency adds to every step of the serial order, so the semaphore is
+  // polled back to back (one L2 round trip per poll); the failure flag and the timer are
+  // looked at every 32nd poll. The iteration cap is a second bound, independent of the
+  // timer (a poll takes well over 16 ns).
   const long long max_iter = timeout_ns / 16 + (1ll << 20);
-  for (long long it = 0; it < max_iter; ++it) {
-    __nanosleep(40);
+  for (long long it = 1; it <= max_iter; ++it) {
     seen = ld_acquire_gpu(sem);
     if (seen == target) return true;
-    if (ld_relaxed_gpu(ws + WS_STATUS) != 0) return false;
-    if (global_timer_ns() - t0 > timeout_ns) break;
+    if ((it & 31) == 0) {
+      if (ld_relaxed_gpu(ws + WS_STATUS) != 0) return false;
+      if (global_timer_ns() - t0 > timeout_ns) break;
+    }
   }
   if (atomicCAS(ws + WS_STATUS, 0, kStatusSyncTimeout) == 0) {
     ws[WS_BH] = bh;

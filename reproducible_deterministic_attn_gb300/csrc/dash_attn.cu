@@ -199,14 +199,15 @@ bool map_acc(CUtensorMap* m, float* ptr, long long rows_total, int D, int rows) 
 }
 
 struct WsLayout {
-  size_t dsum, dq_acc, sems, total;
+  size_t dsum, nlse2, dq_acc, sems, total;
 };
 
 WsLayout ws_layout(int B, int S, int H, int D) {
   WsLayout w;
   const size_t rows = (size_t)B * H * S;
   w.dsum = dash::kWsHeaderBytes;
-  w.dq_acc = round_up(w.dsum + rows * sizeof(float), 256);
+  w.nlse2 = round_up(w.dsum + rows * sizeof(float), 256);
+  w.dq_acc = round_up(w.nlse2 + rows * sizeof(float), 256);
   w.sems = round_up(w.dq_acc + rows * D * sizeof(float), 256);
   w.total = round_up(w.sems + (size_t)B * H * (S / dash::kTile) * sizeof(int), 256);
   return w;
@@ -329,6 +330,7 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
   p.dv = (__nv_bfloat16*)dv;
   p.ws_header = (int*)ws;
   p.Dsum = (float*)(ws + wl.dsum);
+  p.nlse2 = (float*)(ws + wl.nlse2);
   p.dq_acc = (float*)(ws + wl.dq_acc);
   p.sems = (int*)(ws + wl.sems);
   p.slot_off = tb.slot_off;
@@ -600,6 +602,7 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
   p.dv = (__nv_bfloat16*)dv;
   p.ws_header = (int*)ws;
   p.Dsum = (float*)(ws + wl.dsum);
+  p.nlse2 = (float*)(ws + wl.nlse2);
   p.dq_acc = (float*)(ws + wl.dq_acc);
   p.sems = (int*)(ws + wl.sems);
   p.slot_off = (const int32_t*)(ws + t_off);

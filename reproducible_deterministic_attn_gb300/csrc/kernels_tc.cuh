@@ -1,19 +1,20 @@
-// Backward main kernel on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+// Backward main kernel on the 5th-generation tensor cores (tcgen05 + TMEM + TMA), head
+// dimension 64 (head dimension 128 runs the kernel of kernels_tc128.cuh, which reuses the
+// walk, trace and TMA-map definitions here).
 //
 // One persistent CTA per SM. A unit is one schedule chain (slot) of one (batch, head);
 // CTA c runs units c, c + grid, ... Each schedule task (KV_i, Q_j) covers a 128 x 128
 // tile of the score matrix; KV_i's K and V tiles stay in shared memory for all its
 // tasks and its dK/dV accumulate in TMEM (DASH's "each KV tile's dK/dV stay on one SM").
 //
-// Per Q sub-tile (BR query rows; BR = 128 for D = 64, 64 for D = 128):
+// Per task (BR = 128 query rows, one sub-tile; the walk supports SUB > 1 sub-tiles):
 //   S^T  = K Q^T          (M = 128 kv, N = BR, K = D)      -> TMEM
 //   dP^T = V dO^T         (M = 128 kv, N = BR, K = D)      -> TMEM
 //   P^T  = exp2(S^T * scale*log2e - LSE*log2e)            softmax-gradient warps -> smem bf16
 //   dS^T = P^T * (dP^T - Dsum)                            softmax-gradient warps -> smem bf16
 //   dV  += P^T dO         (M = 128 kv, N = D, K = BR)
 //   dK  += dS^T Q         (M = 128 kv, N = D, K = BR)
-//   D = 64 : dQ   = dS K    (M = 128 q, N = 64, K = 128 kv)   TMEM lanes = q rows
-//   D = 128: dQ^T = K^T dS^T (M = 128 d, N = 64, K = 128 kv)  TMEM lanes = d columns
+//   dQ   = dS K           (M = 128 q, N = 64, K = 128 kv)   TMEM lanes = q rows
 //   then the dQ partial is staged in smem and added into the fp32 dQ accumulator with a
 //   TMA bulk reduce-add: deterministic mode waits on the block's L2 semaphore for its
 //   ordinal first and releases ordinal + 1 after the add has completed (the pages' fixed
@@ -42,13 +43,6 @@ struct Cfg<64> {
   static constexpr int T_S = 0, T_DP = 128, T_DV = 256, T_DK = 320, T_DQ = 384;
 };
 
-template <>
-struct Cfg<128> {
-  static constexpr int BR = 64;
-  static constexpr int SUB = 2;
-  static constexpr int STAGES = 3;
-  static constexpr int T_S = 0, T_DP = 64, T_DV = 128, T_DK = 256, T_DQ = 384;
-};
 
 constexpr int kThreads = 512;
 constexpr int kMaxStages = 3;
@@ -386,16 +380,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int ks = 0; ks < BR / 16; ++ks)
             ptx::mma_lo(tmem + C::T_DK, dS_k + kstep(ks, kTile), dQ_mn + ks * MN_STEP, ID_ACC,
                         ks > 0 ? 1u : acc0);
+          // dQ = dS K: A = dS (MN-major view of the dS^T tile), B = K (MN-major, 64 d)
 #pragma unroll
-          for (int ks = 0; ks < kTile / 16; ++ks) {
-            if (D == 64) {
-              // dQ = dS K: A = dS (MN-major view of the dS^T tile), B = K (MN-major, 64 d)
-              ptx::mma_lo(tmem + C::T_DQ, dS_mn + ks * MN_STEP, dK_mn + ks * MN_STEP, ID_DQ, ks > 0);
-            } else {
-              // dQ^T = K^T dS^T: A = K^T (MN-major over 128 d), B = dS^T (MN-major, 64 q)
-              ptx::mma_lo(tmem + C::T_DQ, dK_mn + ks * MN_STEP, dS_mn + ks * MN_STEP, ID_DQ, ks > 0);
-            }
-          }
+          for (int ks = 0; ks < kTile / 16; ++ks)
+            ptx::mma_lo(tmem + C::T_DQ, dS_mn + ks * MN_STEP, dK_mn + ks * MN_STEP, ID_DQ, ks > 0);
           ptx::mma_commit(bars + B_DS_EMPTY);
           ptx::mma_commit(bars + B_DQ_FULL);
           tr.add(TR_ISSUE_DKDQ, t0);
@@ -591,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it > 0) ok = ptx::warp_wait(bars + B_STG_EMPTY, (it - 1) & 1, abort_flag, tmo);
         trq.add(TR_DQ_STAGE, t0);
         if (!ok) break;
-        if (D == 64) {
+        {
           // lanes = q rows; 64 d values; boxes of 32 fp32 columns x BR rows
           const int row = quarter * 32 + lane;
 #pragma unroll
@@ -600,14 +588,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t a = stg + bx * (BR * 128) + row * 128 + ((ch ^ (row & 7)) << 4);
             ptx::st_shared_v4(a, __float_as_uint(v[4 * c]), __float_as_uint(v[4 * c + 1]),
                               __float_as_uint(v[4 * c + 2]), __float_as_uint(v[4 * c + 3]));
-          }
-        } else {
-          // lanes = d (= 32 * quarter + lane); 64 q values; box = quarter
-#pragma unroll
-          for (int q = 0; q < 64; ++q) {
-            const uint32_t a = stg + quarter * (BR * 128) + q * 128 +
-                               ((((lane >> 2) ^ (q & 7))) << 4) + (lane & 3) * 4;
-            ptx::st_shared_f32(a, v[q]);
           }
         }
         ptx::fence_proxy_async_smem();

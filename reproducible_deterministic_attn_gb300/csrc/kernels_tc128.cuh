@@ -5,15 +5,17 @@
 //
 //   S^T  = K Q^T        M = 128 kv, N = 128 q, K = 128 d     TMEM cols [0, 128)
 //   dP^T = V dO^T       M = 128 kv, N = 128 q, K = 128 d     TMEM cols [128, 256)
-//   P^T  = exp2(S^T * scale*log2e - LSE*log2e), packed to bf16 pairs and written back
-//          into the S^T columns it came from (half h of the q columns -> cols 64h..64h+31)
-//   dS^T = P^T * (dP^T - Dsum)                               smem bf16 [kv][q]
-//   dV  += P^T dO       A = P^T read from TMEM, B = dO       TMEM cols [256, 384)
+//   P^T  = exp2(S^T * scale*log2e - LSE*log2e)               smem bf16 [kv][q]
+//   dS^T = P^T * (dP^T - Dsum)                               the same buffer, once dV
+//                                                            has read P^T
+//   dV  += P^T dO                                            TMEM cols [256, 384)
 //   dQ^T = K^T dS^T     M = 128 d, N = 128 q, K = 128 kv     into the dP^T columns
 //   dK  += dS^T Q                                            TMEM cols [384, 512)
 //
 // Every MMA is 128 x 128 x 128, so the tensor pipe reads at most 8 KB of shared memory
-// per 64-cycle K step, and dV's A operand does not touch shared memory at all. dQ^T
+// per 64-cycle K step. The S^T columns are handed back as soon as the softmax-gradient
+// warps have loaded them, so S^T of the next task runs while P^T of this one is being
+// computed (exp2 on 16K elements is the longest single step of a task). dQ^T
 // reuses the dP^T columns once the softmax-gradient warps have read them, so the next
 // dP^T waits for the dQ read-out: the read-out warps load all 128 columns into registers
 // (their warpgroup takes registers from the single-thread roles' warpgroup), hand the
@@ -22,8 +24,8 @@
 // of one row: a full 128-byte line). In deterministic mode the adds of a 128-row block
 // wait for the block's turn and the turn is handed on after they have been performed.
 //
-// Shared memory (1024-aligned base, checked): K, V, Q x 2, dO x 2, dS^T, LSE/Dsum per Q
-// buffer, barriers, trace: 231,936 bytes.
+// Shared memory (1024-aligned base, checked): K, V, Q x 2, dO x 2, P^T/dS^T, -LSE*log2e
+// and Dsum per Q buffer, barriers, trace: 231,936 bytes.
 //
 // Warp roles (512 threads): 0 = TMA producer, 1 = S^T/dP^T issuer, 3 = dV/dQ^T/dK issuer,
 // 2 = idle, 4..11 = softmax-gradient (quarter = TMEM lanes, half = 64 q columns),
@@ -42,8 +44,8 @@ struct L128 {
   static constexpr int V_OFF = K_OFF + TILE_BYTES;
   static constexpr int Q_OFF = V_OFF + TILE_BYTES;            // two Q buffers
   static constexpr int DO_OFF = Q_OFF + 2 * TILE_BYTES;       // two dO buffers
-  static constexpr int DS_OFF = DO_OFF + 2 * TILE_BYTES;      // dS^T [kv][q]
-  static constexpr int LD_OFF = DS_OFF + TILE_BYTES;          // per Q buffer: LSE, Dsum
+  static constexpr int PS_OFF = DO_OFF + 2 * TILE_BYTES;      // P^T, then dS^T [kv][q]
+  static constexpr int LD_OFF = PS_OFF + TILE_BYTES;          // per Q buffer: -LSE*log2e, Dsum
   static constexpr int LD_BYTES = 2 * kTile * 4;
   static constexpr int BAR_OFF = LD_OFF + 2 * LD_BYTES;
   static constexpr int TRACE_OFF = BAR_OFF + 320;
@@ -59,16 +61,37 @@ struct L128 {
 
 enum {
   E_KV_FULL = 0, E_KV_EMPTY, E_Q_FULL, E_Q_EMPTY = E_Q_FULL + 2, E_DO_FULL = E_Q_EMPTY + 2,
-  E_DO_EMPTY = E_DO_FULL + 2, E_S_FULL = E_DO_EMPTY + 2, E_P_FULL, E_P_EMPTY, E_DP_FULL,
+  E_DO_EMPTY = E_DO_FULL + 2, E_S_FULL = E_DO_EMPTY + 2, E_S_EMPTY, E_P_FULL, E_P_EMPTY,
+  E_DP_FULL,
   E_DS_FULL, E_DS_EMPTY, E_DQ_FULL, E_DQ_EMPTY, E_ACC_FULL, E_ACC_EMPTY, E_DRAIN, E_DRAIN2,
   E_TURN, E_REDS, E_COUNT
 };
 static_assert(8 * E_COUNT + 8 <= 320, "barrier area");
 
-// TMEM column of K step ks (16 q values) of the packed P^T operand.
-__device__ __forceinline__ uint32_t p_col(int ks) {
-  return (uint32_t)(ks < 4 ? ks * 8 : 64 + (ks - 4) * 8);
+// 2^x on the FMA pipe, for x <= ~0 (P = 2^x with x = S*scale*log2e - LSE*log2e).
+// Range reduction x = n + f with n = round(x) (adding and subtracting 1.5 * 2^23 leaves
+// round-to-nearest(x) in the low mantissa bits of the sum), f in [-1/2, 1/2]; 2^f from a
+// cubic fitted for minimax relative error on that interval (fit_exp2_poly.py; max relative
+// error 7.5e-5, a 26th of a bf16 half-ulp); 2^n by adding n to the exponent field. x is
+// clamped at -126 so the result stays a normal float. The special-function unit that
+// evaluates ex2 handles 16 lanes per clock per SM, the FMA pipe 128, so evaluating a share
+// of the exponentials here shortens the softmax-gradient step.
+__device__ __forceinline__ float exp2_fma(float x) {
+  constexpr float kRound = 12582912.0f;                  // 1.5 * 2^23
+  constexpr float c0 = 0.9999281168f, c1 = 0.6932609677f, c2 = 0.2426105440f,
+                  c3 = 0.0551713221f;
+  x = fmaxf(x, -126.0f);
+  const float t = x + kRound;
+  const float f = x - (t - kRound);
+  const float p = fmaf(fmaf(fmaf(c3, f, c2), f, c1), f, c0);
+  return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
 }
+
+// Columns c with (c & 3) < kFmaExpQuarters take exp2_fma, the rest the ex2 instruction.
+// Measured on the full 2 x 8192 x 16 x 128 backward: 2 (half the columns) lengthened the
+// P^T step from ~3100 to ~4000 cycles per task -- that step is latency-bound here, not
+// limited by the special-function unit -- so this kernel keeps every exponential on ex2.
+constexpr int kFmaExpQuarters = 0;
 
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc128_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ TmaMaps maps) {
@@ -97,6 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(bars + E_DO_EMPTY + b, 1);
     }
     ptx::mbar_init(bars + E_S_FULL, 1);
+    ptx::mbar_init(bars + E_S_EMPTY, 8);
     ptx::mbar_init(bars + E_P_FULL, 8);
     ptx::mbar_init(bars + E_P_EMPTY, 1);
     ptx::mbar_init(bars + E_DP_FULL, 1);
@@ -139,7 +163,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (ok && w.next()) {
         const int b = w.bh / p.H, h = w.bh % p.H;
         const int q0 = w.j * kTile, qb = it & 1;
-        // Q_j with its LSE and Dsum rows into Q buffer qb (free once dK of task it-2 is done)
+        // Q_j with its -LSE*log2e and Dsum rows into Q buffer qb (free once dK of task it-2
+        // is done)
         long long t0 = tr.t0();
         if (it >= 2 && !(ok = ptx::mbar_wait(bars + E_Q_EMPTY + qb, ((it >> 1) - 1) & 1, abort_flag, tmo)))
           break;
@@ -149,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_expect_tx(bars + E_Q_FULL + qb, L::TILE_BYTES + L::LD_BYTES);
         for (int cb = 0; cb < 2; ++cb)
           ptx::tma_load_3d(qs + cb * kTile * 128, &maps.q, cb * 64, h, b * p.S + q0, bars + E_Q_FULL + qb);
-        ptx::bulk_load(ld, p.lse + (size_t)w.bh * p.S + q0, kTile * 4, bars + E_Q_FULL + qb);
+        ptx::bulk_load(ld, p.nlse2 + (size_t)w.bh * p.S + q0, kTile * 4, bars + E_Q_FULL + qb);
         ptx::bulk_load(ld + kTile * 4, p.Dsum + (size_t)w.bh * p.S + q0, kTile * 4, bars + E_Q_FULL + qb);
         // K and V of a new KV tile, once the previous tile's last MMA has read them
         if (w.first_of_tile) {
@@ -165,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ++tl;
         }
-        // dO_j into dO buffer qb (free once dV of task it-2 is done)
+        // dO_j into dO buffer qb (free once the MMAs of task it-2 are done)
         t0 = tr.t0();
         if (it >= 2 && !(ok = ptx::mbar_wait(bars + E_DO_EMPTY + qb, ((it >> 1) - 1) & 1, abort_flag, tmo)))
           break;
@@ -188,12 +213,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t sK = ptx::smem_u32(sm + L::K_OFF), sV = ptx::smem_u32(sm + L::V_OFF);
       const uint32_t sQ = ptx::smem_u32(sm + L::Q_OFF), sdO = ptx::smem_u32(sm + L::DO_OFF);
-      const uint32_t sdS = ptx::smem_u32(sm + L::DS_OFF);
+      const uint32_t sPS = ptx::smem_u32(sm + L::PS_OFF);
       const uint32_t dK_k = ptx::sdesc_lo(sK, 16), dV_k = ptx::sdesc_lo(sV, 16);
       const uint32_t dK_mn = ptx::sdesc_lo(sK, kTile * 128);
-      const uint32_t dS_k = ptx::sdesc_lo(sdS, 16), dS_mn = ptx::sdesc_lo(sdS, kTile * 128);
+      // P^T and dS^T share one buffer: K-major (over q) for dV and dK, MN-major for dQ^T
+      const uint32_t dPS_k = ptx::sdesc_lo(sPS, 16), dS_mn = ptx::sdesc_lo(sPS, kTile * 128);
       constexpr uint32_t ID_S = ptx::idesc_bf16(128, 128, 0, 0);    // S^T, dP^T
-      constexpr uint32_t ID_ACC = ptx::idesc_bf16(128, 128, 0, 1);  // dV (A in TMEM), dK
+      constexpr uint32_t ID_ACC = ptx::idesc_bf16(128, 128, 0, 1);  // dV, dK
       constexpr uint32_t ID_DQT = ptx::idesc_bf16(128, 128, 1, 1);  // dQ^T = K^T dS^T
       constexpr uint32_t BUF_STEP = L::TILE_BYTES >> 4;             // next Q or dO buffer
       // K-major step ks of a [128 rows][128] tile in 64-column blocks; MN-major step: 16
@@ -216,8 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = ptx::mbar_wait(bars + E_Q_FULL + (it & 1), (it >> 1) & 1, abort_flag, tmo);
           tr.add(TR_MMA_STAGE_FULL, t0);
           t0 = tr.t0();
-          // S^T overwrites the packed P^T of the previous task: dV must have read it
-          if (ok && it > 0) ok = ptx::mbar_wait(bars + E_P_EMPTY, (it - 1) & 1, abort_flag, tmo);
+          // S^T overwrites the previous task's S^T: the softmax-gradient warps must have
+          // loaded it
+          if (ok && it > 0) ok = ptx::mbar_wait(bars + E_S_EMPTY, (it - 1) & 1, abort_flag, tmo);
           tr.add(TR_MMA_S_EMPTY, t0);
           if (!ok) break;
           ptx::tc_fence_after();
@@ -249,8 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ddO_mn0 = ptx::sdesc_lo(sdO, kTile * 128);
         while (ok && w.next()) {
           if (w.first_of_tile) ++tile;
-          // P^T is in TMEM and dP^T of this task has completed (the softmax-gradient
-          // warps arrive only after both)
+          // P^T is in shared memory
           long long t0 = tr.t0();
           ok = ptx::mbar_wait(bars + E_P_FULL, it & 1, abort_flag, tmo);
           tr.add(TR_MMA_P_FULL, t0);
@@ -261,16 +287,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           ptx::tc_fence_after();
           const uint32_t acc0 = w.first_of_tile ? 0u : 1u;
-          // dV += P^T dO: A = packed P^T from TMEM, B = dO (MN-major over d)
+          // dV += P^T dO: A = P^T (K-major over q), B = dO (MN-major over d)
           const uint32_t ddO_mn = ddO_mn0 + (it & 1) * BUF_STEP;
           t0 = tr.t0();
 #pragma unroll
           for (int ks = 0; ks < kTile / 16; ++ks)
-            ptx::mma_ts(tmem + L::T_DV, tmem + L::T_S + p_col(ks), ddO_mn + ks * MN_STEP, ID_ACC,
+            ptx::mma_lo(tmem + L::T_DV, dPS_k + kstep(ks), ddO_mn + ks * MN_STEP, ID_ACC,
                         ks > 0 ? 1u : acc0);
-          // (dP^T, the other reader of this dO buffer, completed before P_FULL)
+          // P^T has been read: dS^T may overwrite it
           ptx::mma_commit(bars + E_P_EMPTY);
-          ptx::mma_commit(bars + E_DO_EMPTY + (it & 1));
           tr.add(TR_ISSUE_DV, t0);
           t0 = tr.t0();
           ok = ptx::mbar_wait(bars + E_DS_FULL, it & 1, abort_flag, tmo);
@@ -288,10 +313,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           // dK += dS^T Q: A = dS^T (K-major over q), B = Q (MN-major over d)
 #pragma unroll
           for (int ks = 0; ks < kTile / 16; ++ks)
-            ptx::mma_lo(tmem + L::T_DK, dS_k + kstep(ks), dQ_mn + ks * MN_STEP, ID_ACC,
+            ptx::mma_lo(tmem + L::T_DK, dPS_k + kstep(ks), dQ_mn + ks * MN_STEP, ID_ACC,
                         ks > 0 ? 1u : acc0);
           ptx::mma_commit(bars + E_DS_EMPTY);
           ptx::mma_commit(bars + E_Q_EMPTY + (it & 1));
+          // this dO buffer's readers are done: dV above, and dP^T, which completed before
+          // the softmax-gradient warps published dS^T
+          ptx::mma_commit(bars + E_DO_EMPTY + (it & 1));
           if (w.last_of_tile) {
             ptx::mma_commit(bars + E_ACC_FULL);
             ptx::mma_commit(bars + E_KV_EMPTY);
@@ -312,18 +340,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quarter * 32 + lane;         // kv row within the tile
     const int col0 = half * 64;                // this thread's 64 q columns
     const uint32_t lane_addr = ((uint32_t)(quarter * 32) << 16);
-    const uint32_t sdS = ptx::smem_u32(sm + L::DS_OFF);
+    const uint32_t sPS = ptx::smem_u32(sm + L::PS_OFF);
     const Trace& trs = (warp == 4 && lane == 0) ? tr : tr_none;
+    // writes 64 values of row r (q columns col0..col0+63) as bf16 into the P^T/dS^T buffer
+    auto store_row = [&](const float (&v)[64]) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        ptx::st_shared_v4(sPS + sw_chunk(r, (col0 >> 3) + k, kTile),
+                          ptx::pack_bf16(v[8 * k], v[8 * k + 1]), ptx::pack_bf16(v[8 * k + 2], v[8 * k + 3]),
+                          ptx::pack_bf16(v[8 * k + 4], v[8 * k + 5]), ptx::pack_bf16(v[8 * k + 6], v[8 * k + 7]));
+      ptx::fence_proxy_async_smem();
+    };
     Walk w(p);
     int it = 0;
     bool ok = true;
     while (ok && w.next()) {
       const int qb = it & 1;
-      const float* lse_s = (const float*)(sm + L::LD_OFF + qb * L::LD_BYTES);
-      const float* dsum_s = lse_s + kTile;
-      const int q0 = w.j * kTile;
-      const bool diag = p.causal && (w.i == w.j);
-      const int kv_g = w.i * kTile + r;
+      const float* nlse_s = (const float*)(sm + L::LD_OFF + qb * L::LD_BYTES);   // -LSE*log2e
+      const float* dsum_s = nlse_s + kTile;
       long long t0 = trs.t0();
       ok = ptx::warp_wait(bars + E_Q_FULL + qb, (it >> 1) & 1, abort_flag, tmo);
       if (ok) ok = ptx::warp_wait(bars + E_S_FULL, it & 1, abort_flag, tmo);
@@ -339,54 +373,73 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 32; ++c) pv[c0 + c] = sv[c];
       }
+      // S^T is in registers: the next task's S^T may be issued
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bars + E_S_EMPTY);
+      const float4* nl4 = reinterpret_cast<const float4*>(nlse_s + col0);
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const int qc = col0 + c;
-        const float e = ptx::ex2(fmaf(pv[c], p.scale_log2, -lse_s[qc] * kLog2e));
-        pv[c] = (diag && kv_g > q0 + qc) ? 0.f : e;
-      }
-      {
-        uint32_t pk[32];
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 nl = nl4[c4];
+        const float x[4] = {fmaf(pv[4 * c4 + 0], p.scale_log2, nl.x),
+                            fmaf(pv[4 * c4 + 1], p.scale_log2, nl.y),
+                            fmaf(pv[4 * c4 + 2], p.scale_log2, nl.z),
+                            fmaf(pv[4 * c4 + 3], p.scale_log2, nl.w)};
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pk[c] = ptx::pack_bf16(pv[2 * c], pv[2 * c + 1]);
-        // packed P^T over the first half of this thread's S^T columns (already read)
-        ptx::tmem_st32(tmem + lane_addr + L::T_S + col0, pk);
+        for (int k = 0; k < 4; ++k) pv[4 * c4 + k] = k < kFmaExpQuarters ? exp2_fma(x[k]) : ptx::ex2(x[k]);
       }
+      if (p.causal && w.i == w.j) {
+        // diagonal tile: keys after the query are masked out
+        const int d = r - col0;                // kv_row - q_col offset of column 0
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (d > c) pv[c] = 0.f;
+      }
+      // P^T goes where the previous task's dS^T was: dK and dQ^T must have read it
+      trs.add(TR_DQ_FULL, tp);   // (slot reused: P^T compute)
+      t0 = trs.t0();
+      if (it > 0) ok = ptx::warp_wait(bars + E_DS_EMPTY, (it - 1) & 1, abort_flag, tmo);
+      trs.add(TR_SG_DS_EMPTY, t0);
+      if (!ok) break;
+      tp = trs.t0();
+      store_row(pv);
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bars + E_P_FULL);
       trs.add(TR_DQ_FULL, tp);   // (slot reused: P^T compute)
       t0 = trs.t0();
       ok = ptx::warp_wait(bars + E_DP_FULL, it & 1, abort_flag, tmo);
       trs.add(TR_SG_DP_FULL, t0);
       if (!ok) break;
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bars + E_P_FULL);
       ptx::tc_fence_after();
       tp = trs.t0();
+      const float4* ds4 = reinterpret_cast<const float4*>(dsum_s + col0);
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 32) {
         float dp[32];
-        ptx::tmem_ld32(tmem + lane_addr + L::T_DP + col0 + c0, dp);
+        ptx::tmem_ld32(tmem + lane_addr + L::T_DP + c0 + col0, dp);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pv[c0 + c] = pv[c0 + c] * (dp[c] - dsum_s[col0 + c0 + c]);
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 ds = ds4[(c0 >> 2) + c4];
+          float* pc = pv + c0 + 4 * c4;
+          pc[0] *= dp[4 * c4 + 0] - ds.x;
+          pc[1] *= dp[4 * c4 + 1] - ds.y;
+          pc[2] *= dp[4 * c4 + 2] - ds.z;
+          pc[3] *= dp[4 * c4 + 3] - ds.w;
+        }
       }
+      // dS^T overwrites P^T: dV must have read it
+      trs.add(TR_DQ_STAGE, tp);  // (slot reused: dS^T compute)
       t0 = trs.t0();
-      if (it > 0) ok = ptx::warp_wait(bars + E_DS_EMPTY, (it - 1) & 1, abort_flag, tmo);
+      ok = ptx::warp_wait(bars + E_P_EMPTY, it & 1, abort_flag, tmo);
       trs.add(TR_SG_DS_EMPTY, t0);
       if (!ok) break;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint32_t a = sdS + sw_chunk(r, (col0 >> 3) + k, kTile);
-        ptx::st_shared_v4(a, ptx::pack_bf16(pv[8 * k], pv[8 * k + 1]),
-                          ptx::pack_bf16(pv[8 * k + 2], pv[8 * k + 3]),
-                          ptx::pack_bf16(pv[8 * k + 4], pv[8 * k + 5]),
-                          ptx::pack_bf16(pv[8 * k + 6], pv[8 * k + 7]));
-      }
-      ptx::fence_proxy_async_smem();
+      tp = trs.t0();
+      store_row(pv);
       // the dP^T loads above have completed: dQ^T may now overwrite those columns
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bars + E_DS_FULL);
-      trs.add(TR_DQ_STAGE, tp);  // (slot reused: dS^T compute, including the DS_EMPTY wait)
+      trs.add(TR_DQ_STAGE, tp);
       ++it;
     }
   } else {

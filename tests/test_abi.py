@@ -46,7 +46,7 @@ def test_status_strings(lib):
 def test_workspace_size(lib):
     B, S, H, D = 2, 256, 3, 64
     ws = da.dash_attn_bwd_workspace_size(B, S, H, D)
-    need = 256 + B * H * S * 4 + B * H * S * D * 4 + B * H * (S // 128) * 4
+    need = 256 + 2 * B * H * S * 4 + B * H * S * D * 4 + B * H * (S // 128) * 4
     assert need <= ws <= need + 4 * 256 and ws % 256 == 0
     assert da.dash_attn_bwd_workspace_size(1, 100, 1, 64) == 0      # S not a multiple of 128
     assert da.dash_attn_bwd_workspace_size(1, 128, 1, 96) == 0      # unsupported head dim
