@@ -276,9 +276,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ddO_mn0 = ptx::sdesc_lo(sdO, kTile * 128);
         while (ok && w.next()) {
           if (w.first_of_tile) ++tile;
-          // P^T is in shared memory
+          // P^T is in shared memory, and dO of this task has landed (P_FULL does not imply
+          // it: the softmax-gradient warps publish P^T before dP^T, the other reader of dO,
+          // has run)
           long long t0 = tr.t0();
           ok = ptx::mbar_wait(bars + E_P_FULL, it & 1, abort_flag, tmo);
+          if (ok) ok = ptx::mbar_wait(bars + E_DO_FULL + (it & 1), (it >> 1) & 1, abort_flag, tmo);
           tr.add(TR_MMA_P_FULL, t0);
           t0 = tr.t0();
           if (ok && w.first_of_tile && tile > 0)

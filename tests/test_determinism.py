@@ -36,6 +36,8 @@ def _runs(args, causal, sched, det, runs):
     outs = []
     for _ in range(runs):
         outs.append(da.attn_backward(q, k, v, o, do, lse, scale, causal, sched, det, workspace=ws))
+        st = da.dash_attn_get_status(ws)          # every run must have completed cleanly
+        assert st == da.DASH_OK, (sched, st, da.dash_last_error())
     torch.cuda.synchronize()
     return outs
 
