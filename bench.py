@@ -398,7 +398,7 @@ def run_gpu(args, w, rank, world, local_rank):
     if world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w)
     achieved = bwd_flops(w) / (main_ms / 1e3) / 1e12 if main_ms else None
-    launches_per_step = 2          # preprocess + main (deterministic path)
+    launches_per_step = 3          # preprocess, main backward, dQ convert
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": steps,
         "warmup": warm, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
