@@ -47,7 +47,11 @@ WORKLOADS = {
     "full-2x4096x16x128": dict(mask="full", B=2, S=4096, H=16, D=128),
 }
 DEFAULT_WORKLOAD = "full-2x8192x16x128"
-BEST_DASH = {"full": "shift", "causal": "symmetric_shift"}
+BEST_DASH = {"full": "shift", "causal": "symmetric_shift"}   # reference arm's naming only
+# Cost model of the run-time selector (dash_sched_select), cycles per 128 x 128 task measured
+# on GB300 with the head-dim-128 kernel: compute step, hold of a dQ block's turn, hand-off
+# between SMs; two-engine SM.
+SELECT_COSTS = {"c": 6900.0, "r": 5600.0, "h": 3000.0, "overlapped": 1}
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -283,6 +287,14 @@ def run_gpu(args, w, rank, world, local_rank):
     causal = w["mask"] == "causal"
     mask = da.MASK_CAUSAL if causal else da.MASK_FULL
     scale = 1.0 / math.sqrt(D)
+    selected_by = "command line"
+    if args.schedule == "auto":
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        choice, _ = da.dash_sched_select(mask, S // 128, B * H, sms, SELECT_COSTS["c"],
+                                         SELECT_COSTS["r"], SELECT_COSTS["h"],
+                                         SELECT_COSTS["overlapped"])
+        args.schedule = {v: k for k, v in da.SCHEDULES.items()}[choice]
+        selected_by = "dash_sched_select, costs " + json.dumps(SELECT_COSTS)
     sched = da.SCHEDULES[args.schedule]
 
     x = make_inputs(B, S, H, D, seed=rank)
@@ -403,7 +415,7 @@ def run_gpu(args, w, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": steps,
         "warmup": warm, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": workload_config(args, w),
+        "config": {**workload_config(args, w), "schedule_selected_by": selected_by},
         "pct_of_peak": 100.0 * value / world / peak_tf,
         "nondet_tflops": side.get("nondet"),
         "det_vs_nondet": value / side["nondet"] if side.get("nondet") else None,
@@ -429,12 +441,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
-    ap.add_argument("--schedule", default=None,
-                    choices=["ascending", "descending", "shift", "symmetric_shift"])
+    ap.add_argument("--schedule", default="auto",
+                    choices=["auto", "ascending", "descending", "shift", "symmetric_shift"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     w = WORKLOADS[args.workload]
-    if args.schedule is None:
+    if args.schedule == "auto" and args.impl == "reference":
         args.schedule = BEST_DASH[w["mask"]]
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

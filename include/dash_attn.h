@@ -220,6 +220,39 @@ int dash_sched_table(int mask, int schedule, int n, int32_t* slot_offsets, int32
 dash_status_t dash_sched_simulate(int mask, int schedule, int n, int heads, int num_sms,
                                   double c, double r, double* makespan, double* sm_end);
 
+/*
+ * The same critical path with synchronisation cost (the Pith review's "What would settle
+ * it": nonzero edge costs; its ledger lists zero-cost order edges as a modelling choice):
+ *   h          : cost of handing a dQ block's turn from one SM to another (the order edge's
+ *                weight; 0 when consecutive reductions of the block run on one SM);
+ *   overlapped : 0 = the SM runs C then R task after task (dash_sched_simulate's model);
+ *                1 = two engines per SM: C phases in order, R phases in order, and the
+ *                k-th task's C waits for the (k-2)-th task's R (the accumulator reuse of
+ *                this library's kernels, which read one dQ partial out while the next
+ *                is computed).
+ * With h = 0 and overlapped = 0 the result equals dash_sched_simulate's. Same outputs and
+ * errors as dash_sched_simulate; DASH_ERR_INVALID_ARG for a negative cost or overlapped
+ * not in {0, 1}.
+ */
+dash_status_t dash_sched_simulate_ex(int mask, int schedule, int n, int heads, int num_sms,
+                                     double c, double r, double h, int overlapped,
+                                     double* makespan, double* sm_end);
+
+/*
+ * Run-time schedule selector: among the schedules defined for `mask` and n (ascending and
+ * descending always; shift for the full mask; symmetric shift for the causal mask and even
+ * n) whose waits are acyclic on `num_sms` SMs, the one with the smallest
+ * dash_sched_simulate_ex makespan (ties: the lower enum value). Writes it to
+ * *schedule_out and, if makespan_out is not NULL, its makespan. The pages pick schedules by
+ * configuration (Descending vs Symmetric Shift at d = 128, Shift vs the baseline at long
+ * sequences); this makes that choice from the cost model. Costs measured on GB300 with
+ * this library (head dim 128, cycles per 128x128 task): c ~ 6900, r ~ 5600, h ~ 3000,
+ * overlapped = 1. Returns DASH_ERR_INVALID_ARG for bad arguments.
+ */
+dash_status_t dash_sched_select(int mask, int n, int heads, int num_sms, double c, double r,
+                                double h, int overlapped, int* schedule_out,
+                                double* makespan_out);
+
 #ifdef __cplusplus
 }
 #endif

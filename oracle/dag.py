@@ -54,6 +54,8 @@ __all__ = [
     "schedule_dag",
     "longest_path",
     "simulate",
+    "schedule_dag_ex",
+    "simulate_ex",
 ]
 
 SCHEDULES = ("ascending", "descending", "shift", "symmetric_shift")
@@ -187,3 +189,80 @@ def simulate(mask: str, sched: str, n: int, m: int, num_sms: int, c: float, r: f
     makespan = max(sm_end) if tasks else 0.0
     return {"makespan": makespan, "sm_end": sm_end,
             "sm_idle": [e - b for e, b in zip(sm_end, sm_busy)]}
+
+
+# ---------------------------------------------------------------------------------------
+# Sync-cost-aware extension (the Pith review's "What would settle it" asks for nonzero
+# synchronisation edge costs; its ledger lists the zero-cost edge as a modelling choice).
+#
+# * h: cost of handing a dQ block's turn from one SM to another -- the weight of an order
+#   edge between consecutive reductions of one dQ block that run on different SMs (0 when
+#   both run on the same SM).
+# * overlapped: the SM has two engines instead of running C then R back to back. The
+#   compute engine runs the C phases in order, the reduce engine the R phases in order,
+#   and C of the k-th task waits for R of the (k-2)-th: the partial of task k needs the
+#   accumulator that the read-out of task k-1 frees, and that read-out starts once the
+#   reduce engine has finished task k-2.
+# With h = 0 and overlapped = False this is exactly schedule_dag / simulate above.
+# ---------------------------------------------------------------------------------------
+def schedule_dag_ex(mask: str, sched: str, n: int, m: int, num_sms: int, c: float, r: float,
+                    h: float, overlapped: bool):
+    """The schedule DAG with hand-off cost ``h`` and, optionally, the two-engine SM.
+
+    Same vertex numbering and return value as schedule_dag.
+    """
+    ch = chains(mask, sched, n)
+    order = reduction_order(mask, sched, n)
+    units = [(hd, slot) for hd in range(m) for slot in range(len(ch))]   # head-major deal
+    per_sm: list[list[int]] = [[] for _ in range(num_sms)]
+    tasks: list[tuple[int, int, int]] = []
+    sm_of_task: list[int] = []
+    index: dict[tuple[int, int, int], int] = {}
+    for u, (hd, slot) in enumerate(units):
+        sm = u % num_sms
+        for (i, j) in ch[slot]:
+            k = len(tasks)
+            tasks.append((hd, i, j))
+            sm_of_task.append(sm)
+            index[(hd, i, j)] = k
+            per_sm[sm].append(k)
+    edges: list[tuple[int, int, float]] = []
+    for k in range(len(tasks)):
+        cs, ce, rs, re = 4 * k, 4 * k + 1, 4 * k + 2, 4 * k + 3
+        edges += [(cs, ce, c), (ce, rs, 0.0), (rs, re, r)]
+    for lst in per_sm:
+        for pos in range(1, len(lst)):
+            a, b = lst[pos - 1], lst[pos]
+            if overlapped:
+                edges.append((4 * a + 1, 4 * b, 0.0))          # compute engine in order
+                edges.append((4 * a + 3, 4 * b + 2, 0.0))      # reduce engine in order
+                if pos >= 2:                                   # accumulator reuse
+                    edges.append((4 * lst[pos - 2] + 3, 4 * b, 0.0))
+            else:
+                edges.append((4 * a + 3, 4 * b, 0.0))          # C then R, task after task
+    for hd in range(m):                                        # fixed dQ reduction order
+        for j, kv in order.items():
+            for a, b in zip(kv, kv[1:]):
+                ka, kb = index[(hd, a, j)], index[(hd, b, j)]
+                w = 0.0 if sm_of_task[ka] == sm_of_task[kb] else h
+                edges.append((4 * ka + 3, 4 * kb + 2, w))
+    return 4 * len(tasks), edges, tasks, sm_of_task
+
+
+def simulate_ex(mask: str, sched: str, n: int, m: int, num_sms: int, c: float, r: float,
+                h: float = 0.0, overlapped: bool = False):
+    """Critical path of schedule_dag_ex; same return value as simulate."""
+    nv, edges, tasks, sm_of_task = schedule_dag_ex(mask, sched, n, m, num_sms, c, r, h,
+                                                   overlapped)
+    depth = longest_path(nv, edges)
+    if depth is None:
+        return {"makespan": None, "sm_end": None, "sm_idle": None}
+    sm_end = [0.0] * num_sms
+    sm_busy = [0.0] * num_sms
+    for k, sm in enumerate(sm_of_task):
+        sm_end[sm] = max(sm_end[sm], depth[4 * k + 3])
+        sm_busy[sm] += c + r
+    makespan = max(sm_end) if tasks else 0.0
+    return {"makespan": makespan, "sm_end": sm_end,
+            "sm_idle": [e - b for e, b in zip(sm_end, sm_busy)]}
+

@@ -493,6 +493,50 @@ dash_status_t dash_sched_simulate(int mask, int schedule, int n, int heads, int 
   return DASH_OK;
 }
 
+dash_status_t dash_sched_simulate_ex(int mask, int schedule, int n, int heads, int num_sms,
+                                     double c, double r, double h, int overlapped,
+                                     double* makespan, double* sm_end) {
+  if (heads < 1 || num_sms < 1 || !makespan || !(c >= 0) || !(r >= 0) || !(h >= 0) ||
+      (overlapped != 0 && overlapped != 1))
+    return DASH_ERR_INVALID_ARG;
+  dash::Schedule sc;
+  int rc = dash::build_schedule(mask, schedule, n, &sc);
+  if (rc) return (dash_status_t)rc;
+  std::vector<double> ends;
+  if (!dash::simulate_ex(sc, heads, num_sms, c, r, h, overlapped != 0, makespan, &ends))
+    return DASH_ERR_DEADLOCK_RISK;
+  if (sm_end) std::memcpy(sm_end, ends.data(), ends.size() * sizeof(double));
+  return DASH_OK;
+}
+
+dash_status_t dash_sched_select(int mask, int n, int heads, int num_sms, double c, double r,
+                                double h, int overlapped, int* schedule_out,
+                                double* makespan_out) {
+  if (!schedule_out || heads < 1 || num_sms < 1 || !(c >= 0) || !(r >= 0) || !(h >= 0) ||
+      (overlapped != 0 && overlapped != 1))
+    return DASH_ERR_INVALID_ARG;
+  if (mask != DASH_MASK_FULL && mask != DASH_MASK_CAUSAL) return DASH_ERR_INVALID_ARG;
+  int best = -1;
+  double best_mk = 0.0;
+  for (int s = DASH_SCHED_ASCENDING; s <= DASH_SCHED_SYMMETRIC_SHIFT; ++s) {
+    dash::Schedule sc;
+    const int rc = dash::build_schedule(mask, s, n, &sc);
+    if (rc == DASH_ERR_UNSUPPORTED) continue;          // schedule not defined for this mask/n
+    if (rc) return (dash_status_t)rc;
+    double mk = 0.0;
+    if (!dash::simulate_ex(sc, heads, num_sms, c, r, h, overlapped != 0, &mk, nullptr))
+      continue;                                        // its waits would deadlock this grid
+    if (best < 0 || mk < best_mk) {                    // ties keep the lower enum value
+      best = s;
+      best_mk = mk;
+    }
+  }
+  if (best < 0) return DASH_ERR_DEADLOCK_RISK;
+  *schedule_out = best;
+  if (makespan_out) *makespan_out = best_mk;
+  return DASH_OK;
+}
+
 }  // extern "C"
 
 // =====================================================================================

@@ -100,6 +100,11 @@ int build_schedule(int mask, int sched, int n, Schedule* out) {
 
 bool simulate(const Schedule& sc, int heads, int num_sms, double c, double r,
               double* makespan, std::vector<double>* sm_end) {
+  return simulate_ex(sc, heads, num_sms, c, r, 0.0, false, makespan, sm_end);
+}
+
+bool simulate_ex(const Schedule& sc, int heads, int num_sms, double c, double r, double h,
+                 bool overlapped, double* makespan, std::vector<double>* sm_end) {
   const int n = sc.n;
   const long long units = (long long)heads * sc.num_slots;
   // who reduces at position k of dQ_j: inv[j * n + k] = kv tile
@@ -112,9 +117,11 @@ bool simulate(const Schedule& sc, int heads, int num_sms, double c, double r,
   std::vector<std::vector<long long>> sm_units(num_sms);
   for (long long u = 0; u < units; ++u) sm_units[u % num_sms].push_back(u);
   std::vector<size_t> unit_pos(num_sms, 0), task_pos(num_sms, 0);
-  std::vector<double> t_sm(num_sms, 0.0);
-  // reduce-end time of (head, kv, q); NaN-free sentinel -1 = not yet done
+  // per SM: end of its last C phase, of its last R phase and of the R phase before that
+  std::vector<double> c_last(num_sms, 0.0), r_last(num_sms, 0.0), r_prev(num_sms, 0.0);
+  // reduce-end time and SM of (head, kv, q); sentinel -1 = not yet done
   std::vector<double> rend((size_t)heads * n * n, -1.0);
+  std::vector<int> rsm((size_t)heads * n * n, -1);
 
   long long remaining = (long long)heads * (long long)sc.tasks.size();
   while (remaining > 0) {
@@ -127,16 +134,27 @@ bool simulate(const Schedule& sc, int heads, int num_sms, double c, double r,
         const int32_t tk = sc.tasks[beg + task_pos[sm]];
         const int i = tk >> 16, j = tk & 0xffff;
         const int o = sc.ord[(size_t)i * n + j];
-        double pred_end = 0.0;
+        double pred_ready = 0.0;
         if (o > 0) {
           const int ip = inv[(size_t)j * n + o - 1];
-          pred_end = rend[((size_t)head * n + ip) * n + j];
-          if (pred_end < 0) break;                              // predecessor not done
+          const size_t pk = ((size_t)head * n + ip) * n + j;
+          if (rend[pk] < 0) break;                              // predecessor not done
+          pred_ready = rend[pk] + (rsm[pk] == sm ? 0.0 : h);
         }
-        const double c_end = t_sm[sm] + c;
-        const double r_end = std::max(c_end, pred_end) + r;
-        rend[((size_t)head * n + i) * n + j] = r_end;
-        t_sm[sm] = r_end;
+        double c_end, r_end;
+        if (overlapped) {
+          c_end = std::max(c_last[sm], r_prev[sm]) + c;
+          r_end = std::max(std::max(c_end, r_last[sm]), pred_ready) + r;
+        } else {
+          c_end = r_last[sm] + c;
+          r_end = std::max(c_end, pred_ready) + r;
+        }
+        const size_t k = ((size_t)head * n + i) * n + j;
+        rend[k] = r_end;
+        rsm[k] = sm;
+        c_last[sm] = c_end;
+        r_prev[sm] = r_last[sm];
+        r_last[sm] = r_end;
         --remaining;
         progress = true;
         if (++task_pos[sm] == (size_t)len) {
@@ -148,9 +166,9 @@ bool simulate(const Schedule& sc, int heads, int num_sms, double c, double r,
     if (!progress) return false;
   }
   double mk = 0.0;
-  for (double t : t_sm) mk = std::max(mk, t);
+  for (double t : r_last) mk = std::max(mk, t);
   if (makespan) *makespan = mk;
-  if (sm_end) *sm_end = t_sm;
+  if (sm_end) *sm_end = r_last;
   return true;
 }
 

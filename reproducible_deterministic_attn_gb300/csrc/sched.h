@@ -31,4 +31,15 @@ int build_schedule(int mask, int sched, int n, Schedule* out);
 bool simulate(const Schedule& sc, int heads, int num_sms, double c, double r,
               double* makespan, std::vector<double>* sm_end);
 
+// The same with synchronisation cost and the two-engine SM (the Pith review's "What
+// would settle it": nonzero edge costs):
+//   h          -- cost of handing a dQ block's turn to another SM (0 within one SM);
+//   overlapped -- each SM runs C phases in order on one engine and R phases in order on
+//                 another, and C of its k-th task waits for R of its (k-2)-th (the
+//                 accumulator reuse of a kernel that reads one partial out while the
+//                 next is computed); false = C then R, task after task.
+// h = 0, overlapped = false is simulate() above.
+bool simulate_ex(const Schedule& sc, int heads, int num_sms, double c, double r, double h,
+                 bool overlapped, double* makespan, std::vector<double>* sm_end);
+
 }  // namespace dash

@@ -58,6 +58,10 @@ _SIGNATURES = {
     "dash_sched_table": (_c_int, [_c_int, _c_int, _c_int, _i32p, _i32p, _c_int, _i32p]),
     "dash_sched_simulate": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_double, _c_double,
                                      _dblp, _dblp]),
+    "dash_sched_simulate_ex": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_double,
+                                        _c_double, _c_double, _c_int, _dblp, _dblp]),
+    "dash_sched_select": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_double, _c_double,
+                                   _c_double, _c_int, ctypes.POINTER(_c_int), _dblp]),
 }
 
 
@@ -208,6 +212,32 @@ def dash_sched_simulate(mask: int, schedule: int, n: int, heads: int, num_sms: i
         return None, None
     _check(st, "dash_sched_simulate")
     return mk.value, list(ends)
+
+
+def dash_sched_simulate_ex(mask: int, schedule: int, n: int, heads: int, num_sms: int,
+                           c: float, r: float, h: float, overlapped: int):
+    """Returns (makespan, per-SM finish times), or (None, None) on a deadlock."""
+    mk = ctypes.c_double(0.0)
+    ends = (ctypes.c_double * num_sms)()
+    st = load().dash_sched_simulate_ex(int(mask), int(schedule), int(n), int(heads),
+                                       int(num_sms), float(c), float(r), float(h),
+                                       int(overlapped), ctypes.byref(mk), ends)
+    if st == DASH_ERR_DEADLOCK_RISK:
+        return None, None
+    _check(st, "dash_sched_simulate_ex")
+    return mk.value, list(ends)
+
+
+def dash_sched_select(mask: int, n: int, heads: int, num_sms: int, c: float, r: float,
+                      h: float, overlapped: int):
+    """Returns (schedule, makespan) chosen by the library's cost model."""
+    sched = _c_int(-1)
+    mk = ctypes.c_double(0.0)
+    st = load().dash_sched_select(int(mask), int(n), int(heads), int(num_sms), float(c),
+                                  float(r), float(h), int(overlapped), ctypes.byref(sched),
+                                  ctypes.byref(mk))
+    _check(st, "dash_sched_select")
+    return sched.value, mk.value
 
 
 # ---- conveniences (allocation through torch; the compute stays in the library) ----

@@ -185,3 +185,84 @@ def test_deadlock_detected_when_order_contradicts_program_order():
     # force R(1, 0) before R(0, 0): KV_1 runs after KV_0 on the only SM
     edges = edges + [(4 * idx[(0, 1, 0)] + 3, 4 * idx[(0, 0, 0)] + 2, 0.0)]
     assert longest_path(nv, edges) is None
+
+
+# ---- sync-cost-aware model (simulate_ex) ----------------------------------------------
+
+from oracle.dag import simulate_ex  # noqa: E402
+
+SYNC_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "dag_sync_closed_forms.txt")
+
+
+def _sync_rows():
+    rows = []
+    with open(SYNC_GOLDEN) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#") or line.startswith("EXAMPLE"):
+                continue
+            mode, mask, sched, sms, heads, formula, _src = (x.strip() for x in line.split("|"))
+            rows.append((mode, mask, sched, sms, heads, formula))
+    return rows
+
+
+@pytest.mark.parametrize("row", _sync_rows(), ids=lambda r: f"{r[0]}-{r[1]}-{r[2]}-P{r[3]}")
+@pytest.mark.parametrize("c,r,h", [(3, 1, 0), (3, 1, 2), (3, 1, 5), (1, 3, 1), (2, 2, 4), (5, 2, 1)])
+def test_sync_closed_forms(row, c, r, h):
+    mode, mask, sched, sms_spec, heads_spec, formula = row
+    for n in range(1, 13):
+        if sched == "shift" and n < 2:
+            continue
+        for m in ([1] if heads_spec == "1" else [1, 2, 3]):
+            sms = n if sms_spec == "n" else 1
+            got = simulate_ex(mask, sched, n, m, sms, c, r, h, mode == "overlapped")["makespan"]
+            want = eval(formula, {"max": max}, {"n": n, "m": m, "c": c, "r": r, "h": h})
+            assert got == want, (row, n, m, c, r, h, got, want)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_sync_model_reduces_to_the_pages_model(seed):
+    rng = random.Random(500 + seed)
+    for _ in range(15):
+        mask, sched = rng.choice([("full", "ascending"), ("full", "descending"), ("full", "shift"),
+                                  ("causal", "ascending"), ("causal", "descending"),
+                                  ("causal", "symmetric_shift")])
+        n = rng.choice([2, 4, 6, 8])
+        m, sms = rng.randint(1, 4), rng.randint(1, 2 * n + 1)
+        c, r = rng.choice([(3.0, 1.0), (1.0, 2.0), (2.0, 2.0)])
+        a = simulate(mask, sched, n, m, sms, c, r)["makespan"]
+        b = simulate_ex(mask, sched, n, m, sms, c, r, 0.0, False)["makespan"]
+        assert a == b
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_overlap_never_slower_and_monotone_in_h(seed):
+    rng = random.Random(900 + seed)
+    for _ in range(10):
+        mask, sched = rng.choice([("full", "ascending"), ("full", "shift"),
+                                  ("causal", "descending"), ("causal", "symmetric_shift")])
+        n = rng.choice([2, 4, 6])
+        m, sms = rng.randint(1, 3), rng.randint(2 * n, 3 * n)   # co-resident: no deadlock
+        c, r = rng.choice([(3.0, 1.0), (1.0, 2.0), (2.0, 2.0)])
+        prev = None
+        for h in (0.0, 0.5, 1.0, 3.0):
+            ser = simulate_ex(mask, sched, n, m, sms, c, r, h, False)["makespan"]
+            ovl = simulate_ex(mask, sched, n, m, sms, c, r, h, True)["makespan"]
+            assert ovl <= ser
+            if prev is not None:
+                assert ser >= prev[0] and ovl >= prev[1]
+            prev = (ser, ovl)
+
+
+def test_sync_worked_example_accumulator_reuse():
+    rows = []
+    with open(SYNC_GOLDEN) as f:
+        for line in f:
+            if line.startswith("EXAMPLE"):
+                rows.append([x.strip() for x in line.split("|")[1:]])
+    assert rows
+    for mode, mask, sched, n, m, sms, c, r, h, want in rows:
+        got = simulate_ex(mask, sched, int(n), int(m), int(sms), float(c), float(r), float(h),
+                          mode == "overlapped")["makespan"]
+        assert got == float(want)
+

@@ -75,3 +75,69 @@ def test_simulator_closed_forms_large_n():
             assert mk == m * n * 4.0
             mk, _ = da.dash_sched_simulate(1, 3, n, m, n, 3.0, 1.0)
             assert mk == ((m + 1) // 2) * (n + 1) * 4.0
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_sync_simulator_matches_oracle(seed):
+    rng = random.Random(4000 + seed)
+    for _ in range(20):
+        mask, sched = rng.choice([(0, 0), (0, 1), (0, 2), (1, 0), (1, 1), (1, 3)])
+        n = rng.choice([1, 2, 3, 4, 6, 8]) if sched != 3 else rng.choice([2, 4, 6, 8])
+        m = rng.randint(1, 4)
+        sms = rng.randint(1, 2 * n + 2)
+        c, r = rng.choice([(3.0, 1.0), (1.0, 0.25), (2.0, 2.0), (0.5, 1.5)])
+        h = rng.choice([0.0, 0.5, 2.0, 5.0])
+        ovl = rng.randint(0, 1)
+        want = dag.simulate_ex(MASKS[mask], NAMES[sched], n, m, sms, c, r, h, bool(ovl))
+        mk, ends = da.dash_sched_simulate_ex(mask, sched, n, m, sms, c, r, h, ovl)
+        if want["makespan"] is None:
+            assert mk is None
+        else:
+            assert mk == pytest.approx(want["makespan"], rel=1e-12, abs=1e-9)
+            assert ends == pytest.approx(want["sm_end"], rel=1e-12, abs=1e-9)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_selector_is_the_oracle_argmin(seed):
+    rng = random.Random(7000 + seed)
+    for _ in range(12):
+        mask = rng.randint(0, 1)
+        n = rng.choice([2, 4, 6, 8])
+        m, sms = rng.randint(1, 4), rng.randint(1, 3 * n)
+        c, r, h = rng.choice([3.0, 1.0]), rng.choice([1.0, 2.5]), rng.choice([0.0, 1.0, 4.0])
+        ovl = rng.randint(0, 1)
+        best, best_mk = None, None
+        for s in (0, 1, 2, 3):
+            if not _valid(mask, s, n):
+                continue
+            mk = dag.simulate_ex(MASKS[mask], NAMES[s], n, m, sms, c, r, h, bool(ovl))["makespan"]
+            if mk is not None and (best is None or mk < best_mk):
+                best, best_mk = s, mk
+        got, got_mk = da.dash_sched_select(mask, n, m, sms, c, r, h, ovl)
+        assert got == best and got_mk == pytest.approx(best_mk)
+
+
+# Cycles per 128 x 128 task measured on GB300 for the head-dim-128 kernel: compute step
+# (non-deterministic), hold of a dQ block's turn (adds + fence + read-out), hand-off.
+GB300_COSTS = (6900.0, 5600.0, 3000.0, 1)
+
+
+@pytest.mark.parametrize("mask,n,heads,measured_best", [
+    (0, 64, 32, 2),     # full 2x16x8192x128: shift measured fastest
+    (1, 128, 32, 3),    # causal 1x32x16384x128: symmetric shift measured fastest
+    (1, 16, 64, 3),     # causal 4x16x2048x64: symmetric shift measured fastest
+])
+def test_selector_picks_the_measured_best_on_gb300(mask, n, heads, measured_best):
+    got, _ = da.dash_sched_select(mask, n, heads, 152, *GB300_COSTS)
+    assert got == measured_best
+
+
+def test_selector_and_simulate_ex_argument_errors():
+    with pytest.raises(da.DashError):
+        da.dash_sched_select(0, 8, 1, 8, -1.0, 1.0, 0.0, 0)
+    with pytest.raises(da.DashError):
+        da.dash_sched_select(2, 8, 1, 8, 1.0, 1.0, 0.0, 0)
+    with pytest.raises(da.DashError):
+        da.dash_sched_simulate_ex(0, 0, 8, 1, 8, 1.0, 1.0, -1.0, 0)
+    with pytest.raises(da.DashError):
+        da.dash_sched_simulate_ex(0, 0, 8, 1, 8, 1.0, 1.0, 0.0, 2)
