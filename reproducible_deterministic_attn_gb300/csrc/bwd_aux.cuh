@@ -4,9 +4,10 @@
 #pragma once
 
 #include "common.cuh"
-#include "fwd_simt.cuh"
 
 namespace dash {
+
+__device__ __forceinline__ float bf(const __nv_bfloat16 x) { return __bfloat162float(x); }
 
 // ---------------------------------------------------------------------------------
 // Preprocess: D = rowsum(dO * O) (one warp per row, fixed shuffle tree) and -LSE*log2(e)

@@ -8,6 +8,7 @@ namespace dash {
 
 constexpr int kTile = 128;             // KV tile rows = Q tile rows (square task grid)
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 
 // Workspace header (int32 words). The header occupies the first 256 bytes.
 enum : int {
@@ -30,6 +31,7 @@ struct FwdParams {
   int B, S, H, D;
   float scale;
   int causal;
+  float scale_log2;          // scale * log2(e)
 };
 
 struct BwdParams {

@@ -15,9 +15,9 @@
 
 #include "common.cuh"
 #include "bwd_aux.cuh"
-#include "fwd_simt.cuh"
 #include "kernels_tc.cuh"
 #include "kernels_tc128.cuh"
+#include "fwd_tc.cuh"
 #include "sched.h"
 
 namespace {
@@ -269,19 +269,26 @@ dash_status_t dash_attn_fwd(const void* q, const void* k, const void* v, void* o
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return DASH_ERR_INVALID_ARG;
   dash::FwdParams p{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v,
-                    (__nv_bfloat16*)o, lse, B, S, H, D, scale, mask == DASH_MASK_CAUSAL};
-  dim3 grid(S / 64, B * H);
-  const size_t smem = (size_t)(64 * D + 2 * 64 * D + 64 * 65 + 3 * 64) * sizeof(float);
-  if (D == 64) {
-    DASH_CUDA(cudaFuncSetAttribute(dash::fwd_simt_kernel<64>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    dash::fwd_simt_kernel<64><<<grid, 256, smem, stream>>>(p);
-  } else {
-    DASH_CUDA(cudaFuncSetAttribute(dash::fwd_simt_kernel<128>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    dash::fwd_simt_kernel<128><<<grid, 256, smem, stream>>>(p);
+                    (__nv_bfloat16*)o, lse, B, S, H, D, scale, mask == DASH_MASK_CAUSAL,
+                    scale * dash::kLog2e};
+  if (!encoder()) {
+    g_last_error = "cuTensorMapEncodeTiled is not available from the driver";
+    return DASH_ERR_CUDA;
   }
-  DASH_CUDA(cudaGetLastError());
+  dash::tc::TmaMaps maps;
+  if (!map_bshd(&maps.q, q, B, S, H, D, dash::kTile) ||
+      !map_bshd(&maps.k, k, B, S, H, D, dash::kTile) ||
+      !map_bshd(&maps.v, v, B, S, H, D, dash::kTile)) {
+    g_last_error = "cuTensorMapEncodeTiled rejected a tensor";
+    return DASH_ERR_CUDA;
+  }
+  // one CTA per (128-row Q tile, batch * head); blockIdx.x counts the Q tiles from the last
+  dim3 grid(S / dash::kTile, B * H);
+  void* kfn = D == 64 ? (void*)dash::tc::fwd_tc_kernel<64> : (void*)dash::tc::fwd_tc_kernel<128>;
+  const size_t smem = D == 64 ? dash::tc::FwdL<64>::ALLOC : dash::tc::FwdL<128>::ALLOC;
+  DASH_CUDA(cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  void* args[] = {&p, &maps};
+  DASH_CUDA(cudaLaunchKernel(kfn, grid, dim3(dash::tc::kFwdThreads), args, smem, stream));
   return DASH_OK;
 }
 
