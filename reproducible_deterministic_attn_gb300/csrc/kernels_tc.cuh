@@ -535,8 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mbar_arrive(bars + B_STG_EMPTY);
           if (p.deterministic && hs == SUB - 1) {
             ptx::bulk_wait_all();
-            ptx::fence_proxy_async_global();
-            __threadfence();
+            ptx::fence_proxy_async_global();   // the completed bulk adds, then the release
             st_release_gpu(p.sems + sem_idx, o + 1 + p.ordinal_skew);
           }
           tr.add(TR_DQ_REDUCE, t0);

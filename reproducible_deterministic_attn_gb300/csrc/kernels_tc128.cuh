@@ -500,8 +500,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 128; ++c) ptx::red_add_f32(dst + (size_t)c * D, v[c]);
       if (p.deterministic) {
         // Hand the turn on once every read-out thread's adds are ordered before it: warps
-        // 13..15 arrive on E_REDS (release), warp 12's lane 0 waits on it (acquire), then a
-        // gpu-scope fence and the releasing store.
+        // 13..15 arrive on E_REDS (release), warp 12's lane 0 waits on it (acquire), then
+        // the releasing store.
         __syncwarp();
         int done = 1;
         if (warp != 12) {
@@ -509,10 +509,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           if (lane == 0) {
             done = ptx::mbar_wait(bars + E_REDS, it & 1, abort_flag, tmo) ? 1 : 0;
-            if (done) {
-              __threadfence();
+            if (done)   // release store: orders every add above (this warp's via __syncwarp,
+                        // the others' via E_REDS) before the new ordinal at gpu scope
               st_release_gpu(p.sems + sem_idx, o + 1 + p.ordinal_skew);
-            }
           }
           done = __shfl_sync(0xffffffffu, done, 0);
         }
