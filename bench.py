@@ -296,6 +296,10 @@ def run_gpu(args, w, rank, world, local_rank):
         args.schedule = {v: k for k, v in da.SCHEDULES.items()}[choice]
         selected_by = "dash_sched_select, costs " + json.dumps(SELECT_COSTS)
     sched = da.SCHEDULES[args.schedule]
+    # deterministic mode: 1 = one fixed chain per dQ block (the pages' order as one serial
+    # chain), 2 = the same order as two interleaved chains; measured on GB300 the second is
+    # faster at head dim 128 (687 vs 588 TF/s on full 2x8192x16x128) and not at 64
+    DET = (2 if D == 128 else 1) if args.dq_chains == "auto" else int(args.dq_chains)
 
     x = make_inputs(B, S, H, D, seed=rank)
     q, k, v, do = (x[nm].to(dev) for nm in ("q", "k", "v", "do"))
@@ -306,7 +310,7 @@ def run_gpu(args, w, rank, world, local_rank):
     if input_bytes(w) <= L2_BYTES:
         flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
 
-    def step(det=1, s=sched):
+    def step(det=DET, s=sched):
         if flush is not None:
             flush.fill_(1)
         da.dash_attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, scale, mask, s, det)
@@ -316,7 +320,7 @@ def run_gpu(args, w, rank, world, local_rank):
         if world > 1:
             dist.barrier()
 
-    def timed(n_steps, det=1, s=sched, profile=False):
+    def timed(n_steps, det=DET, s=sched, profile=False):
         barrier()
         if profile:
             da.dash_profile_enable(True)
@@ -364,8 +368,11 @@ def run_gpu(args, w, rank, world, local_rank):
     # FA3-baseline ascending order
     side = {}
     n_side = max(3, steps // 4)
-    for name, det, s in (("nondet", 0, da.SCHED_ASCENDING), ("ascending", 1, da.SCHED_ASCENDING),
-                         ("descending", 1, da.SCHED_DESCENDING)):
+    variants = [("nondet", 0, da.SCHED_ASCENDING), ("ascending", DET, da.SCHED_ASCENDING),
+                ("descending", DET, da.SCHED_DESCENDING)]
+    if DET != 1:
+        variants.append(("single_chain", 1, sched))
+    for name, det, s in variants:
         if name == args.schedule:
             continue
         for _ in range(2):
@@ -389,7 +396,7 @@ def run_gpu(args, w, rank, world, local_rank):
         o.copy_(host["o"], non_blocking=True)
         do.copy_(host["do"], non_blocking=True)
         lse.copy_(host["lse"], non_blocking=True)
-        da.dash_attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, scale, mask, sched, 1)
+        da.dash_attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, scale, mask, sched, DET)
         outs["dq"].copy_(dq, non_blocking=True)
         outs["dk"].copy_(dk, non_blocking=True)
         outs["dv"].copy_(dv, non_blocking=True)
@@ -415,11 +422,14 @@ def run_gpu(args, w, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": steps,
         "warmup": warm, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {**workload_config(args, w), "schedule_selected_by": selected_by},
+        "config": {**workload_config(args, w), "schedule_selected_by": selected_by,
+                   "dq_chains": DET},
         "pct_of_peak": 100.0 * value / world / peak_tf,
         "nondet_tflops": side.get("nondet"),
         "det_vs_nondet": value / side["nondet"] if side.get("nondet") else None,
-        "schedules": {args.schedule: value, **{kk: vv for kk, vv in side.items() if kk != "nondet"}},
+        "schedules": {args.schedule: value,
+                      **{kk: vv for kk, vv in side.items() if kk not in ("nondet", "single_chain")}},
+        "det_single_chain_tflops": side.get("single_chain", value if DET == 1 else None),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf,
                      "unit": "TFLOP/s", "frac": (achieved / peak_tf) if achieved else None,
                      "traffic": traffic_from_profile(w, args.schedule),
@@ -444,6 +454,8 @@ def main():
     ap.add_argument("--schedule", default="auto",
                     choices=["auto", "ascending", "descending", "shift", "symmetric_shift"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dq-chains", default="auto", choices=["auto", "1", "2"],
+                    help="deterministic dQ order as 1 chain or 2 interleaved chains")
     args = ap.parse_args()
     w = WORKLOADS[args.workload]
     if args.schedule == "auto" and args.impl == "reference":

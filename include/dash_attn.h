@@ -79,8 +79,9 @@ dash_status_t dash_attn_fwd(const void* q, const void* k, const void* v, void* o
 
 /*
  * Bytes of scratch dash_attn_bwd needs for this shape: a status header, D = rowsum(dO*O)
- * and -LSE*log2(e) (two fp32 [B,H,S] arrays), the fp32 dQ accumulator [B,H,S,D] and one
- * int32 semaphore per dQ block [B,H,S/128]. Returns 0 for an unsupported shape.
+ * and -LSE*log2(e) (two fp32 [B,H,S] arrays), two copies of the fp32 dQ accumulator
+ * [2,B,H,S,D] (deterministic = 2 uses both) and two int32 semaphores per 128-row dQ block,
+ * one per chain [B,H,S/128,2]. Returns 0 for an unsupported shape.
  */
 size_t dash_attn_bwd_workspace_size(int B, int S, int H, int D);
 
@@ -90,10 +91,17 @@ size_t dash_attn_bwd_workspace_size(int B, int S, int H, int D);
  * KV tile's dK/dV accumulates on one SM. Each dQ block is the sum of one partial per KV
  * tile that sees it:
  *   deterministic = 1: the partials are added in the fixed order `schedule` defines,
- *                      serialised through one semaphore per dQ block. The result is
+ *                      serialised through semaphores per dQ block. The result is
  *                      bitwise identical for identical inputs, shape and schedule on the
  *                      same GPU model and build. Different schedules may differ in the
  *                      last bits (their dQ orders differ).
+ *   deterministic = 2: the same fixed order run as two interleaved chains: the partial
+ *                      at position p of the order is added, in order, into fp32
+ *                      accumulator copy p mod 2, after the partial at position p - 2, and
+ *                      dQ = copy 0 + copy 1. A partial waits only for the one two places
+ *                      before it, so the hand-off between SMs leaves the critical path.
+ *                      Bitwise identical run to run like 1 (its bits differ from 1's: the
+ *                      additions are grouped differently).
  *   deterministic = 0: the partials are added atomically in arrival order (the speed
  *                      reference; results vary in the last bits run to run).
  *   q, k, v, o, dO : [B, S, H, D] bf16 (read);  lse : [B, H, S] fp32 (read)

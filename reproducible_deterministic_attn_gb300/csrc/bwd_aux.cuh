@@ -37,7 +37,7 @@ __global__ void bwd_preprocess_kernel(BwdParams p) {
   const long long nth = (long long)gridDim.x * blockDim.x;
   for (long long e = tid; e < p.num_sems; e += nth) p.sems[e] = 0;
   if (tid < (long long)(kWsHeaderBytes / sizeof(int))) p.ws_header[tid] = 0;
-  const long long nacc4 = (long long)p.B * p.H * p.S * p.D / 4;
+  const long long nacc4 = (long long)p.chains * p.B * p.H * p.S * p.D / 4;   // copies in use
   float4* acc4 = reinterpret_cast<float4*>(p.dq_acc);
   for (long long e = tid; e < nacc4; e += nth) acc4[e] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
@@ -52,7 +52,10 @@ __global__ void dq_convert_kernel(BwdParams p) {
     const int s = (int)(row % p.S);
     const long long bh = row / p.S;
     const int h = (int)(bh % p.H), b = (int)(bh / p.H);
-    p.dq[(((size_t)b * p.S + s) * p.H + h) * p.D + c] = __float2bfloat16(p.scale * p.dq_acc[e]);
+    // k interleaved chains: the copies added in index order
+    float a = p.dq_acc[e];
+    for (int c = 1; c < p.chains; ++c) a += p.dq_acc[e + (long long)c * n];
+    p.dq[(((size_t)b * p.S + s) * p.H + h) * p.D + c] = __float2bfloat16(p.scale * a);
   }
 }
 

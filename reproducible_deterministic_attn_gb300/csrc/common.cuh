@@ -20,6 +20,14 @@ enum : int {
 };
 constexpr size_t kWsHeaderBytes = 256;
 constexpr int kStatusSyncTimeout = 5;
+// The fixed dQ order of a block runs as k = deterministic interleaved chains (1 <= k <=
+// kDqChains): contribution o adds, in order, into accumulator copy o % k after
+// contribution o - k, so k = 1 is one serial chain; the convert adds the copies in index
+// order. Semaphore of (bh, block j, chain c): sems[(bh * n + j) * kDqChains + c]; copy c
+// of the accumulator starts at dq_acc + c * B*H*S*D. Measured on GB300 (full 2x8192x16x128,
+// shift): k = 1, 2, 3, 4 give 588, 687, 666, 675 TFLOP/s -- beyond two chains the extra
+// copies cost more than the shorter waits save, so two is the maximum.
+constexpr int kDqChains = 2;
 constexpr int kStatusSmemLayout = 4;   // reported as DASH_ERR_CUDA: unusable shared-memory base
 
 struct FwdParams {
@@ -49,7 +57,8 @@ struct BwdParams {
   float* nlse2;              // [B, H, S] -LSE * log2(e) (the exponent offset of P in base 2)
   float* dq_acc;             // [B, H, S, D] fp32
   int* sems;                 // [B, H, n]: one per 128-row dQ block
-  int num_sems;
+  int num_sems;               // B * H * n * kDqChains
+  int chains;                 // interleaved dQ chains, 1..kDqChains (deterministic mode)
   const int32_t* slot_off;   // schedule: chain offsets
   const int32_t* tasks;      // schedule: (kv << 16) | q
   const int32_t* ord;        // schedule: n * n ordinals

@@ -208,8 +208,9 @@ WsLayout ws_layout(int B, int S, int H, int D) {
   w.dsum = dash::kWsHeaderBytes;
   w.nlse2 = round_up(w.dsum + rows * sizeof(float), 256);
   w.dq_acc = round_up(w.nlse2 + rows * sizeof(float), 256);
-  w.sems = round_up(w.dq_acc + rows * D * sizeof(float), 256);
-  w.total = round_up(w.sems + (size_t)B * H * (S / dash::kTile) * sizeof(int), 256);
+  w.sems = round_up(w.dq_acc + dash::kDqChains * rows * D * sizeof(float), 256);   // k copies
+  w.total = round_up(w.sems + (size_t)B * H * (S / dash::kTile) * dash::kDqChains * sizeof(int),
+                     256);
   return w;
 }
 
@@ -303,7 +304,7 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
   if (mask != DASH_MASK_FULL && mask != DASH_MASK_CAUSAL) return DASH_ERR_INVALID_ARG;
   if (schedule < DASH_SCHED_ASCENDING || schedule > DASH_SCHED_SYMMETRIC_SHIFT)
     return DASH_ERR_INVALID_ARG;
-  if (deterministic != 0 && deterministic != 1) return DASH_ERR_INVALID_ARG;
+  if (deterministic < 0 || deterministic > dash::kDqChains) return DASH_ERR_INVALID_ARG;
   if (!(scale > 0.f)) return DASH_ERR_INVALID_ARG;
   if (!shape_ok(B, S, H, D)) return DASH_ERR_UNSUPPORTED;
   for (const void* ptr : {q, k, v, o, dO, (const void*)lse, (const void*)dq, (const void*)dk,
@@ -354,12 +355,13 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
   p.scale = scale;
   p.scale_log2 = scale * dash::kLog2e;
   p.causal = mask == DASH_MASK_CAUSAL;
-  p.deterministic = deterministic;
+  p.deterministic = deterministic != 0;
+  p.chains = deterministic > 1 ? deterministic : 1;
   p.timeout_ns = g_timeout_ns;
   p.ordinal_skew = g_ordinal_skew;
   p.trace = g_trace;
 
-  p.num_sems = B * H * n;
+  p.num_sems = B * H * n * dash::kDqChains;
 
   // Persistent grid, one CTA per SM: every CTA must be resident at once (the ordered
   // reduction waits on other CTAs), so the launch is cooperative.
@@ -373,7 +375,7 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
   if (!map_bshd(&maps.q, q, B, S, H, D, br) || !map_bshd(&maps.dO, dO, B, S, H, D, br) ||
       !map_bshd(&maps.k, k, B, S, H, D, dash::kTile) ||
       !map_bshd(&maps.v, v, B, S, H, D, dash::kTile) ||
-      !map_acc(&maps.acc, p.dq_acc, (long long)B * H * S, D, br)) {
+      !map_acc(&maps.acc, p.dq_acc, (long long)dash::kDqChains * B * H * S, D, br)) {
     g_last_error = "cuTensorMapEncodeTiled rejected a tensor";
     return DASH_ERR_CUDA;
   }
@@ -598,7 +600,7 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
   if (mask != DASH_MASK_FULL && mask != DASH_MASK_CAUSAL) return DASH_ERR_INVALID_ARG;
   if (schedule < DASH_SCHED_ASCENDING || schedule > DASH_SCHED_SYMMETRIC_SHIFT)
     return DASH_ERR_INVALID_ARG;
-  if (deterministic != 0 && deterministic != 1) return DASH_ERR_INVALID_ARG;
+  if (deterministic < 0 || deterministic > dash::kDqChains) return DASH_ERR_INVALID_ARG;
   if (!(scale > 0.f)) return DASH_ERR_INVALID_ARG;
   if (!shape_ok(B, S, H, D)) return DASH_ERR_UNSUPPORTED;
   for (const void* ptr : {q, k, v, o, dO, (const void*)lse, (const void*)dq, (const void*)dk,
@@ -670,11 +672,12 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
   p.scale = scale;
   p.scale_log2 = scale * dash::kLog2e;
   p.causal = mask == DASH_MASK_CAUSAL;
-  p.deterministic = deterministic;
+  p.deterministic = deterministic != 0;
+  p.chains = deterministic > 1 ? deterministic : 1;
   p.timeout_ns = g_timeout_ns;
   p.ordinal_skew = g_ordinal_skew;
   p.trace = nullptr;
-  p.num_sems = B * H * n;
+  p.num_sems = B * H * n * dash::kDqChains;
 
   if (!encoder()) {
     g_last_error = "cuTensorMapEncodeTiled is not available from the driver";
@@ -686,7 +689,7 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
   if (!map_bshd(&maps.q, q, B, S, H, D, br) || !map_bshd(&maps.dO, dO, B, S, H, D, br) ||
       !map_bshd(&maps.k, k, B, S, H, D, dash::kTile) ||
       !map_bshd(&maps.v, v, B, S, H, D, dash::kTile) ||
-      !map_acc(&maps.acc, p.dq_acc, (long long)B * H * S, D, br)) {
+      !map_acc(&maps.acc, p.dq_acc, (long long)dash::kDqChains * B * H * S, D, br)) {
     g_last_error = "cuTensorMapEncodeTiled rejected a tensor";
     return DASH_ERR_CUDA;
   }

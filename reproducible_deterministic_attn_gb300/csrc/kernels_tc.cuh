@@ -512,8 +512,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = ptx::mbar_wait(bars + B_STG_FULL, it & 1, abort_flag, tmo);
           tr.add(TR_DQ_FULL, t0);
           if (!ok) break;
-          const int sem_idx = w.bh * p.n + w.j;
-          const int o = p.ord[w.i * p.n + w.j];
+          const int ord = p.ord[w.i * p.n + w.j];
+          const int chain = ord % p.chains, o = ord / p.chains;   // interleaved chains
+          const int sem_idx = (w.bh * p.n + w.j) * kDqChains + chain;
           if (p.deterministic && hs == 0) {
             t0 = tr.t0();
             ok = wait_turn(p.sems + sem_idx, o + p.ordinal_skew, p.ws_header, p.timeout_ns,
@@ -529,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int bx = 0; bx < D / 32; ++bx)
             ptx::tma_reduce_add_2d(&maps.acc, sm + L::STG_OFF + bx * (BR * 128), bx * 32,
-                                   w.bh * p.S + q0);
+                                   chain * p.B * p.H * p.S + w.bh * p.S + q0);
           ptx::bulk_commit();
           ptx::bulk_wait_read_all();
           ptx::mbar_arrive(bars + B_STG_EMPTY);

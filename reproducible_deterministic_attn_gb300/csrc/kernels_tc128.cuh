@@ -473,8 +473,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bars + E_DQ_EMPTY);   // dQ^T(it) has left TMEM
-      const int sem_idx = w.bh * p.n + w.j;
-      const int o = p.ord[w.i * p.n + w.j];
+      // The block's fixed order runs as p.chains interleaved chains: contribution o waits
+      // for o - chains, in chain o % chains, adding into accumulator copy o % chains.
+      const int ord = p.ord[w.i * p.n + w.j];
+      const int chain = ord % p.chains, o = ord / p.chains;
+      const int sem_idx = (w.bh * p.n + w.j) * kDqChains + chain;
       if (p.deterministic) {
         // The 128-row block's turn: lane 0 of warp 12 polls the semaphore and signals
         // E_TURN; the other read-out warps wait on it (bounded, like every wait here).
@@ -495,7 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!got) break;
       }
       t0 = trq.t0();
-      float* dst = p.dq_acc + ((size_t)w.bh * p.S + (size_t)w.j * kTile) * D + row;
+      float* dst = p.dq_acc + (size_t)chain * p.B * p.H * p.S * D +
+                   ((size_t)w.bh * p.S + (size_t)w.j * kTile) * D + row;
 #pragma unroll
       for (int c = 0; c < 128; ++c) ptx::red_add_f32(dst + (size_t)c * D, v[c]);
       if (p.deterministic) {

@@ -259,15 +259,18 @@ def attn_forward(q, k, v, scale: float, causal: bool, stream=None):
 
 
 def attn_backward(q, k, v, o, dO, lse, scale: float, causal: bool, schedule="ascending",
-                  deterministic: bool = True, workspace=None, stream=None, check: bool = True):
-    """Allocates dQ/dK/dV (and a workspace if none is given) and runs dash_attn_bwd."""
+                  deterministic=True, workspace=None, stream=None, check: bool = True):
+    """Allocates dQ/dK/dV (and a workspace if none is given) and runs dash_attn_bwd.
+
+    deterministic: False/0 (arrival order), True/1 (one fixed chain per dQ block) or 2 (the
+    fixed order as two interleaved chains)."""
     B, S, H, D = _shape(q)
     if workspace is None:
         workspace = new_workspace(B, S, H, D, q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     sched = SCHEDULES[schedule] if isinstance(schedule, str) else int(schedule)
     dash_attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, workspace, scale,
-                  MASK_CAUSAL if causal else MASK_FULL, sched, int(bool(deterministic)), stream)
+                  MASK_CAUSAL if causal else MASK_FULL, sched, int(deterministic), stream)
     if check:
         _check(dash_attn_get_status(workspace, stream), "dash_attn_bwd (device status)")
     return dq, dk, dv

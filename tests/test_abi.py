@@ -46,7 +46,7 @@ def test_status_strings(lib):
 def test_workspace_size(lib):
     B, S, H, D = 2, 256, 3, 64
     ws = da.dash_attn_bwd_workspace_size(B, S, H, D)
-    need = 256 + 2 * B * H * S * 4 + B * H * S * D * 4 + B * H * (S // 128) * 4
+    need = 256 + 2 * B * H * S * 4 + 2 * B * H * S * D * 4 + B * H * (S // 128) * 2 * 4
     assert need <= ws <= need + 4 * 256 and ws % 256 == 0
     assert da.dash_attn_bwd_workspace_size(1, 100, 1, 64) == 0      # S not a multiple of 128
     assert da.dash_attn_bwd_workspace_size(1, 128, 1, 96) == 0      # unsupported head dim
@@ -66,7 +66,8 @@ def test_bwd_rejects_bad_arguments_without_touching_the_device(lib):
     assert _bwd(lib, B=0) == da.DASH_ERR_INVALID_ARG
     assert _bwd(lib, mask=2) == da.DASH_ERR_INVALID_ARG
     assert _bwd(lib, sched=4) == da.DASH_ERR_INVALID_ARG
-    assert _bwd(lib, det=2) == da.DASH_ERR_INVALID_ARG
+    assert _bwd(lib, det=3) == da.DASH_ERR_INVALID_ARG
+    assert _bwd(lib, det=-1) == da.DASH_ERR_INVALID_ARG
     assert _bwd(lib, scale=0.0) == da.DASH_ERR_INVALID_ARG
     assert _bwd(lib, D=96) == da.DASH_ERR_UNSUPPORTED
     assert _bwd(lib, S=200) == da.DASH_ERR_UNSUPPORTED

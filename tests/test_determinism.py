@@ -52,11 +52,25 @@ CASES = [
 def test_bitwise_reproducible(shape, causal, scheds):
     args = _setup(*shape, causal)
     for sched in scheds:
-        outs = _runs(args, causal, sched, 1, RUNS)
-        for t in range(3):
-            ref = outs[0][t]
-            for other in outs[1:]:
-                assert torch.equal(other[t], ref), (sched, "dq dk dv".split()[t])
+        for det in (1, 2):                       # one chain; two interleaved chains
+            outs = _runs(args, causal, sched, det, RUNS)
+            for t in range(3):
+                ref = outs[0][t]
+                for other in outs[1:]:
+                    assert torch.equal(other[t], ref), (sched, det, "dq dk dv".split()[t])
+
+
+@pytest.mark.parametrize("shape,causal,sched", [((4, 2048, 16, 64), True, "symmetric_shift"),
+                                                ((1, 4096, 8, 128), False, "shift")])
+def test_two_chains_change_only_the_grouping_of_dq(shape, causal, sched):
+    # dK and dV never pass through the dQ chains; dQ differs from one chain only by
+    # rounding (the same partials, grouped as even + odd positions)
+    args = _setup(*shape, causal)
+    one = _runs(args, causal, sched, 1, 1)[0]
+    two = _runs(args, causal, sched, 2, 1)[0]
+    assert torch.equal(one[1], two[1]) and torch.equal(one[2], two[2])
+    ref = one[0].float()
+    assert float((two[0].float() - ref).abs().max()) <= 2e-2 * float(ref.abs().max())
 
 
 @pytest.mark.parametrize("shape,causal", [((4, 2048, 16, 64), True), ((1, 4096, 8, 128), False)])

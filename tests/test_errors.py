@@ -24,26 +24,26 @@ def _built():
     ensure_built()
 
 
-@pytest.mark.parametrize("D", [64, 128])
-def test_sync_timeout_is_reported_and_context_survives(D):
+@pytest.mark.parametrize("D,det", [(64, 1), (128, 1), (128, 2)])
+def test_sync_timeout_is_reported_and_context_survives(D, det):
     B, S, H = 1, 512, 2
     x = make_inputs(B, S, H, D, 3)
     q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
     scale = 1 / math.sqrt(D)
     o, lse = da.attn_forward(q, k, v, scale, False)
-    ref = da.attn_backward(q, k, v, o, do, lse, scale, False, "shift", 1)
+    ref = da.attn_backward(q, k, v, o, do, lse, scale, False, "shift", det)
     ws = da.new_workspace(B, S, H, D, q.device)
     try:
         da.dash_debug_set_sync(50_000_000, 1)          # 50 ms per wait, unreachable ordinals
         dq, dk, dv = (torch.empty_like(q) for _ in range(3))
         da.dash_attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, scale, da.MASK_FULL,
-                         da.SCHED_SHIFT, 1)
+                         da.SCHED_SHIFT, det)
         st = da.dash_attn_get_status(ws)
         assert st == da.DASH_ERR_SYNC_TIMEOUT
         assert "timed out" in da.dash_last_error()
     finally:
         da.dash_debug_set_sync(0, 0)
-    again = da.attn_backward(q, k, v, o, do, lse, scale, False, "shift", 1, workspace=ws)
+    again = da.attn_backward(q, k, v, o, do, lse, scale, False, "shift", det, workspace=ws)
     for a, b in zip(again, ref):
         assert torch.equal(a, b)
 

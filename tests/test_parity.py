@@ -33,7 +33,7 @@ PAIRS = [("full", "ascending"), ("full", "descending"), ("full", "shift"),
 
 @pytest.mark.parametrize("shape", SMALL, ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("mask,sched", PAIRS, ids=lambda x: x)
-@pytest.mark.parametrize("det", [1, 0])
+@pytest.mark.parametrize("det", [1, 0, 2])
 def test_small_shapes(shape, mask, sched, det):
     B, S, H, D = shape
     n = S // 128
@@ -55,7 +55,8 @@ def test_config2_causal_4x2048x16x64(sched):
     assert_within(check_against_oracle(res, True, heads=[(0, 0), (1, 7), (3, 15)]))
 
 
-@pytest.mark.parametrize("sched,det", [("ascending", 1), ("shift", 1), ("ascending", 0)])
+@pytest.mark.parametrize("sched,det", [("ascending", 1), ("shift", 1), ("ascending", 0),
+                                       ("shift", 2)])
 def test_config3_full_2x8192x16x128_sampled(sched, det):
     res = run_case(2, 8192, 16, 128, False, sched, det)
     assert_within(check_against_oracle(res, False, heads=[(0, 3), (1, 15)]))
