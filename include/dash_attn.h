@@ -261,6 +261,26 @@ dash_status_t dash_sched_select(int mask, int n, int heads, int num_sms, double 
                                 double h, int overlapped, int* schedule_out,
                                 double* makespan_out);
 
+/*
+ * Deterministic split-K GEMM with the same ordered cross-SM reduction (the Pith review's
+ * "What would settle it" names a deterministic split-K GEMM as the DAG framing's next
+ * application): C = A B^T with
+ *   a : bf16 [M, K] row-major (read);  b : bf16 [N, K] row-major (read);
+ *   c : fp32 [M, N] row-major (written: zeroed, then every K chunk's partial added);
+ *   workspace : device scratch of dash_gemm_splitk_workspace_size(M, N) bytes, 256-byte
+ *               aligned (status header + one int32 semaphore per 128 x 128 output tile);
+ *   splits : K is cut into `splits` equal chunks, one unit of work each per output tile;
+ *   deterministic = 1: a tile's chunks are added in ascending chunk order (bitwise
+ *               identical run to run); 0: in arrival order.
+ * Requires M, N multiples of 128, K a multiple of 64 * splits, M * N < 2^31
+ * (else DASH_ERR_UNSUPPORTED). Asynchronous on `stream`; dash_attn_get_status(workspace)
+ * reports a timed-out wait (DASH_ERR_SYNC_TIMEOUT) as for the backward.
+ */
+size_t dash_gemm_splitk_workspace_size(int M, int N);
+dash_status_t dash_gemm_splitk(const void* a, const void* b, float* c, void* workspace,
+                               size_t workspace_bytes, int M, int N, int K, int splits,
+                               int deterministic, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

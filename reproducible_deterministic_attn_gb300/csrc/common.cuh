@@ -107,6 +107,10 @@ __device__ __forceinline__ void st_release_gpu(int* p, int v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+__device__ __forceinline__ void red_release_add_gpu(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // Spin (one thread) until *sem == target. Gives up when another CTA has already
 // reported a failure, or after timeout_ns, recording the first failure in the
 // workspace header. Returns true when it is this CTA's turn.
@@ -123,6 +127,37 @@ __device__ __noinline__ bool wait_turn(const int* sem, int target, int* ws, long
   for (long long it = 1; it <= max_iter; ++it) {
     seen = ld_acquire_gpu(sem);
     if (seen == target) return true;
+    if ((it & 31) == 0) {
+      if (ld_relaxed_gpu(ws + WS_STATUS) != 0) return false;
+      if (global_timer_ns() - t0 > timeout_ns) break;
+    }
+  }
+  if (atomicCAS(ws + WS_STATUS, 0, kStatusSyncTimeout) == 0) {
+    ws[WS_BH] = bh;
+    ws[WS_QTILE] = qtile;
+    ws[WS_EXPECT] = target;
+    ws[WS_SEEN] = seen;
+    __threadfence();
+  }
+  return false;
+}
+
+// Spin (one thread) until *sem >= target (a counter that only grows). Gives up when another CTA has already
+// reported a failure, or after timeout_ns, recording the first failure in the
+// workspace header. Returns true when it is this CTA's turn.
+__device__ __noinline__ bool wait_at_least(const int* sem, int target, int* ws, long long timeout_ns,
+                                       int bh, int qtile) {
+  int seen = ld_acquire_gpu(sem);
+  if (seen >= target) return true;
+  const long long t0 = global_timer_ns();
+  // The hand-off latency adds to every step of the serial order, so the semaphore is
+  // polled back to back (one L2 round trip per poll); the failure flag and the timer are
+  // looked at every 32nd poll. The iteration cap is a second bound, independent of the
+  // timer (a poll takes well over 16 ns).
+  const long long max_iter = timeout_ns / 16 + (1ll << 20);
+  for (long long it = 1; it <= max_iter; ++it) {
+    seen = ld_acquire_gpu(sem);
+    if (seen >= target) return true;
     if ((it & 31) == 0) {
       if (ld_relaxed_gpu(ws + WS_STATUS) != 0) return false;
       if (global_timer_ns() - t0 > timeout_ns) break;

@@ -18,6 +18,7 @@
 #include "kernels_tc.cuh"
 #include "kernels_tc128.cuh"
 #include "fwd_tc.cuh"
+#include "gemm_splitk.cuh"
 #include "sched.h"
 
 namespace {
@@ -194,6 +195,19 @@ bool map_acc(CUtensorMap* m, float* ptr, long long rows_total, int D, int rows) 
   const cuuint32_t es[2] = {1, 1};
   return encoder()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2D view [rows][K] of a row-major bf16 matrix; box = 64 K-columns x 128 rows, 128-byte
+// swizzle.
+bool map_rows_k(CUtensorMap* m, const void* ptr, int rows, int K) {
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t es[2] = {1, 1};
+  return encoder()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -499,6 +513,65 @@ dash_status_t dash_sched_simulate(int mask, int schedule, int n, int heads, int 
   std::vector<double> ends;
   if (!dash::simulate(sc, heads, num_sms, c, r, makespan, &ends)) return DASH_ERR_DEADLOCK_RISK;
   if (sm_end) std::memcpy(sm_end, ends.data(), ends.size() * sizeof(double));
+  return DASH_OK;
+}
+
+size_t dash_gemm_splitk_workspace_size(int M, int N) {
+  if (M < 128 || N < 128 || M % 128 || N % 128) return 0;
+  return round_up(dash::kWsHeaderBytes + (size_t)(M / 128) * (N / 128) * sizeof(int), 256);
+}
+
+dash_status_t dash_gemm_splitk(const void* a, const void* b, float* c, void* workspace,
+                               size_t workspace_bytes, int M, int N, int K, int splits,
+                               int deterministic, cudaStream_t stream) {
+  if (!a || !b || !c || !workspace) return DASH_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1 || splits < 1) return DASH_ERR_INVALID_ARG;
+  if (deterministic != 0 && deterministic != 1) return DASH_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(c) || ((uintptr_t)workspace & 255))
+    return DASH_ERR_INVALID_ARG;
+  if (M % 128 || N % 128 || K % (64 * splits) || (long long)M * N >= (1ll << 31))
+    return DASH_ERR_UNSUPPORTED;
+  if (workspace_bytes < dash_gemm_splitk_workspace_size(M, N)) return DASH_ERR_WORKSPACE_TOO_SMALL;
+  if (!encoder()) {
+    g_last_error = "cuTensorMapEncodeTiled is not available from the driver";
+    return DASH_ERR_CUDA;
+  }
+  dash::tc::GemmMaps maps;
+  if (!map_rows_k(&maps.a, a, M, K) || !map_rows_k(&maps.b, b, N, K)) {
+    g_last_error = "cuTensorMapEncodeTiled rejected a tensor";
+    return DASH_ERR_CUDA;
+  }
+  unsigned char* ws = (unsigned char*)workspace;
+  dash::tc::GemmParams p;
+  p.c = c;
+  p.status = (int*)ws;
+  p.sems = (int*)(ws + dash::kWsHeaderBytes);
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.splits = splits;
+  p.kchunk = K / splits;
+  p.deterministic = deterministic;
+  p.timeout_ns = g_timeout_ns;
+  // C, the status header and the tile semaphores start at zero
+  DASH_CUDA(cudaMemsetAsync(c, 0, (size_t)M * N * sizeof(float), stream));
+  DASH_CUDA(cudaMemsetAsync(ws, 0, dash_gemm_splitk_workspace_size(M, N), stream));
+  int dev = 0, sms = 0;
+  DASH_CUDA(cudaGetDevice(&dev));
+  DASH_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const int units = (M / 128) * (N / 128) * splits;
+  const int grid = units < sms ? units : sms;
+  void* kfn = (void*)dash::tc::gemm_splitk_kernel;
+  const size_t smem = dash::tc::GemmL::ALLOC;
+  DASH_CUDA(cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  void* args[] = {&p, &maps};
+  // deterministic: chunks wait on other CTAs' adds, so every CTA must be resident at once;
+  // the waits follow the dealing order, so they cannot form a cycle on any grid
+  if (deterministic)
+    DASH_CUDA(cudaLaunchCooperativeKernel(kfn, dim3(grid), dim3(dash::tc::kGemmThreads), args,
+                                          smem, stream));
+  else
+    DASH_CUDA(cudaLaunchKernel(kfn, dim3(grid), dim3(dash::tc::kGemmThreads), args, smem, stream));
   return DASH_OK;
 }
 

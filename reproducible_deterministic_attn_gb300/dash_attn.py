@@ -62,6 +62,9 @@ _SIGNATURES = {
                                         _c_double, _c_double, _c_int, _dblp, _dblp]),
     "dash_sched_select": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_double, _c_double,
                                    _c_double, _c_int, ctypes.POINTER(_c_int), _dblp]),
+    "dash_gemm_splitk_workspace_size": (ctypes.c_size_t, [_c_int, _c_int]),
+    "dash_gemm_splitk": (_c_int, [_vp, _vp, _vp, _vp, ctypes.c_size_t, _c_int, _c_int, _c_int,
+                                  _c_int, _c_int, _vp]),
 }
 
 
@@ -238,6 +241,35 @@ def dash_sched_select(mask: int, n: int, heads: int, num_sms: int, c: float, r: 
                                   ctypes.byref(mk))
     _check(st, "dash_sched_select")
     return sched.value, mk.value
+
+
+def dash_gemm_splitk_workspace_size(M: int, N: int) -> int:
+    return int(load().dash_gemm_splitk_workspace_size(int(M), int(N)))
+
+
+def dash_gemm_splitk(a: torch.Tensor, b: torch.Tensor, c: torch.Tensor, workspace: torch.Tensor,
+                     splits: int, deterministic: int, stream=None) -> None:
+    """C = A B^T (a: bf16 [M, K], b: bf16 [N, K], c: fp32 [M, N]), K in `splits` chunks."""
+    M, K = a.shape
+    N = b.shape[0]
+    _check(load().dash_gemm_splitk(a.data_ptr(), b.data_ptr(), c.data_ptr(), workspace.data_ptr(),
+                                   workspace.numel() * workspace.element_size(), int(M), int(N),
+                                   int(K), int(splits), int(deterministic), _stream(a, stream)),
+           "dash_gemm_splitk")
+
+
+def gemm_splitk(a: torch.Tensor, b: torch.Tensor, splits: int, deterministic: int = 1,
+                workspace=None, stream=None, check: bool = True) -> torch.Tensor:
+    """Allocates C (and a workspace if none is given) and runs dash_gemm_splitk."""
+    M, N = a.shape[0], b.shape[0]
+    if workspace is None:
+        workspace = torch.empty(dash_gemm_splitk_workspace_size(M, N), dtype=torch.uint8,
+                                device=a.device)
+    c = torch.empty((M, N), dtype=torch.float32, device=a.device)
+    dash_gemm_splitk(a, b, c, workspace, splits, deterministic, stream)
+    if check:
+        _check(dash_attn_get_status(workspace, stream), "dash_gemm_splitk (device status)")
+    return c
 
 
 # ---- conveniences (allocation through torch; the compute stays in the library) ----

@@ -11,7 +11,7 @@ from __future__ import annotations
 
 import torch
 
-__all__ = ["make_inputs"]
+__all__ = ["make_inputs", "make_gemm_inputs"]
 
 
 def make_inputs(b: int, s: int, h: int, d: int, seed: int = 0) -> dict[str, torch.Tensor]:
@@ -21,3 +21,13 @@ def make_inputs(b: int, s: int, h: int, d: int, seed: int = 0) -> dict[str, torc
     for name in ("q", "k", "v", "do"):
         out[name] = torch.randn((b, s, h, d), generator=gen, dtype=torch.float32).to(torch.bfloat16)
     return out
+
+
+def make_gemm_inputs(m: int, n: int, k: int, seed: int = 0) -> dict[str, torch.Tensor]:
+    """Return {'a': [m, k], 'b': [n, k]}: N(0, 1) drawn in float32 in the order a, b from
+    ``torch.Generator().manual_seed(seed)``, rounded to contiguous bf16 CPU tensors."""
+    gen = torch.Generator().manual_seed(seed)
+    a = torch.randn((m, k), generator=gen, dtype=torch.float32).to(torch.bfloat16)
+    b = torch.randn((n, k), generator=gen, dtype=torch.float32).to(torch.bfloat16)
+    return {"a": a, "b": b}
+

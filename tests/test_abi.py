@@ -83,3 +83,21 @@ def test_fwd_rejects_bad_arguments(lib):
     assert f(None, 16, 16, 16, 16, 1, 128, 1, 64, 0.1, 0, None) == da.DASH_ERR_INVALID_ARG
     assert f(16, 16, 16, 16, 16, 1, 128, 1, 32, 0.1, 0, None) == da.DASH_ERR_UNSUPPORTED
     assert f(16, 16, 16, 16, 16, 1, 128, 1, 64, 0.1, 7, None) == da.DASH_ERR_INVALID_ARG
+
+
+def test_gemm_splitk_rejects_bad_arguments_without_touching_the_device(lib):
+    f = lib.dash_gemm_splitk
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_size_t] + [ctypes.c_int] * 5 + [ctypes.c_void_p]
+    ws_need = da.dash_gemm_splitk_workspace_size(256, 256)
+    assert ws_need == 256 + 4 * 4 or ws_need % 256 == 0
+    def call(a=16, b=16, c=16, ws=256, wsb=1 << 20, M=256, N=256, K=512, splits=2, det=1):
+        return f(a, b, c, ws, wsb, M, N, K, splits, det, None)
+    assert call(a=None) == da.DASH_ERR_INVALID_ARG
+    assert call(splits=0) == da.DASH_ERR_INVALID_ARG
+    assert call(det=2) == da.DASH_ERR_INVALID_ARG
+    assert call(ws=128) == da.DASH_ERR_INVALID_ARG                  # workspace not 256-aligned
+    assert call(M=200) == da.DASH_ERR_UNSUPPORTED                   # M not a multiple of 128
+    assert call(K=500) == da.DASH_ERR_UNSUPPORTED                   # K not 64 * splits aligned
+    assert call(wsb=16) == da.DASH_ERR_WORKSPACE_TOO_SMALL
+    assert da.dash_gemm_splitk_workspace_size(100, 128) == 0
