@@ -1,4 +1,4 @@
-// Backward main kernel for head dimension 128: whole 128 x 128 tasks, P kept in TMEM.
+// Backward main kernel for head dimension 128: whole 128 x 128 tasks.
 //
 // Same persistent grid, units, schedule walk and ordered dQ reduction as the general
 // kernel (kernels_tc.cuh); what differs is how one task (KV_i, Q_j) maps onto the SM:
@@ -6,8 +6,7 @@
 //   S^T  = K Q^T        M = 128 kv, N = 128 q, K = 128 d     TMEM cols [0, 128)
 //   dP^T = V dO^T       M = 128 kv, N = 128 q, K = 128 d     TMEM cols [128, 256)
 //   P^T  = exp2(S^T * scale*log2e - LSE*log2e)               smem bf16 [kv][q]
-//   dS^T = P^T * (dP^T - Dsum)                               the same buffer, once dV
-//                                                            has read P^T
+//   dS^T = P^T * (dP^T - Dsum)                               smem bf16 [kv][q]
 //   dV  += P^T dO                                            TMEM cols [256, 384)
 //   dQ^T = K^T dS^T     M = 128 d, N = 128 q, K = 128 kv     into the dP^T columns
 //   dK  += dS^T Q                                            TMEM cols [384, 512)
@@ -15,7 +14,7 @@
 // Every MMA is 128 x 128 x 128, so the tensor pipe reads at most 8 KB of shared memory
 // per 64-cycle K step. The S^T columns are handed back as soon as the softmax-gradient
 // warps have loaded them, so S^T of the next task runs while P^T of this one is being
-// computed (exp2 on 16K elements is the longest single step of a task). dQ^T
+// computed. dQ^T
 // reuses the dP^T columns once the softmax-gradient warps have read them, so the next
 // dP^T waits for the dQ read-out: the read-out warps load all 128 columns into registers
 // (their warpgroup takes registers from the single-thread roles' warpgroup), hand the
@@ -24,8 +23,12 @@
 // of one row: a full 128-byte line). In deterministic mode the adds of a 128-row block
 // wait for the block's turn and the turn is handed on after they have been performed.
 //
-// Shared memory (1024-aligned base, checked): K, V, Q x 2, dO x 2, P^T/dS^T, -LSE*log2e
-// and Dsum per Q buffer, barriers, trace: 231,936 bytes.
+// Q is double-buffered by task parity; dO has one buffer, reloaded as soon as dP^T and dV
+// have read it (the next dP^T waits for the dQ read-out anyway); P^T and dS^T have a
+// buffer each, so forming dS^T never waits for dV.
+//
+// Shared memory (1024-aligned base, checked): K, V, Q x 2, dO, P^T, dS^T, -LSE*log2e and
+// Dsum per Q buffer, barriers, trace: 231,936 bytes.
 //
 // Warp roles (512 threads): 0 = TMA producer, 1 = S^T/dP^T issuer, 3 = dV/dQ^T/dK issuer,
 // 2 = idle, 4..11 = softmax-gradient (quarter = TMEM lanes, half = 64 q columns),
@@ -43,9 +46,10 @@ struct L128 {
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = K_OFF + TILE_BYTES;
   static constexpr int Q_OFF = V_OFF + TILE_BYTES;            // two Q buffers
-  static constexpr int DO_OFF = Q_OFF + 2 * TILE_BYTES;       // two dO buffers
-  static constexpr int PS_OFF = DO_OFF + 2 * TILE_BYTES;      // P^T, then dS^T [kv][q]
-  static constexpr int LD_OFF = PS_OFF + TILE_BYTES;          // per Q buffer: -LSE*log2e, Dsum
+  static constexpr int DO_OFF = Q_OFF + 2 * TILE_BYTES;       // one dO buffer
+  static constexpr int P_OFF = DO_OFF + TILE_BYTES;           // P^T [kv][q]
+  static constexpr int DS_OFF = P_OFF + TILE_BYTES;           // dS^T [kv][q]
+  static constexpr int LD_OFF = DS_OFF + TILE_BYTES;          // per Q buffer: -LSE*log2e, Dsum
   static constexpr int LD_BYTES = 2 * kTile * 4;
   static constexpr int BAR_OFF = LD_OFF + 2 * LD_BYTES;
   static constexpr int TRACE_OFF = BAR_OFF + 320;
@@ -61,8 +65,7 @@ struct L128 {
 
 enum {
   E_KV_FULL = 0, E_KV_EMPTY, E_Q_FULL, E_Q_EMPTY = E_Q_FULL + 2, E_DO_FULL = E_Q_EMPTY + 2,
-  E_DO_EMPTY = E_DO_FULL + 2, E_S_FULL = E_DO_EMPTY + 2, E_S_EMPTY, E_P_FULL, E_P_EMPTY,
-  E_DP_FULL,
+  E_DO_EMPTY, E_S_FULL, E_S_EMPTY, E_P_FULL, E_P_EMPTY, E_DP_FULL,
   E_DS_FULL, E_DS_EMPTY, E_DQ_FULL, E_DQ_EMPTY, E_ACC_FULL, E_ACC_EMPTY, E_DRAIN, E_DRAIN2,
   E_TURN, E_REDS, E_COUNT
 };
@@ -116,9 +119,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(bars + E_Q_FULL + b, 1);
       ptx::mbar_init(bars + E_Q_EMPTY + b, 1);
-      ptx::mbar_init(bars + E_DO_FULL + b, 1);
-      ptx::mbar_init(bars + E_DO_EMPTY + b, 1);
     }
+    ptx::mbar_init(bars + E_DO_FULL, 1);
+    ptx::mbar_init(bars + E_DO_EMPTY, 1);
     ptx::mbar_init(bars + E_S_FULL, 1);
     ptx::mbar_init(bars + E_S_EMPTY, 8);
     ptx::mbar_init(bars + E_P_FULL, 8);
@@ -190,22 +193,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ++tl;
         }
-        // dO_j into dO buffer qb (free once the MMAs of task it-2 are done)
+        // dO_j into the dO buffer (free once dP^T and dV of task it-1 have read it)
         t0 = tr.t0();
-        if (it >= 2 && !(ok = ptx::mbar_wait(bars + E_DO_EMPTY + qb, ((it >> 1) - 1) & 1, abort_flag, tmo)))
-          break;
+        if (it >= 1 && !(ok = ptx::mbar_wait(bars + E_DO_EMPTY, (it - 1) & 1, abort_flag, tmo))) break;
         tr.add(TR_MMA_DQ_EMPTY, t0);
-        ptx::mbar_expect_tx(bars + E_DO_FULL + qb, L::TILE_BYTES);
+        ptx::mbar_expect_tx(bars + E_DO_FULL, L::TILE_BYTES);
         for (int cb = 0; cb < 2; ++cb)
-          ptx::tma_load_3d(sm + L::DO_OFF + qb * L::TILE_BYTES + cb * kTile * 128, &maps.dO, cb * 64,
-                           h, b * p.S + q0, bars + E_DO_FULL + qb);
+          ptx::tma_load_3d(sm + L::DO_OFF + cb * kTile * 128, &maps.dO, cb * 64, h, b * p.S + q0,
+                           bars + E_DO_FULL);
         ++it;
       }
       // drain: every issued load has landed before the CTA may exit
-      for (int k = (it > 2 ? it - 2 : 0); k < it; ++k) {
+      for (int k = (it > 2 ? it - 2 : 0); k < it; ++k)
         ptx::mbar_drain(bars + E_Q_FULL + (k & 1), (k >> 1) & 1, 100000000ll);
-        ptx::mbar_drain(bars + E_DO_FULL + (k & 1), (k >> 1) & 1, 100000000ll);
-      }
+      if (it > 0) ptx::mbar_drain(bars + E_DO_FULL, (it - 1) & 1, 100000000ll);
       if (tl > 0) ptx::mbar_drain(bars + E_KV_FULL, (tl - 1) & 1, 100000000ll);
     }
   } else if (warp == 1 || warp == 3) {
@@ -213,15 +214,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t sK = ptx::smem_u32(sm + L::K_OFF), sV = ptx::smem_u32(sm + L::V_OFF);
       const uint32_t sQ = ptx::smem_u32(sm + L::Q_OFF), sdO = ptx::smem_u32(sm + L::DO_OFF);
-      const uint32_t sPS = ptx::smem_u32(sm + L::PS_OFF);
+      const uint32_t sP = ptx::smem_u32(sm + L::P_OFF), sdS = ptx::smem_u32(sm + L::DS_OFF);
       const uint32_t dK_k = ptx::sdesc_lo(sK, 16), dV_k = ptx::sdesc_lo(sV, 16);
       const uint32_t dK_mn = ptx::sdesc_lo(sK, kTile * 128);
-      // P^T and dS^T share one buffer: K-major (over q) for dV and dK, MN-major for dQ^T
-      const uint32_t dPS_k = ptx::sdesc_lo(sPS, 16), dS_mn = ptx::sdesc_lo(sPS, kTile * 128);
+      // P^T: K-major (over q) for dV; dS^T: K-major for dK, MN-major for dQ^T
+      const uint32_t dP_k = ptx::sdesc_lo(sP, 16);
+      const uint32_t dS_k = ptx::sdesc_lo(sdS, 16), dS_mn = ptx::sdesc_lo(sdS, kTile * 128);
       constexpr uint32_t ID_S = ptx::idesc_bf16(128, 128, 0, 0);    // S^T, dP^T
       constexpr uint32_t ID_ACC = ptx::idesc_bf16(128, 128, 0, 1);  // dV, dK
       constexpr uint32_t ID_DQT = ptx::idesc_bf16(128, 128, 1, 1);  // dQ^T = K^T dS^T
-      constexpr uint32_t BUF_STEP = L::TILE_BYTES >> 4;             // next Q or dO buffer
+      constexpr uint32_t BUF_STEP = L::TILE_BYTES >> 4;             // next Q buffer
       // K-major step ks of a [128 rows][128] tile in 64-column blocks; MN-major step: 16
       // rows of 128 bytes.
       auto kstep = [](int ks) -> uint32_t { return ((ks >> 2) * kTile * 128 + (ks & 3) * 32) >> 4; };
@@ -230,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0, tile = -1;
       bool ok = true;
       if (warp == 1) {
-        const uint32_t dQ_k0 = ptx::sdesc_lo(sQ, 16), ddO_k0 = ptx::sdesc_lo(sdO, 16);
+        const uint32_t dQ_k0 = ptx::sdesc_lo(sQ, 16), ddO_k = ptx::sdesc_lo(sdO, 16);
         while (ok && w.next()) {
           long long t0 = tr.t0();
           if (w.first_of_tile) {
@@ -256,13 +258,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mma_commit(bars + E_S_FULL);
           tr.add(TR_ISSUE_S, t0);
           t0 = tr.t0();
-          ok = ptx::mbar_wait(bars + E_DO_FULL + (it & 1), (it >> 1) & 1, abort_flag, tmo);
+          ok = ptx::mbar_wait(bars + E_DO_FULL, it & 1, abort_flag, tmo);
           // dP^T overwrites the previous task's dQ^T: the read-out must have taken it
           if (ok && it > 0) ok = ptx::mbar_wait(bars + E_DQ_EMPTY, (it - 1) & 1, abort_flag, tmo);
           tr.add(TR_MMA_DP_EMPTY, t0);
           if (!ok) break;
           ptx::tc_fence_after();
-          const uint32_t ddO_k = ddO_k0 + (it & 1) * BUF_STEP;
           t0 = tr.t0();
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks)
@@ -273,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         const uint32_t dQ_mn0 = ptx::sdesc_lo(sQ, kTile * 128);
-        const uint32_t ddO_mn0 = ptx::sdesc_lo(sdO, kTile * 128);
+        const uint32_t ddO_mn = ptx::sdesc_lo(sdO, kTile * 128);
         while (ok && w.next()) {
           if (w.first_of_tile) ++tile;
           // P^T is in shared memory, and dO of this task has landed (P_FULL does not imply
@@ -281,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // has run)
           long long t0 = tr.t0();
           ok = ptx::mbar_wait(bars + E_P_FULL, it & 1, abort_flag, tmo);
-          if (ok) ok = ptx::mbar_wait(bars + E_DO_FULL + (it & 1), (it >> 1) & 1, abort_flag, tmo);
+          if (ok) ok = ptx::mbar_wait(bars + E_DO_FULL, it & 1, abort_flag, tmo);
           tr.add(TR_MMA_P_FULL, t0);
           t0 = tr.t0();
           if (ok && w.first_of_tile && tile > 0)
@@ -291,15 +292,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tc_fence_after();
           const uint32_t acc0 = w.first_of_tile ? 0u : 1u;
           // dV += P^T dO: A = P^T (K-major over q), B = dO (MN-major over d)
-          const uint32_t ddO_mn = ddO_mn0 + (it & 1) * BUF_STEP;
           t0 = tr.t0();
 #pragma unroll
           for (int ks = 0; ks < kTile / 16; ++ks)
-            ptx::mma_lo(tmem + L::T_DV, dPS_k + kstep(ks), ddO_mn + ks * MN_STEP, ID_ACC,
+            ptx::mma_lo(tmem + L::T_DV, dP_k + kstep(ks), ddO_mn + ks * MN_STEP, ID_ACC,
                         ks > 0 ? 1u : acc0);
-          // P^T has been read: dS^T may overwrite it
+          // P^T has been read: the next P^T may overwrite it
           ptx::mma_commit(bars + E_P_EMPTY);
           tr.add(TR_ISSUE_DV, t0);
+          // dO's other reader, dP^T, has completed too: then the next dO may be loaded
+          t0 = tr.t0();
+          ok = ptx::mbar_wait(bars + E_DP_FULL, it & 1, abort_flag, tmo);
+          tr.add(TR_MMA_DS_FULL, t0);
+          if (!ok) break;
+          ptx::mma_commit(bars + E_DO_EMPTY);
           t0 = tr.t0();
           ok = ptx::mbar_wait(bars + E_DS_FULL, it & 1, abort_flag, tmo);
           tr.add(TR_MMA_DS_FULL, t0);
@@ -316,13 +322,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           // dK += dS^T Q: A = dS^T (K-major over q), B = Q (MN-major over d)
 #pragma unroll
           for (int ks = 0; ks < kTile / 16; ++ks)
-            ptx::mma_lo(tmem + L::T_DK, dPS_k + kstep(ks), dQ_mn + ks * MN_STEP, ID_ACC,
+            ptx::mma_lo(tmem + L::T_DK, dS_k + kstep(ks), dQ_mn + ks * MN_STEP, ID_ACC,
                         ks > 0 ? 1u : acc0);
           ptx::mma_commit(bars + E_DS_EMPTY);
           ptx::mma_commit(bars + E_Q_EMPTY + (it & 1));
-          // this dO buffer's readers are done: dV above, and dP^T, which completed before
-          // the softmax-gradient warps published dS^T
-          ptx::mma_commit(bars + E_DO_EMPTY + (it & 1));
           if (w.last_of_tile) {
             ptx::mma_commit(bars + E_ACC_FULL);
             ptx::mma_commit(bars + E_KV_EMPTY);
@@ -343,13 +346,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quarter * 32 + lane;         // kv row within the tile
     const int col0 = half * 64;                // this thread's 64 q columns
     const uint32_t lane_addr = ((uint32_t)(quarter * 32) << 16);
-    const uint32_t sPS = ptx::smem_u32(sm + L::PS_OFF);
+    const uint32_t sP = ptx::smem_u32(sm + L::P_OFF), sdS = ptx::smem_u32(sm + L::DS_OFF);
     const Trace& trs = (warp == 4 && lane == 0) ? tr : tr_none;
-    // writes 64 values of row r (q columns col0..col0+63) as bf16 into the P^T/dS^T buffer
-    auto store_row = [&](const float (&v)[64]) {
+    // writes 64 values of row r (q columns col0..col0+63) as bf16 into a [kv][q] tile
+    auto store_row = [&](uint32_t base, const float (&v)[64]) {
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        ptx::st_shared_v4(sPS + sw_chunk(r, (col0 >> 3) + k, kTile),
+        ptx::st_shared_v4(base + sw_chunk(r, (col0 >> 3) + k, kTile),
                           ptx::pack_bf16(v[8 * k], v[8 * k + 1]), ptx::pack_bf16(v[8 * k + 2], v[8 * k + 3]),
                           ptx::pack_bf16(v[8 * k + 4], v[8 * k + 5]), ptx::pack_bf16(v[8 * k + 6], v[8 * k + 7]));
       ptx::fence_proxy_async_smem();
@@ -398,14 +401,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 64; ++c)
           if (d > c) pv[c] = 0.f;
       }
-      // P^T goes where the previous task's dS^T was: dK and dQ^T must have read it
+      // P^T replaces the previous task's: dV must have read it
       trs.add(TR_DQ_FULL, tp);   // (slot reused: P^T compute)
       t0 = trs.t0();
-      if (it > 0) ok = ptx::warp_wait(bars + E_DS_EMPTY, (it - 1) & 1, abort_flag, tmo);
+      if (it > 0) ok = ptx::warp_wait(bars + E_P_EMPTY, (it - 1) & 1, abort_flag, tmo);
       trs.add(TR_SG_DS_EMPTY, t0);
       if (!ok) break;
       tp = trs.t0();
-      store_row(pv);
+      store_row(sP, pv);
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bars + E_P_FULL);
       trs.add(TR_DQ_FULL, tp);   // (slot reused: P^T compute)
@@ -430,14 +433,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           pc[3] *= dp[4 * c4 + 3] - ds.w;
         }
       }
-      // dS^T overwrites P^T: dV must have read it
+      // dS^T replaces the previous task's: dQ^T and dK must have read it
       trs.add(TR_DQ_STAGE, tp);  // (slot reused: dS^T compute)
       t0 = trs.t0();
-      ok = ptx::warp_wait(bars + E_P_EMPTY, it & 1, abort_flag, tmo);
+      if (it > 0) ok = ptx::warp_wait(bars + E_DS_EMPTY, (it - 1) & 1, abort_flag, tmo);
       trs.add(TR_SG_DS_EMPTY, t0);
       if (!ok) break;
       tp = trs.t0();
-      store_row(pv);
+      store_row(sdS, pv);
       // the dP^T loads above have completed: dQ^T may now overwrite those columns
       ptx::tc_fence_before();
       __syncwarp();
