@@ -71,6 +71,32 @@ enum {
 };
 static_assert(8 * E_COUNT + 8 <= 320, "barrier area");
 
+// Wait- and work-cycle sites of this kernel's optional trace, each counted in one of the
+// shared trace slots (dash_debug_set_trace; one writer per slot).
+enum : int {
+  K_PROD_Q_EMPTY = TR_PROD_STAGE_EMPTY,   // producer: a Q buffer is free
+  K_PROD_KV_EMPTY = TR_PROD_KV_EMPTY,     // producer: K and V are free
+  K_PROD_DO_EMPTY = TR_MMA_DQ_EMPTY,      // producer: the dO buffer is free
+  K_X_KV_FULL = TR_MMA_KV_FULL,           // S/dP issuer: K and V landed
+  K_X_Q_FULL = TR_MMA_STAGE_FULL,         // S/dP issuer: Q landed
+  K_X_S_EMPTY = TR_MMA_S_EMPTY,           // S/dP issuer: previous S^T loaded out of TMEM
+  K_X_DO_DQ_EMPTY = TR_MMA_DP_EMPTY,      // S/dP issuer: dO landed, previous dQ^T read out
+  K_Y_P_DO_FULL = TR_MMA_P_FULL,          // dV/dQ/dK issuer: P^T stored and dO landed
+  K_Y_ACC_EMPTY = TR_MMA_ACC_EMPTY,       // dV/dQ/dK issuer: dK/dV accumulators read out
+  K_Y_DP_DS_FULL = TR_MMA_DS_FULL,        // dV/dQ/dK issuer: dP^T done, dS^T stored
+  K_SG_S_FULL = TR_SG_S_FULL,             // softmax-gradient: S^T ready
+  K_SG_P_COMPUTE = TR_DQ_FULL,            // softmax-gradient: S^T load, exp2, P^T store
+  K_SG_DP_FULL = TR_SG_DP_FULL,           // softmax-gradient: dP^T ready
+  K_SG_BUF_EMPTY = TR_SG_DS_EMPTY,        // softmax-gradient: P^T or dS^T buffer free
+  K_SG_DS_COMPUTE = TR_DQ_STAGE,          // softmax-gradient: dP^T load, dS^T, store
+  K_RO_DQ_FULL = TR_SG_P_EMPTY,           // read-out: dQ^T ready
+  K_RO_SEM = TR_DQ_SEM,                   // read-out: the block's turn (deterministic)
+  K_RO_REDUCE = TR_DQ_REDUCE,             // read-out: adds and hand-off
+  K_RO_ACC_FULL = TR_DQ_ACC_FULL,         // read-out: dK/dV accumulators final
+  K_ISSUE_S = TR_ISSUE_S, K_ISSUE_DP = TR_ISSUE_DP, K_ISSUE_DV = TR_ISSUE_DV,
+  K_ISSUE_DQDK = TR_ISSUE_DKDQ            // MMA issue time of each group
+};
+
 // 2^x on the FMA pipe, for x <= ~0 (P = 2^x with x = S*scale*log2e - LSE*log2e).
 // Range reduction x = n + f with n = round(x) (adding and subtracting 1.5 * 2^23 leaves
 // round-to-nearest(x) in the low mantissa bits of the sum), f in [-1/2, 1/2]; 2^f from a
@@ -171,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         long long t0 = tr.t0();
         if (it >= 2 && !(ok = ptx::mbar_wait(bars + E_Q_EMPTY + qb, ((it >> 1) - 1) & 1, abort_flag, tmo)))
           break;
-        tr.add(TR_PROD_STAGE_EMPTY, t0);
+        tr.add(K_PROD_Q_EMPTY, t0);
         uint8_t* qs = sm + L::Q_OFF + qb * L::TILE_BYTES;
         uint8_t* ld = sm + L::LD_OFF + qb * L::LD_BYTES;
         ptx::mbar_expect_tx(bars + E_Q_FULL + qb, L::TILE_BYTES + L::LD_BYTES);
@@ -183,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (w.first_of_tile) {
           t0 = tr.t0();
           if (tl > 0 && !(ok = ptx::mbar_wait(bars + E_KV_EMPTY, (tl - 1) & 1, abort_flag, tmo))) break;
-          tr.add(TR_PROD_KV_EMPTY, t0);
+          tr.add(K_PROD_KV_EMPTY, t0);
           ptx::mbar_expect_tx(bars + E_KV_FULL, 2 * L::TILE_BYTES);
           for (int cb = 0; cb < 2; ++cb) {
             ptx::tma_load_3d(sm + L::K_OFF + cb * kTile * 128, &maps.k, cb * 64, h,
@@ -196,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dO_j into the dO buffer (free once dP^T and dV of task it-1 have read it)
         t0 = tr.t0();
         if (it >= 1 && !(ok = ptx::mbar_wait(bars + E_DO_EMPTY, (it - 1) & 1, abort_flag, tmo))) break;
-        tr.add(TR_MMA_DQ_EMPTY, t0);
+        tr.add(K_PROD_DO_EMPTY, t0);
         ptx::mbar_expect_tx(bars + E_DO_FULL, L::TILE_BYTES);
         for (int cb = 0; cb < 2; ++cb)
           ptx::tma_load_3d(sm + L::DO_OFF + cb * kTile * 128, &maps.dO, cb * 64, h, b * p.S + q0,
@@ -239,15 +265,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++tile;
             if (!(ok = ptx::mbar_wait(bars + E_KV_FULL, tile & 1, abort_flag, tmo))) break;
           }
-          tr.add(TR_MMA_KV_FULL, t0);
+          tr.add(K_X_KV_FULL, t0);
           t0 = tr.t0();
           ok = ptx::mbar_wait(bars + E_Q_FULL + (it & 1), (it >> 1) & 1, abort_flag, tmo);
-          tr.add(TR_MMA_STAGE_FULL, t0);
+          tr.add(K_X_Q_FULL, t0);
           t0 = tr.t0();
           // S^T overwrites the previous task's S^T: the softmax-gradient warps must have
           // loaded it
           if (ok && it > 0) ok = ptx::mbar_wait(bars + E_S_EMPTY, (it - 1) & 1, abort_flag, tmo);
-          tr.add(TR_MMA_S_EMPTY, t0);
+          tr.add(K_X_S_EMPTY, t0);
           if (!ok) break;
           ptx::tc_fence_after();
           const uint32_t dQ_k = dQ_k0 + (it & 1) * BUF_STEP;
@@ -256,12 +282,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int ks = 0; ks < D / 16; ++ks)
             ptx::mma_lo(tmem + L::T_S, dK_k + kstep(ks), dQ_k + kstep(ks), ID_S, ks > 0);
           ptx::mma_commit(bars + E_S_FULL);
-          tr.add(TR_ISSUE_S, t0);
+          tr.add(K_ISSUE_S, t0);
           t0 = tr.t0();
           ok = ptx::mbar_wait(bars + E_DO_FULL, it & 1, abort_flag, tmo);
           // dP^T overwrites the previous task's dQ^T: the read-out must have taken it
           if (ok && it > 0) ok = ptx::mbar_wait(bars + E_DQ_EMPTY, (it - 1) & 1, abort_flag, tmo);
-          tr.add(TR_MMA_DP_EMPTY, t0);
+          tr.add(K_X_DO_DQ_EMPTY, t0);
           if (!ok) break;
           ptx::tc_fence_after();
           t0 = tr.t0();
@@ -269,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int ks = 0; ks < D / 16; ++ks)
             ptx::mma_lo(tmem + L::T_DP, dV_k + kstep(ks), ddO_k + kstep(ks), ID_S, ks > 0);
           ptx::mma_commit(bars + E_DP_FULL);
-          tr.add(TR_ISSUE_DP, t0);
+          tr.add(K_ISSUE_DP, t0);
           ++it;
         }
       } else {
@@ -283,11 +309,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           long long t0 = tr.t0();
           ok = ptx::mbar_wait(bars + E_P_FULL, it & 1, abort_flag, tmo);
           if (ok) ok = ptx::mbar_wait(bars + E_DO_FULL, it & 1, abort_flag, tmo);
-          tr.add(TR_MMA_P_FULL, t0);
+          tr.add(K_Y_P_DO_FULL, t0);
           t0 = tr.t0();
           if (ok && w.first_of_tile && tile > 0)
             ok = ptx::mbar_wait(bars + E_ACC_EMPTY, (tile - 1) & 1, abort_flag, tmo);
-          tr.add(TR_MMA_ACC_EMPTY, t0);
+          tr.add(K_Y_ACC_EMPTY, t0);
           if (!ok) break;
           ptx::tc_fence_after();
           const uint32_t acc0 = w.first_of_tile ? 0u : 1u;
@@ -299,16 +325,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ks > 0 ? 1u : acc0);
           // P^T has been read: the next P^T may overwrite it
           ptx::mma_commit(bars + E_P_EMPTY);
-          tr.add(TR_ISSUE_DV, t0);
+          tr.add(K_ISSUE_DV, t0);
           // dO's other reader, dP^T, has completed too: then the next dO may be loaded
           t0 = tr.t0();
           ok = ptx::mbar_wait(bars + E_DP_FULL, it & 1, abort_flag, tmo);
-          tr.add(TR_MMA_DS_FULL, t0);
+          tr.add(K_Y_DP_DS_FULL, t0);
           if (!ok) break;
           ptx::mma_commit(bars + E_DO_EMPTY);
           t0 = tr.t0();
           ok = ptx::mbar_wait(bars + E_DS_FULL, it & 1, abort_flag, tmo);
-          tr.add(TR_MMA_DS_FULL, t0);
+          tr.add(K_Y_DP_DS_FULL, t0);
           if (!ok) break;
           ptx::tc_fence_after();
           const uint32_t dQ_mn = dQ_mn0 + (it & 1) * BUF_STEP;
@@ -330,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mma_commit(bars + E_ACC_FULL);
             ptx::mma_commit(bars + E_KV_EMPTY);
           }
-          tr.add(TR_ISSUE_DKDQ, t0);
+          tr.add(K_ISSUE_DQDK, t0);
           ++it;
         }
       }
@@ -367,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       long long t0 = trs.t0();
       ok = ptx::warp_wait(bars + E_Q_FULL + qb, (it >> 1) & 1, abort_flag, tmo);
       if (ok) ok = ptx::warp_wait(bars + E_S_FULL, it & 1, abort_flag, tmo);
-      trs.add(TR_SG_S_FULL, t0);
+      trs.add(K_SG_S_FULL, t0);
       if (!ok) break;
       ptx::tc_fence_after();
       long long tp = trs.t0();
@@ -402,19 +428,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (d > c) pv[c] = 0.f;
       }
       // P^T replaces the previous task's: dV must have read it
-      trs.add(TR_DQ_FULL, tp);   // (slot reused: P^T compute)
+      trs.add(K_SG_P_COMPUTE, tp); 
       t0 = trs.t0();
       if (it > 0) ok = ptx::warp_wait(bars + E_P_EMPTY, (it - 1) & 1, abort_flag, tmo);
-      trs.add(TR_SG_DS_EMPTY, t0);
+      trs.add(K_SG_BUF_EMPTY, t0);
       if (!ok) break;
       tp = trs.t0();
       store_row(sP, pv);
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bars + E_P_FULL);
-      trs.add(TR_DQ_FULL, tp);   // (slot reused: P^T compute)
+      trs.add(K_SG_P_COMPUTE, tp); 
       t0 = trs.t0();
       ok = ptx::warp_wait(bars + E_DP_FULL, it & 1, abort_flag, tmo);
-      trs.add(TR_SG_DP_FULL, t0);
+      trs.add(K_SG_DP_FULL, t0);
       if (!ok) break;
       ptx::tc_fence_after();
       tp = trs.t0();
@@ -434,10 +460,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // dS^T replaces the previous task's: dQ^T and dK must have read it
-      trs.add(TR_DQ_STAGE, tp);  // (slot reused: dS^T compute)
+      trs.add(K_SG_DS_COMPUTE, tp);
       t0 = trs.t0();
       if (it > 0) ok = ptx::warp_wait(bars + E_DS_EMPTY, (it - 1) & 1, abort_flag, tmo);
-      trs.add(TR_SG_DS_EMPTY, t0);
+      trs.add(K_SG_BUF_EMPTY, t0);
       if (!ok) break;
       tp = trs.t0();
       store_row(sdS, pv);
@@ -445,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bars + E_DS_FULL);
-      trs.add(TR_DQ_STAGE, tp);
+      trs.add(K_SG_DS_COMPUTE, tp);
       ++it;
     }
   } else {
@@ -462,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int b = w.bh / p.H, h = w.bh % p.H;
       long long t0 = trq.t0();
       ok = ptx::warp_wait(bars + E_DQ_FULL, it & 1, abort_flag, tmo);
-      trq.add(TR_SG_P_EMPTY, t0);
+      trq.add(K_RO_DQ_FULL, t0);
       if (!ok) break;
       ptx::tc_fence_after();
       float v[128];                            // dQ[q0 + c][row], c = 0..127
@@ -497,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           got = ptx::warp_wait(bars + E_TURN, it & 1, abort_flag, tmo) ? 1 : 0;
         }
-        trq.add(TR_DQ_SEM, t0);
+        trq.add(K_RO_SEM, t0);
         if (!got) break;
       }
       t0 = trq.t0();
@@ -524,12 +550,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!done) break;
       }
-      trq.add(TR_DQ_REDUCE, t0);
+      trq.add(K_RO_REDUCE, t0);
       // ---- dK/dV epilogue after the tile's last task ----
       if (w.last_of_tile) {
         t0 = trq.t0();
         ok = ptx::warp_wait(bars + E_ACC_FULL, tl & 1, abort_flag, tmo);
-        trq.add(TR_DQ_ACC_FULL, t0);
+        trq.add(K_RO_ACC_FULL, t0);
         if (!ok) break;
         ptx::tc_fence_after();
         const size_t g = ((size_t)b * p.S + (size_t)w.i * kTile + row) * rs + (size_t)h * D;
