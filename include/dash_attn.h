@@ -94,7 +94,10 @@ size_t dash_attn_bwd_workspace_size(int B, int S, int H, int D);
  *                      serialised through semaphores per dQ block. The result is
  *                      bitwise identical for identical inputs, shape and schedule on the
  *                      same GPU model and build. Different schedules may differ in the
- *                      last bits (their dQ orders differ).
+ *                      last bits (their dQ orders differ). SHIFT and SYMMETRIC_SHIFT
+ *                      order by arrival on the persistent grid of min(SMs, B*H*chains)
+ *                      CTAs (dash_sched_dealt_table), so their bits also depend on the
+ *                      GPU's SM count.
  *   deterministic = 2: the same fixed order run as two interleaved chains: the partial
  *                      at position p of the order is added, in order, into fp32
  *                      accumulator copy p mod 2, after the partial at position p - 2, and
@@ -111,7 +114,8 @@ size_t dash_attn_bwd_workspace_size(int B, int S, int H, int D);
  *   schedule       : dash_sched_t. SHIFT needs the full mask, SYMMETRIC_SHIFT the causal
  *                    mask; other pairs return DASH_ERR_UNSUPPORTED.
  * Returns DASH_ERR_DEADLOCK_RISK (nothing queued) if the schedule's reduction waits would
- * form a cycle on the persistent grid this GPU can hold.
+ * form a cycle on the persistent grid this GPU can hold (none of the four schedules'
+ * orders can: ascending KV index is the dealing order, and arrival orders follow it).
  */
 dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const void* o,
                             const void* dO, const float* lse, void* dq, void* dk, void* dv,
@@ -210,7 +214,9 @@ int dash_sched_num_slots(int mask, int schedule, int n);
  *   slot_offsets : int32[num_slots + 1]; chain p is tasks[slot_offsets[p] .. slot_offsets[p+1])
  *   tasks        : int32[cap]; each entry packs (kv_tile << 16) | q_tile, in execution order
  *   ordinals     : int32[n * n]; ordinals[i * n + j] = position of KV_i's partial in the dQ_j
- *                  reduction order, or -1 where the mask removes task (i, j)
+ *                  reduction order, or -1 where the mask removes task (i, j). This is the
+ *                  schedule's order when all chains of a head start together (one head on
+ *                  n SMs); dash_sched_dealt_table gives the orders the kernel follows.
  * Returns the number of tasks, or a negative dash_status_t value (cap too small:
  * -DASH_ERR_INVALID_ARG).
  */
@@ -218,9 +224,27 @@ int dash_sched_table(int mask, int schedule, int n, int32_t* slot_offsets, int32
                      int cap, int32_t* ordinals);
 
 /*
+ * The dQ orders dash_attn_bwd follows when `heads` (= B * H) heads' chains are dealt round
+ * robin, head-major, onto `grid` persistent CTAs:
+ *   ordinals : int32[heads * n * n]; ordinals[(h * n + i) * n + j] = position of KV_i's
+ *              partial in head h's dQ_j order, -1 where the mask removes the task.
+ * ASCENDING and DESCENDING: ascending KV index in every head. SHIFT and SYMMETRIC_SHIFT
+ * (whose order the pages define as the order of arrival): a partial's place in its
+ * CTA's task sequence -- the tasks of the CTA's earlier units, then its step in the chain
+ * -- the lower KV index first on a tie. With whole heads per round of the grid this is
+ * dash_sched_table's order; when the grid splits a head over two rounds, the chains run
+ * in the earlier round come first, so no partial waits for a chain that has not started.
+ * Returns DASH_OK, DASH_ERR_INVALID_ARG (heads or grid < 1, null ordinals), or the
+ * schedule's error for an unsupported (mask, schedule, n).
+ */
+dash_status_t dash_sched_dealt_table(int mask, int schedule, int n, int heads, int grid,
+                                     int32_t* ordinals);
+
+/*
  * Critical path of the compute/reduce DAG (Pith review, "What carries the argument"):
  * every task is a compute phase of cost c then a reduce phase of cost r; one SM runs its
- * tasks back to back; reductions into one dQ block follow the schedule's order. `heads`
+ * tasks back to back; reductions into one dQ block follow the orders the kernel uses on a
+ * grid of num_sms CTAs (dash_sched_dealt_table(mask, schedule, n, heads, num_sms)). `heads`
  * heads' chains are dealt round robin, head-major, onto `num_sms` SMs (the kernel's own
  * dealing). Writes the makespan and, if sm_end is not NULL, each SM's finish time
  * (double[num_sms]). Returns DASH_ERR_DEADLOCK_RISK when the waits form a cycle.

@@ -41,6 +41,14 @@ Readings where the pages are silent (listed in the design notes as well):
   KV_(n-1-p) visits Q_(n-1) down to Q_(n-1-p).
 * m heads are spread over P SMs by dealing the units (head, chain slot) round robin in
   head-major order; each SM runs its units in dealing order.
+* With a fixed order per schedule (``dealt=False``), a head whose chains the dealing
+  spreads over two rounds of the SMs can wait on itself: a partial of the first round
+  may come after one of a chain that only starts in the second round. The pages set
+  shift's and symmetric shift's order by arrival and study one head on n SMs, where all
+  chains start together. ``dealt=True`` takes "order of arrival" literally on the dealt
+  SMs: a partial arrives when its SM has run all the tasks dealt to it before this one
+  (the lower KV index first on a tie). Where a head's chains all start together this is
+  the fixed order above; ascending and descending keep ascending KV index either way.
 """
 
 from __future__ import annotations
@@ -51,6 +59,7 @@ __all__ = [
     "SCHEDULES",
     "chains",
     "reduction_order",
+    "dealt_reduction_order",
     "schedule_dag",
     "longest_path",
     "simulate",
@@ -135,7 +144,37 @@ def longest_path(n_vertices: int, edges: list[tuple[int, int, float]]):
     return depth if seen == n_vertices else None
 
 
-def schedule_dag(mask: str, sched: str, n: int, m: int, num_sms: int, c: float, r: float):
+def dealt_reduction_order(mask: str, sched: str, n: int, m: int, num_sms: int):
+    """For each (head, dQ block j), the KV tiles that reduce into it, in the order the
+    dealt SMs produce them (the ``dealt=True`` reading in the module docstring)."""
+    if sched in ("ascending", "descending"):
+        fixed = reduction_order(mask, sched, n)
+        return {(h, j): list(fixed[j]) for h in range(m) for j in range(n)}
+    ch = chains(mask, sched, n)
+    done = [0] * num_sms                     # tasks each SM has run so far
+    arrivals: dict[tuple[int, int], list[tuple[int, int]]] = {
+        (h, j): [] for h in range(m) for j in range(n)}
+    unit = 0
+    for h in range(m):
+        for chain in ch:
+            sm = unit % num_sms
+            for (i, j) in chain:
+                arrivals[(h, j)].append((done[sm], i))
+                done[sm] += 1
+            unit += 1
+    return {key: [i for _, i in sorted(lst)] for key, lst in arrivals.items()}
+
+
+def _orders(mask: str, sched: str, n: int, m: int, num_sms: int, dealt: bool):
+    """(head, j) -> dQ_j order of that head, fixed per schedule or dealt."""
+    if dealt:
+        return dealt_reduction_order(mask, sched, n, m, num_sms)
+    fixed = reduction_order(mask, sched, n)
+    return {(h, j): fixed[j] for h in range(m) for j in fixed}
+
+
+def schedule_dag(mask: str, sched: str, n: int, m: int, num_sms: int, c: float, r: float,
+                 dealt: bool = False):
     """Build the explicit DAG of m heads' tasks dealt onto ``num_sms`` SMs.
 
     Every task (head, i, j) owns four vertices: compute start/end and reduce start/end.
@@ -143,7 +182,7 @@ def schedule_dag(mask: str, sched: str, n: int, m: int, num_sms: int, c: float, 
     owns vertices 4k..4k+3.
     """
     ch = chains(mask, sched, n)
-    order = reduction_order(mask, sched, n)
+    order = _orders(mask, sched, n, m, num_sms, dealt)
     units = [(h, slot) for h in range(m) for slot in range(len(ch))]   # head-major deal
     per_sm: list[list[int]] = [[] for _ in range(num_sms)]
     tasks: list[tuple[int, int, int]] = []
@@ -164,20 +203,20 @@ def schedule_dag(mask: str, sched: str, n: int, m: int, num_sms: int, c: float, 
     for lst in per_sm:                               # one SM runs its tasks back to back
         for a, b in zip(lst, lst[1:]):
             edges.append((4 * a + 3, 4 * b, 0.0))
-    for h in range(m):                               # fixed dQ reduction order
-        for j, kv in order.items():
-            for a, b in zip(kv, kv[1:]):
-                edges.append((4 * index[(h, a, j)] + 3, 4 * index[(h, b, j)] + 2, 0.0))
+    for (h, j), kv in order.items():                 # fixed dQ reduction order
+        for a, b in zip(kv, kv[1:]):
+            edges.append((4 * index[(h, a, j)] + 3, 4 * index[(h, b, j)] + 2, 0.0))
     return 4 * len(tasks), edges, tasks, sm_of_task
 
 
-def simulate(mask: str, sched: str, n: int, m: int, num_sms: int, c: float, r: float):
+def simulate(mask: str, sched: str, n: int, m: int, num_sms: int, c: float, r: float,
+             dealt: bool = False):
     """Critical path of the schedule DAG.
 
     Returns a dict with ``makespan`` (None on a cycle, i.e. a deadlock), ``sm_end`` (finish
     time per SM) and ``sm_idle`` (finish time minus busy time per SM).
     """
-    nv, edges, tasks, sm_of_task = schedule_dag(mask, sched, n, m, num_sms, c, r)
+    nv, edges, tasks, sm_of_task = schedule_dag(mask, sched, n, m, num_sms, c, r, dealt)
     depth = longest_path(nv, edges)
     if depth is None:
         return {"makespan": None, "sm_end": None, "sm_idle": None}
@@ -206,13 +245,13 @@ def simulate(mask: str, sched: str, n: int, m: int, num_sms: int, c: float, r: f
 # With h = 0 and overlapped = False this is exactly schedule_dag / simulate above.
 # ---------------------------------------------------------------------------------------
 def schedule_dag_ex(mask: str, sched: str, n: int, m: int, num_sms: int, c: float, r: float,
-                    h: float, overlapped: bool):
+                    h: float, overlapped: bool, dealt: bool = False):
     """The schedule DAG with hand-off cost ``h`` and, optionally, the two-engine SM.
 
     Same vertex numbering and return value as schedule_dag.
     """
     ch = chains(mask, sched, n)
-    order = reduction_order(mask, sched, n)
+    order = _orders(mask, sched, n, m, num_sms, dealt)
     units = [(hd, slot) for hd in range(m) for slot in range(len(ch))]   # head-major deal
     per_sm: list[list[int]] = [[] for _ in range(num_sms)]
     tasks: list[tuple[int, int, int]] = []
@@ -240,20 +279,19 @@ def schedule_dag_ex(mask: str, sched: str, n: int, m: int, num_sms: int, c: floa
                     edges.append((4 * lst[pos - 2] + 3, 4 * b, 0.0))
             else:
                 edges.append((4 * a + 3, 4 * b, 0.0))          # C then R, task after task
-    for hd in range(m):                                        # fixed dQ reduction order
-        for j, kv in order.items():
-            for a, b in zip(kv, kv[1:]):
-                ka, kb = index[(hd, a, j)], index[(hd, b, j)]
-                w = 0.0 if sm_of_task[ka] == sm_of_task[kb] else h
-                edges.append((4 * ka + 3, 4 * kb + 2, w))
+    for (hd, j), kv in order.items():                          # fixed dQ reduction order
+        for a, b in zip(kv, kv[1:]):
+            ka, kb = index[(hd, a, j)], index[(hd, b, j)]
+            w = 0.0 if sm_of_task[ka] == sm_of_task[kb] else h
+            edges.append((4 * ka + 3, 4 * kb + 2, w))
     return 4 * len(tasks), edges, tasks, sm_of_task
 
 
 def simulate_ex(mask: str, sched: str, n: int, m: int, num_sms: int, c: float, r: float,
-                h: float = 0.0, overlapped: bool = False):
+                h: float = 0.0, overlapped: bool = False, dealt: bool = False):
     """Critical path of schedule_dag_ex; same return value as simulate."""
     nv, edges, tasks, sm_of_task = schedule_dag_ex(mask, sched, n, m, num_sms, c, r, h,
-                                                   overlapped)
+                                                   overlapped, dealt)
     depth = longest_path(nv, edges)
     if depth is None:
         return {"makespan": None, "sm_end": None, "sm_idle": None}

@@ -61,7 +61,8 @@ struct BwdParams {
   int chains;                 // interleaved dQ chains, 1..kDqChains (deterministic mode)
   const int32_t* slot_off;   // schedule: chain offsets
   const int32_t* tasks;      // schedule: (kv << 16) | q
-  const int32_t* ord;        // schedule: n * n ordinals
+  const int32_t* ord;        // schedule: ordinals, ord[bh * ord_stride + i * n + j]
+  long long ord_stride;      // n * n when every head has its own order, else 0
   const int32_t* cnt;        // schedule: contributors per dQ block
   int B, S, H, D;
   int n;                     // tiles per head

@@ -53,6 +53,8 @@ struct DeviceTables {
 std::mutex g_mu;
 std::map<std::tuple<int, int, int, int>, DeviceTables> g_tables;        // (dev, mask, sched, n)
 std::map<std::tuple<int, int, int, int, int>, bool> g_deadlock_free;    // (mask, sched, n, heads, grid)
+// per-head dQ orders of the arrival-ordered schedules, (dev, mask, sched, n, heads, grid)
+std::map<std::tuple<int, int, int, int, int, int>, int32_t*> g_dealt;
 
 dash_status_t get_tables(int dev, int mask, int sched, int n, DeviceTables* out) {
   std::lock_guard<std::mutex> lk(g_mu);
@@ -78,6 +80,37 @@ dash_status_t get_tables(int dev, int mask, int sched, int n, DeviceTables* out)
   DASH_CUDA(upload(sc.cnt, &t.cnt));
   g_tables[key] = t;
   *out = t;
+  return DASH_OK;
+}
+
+// Points p->ord at the dQ orders the kernel follows on a grid of `grid` CTAs: the
+// schedule's own table for ascending/descending (one order for all heads), the per-head
+// arrival orders of dash::dealt_orders for shift and symmetric shift (cached per shape).
+dash_status_t set_orders(int dev, int mask, int sched, int n, int heads, int grid,
+                         const DeviceTables& tb, dash::BwdParams* p) {
+  p->ord = tb.ord;
+  p->ord_stride = 0;
+  if (sched != dash::SCHED_SHIFT && sched != dash::SCHED_SYMMETRIC_SHIFT) return DASH_OK;
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto key = std::make_tuple(dev, mask, sched, n, heads, grid);
+  auto it = g_dealt.find(key);
+  if (it == g_dealt.end()) {
+    dash::Schedule sc;
+    int rc = dash::build_schedule(mask, sched, n, &sc);
+    if (rc) return (dash_status_t)rc;
+    std::vector<int32_t> ord;
+    dash::dealt_orders(sc, heads, grid, &ord);
+    int32_t* d = nullptr;
+    DASH_CUDA(cudaMalloc(&d, ord.size() * sizeof(int32_t)));
+    cudaError_t e = cudaMemcpy(d, ord.data(), ord.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+      cudaFree(d);
+      return cuda_fail(e, "cudaMemcpy(dQ orders)");
+    }
+    it = g_dealt.emplace(key, d).first;
+  }
+  p->ord = it->second;
+  p->ord_stride = (long long)n * n;
   return DASH_OK;
 }
 
@@ -263,8 +296,13 @@ void dash_attn_shutdown(void) {
     cudaFree(kv.second.ord);
     cudaFree(kv.second.cnt);
   }
+  for (auto& kv : g_dealt) {
+    cudaSetDevice(std::get<0>(kv.first));
+    cudaFree(kv.second);
+  }
   if (cur >= 0) cudaSetDevice(cur);
   g_tables.clear();
+  g_dealt.clear();
   g_deadlock_free.clear();
 }
 
@@ -412,6 +450,8 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
   if (grid > p.num_units) grid = p.num_units;
   if (deterministic && !deadlock_free(mask, schedule, n, B * H, grid))
     return DASH_ERR_DEADLOCK_RISK;
+  st = set_orders(dev, mask, schedule, n, B * H, grid, tb, &p);
+  if (st != DASH_OK) return st;
 
   dash::bwd_preprocess_kernel<<<sms * 4, 256, 0, stream>>>(p);
   DASH_CUDA(cudaGetLastError());
@@ -502,6 +542,18 @@ int dash_sched_table(int mask, int schedule, int n, int32_t* slot_offsets, int32
   std::memcpy(tasks, sc.tasks.data(), sc.tasks.size() * sizeof(int32_t));
   std::memcpy(ordinals, sc.ord.data(), sc.ord.size() * sizeof(int32_t));
   return (int)sc.tasks.size();
+}
+
+dash_status_t dash_sched_dealt_table(int mask, int schedule, int n, int heads, int grid,
+                                    int32_t* ordinals) {
+  if (heads < 1 || grid < 1 || !ordinals) return DASH_ERR_INVALID_ARG;
+  dash::Schedule sc;
+  int rc = dash::build_schedule(mask, schedule, n, &sc);
+  if (rc) return (dash_status_t)rc;
+  std::vector<int32_t> ord;
+  dash::dealt_orders(sc, heads, grid, &ord);
+  std::memcpy(ordinals, ord.data(), ord.size() * sizeof(int32_t));
+  return DASH_OK;
 }
 
 dash_status_t dash_sched_simulate(int mask, int schedule, int n, int heads, int num_sms,
@@ -683,13 +735,23 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
   dash::Schedule sc;
   int rc = dash::build_schedule(mask, schedule, n, &sc);
   if (rc) return (dash_status_t)rc;
+  int dev = 0, sms = 0;
+  DASH_CUDA(cudaGetDevice(&dev));
+  DASH_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const int units = B * H * sc.num_slots;
+  const int grid = sms < units ? sms : units;
+  // the dQ orders of this grid (per head for shift and symmetric shift), as the regular
+  // entry point uses them
+  std::vector<int32_t> ord;
+  if (dash::arrival_ordered(sc)) dash::dealt_orders(sc, B * H, grid, &ord);
+  else ord = sc.ord;
 
   // scratch layout: the backward workspace, then the schedule tables
   const WsLayout wl = ws_layout(B, S, H, D);
   const size_t t_off = wl.total;
   const size_t t_task = round_up(t_off + sc.slot_off.size() * 4, 256);
   const size_t t_ord = round_up(t_task + sc.tasks.size() * 4, 256);
-  const size_t t_cnt = round_up(t_ord + sc.ord.size() * 4, 256);
+  const size_t t_cnt = round_up(t_ord + ord.size() * 4, 256);
   const size_t need = round_up(t_cnt + sc.cnt.size() * 4, 256);
   if (need > kStaticScratchBytes) {
     char buf[200];
@@ -700,8 +762,6 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
     g_last_error = buf;
     return DASH_ERR_WORKSPACE_TOO_SMALL;
   }
-  int dev = 0;
-  DASH_CUDA(cudaGetDevice(&dev));
   unsigned char* ws = nullptr;
   dash_status_t st = static_scratch(dev, &ws);
   if (st != DASH_OK) return st;
@@ -711,7 +771,7 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
                             cudaMemcpyHostToDevice, stream));
   DASH_CUDA(cudaMemcpyAsync(ws + t_task, sc.tasks.data(), sc.tasks.size() * 4,
                             cudaMemcpyHostToDevice, stream));
-  DASH_CUDA(cudaMemcpyAsync(ws + t_ord, sc.ord.data(), sc.ord.size() * 4,
+  DASH_CUDA(cudaMemcpyAsync(ws + t_ord, ord.data(), ord.size() * 4,
                             cudaMemcpyHostToDevice, stream));
   DASH_CUDA(cudaMemcpyAsync(ws + t_cnt, sc.cnt.data(), sc.cnt.size() * 4,
                             cudaMemcpyHostToDevice, stream));
@@ -734,6 +794,7 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
   p.slot_off = (const int32_t*)(ws + t_off);
   p.tasks = (const int32_t*)(ws + t_task);
   p.ord = (const int32_t*)(ws + t_ord);
+  p.ord_stride = dash::arrival_ordered(sc) ? (long long)n * n : 0;
   p.cnt = (const int32_t*)(ws + t_cnt);
   p.B = B;
   p.S = S;
@@ -774,10 +835,6 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
     return DASH_ERR_CUDA;
   }
   DASH_CUDA(cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-  int sms = 0;
-  DASH_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  int grid = sms;
-  if (grid > p.num_units) grid = p.num_units;
   if (deterministic && !deadlock_free(mask, schedule, n, B * H, grid))
     return DASH_ERR_DEADLOCK_RISK;
 

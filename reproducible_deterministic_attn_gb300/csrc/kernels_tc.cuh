@@ -512,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = ptx::mbar_wait(bars + B_STG_FULL, it & 1, abort_flag, tmo);
           tr.add(TR_DQ_FULL, t0);
           if (!ok) break;
-          const int ord = p.ord[w.i * p.n + w.j];
+          const int ord = __ldg(p.ord + w.bh * p.ord_stride + w.i * p.n + w.j);
           const int chain = ord % p.chains, o = ord / p.chains;   // interleaved chains
           const int sem_idx = (w.bh * p.n + w.j) * kDqChains + chain;
           if (p.deterministic && hs == 0) {

@@ -504,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) ptx::mbar_arrive(bars + E_DQ_EMPTY);   // dQ^T(it) has left TMEM
       // The block's fixed order runs as p.chains interleaved chains: contribution o waits
       // for o - chains, in chain o % chains, adding into accumulator copy o % chains.
-      const int ord = p.ord[w.i * p.n + w.j];
+      const int ord = __ldg(p.ord + w.bh * p.ord_stride + w.i * p.n + w.j);
       const int chain = ord % p.chains, o = ord / p.chains;
       const int sem_idx = (w.bh * p.n + w.j) * kDqChains + chain;
       if (p.deterministic) {

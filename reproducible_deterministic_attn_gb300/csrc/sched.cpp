@@ -10,7 +10,9 @@
 //                    diagonal, then KV_(n-1-p)'s lower-right triangle downwards.
 // dQ_j reduction order: ascending KV index for ascending/descending; the arrival step
 // (position in the chain) for shift and symmetric shift, which never puts two chains
-// on one dQ block at the same step.
+// on one dQ block at the same step. On a persistent grid that runs a head's chains in
+// more than one round, shift and symmetric shift order by arrival under the dealing
+// (dealt_orders below).
 #include "sched.h"
 
 #include <algorithm>
@@ -98,6 +100,37 @@ int build_schedule(int mask, int sched, int n, Schedule* out) {
   return 0;
 }
 
+void dealt_orders(const Schedule& sc, int heads, int grid, std::vector<int32_t>* out) {
+  const int n = sc.n;
+  out->assign((size_t)heads * n * n, -1);
+  if (!arrival_ordered(sc)) {
+    for (int h = 0; h < heads; ++h)
+      std::copy(sc.ord.begin(), sc.ord.end(), out->begin() + (size_t)h * n * n);
+    return;
+  }
+  // (place in the CTA's task sequence, kv) of every partial, per (head, dQ block)
+  std::vector<std::vector<std::pair<long long, int>>> arrivals((size_t)heads * n);
+  std::vector<long long> place(grid, 0);
+  const long long units = (long long)heads * sc.num_slots;
+  for (long long u = 0; u < units; ++u) {
+    const int cta = (int)(u % grid);
+    const int head = (int)(u / sc.num_slots), slot = (int)(u % sc.num_slots);
+    const int beg = sc.slot_off[slot], len = sc.slot_off[slot + 1] - beg;
+    for (int t = 0; t < len; ++t) {
+      const int32_t tk = sc.tasks[beg + t];
+      arrivals[(size_t)head * n + (tk & 0xffff)].push_back({place[cta] + t, tk >> 16});
+    }
+    place[cta] += len;
+  }
+  for (size_t hj = 0; hj < arrivals.size(); ++hj) {
+    auto& a = arrivals[hj];
+    std::sort(a.begin(), a.end());
+    const size_t head = hj / n, j = hj % n;
+    for (size_t k = 0; k < a.size(); ++k)
+      (*out)[(head * n + (size_t)a[k].second) * n + j] = (int32_t)k;
+  }
+}
+
 bool simulate(const Schedule& sc, int heads, int num_sms, double c, double r,
               double* makespan, std::vector<double>* sm_end) {
   return simulate_ex(sc, heads, num_sms, c, r, 0.0, false, makespan, sm_end);
@@ -107,11 +140,16 @@ bool simulate_ex(const Schedule& sc, int heads, int num_sms, double c, double r,
                  bool overlapped, double* makespan, std::vector<double>* sm_end) {
   const int n = sc.n;
   const long long units = (long long)heads * sc.num_slots;
-  // who reduces at position k of dQ_j: inv[j * n + k] = kv tile
-  std::vector<int32_t> inv((size_t)n * n, -1);
-  for (int i = 0; i < n; ++i)
-    for (int j = 0; j < n; ++j)
-      if (sc.ord[(size_t)i * n + j] >= 0) inv[(size_t)j * n + sc.ord[(size_t)i * n + j]] = i;
+  std::vector<int32_t> ord;
+  dealt_orders(sc, heads, num_sms, &ord);
+  // who reduces at position k of head h's dQ_j: inv[(h * n + j) * n + k] = kv tile
+  std::vector<int32_t> inv((size_t)heads * n * n, -1);
+  for (int hd = 0; hd < heads; ++hd)
+    for (int i = 0; i < n; ++i)
+      for (int j = 0; j < n; ++j) {
+        const int o = ord[((size_t)hd * n + i) * n + j];
+        if (o >= 0) inv[((size_t)hd * n + j) * n + o] = i;
+      }
 
   // per SM: the list of units in dealing order; progress = (unit index, task index)
   std::vector<std::vector<long long>> sm_units(num_sms);
@@ -133,10 +171,10 @@ bool simulate_ex(const Schedule& sc, int heads, int num_sms, double c, double r,
         const int beg = sc.slot_off[slot], len = sc.slot_off[slot + 1] - beg;
         const int32_t tk = sc.tasks[beg + task_pos[sm]];
         const int i = tk >> 16, j = tk & 0xffff;
-        const int o = sc.ord[(size_t)i * n + j];
+        const int o = ord[((size_t)head * n + i) * n + j];
         double pred_ready = 0.0;
         if (o > 0) {
-          const int ip = inv[(size_t)j * n + o - 1];
+          const int ip = inv[((size_t)head * n + j) * n + o - 1];
           const size_t pk = ((size_t)head * n + ip) * n + j;
           if (rend[pk] < 0) break;                              // predecessor not done
           pred_ready = rend[pk] + (rsm[pk] == sm ? 0.0 : h);

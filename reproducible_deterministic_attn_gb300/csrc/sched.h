@@ -26,8 +26,30 @@ struct Schedule {
 // Returns 0 and fills `out`, or a positive dash_status_t code.
 int build_schedule(int mask, int sched, int n, Schedule* out);
 
+// The dQ order the kernels follow when `heads` heads' chains are dealt round robin,
+// head-major, onto `grid` persistent CTAs: out[(h * n + i) * n + j] = position of KV_i's
+// partial in head h's dQ_j order (-1 where the mask removes the task).
+//   ascending, descending  -- ascending KV index in every head (`ord` repeated);
+//   shift, symmetric shift -- order of arrival: a partial's place in its CTA's task
+//                             sequence (the tasks of the CTA's earlier units, then its
+//                             step), the lower KV index first on a tie.
+// When every chain of a head starts together (the pages' setting: one head on n SMs,
+// or whole heads per round of the grid) the arrival order is the step order of `ord`.
+// When the dealing splits a head over two rounds of the grid, the partials of the chains
+// that run in the earlier round come first, so no partial waits for a chain that has not
+// started. An arrival-ordered wait always points to a strictly earlier (place, KV index)
+// and each CTA runs its tasks in increasing place, so these orders cannot deadlock.
+void dealt_orders(const Schedule& sc, int heads, int grid, std::vector<int32_t>* out);
+
+// True when the schedule orders dQ by arrival (its order depends on the dealing).
+inline bool arrival_ordered(const Schedule& sc) {
+  return sc.sched == SCHED_SHIFT || sc.sched == SCHED_SYMMETRIC_SHIFT;
+}
+
 // Event-driven critical path of `heads` heads dealt round robin (head-major) onto
-// `num_sms` SMs. Returns false on a cycle (deadlock). sm_end may be null.
+// `num_sms` SMs, with the dQ orders of dealt_orders(sc, heads, num_sms) -- the orders the
+// kernels follow on a grid of num_sms CTAs. Returns false on a cycle (deadlock). sm_end
+// may be null.
 bool simulate(const Schedule& sc, int heads, int num_sms, double c, double r,
               double* makespan, std::vector<double>* sm_end);
 

@@ -56,6 +56,7 @@ _SIGNATURES = {
     "dash_profile_read": (_c_int, [_dblp, ctypes.POINTER(_c_int)]),
     "dash_sched_num_slots": (_c_int, [_c_int, _c_int, _c_int]),
     "dash_sched_table": (_c_int, [_c_int, _c_int, _c_int, _i32p, _i32p, _c_int, _i32p]),
+    "dash_sched_dealt_table": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _i32p]),
     "dash_sched_simulate": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_double, _c_double,
                                      _dblp, _dblp]),
     "dash_sched_simulate_ex": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_double,
@@ -202,6 +203,15 @@ def dash_sched_table(mask: int, schedule: int, n: int):
         raise DashError(-cnt, "dash_sched_table")
     pairs = [(tasks[k] >> 16, tasks[k] & 0xFFFF) for k in range(cnt)]
     return list(off), pairs, [list(ords[i * n:(i + 1) * n]) for i in range(n)]
+
+
+def dash_sched_dealt_table(mask: int, schedule: int, n: int, heads: int, grid: int):
+    """The dQ orders the backward follows on `grid` CTAs: ords[h][i][j] (-1 = masked)."""
+    ords = (ctypes.c_int32 * (heads * n * n))()
+    _check(load().dash_sched_dealt_table(int(mask), int(schedule), int(n), int(heads),
+                                         int(grid), ords), "dash_sched_dealt_table")
+    return [[list(ords[(h * n + i) * n:(h * n + i + 1) * n]) for i in range(n)]
+            for h in range(heads)]
 
 
 def dash_sched_simulate(mask: int, schedule: int, n: int, heads: int, num_sms: int,

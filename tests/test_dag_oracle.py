@@ -266,3 +266,69 @@ def test_sync_worked_example_accumulator_reuse():
                           mode == "overlapped")["makespan"]
         assert got == float(want)
 
+
+
+# ---------------------------------------------------------------------------------------
+# dQ orders by arrival on a dealt grid (oracle.dag.dealt_reduction_order, dealt=True)
+# ---------------------------------------------------------------------------------------
+DEALT_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "dag_dealt_examples.txt")
+
+
+def _dealt_rows(kind):
+    with open(DEALT_GOLDEN) as f:
+        return [[x.strip() for x in line.split("|")[1:]] for line in f
+                if line.startswith(kind)]
+
+
+def test_dealt_worked_examples_orders():
+    from oracle.dag import dealt_reduction_order
+    rows = _dealt_rows("ORDER")
+    assert len(rows) == 8
+    for mask, sched, n, m, sms, head, j, want in rows:
+        got = dealt_reduction_order(mask, sched, int(n), int(m), int(sms))[(int(head), int(j))]
+        assert got == [int(x) for x in want.split()], (mask, sched, j)
+
+
+def test_dealt_worked_examples_makespans():
+    rows = _dealt_rows("MAKESPAN")
+    assert len(rows) == 2
+    for mask, sched, n, m, sms, c, r, want, ends in rows:
+        res = simulate(mask, sched, int(n), int(m), int(sms), float(c), float(r), dealt=True)
+        assert res["makespan"] == float(want)
+        assert res["sm_end"] == [float(x) for x in ends.split()]
+        # the fixed per-schedule order deadlocks on these grids
+        assert simulate(mask, sched, int(n), int(m), int(sms), float(c), float(r))["makespan"] is None
+
+
+def test_dealt_equals_the_pages_order_when_heads_start_together():
+    from oracle.dag import dealt_reduction_order
+    for mask, sched in [("full", "ascending"), ("full", "descending"), ("full", "shift"),
+                        ("causal", "ascending"), ("causal", "descending"),
+                        ("causal", "symmetric_shift")]:
+        for n in (2, 4, 6, 8):
+            slots = len(chains(mask, sched, n))
+            fixed = reduction_order(mask, sched, n)
+            for m in (1, 2, 3):
+                sms_list = [slots * k for k in (1, 2, 3)]
+                if sched in ("ascending", "descending"):
+                    sms_list += [1, 3, 5]          # their order ignores the dealing
+                for sms in sms_list:
+                    got = dealt_reduction_order(mask, sched, n, m, sms)
+                    for h in range(m):
+                        for j in range(n):
+                            assert got[(h, j)] == fixed[j], (mask, sched, n, m, sms, h, j)
+
+
+def test_dealt_orders_are_permutations_and_never_deadlock():
+    from oracle.dag import dealt_reduction_order
+    for mask, sched in [("full", "shift"), ("causal", "symmetric_shift")]:
+        for n in (2, 4, 6):
+            fixed = reduction_order(mask, sched, n)
+            for m in (1, 2, 3):
+                for sms in range(1, 2 * n + 2):
+                    got = dealt_reduction_order(mask, sched, n, m, sms)
+                    for (h, j), kv in got.items():
+                        assert sorted(kv) == sorted(fixed[j])
+                    assert simulate(mask, sched, n, m, sms, 3, 1, dealt=True)["makespan"] is not None
+                    res = simulate_ex(mask, sched, n, m, sms, 3, 1, 2, True, dealt=True)
+                    assert res["makespan"] is not None, (mask, sched, n, m, sms)

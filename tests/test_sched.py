@@ -44,6 +44,43 @@ def test_tables_match_oracle(mask, sched):
         assert masked == (0 if mask == 0 else n * (n - 1) // 2)
 
 
+@pytest.mark.parametrize("seed", range(8))
+def test_dealt_tables_match_oracle(seed):
+    rng = random.Random(300 + seed)
+    for _ in range(20):
+        mask, sched = rng.choice([(0, 0), (0, 1), (0, 2), (1, 0), (1, 1), (1, 3)])
+        n = rng.choice([1, 2, 3, 4, 6, 8, 12]) if sched != 3 else rng.choice([2, 4, 6, 8, 12])
+        m, grid = rng.randint(1, 5), rng.randint(1, 3 * n + 2)
+        got = da.dash_sched_dealt_table(mask, sched, n, m, grid)
+        want = dag.dealt_reduction_order(MASKS[mask], NAMES[sched], n, m, grid)
+        for h in range(m):
+            for j in range(n):
+                for pos, i in enumerate(want[(h, j)]):
+                    assert got[h][i][j] == pos, (mask, sched, n, m, grid, h, i, j)
+            masked = sum(1 for i in range(n) for j in range(n) if got[h][i][j] < 0)
+            assert masked == (0 if mask == 0 else n * (n - 1) // 2)
+
+
+def test_dealt_tables_at_the_kernel_sizes():
+    # 152 CTAs: full 2x16 heads of n = 64 and causal 32 heads of n = 128 split heads over
+    # two rounds of the grid; the per-head orders still follow the dealing
+    for mask, sched, n, heads in [(0, 2, 64, 32), (1, 3, 128, 32)]:
+        got = da.dash_sched_dealt_table(mask, sched, n, heads, 152)
+        want = dag.dealt_reduction_order(MASKS[mask], NAMES[sched], n, heads, 152)
+        _, _, fixed = da.dash_sched_table(mask, sched, n)
+        differ = 0
+        for h in range(heads):
+            for j in range(n):
+                assert [i for i in sorted(range(n), key=lambda i: got[h][i][j])
+                        if got[h][i][j] >= 0] == want[(h, j)]
+            differ += any(got[h][i] != fixed[i] for i in range(n))
+        assert differ > 0                      # some head is split by the grid
+    with pytest.raises(da.DashError):
+        da.dash_sched_dealt_table(0, 2, 8, 0, 4)
+    with pytest.raises(da.DashError):
+        da.dash_sched_dealt_table(1, 2, 8, 1, 4)      # shift needs the full mask
+
+
 def test_invalid_n():
     assert da.dash_sched_num_slots(0, 0, 0) == -da.DASH_ERR_INVALID_ARG
     assert da.dash_sched_num_slots(0, 0, 40000) == -da.DASH_ERR_INVALID_ARG
@@ -58,7 +95,7 @@ def test_simulator_matches_oracle(seed):
         m = rng.randint(1, 5)
         sms = rng.randint(1, 2 * n + 2)
         c, r = rng.choice([(3.0, 1.0), (1.0, 0.25), (2.0, 2.0), (0.5, 1.5)])
-        want = dag.simulate(MASKS[mask], NAMES[sched], n, m, sms, c, r)
+        want = dag.simulate(MASKS[mask], NAMES[sched], n, m, sms, c, r, dealt=True)
         mk, ends = da.dash_sched_simulate(mask, sched, n, m, sms, c, r)
         if want["makespan"] is None:
             assert mk is None, (mask, sched, n, m, sms)
@@ -88,7 +125,8 @@ def test_sync_simulator_matches_oracle(seed):
         c, r = rng.choice([(3.0, 1.0), (1.0, 0.25), (2.0, 2.0), (0.5, 1.5)])
         h = rng.choice([0.0, 0.5, 2.0, 5.0])
         ovl = rng.randint(0, 1)
-        want = dag.simulate_ex(MASKS[mask], NAMES[sched], n, m, sms, c, r, h, bool(ovl))
+        want = dag.simulate_ex(MASKS[mask], NAMES[sched], n, m, sms, c, r, h, bool(ovl),
+                               dealt=True)
         mk, ends = da.dash_sched_simulate_ex(mask, sched, n, m, sms, c, r, h, ovl)
         if want["makespan"] is None:
             assert mk is None
@@ -110,7 +148,8 @@ def test_selector_is_the_oracle_argmin(seed):
         for s in (0, 1, 2, 3):
             if not _valid(mask, s, n):
                 continue
-            mk = dag.simulate_ex(MASKS[mask], NAMES[s], n, m, sms, c, r, h, bool(ovl))["makespan"]
+            mk = dag.simulate_ex(MASKS[mask], NAMES[s], n, m, sms, c, r, h, bool(ovl),
+                                 dealt=True)["makespan"]
             if mk is not None and (best is None or mk < best_mk):
                 best, best_mk = s, mk
         got, got_mk = da.dash_sched_select(mask, n, m, sms, c, r, h, ovl)
