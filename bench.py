@@ -46,6 +46,11 @@ WORKLOADS = {
     # smaller full-mask case for kernel profiles (inputs still larger than L2)
     "full-2x4096x16x128": dict(mask="full", B=2, S=4096, H=16, D=128),
 }
+# the transformer-block sweep: causal, 16384 tokens (B * S), 32 heads, D = 64 and 128
+for _s in (1024, 2048, 4096, 8192, 16384):
+    for _d in (64, 128):
+        WORKLOADS.setdefault(f"causal-{16384 // _s}x{_s}x32x{_d}",
+                             dict(mask="causal", B=16384 // _s, S=_s, H=32, D=_d))
 DEFAULT_WORKLOAD = "full-2x8192x16x128"
 BEST_DASH = {"full": "shift", "causal": "symmetric_shift"}   # reference arm's naming only
 # Cost model of the run-time selector (dash_sched_select), cycles per 128 x 128 task measured
@@ -297,9 +302,13 @@ def run_gpu(args, w, rank, world, local_rank):
         selected_by = "dash_sched_select, costs " + json.dumps(SELECT_COSTS)
     sched = da.SCHEDULES[args.schedule]
     # deterministic mode: 1 = one fixed chain per dQ block (the pages' order as one serial
-    # chain), 2 = the same order as two interleaved chains; measured on GB300 the second is
-    # faster at head dim 128 (687 vs 588 TF/s on full 2x8192x16x128) and not at 64
-    DET = (2 if D == 128 else 1) if args.dq_chains == "auto" else int(args.dq_chains)
+    # chain), 2 = the same order as two interleaved chains. Measured on GB300 the second is
+    # faster at head dim 128 once blocks have long chains (S >= 8192: 707 vs 673 TF/s on
+    # full 2x8192x16x128, 700 vs 674 on causal 1x16384x32x128) and slower below, where
+    # zeroing and summing the second fp32 copy costs more than the shorter waits save
+    # (causal 4x4096x32x128: 523 vs 539); at head dim 64 one chain.
+    DET = ((2 if D == 128 and S >= 8192 else 1) if args.dq_chains == "auto"
+           else int(args.dq_chains))
 
     x = make_inputs(B, S, H, D, seed=rank)
     q, k, v, do = (x[nm].to(dev) for nm in ("q", "k", "v", "do"))
