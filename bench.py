@@ -389,6 +389,26 @@ def run_gpu(args, w, rank, world, local_rank):
         ms_s, _ = timed(n_side, det, s)
         side[name] = job_tflops(bwd_flops(w), world, ms_s)
 
+    # The ordered reduction's waits, from the kernel's own wait-cycle trace in one extra,
+    # untimed launch of the timed mode: cycles per 128 x 128 task (summed over CTAs,
+    # divided by the tasks) spent waiting for a dQ block's turn and adding + handing it on.
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    trace = torch.zeros(sms * da.TRACE_SITES, dtype=torch.int64, device=dev)
+    da.dash_debug_set_trace(trace)
+    step()
+    torch.cuda.synchronize()
+    da.dash_debug_set_trace(None)
+    st = da.dash_attn_get_status(ws)
+    if st != da.DASH_OK:
+        raise da.DashError(st, "traced backward")
+    n_t = S // 128
+    tasks = B * H * (n_t * (n_t + 1) // 2 if causal else n_t * n_t)
+    tr = trace.view(sms, da.TRACE_SITES).sum(dim=0).double().cpu()
+    dq_sem = {"turn_wait_cycles_per_task": float(tr[da.TRACE_DQ_TURN_WAIT]) / tasks,
+              "add_and_handoff_cycles_per_task": float(tr[da.TRACE_DQ_ADD]) / tasks,
+              "cycles_per_task": float(tr[da.TRACE_TOTAL]) / tasks,
+              "source": "in-kernel clock64 wait trace (dash_debug_set_trace), one untimed launch"}
+
     # End to end through the public API with host buffers: every step uploads its inputs
     # from pinned host memory, runs the backward and downloads dQ/dK/dV. Two device buffer
     # sets and two copy streams let step i+1's upload and step i-1's download run while
@@ -481,6 +501,7 @@ def run_gpu(args, w, rank, world, local_rank):
                            "run on copy streams while step i computes"},
         "gpu_launches": launches_per_step * steps,
         "clocks": clocks,
+        "dq_semaphore": dq_sem,
     }
     print(json.dumps(line), flush=True)
 

@@ -183,10 +183,13 @@ void dash_debug_set_sync(long long timeout_ns, int ordinal_skew);
 /*
  * Tracing hook. When device_counters is not NULL, later dash_attn_bwd main kernels add,
  * per CTA, the clock cycles spent in each of their waits into
- * device_counters[cta * 24 + site] (uint64; the sites are listed in the library's
- * sources: producer, MMA, softmax-gradient and dQ waits, the dQ semaphore wait, the
- * reduce, and the CTA's total cycles at index 19). The buffer must hold 24 counters per
- * SM of the device, zeroed by the caller. NULL turns tracing off.
+ * device_counters[cta * 24 + site] (uint64). Sites with a fixed meaning in both kernels:
+ *   15 : waiting for a dQ block's turn (the ordered mode's semaphore wait),
+ *   16 : adding a dQ partial into the accumulator and handing the turn on,
+ *   19 : the CTA's total cycles.
+ * The other sites (producer, MMA-issue and softmax-gradient waits) are listed in the
+ * library's sources. The buffer must hold 24 counters per SM of the device, zeroed by
+ * the caller. NULL turns tracing off.
  */
 void dash_debug_set_trace(void* device_counters);
 

@@ -169,6 +169,13 @@ def dash_debug_set_sync(timeout_ns: int, ordinal_skew: int) -> None:
     load().dash_debug_set_sync(int(timeout_ns), int(ordinal_skew))
 
 
+# dash_debug_set_trace sites with a fixed meaning (include/dash_attn.h)
+TRACE_SITES = 24
+TRACE_DQ_TURN_WAIT = 15     # waiting for a dQ block's turn (ordered mode)
+TRACE_DQ_ADD = 16           # adding a dQ partial and handing the turn on
+TRACE_TOTAL = 19            # the CTA's total cycles
+
+
 def dash_debug_set_trace(counters) -> None:
     """counters: a zeroed uint64 CUDA tensor of 24 * SM-count entries, or None to stop."""
     load().dash_debug_set_trace(None if counters is None else counters.data_ptr())
