@@ -269,10 +269,15 @@ def traffic_from_profile(w, sched):
     return float(ent) if ent is not None else None
 
 
+# the sources the main head-dim-128 kernel is compiled from (the file and its includes):
+# the traffic record stays valid while none of them changes
+MAIN_KERNEL_SOURCES = ("common.cuh", "kernels_tc.cuh", "kernels_tc128.cuh", "tc_ptx.cuh")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "reproducible_deterministic_attn_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in MAIN_KERNEL_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
