@@ -8,6 +8,7 @@
 #include <cstdio>
 #include <cstring>
 #include <map>
+#include <memory>
 #include <mutex>
 #include <string>
 #include <tuple>
@@ -55,6 +56,23 @@ std::map<std::tuple<int, int, int, int>, DeviceTables> g_tables;        // (dev,
 std::map<std::tuple<int, int, int, int, int>, bool> g_deadlock_free;    // (mask, sched, n, heads, grid)
 // per-head dQ orders of the arrival-ordered schedules, (dev, mask, sched, n, heads, grid)
 std::map<std::tuple<int, int, int, int, int, int>, int32_t*> g_dealt;
+// their host copies, (mask, sched, n, heads, grid): building one sorts every task of the
+// shape, so it is done once per shape
+std::map<std::tuple<int, int, int, int, int>, std::shared_ptr<const std::vector<int32_t>>> g_host_dealt;
+
+// Host copy of the per-head dQ orders of an arrival-ordered schedule on `grid` CTAs
+// (cached; the caller holds g_mu).
+std::shared_ptr<const std::vector<int32_t>> host_dealt_locked(const dash::Schedule& sc,
+                                                              int heads, int grid) {
+  auto key = std::make_tuple(sc.mask, sc.sched, sc.n, heads, grid);
+  auto it = g_host_dealt.find(key);
+  if (it == g_host_dealt.end()) {
+    auto v = std::make_shared<std::vector<int32_t>>();
+    dash::dealt_orders(sc, heads, grid, v.get());
+    it = g_host_dealt.emplace(key, std::move(v)).first;
+  }
+  return it->second;
+}
 
 dash_status_t get_tables(int dev, int mask, int sched, int n, DeviceTables* out) {
   std::lock_guard<std::mutex> lk(g_mu);
@@ -98,8 +116,7 @@ dash_status_t set_orders(int dev, int mask, int sched, int n, int heads, int gri
     dash::Schedule sc;
     int rc = dash::build_schedule(mask, sched, n, &sc);
     if (rc) return (dash_status_t)rc;
-    std::vector<int32_t> ord;
-    dash::dealt_orders(sc, heads, grid, &ord);
+    const std::vector<int32_t>& ord = *host_dealt_locked(sc, heads, grid);
     int32_t* d = nullptr;
     DASH_CUDA(cudaMalloc(&d, ord.size() * sizeof(int32_t)));
     cudaError_t e = cudaMemcpy(d, ord.data(), ord.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
@@ -303,6 +320,7 @@ void dash_attn_shutdown(void) {
   if (cur >= 0) cudaSetDevice(cur);
   g_tables.clear();
   g_dealt.clear();
+  g_host_dealt.clear();
   g_deadlock_free.clear();
 }
 
@@ -741,10 +759,13 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
   const int units = B * H * sc.num_slots;
   const int grid = sms < units ? sms : units;
   // the dQ orders of this grid (per head for shift and symmetric shift), as the regular
-  // entry point uses them
-  std::vector<int32_t> ord;
-  if (dash::arrival_ordered(sc)) dash::dealt_orders(sc, B * H, grid, &ord);
-  else ord = sc.ord;
+  // entry point uses them; the per-head table is built once per shape (host memory)
+  std::shared_ptr<const std::vector<int32_t>> dealt;
+  if (dash::arrival_ordered(sc)) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    dealt = host_dealt_locked(sc, B * H, grid);
+  }
+  const std::vector<int32_t>& ord = dealt ? *dealt : sc.ord;
 
   // scratch layout: the backward workspace, then the schedule tables
   const WsLayout wl = ws_layout(B, S, H, D);
