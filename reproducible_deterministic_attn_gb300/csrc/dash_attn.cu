@@ -251,10 +251,10 @@ bool map_acc(CUtensorMap* m, float* ptr, long long rows_total, int D, int rows) 
 
 // 2D view [rows][K] of a row-major bf16 matrix; box = 64 K-columns x 128 rows, 128-byte
 // swizzle.
-bool map_rows_k(CUtensorMap* m, const void* ptr, int rows, int K) {
+bool map_rows_k(CUtensorMap* m, const void* ptr, int rows, int K, int box_rows) {
   const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   const cuuint32_t es[2] = {1, 1};
   return encoder()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -606,8 +606,11 @@ dash_status_t dash_gemm_splitk(const void* a, const void* b, float* c, void* wor
     g_last_error = "cuTensorMapEncodeTiled is not available from the driver";
     return DASH_ERR_CUDA;
   }
+  // output tiles of 256 rows of C when M allows (the MMA is then 256 wide and runs at the
+  // tensor core's full rate), else 128
+  const int tm = (M % 256 == 0) ? 256 : 128;
   dash::tc::GemmMaps maps;
-  if (!map_rows_k(&maps.a, a, M, K) || !map_rows_k(&maps.b, b, N, K)) {
+  if (!map_rows_k(&maps.a, a, M, K, tm) || !map_rows_k(&maps.b, b, N, K, 128)) {
     g_last_error = "cuTensorMapEncodeTiled rejected a tensor";
     return DASH_ERR_CUDA;
   }
@@ -629,10 +632,10 @@ dash_status_t dash_gemm_splitk(const void* a, const void* b, float* c, void* wor
   int dev = 0, sms = 0;
   DASH_CUDA(cudaGetDevice(&dev));
   DASH_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  const int units = (M / 128) * (N / 128) * splits;
+  const int units = (M / tm) * (N / 128) * splits;
   const int grid = units < sms ? units : sms;
-  void* kfn = (void*)dash::tc::gemm_splitk_kernel;
-  const size_t smem = dash::tc::GemmL::ALLOC;
+  void* kfn = tm == 256 ? (void*)dash::tc::gemm_splitk_kernel<256> : (void*)dash::tc::gemm_splitk_kernel<128>;
+  const size_t smem = tm == 256 ? dash::tc::GemmL<256>::ALLOC : dash::tc::GemmL<128>::ALLOC;
   DASH_CUDA(cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   void* args[] = {&p, &maps};
   // deterministic: chunks wait on other CTAs' adds, so every CTA must be resident at once;
