@@ -295,7 +295,9 @@ dash_status_t dash_sched_select(int mask, int n, int heads, int num_sms, double 
  *   a : bf16 [M, K] row-major (read);  b : bf16 [N, K] row-major (read);
  *   c : fp32 [M, N] row-major (written: zeroed, then every K chunk's partial added);
  *   workspace : device scratch of dash_gemm_splitk_workspace_size(M, N) bytes, 256-byte
- *               aligned (status header + one int32 semaphore per 128 x 128 output tile);
+ *               aligned (status header + room for one int32 semaphore per 128 x 128 block
+ *               of C; the kernel's output tiles are 256 x 128 when M is a multiple of 256
+ *               -- full-rate 256-wide MMAs -- else 128 x 128, one semaphore each);
  *   splits : K is cut into `splits` equal chunks, one unit of work each per output tile;
  *   deterministic = 1: a tile's chunks are added in ascending chunk order (bitwise
  *               identical run to run); 0: in arrival order.
