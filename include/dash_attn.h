@@ -16,7 +16,10 @@
  * - The causal mask is top-left aligned (query i sees keys 0..i).
  * - All device pointers are owned by the caller and must stay valid until the work
  *   queued on `stream` has finished. The library allocates nothing per call; it keeps a
- *   small cache of schedule tables per device (released by dash_attn_shutdown).
+ *   cache of schedule tables per device and shape, built on first use: the task tables
+ *   (O(n^2) int32 per schedule) and, for SHIFT and SYMMETRIC_SHIFT, the per-head dQ
+ *   orders of the grid in use (B * H * n^2 int32, n = S / 128: 0.5 MB for 2x16 heads at
+ *   S = 8192), on the device and in host memory. dash_attn_shutdown releases all of it.
  * - Calls are asynchronous on `stream`. Argument errors are returned synchronously and
  *   queue no work. Device-side failures (a reduction wait that timed out) are recorded
  *   in the workspace and reported by dash_attn_get_status.
