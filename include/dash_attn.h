@@ -259,8 +259,9 @@ dash_status_t dash_sched_simulate(int mask, int schedule, int n, int heads, int 
                                   double c, double r, double* makespan, double* sm_end);
 
 /*
- * The same critical path with synchronisation cost (the Pith review's "What would settle
- * it": nonzero edge costs; its ledger lists zero-cost order edges as a modelling choice):
+ * The same critical path with synchronisation cost (the Pith review's "Where Pith is
+ * reading between the lines" proposes nonzero edge costs; its Axiom & Free-Parameter
+ * Ledger lists zero-cost order edges as a domain assumption):
  *   h          : cost of handing a dQ block's turn from one SM to another (the order edge's
  *                weight; 0 when consecutive reductions of the block run on one SM);
  *   overlapped : 0 = the SM runs C then R task after task (dash_sched_simulate's model);
@@ -293,8 +294,8 @@ dash_status_t dash_sched_select(int mask, int n, int heads, int num_sms, double 
 
 /*
  * Deterministic split-K GEMM with the same ordered cross-SM reduction (the Pith review's
- * "What would settle it" names a deterministic split-K GEMM as the DAG framing's next
- * application): C = A B^T with
+ * section "Where Pith is reading between the lines" lists split-K GEMMs among the kernels
+ * the reduction-order principle applies to): C = A B^T with
  *   a : bf16 [M, K] row-major (read);  b : bf16 [N, K] row-major (read);
  *   c : fp32 [M, N] row-major (written: zeroed, then every K chunk's partial added);
  *   workspace : device scratch of dash_gemm_splitk_workspace_size(M, N) bytes, 256-byte

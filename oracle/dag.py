@@ -231,8 +231,9 @@ def simulate(mask: str, sched: str, n: int, m: int, num_sms: int, c: float, r: f
 
 
 # ---------------------------------------------------------------------------------------
-# Sync-cost-aware extension (the Pith review's "What would settle it" asks for nonzero
-# synchronisation edge costs; its ledger lists the zero-cost edge as a modelling choice).
+# Sync-cost-aware extension (the Pith review's "Where Pith is reading between the lines"
+# proposes nonzero synchronisation edge costs; its Axiom & Free-Parameter Ledger lists the
+# zero-cost edge as a domain assumption).
 #
 # * h: cost of handing a dQ block's turn from one SM to another -- the weight of an order
 #   edge between consecutive reductions of one dQ block that run on different SMs (0 when

@@ -3,9 +3,9 @@
 Only the test suite may use this module; it shares no code with the CUDA path. What the
 library computes is the plain definition C = A B^T (fp64 here), whatever the split of K:
 the Pith review of "DASH: Deterministic Attention Scheduling for High-throughput
-Reproducible LLM Training" ("What would settle it") names a deterministic split-K GEMM as
-the next application of the same reduction-order framing, and the split only changes the
-order in which the partial sums over K are added.
+Reproducible LLM Training" (section "Where Pith is reading between the lines") lists
+split-K GEMMs among the kernels its reduction-order principle applies to, and the split
+only changes the order in which the partial sums over K are added.
 """
 from __future__ import annotations
 

@@ -1,8 +1,8 @@
 // Split-K GEMM with the same ordered cross-SM reduction as the attention backward's dQ:
 // C (fp32, [M, N]) += A B^T for bf16 A [M, K] and B [N, K] (both K-major), the K extent cut
-// into `splits` chunks. The pages name this generalisation ("the same DAG framing" for a
-// deterministic split-K GEMM, Pith review, "What would settle it"); the task grid is
-// (output tile, K chunk) and each output tile is one reduction chain.
+// into `splits` chunks. The pages list split-K GEMMs among the kernels the reduction-order
+// principle applies to (Pith review, "Where Pith is reading between the lines"); the task
+// grid is (output tile, K chunk) and each output tile is one reduction chain.
 //
 // A unit is one (TM x 128 output tile, K chunk), TM = 256 rows of C when M allows it, else
 // 128; units are dealt tile-major, round robin, to a persistent grid (cooperative launch in

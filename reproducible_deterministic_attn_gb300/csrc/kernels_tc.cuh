@@ -5,7 +5,7 @@
 // One persistent CTA per SM. A unit is one schedule chain (slot) of one (batch, head);
 // CTA c runs units c, c + grid, ... Each schedule task (KV_i, Q_j) covers a 128 x 128
 // tile of the score matrix; KV_i's K and V tiles stay in shared memory for all its
-// tasks and its dK/dV accumulate in TMEM (DASH's "each KV tile's dK/dV stay on one SM").
+// tasks and its dK/dV accumulate in TMEM (DASH keeps a KV tile's dK/dV on one SM).
 //
 // Per task (BR = 128 query rows, one sub-tile; the walk supports SUB > 1 sub-tiles):
 //   S^T  = K Q^T          (M = 128 kv, N = BR, K = D)      -> TMEM

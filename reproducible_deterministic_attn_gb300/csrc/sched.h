@@ -53,8 +53,8 @@ inline bool arrival_ordered(const Schedule& sc) {
 bool simulate(const Schedule& sc, int heads, int num_sms, double c, double r,
               double* makespan, std::vector<double>* sm_end);
 
-// The same with synchronisation cost and the two-engine SM (the Pith review's "What
-// would settle it": nonzero edge costs):
+// The same with synchronisation cost and the two-engine SM (the Pith review's "Where Pith
+// is reading between the lines" proposes nonzero edge costs):
 //   h          -- cost of handing a dQ block's turn to another SM (0 within one SM);
 //   overlapped -- each SM runs C phases in order on one engine and R phases in order on
 //                 another, and C of its k-th task waits for R of its (k-2)-th (the
