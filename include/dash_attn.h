@@ -74,11 +74,26 @@ typedef enum {
  * named on the research map page under "Builds on").
  *   q, k, v : [B, S, H, D] bf16 (read)      o : [B, S, H, D] bf16 (written)
  *   lse     : [B, H, S] fp32 (written)      mask : dash_mask_t
- * Returns DASH_OK or an argument/CUDA error; nothing is queued on error.
+ * Returns DASH_OK or an argument/CUDA error; nothing is queued on error. Every wait
+ * inside the kernel is bounded; a CTA whose wait runs out writes NaN into its LSE rows
+ * (dash_attn_fwd_ex also reports it through a status word).
  */
 dash_status_t dash_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                             int B, int S, int H, int D, float scale, int mask,
                             cudaStream_t stream);
+
+/*
+ * dash_attn_fwd with a device status word:
+ *   status : optional device int32 (4-byte aligned; NULL = none). The call clears it on
+ *            `stream` before the kernel; when any wait inside the kernel runs out (which
+ *            only a fault can cause) the kernel sets it to DASH_ERR_SYNC_TIMEOUT and that
+ *            CTA's O and LSE rows are undefined (LSE NaN). Read it after the stream has
+ *            finished the call; the CUDA context stays usable either way.
+ * Same arguments, conventions and errors as dash_attn_fwd otherwise.
+ */
+dash_status_t dash_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                               int B, int S, int H, int D, float scale, int mask, int* status,
+                               cudaStream_t stream);
 
 /*
  * Bytes of scratch dash_attn_bwd needs for this shape: a status header, D = rowsum(dO*O)
@@ -142,12 +157,16 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
  *   status_out : optional device int (may be NULL); after the kernels it receives the
  *                status word that dash_attn_get_status would report (0 = ok).
  * The first call on a device looks up the array's device address (with that device
- * current); make that first call before any stream capture. Every call on a device
- * shares the one array and leaves its contents behind (the kernels clear what has to
- * start at zero), so calls whose work overlaps on the GPU -- on different streams or
- * from different threads -- race with each other and must be serialised by the caller.
- * No cudaMalloc, cudaFree or other allocating routine is called; the schedule tables
- * are built in host memory and copied into the array with cudaMemcpyAsync on `stream`.
+ * current); make that first call before any stream capture. dash_attn_shutdown forgets
+ * the address, and the next call looks it up again. Every call on a device shares the one
+ * array and leaves its contents behind (the kernels clear what has to start at zero), so
+ * calls whose work overlaps on the GPU -- on different streams or from different
+ * threads -- race with each other and must be serialised by the caller.
+ * No cudaMalloc, cudaFree or other allocating CUDA routine is called. The schedule tables
+ * are built once per shape in host memory, kept there until dash_attn_shutdown, and
+ * copied into the array with one cudaMemcpyAsync on `stream` per call. Every refusal
+ * (argument, size, tensor-map, register, occupancy and deadlock checks) happens before
+ * that copy, so a refused call queues nothing and leaves the array as it was.
  */
 dash_status_t dash_attn_bwd_static(const void* q, const void* k, const void* v, const void* o,
                                    const void* dO, const float* lse, void* dq, void* dk,
@@ -174,24 +193,25 @@ const char* dash_last_error(void);
 void dash_attn_shutdown(void);
 
 /*
- * Testing hook for the failure path of the ordered dQ reduction. Sets, for later
- * dash_attn_bwd calls in this process, the time limit of one semaphore wait
- * (timeout_ns <= 0 restores the default of 10 s) and a skew added to every awaited
- * ordinal. With a skew > 0 no wait can ever be satisfied: each one runs out its limit,
- * the kernel records DASH_ERR_SYNC_TIMEOUT in the workspace and returns, and the CUDA
- * context stays usable. Not thread-safe against concurrent dash_attn_bwd calls.
+ * Testing hook for the failure paths. Sets, for later dash_attn_bwd and dash_attn_fwd(_ex)
+ * calls in this process, the time limit of one wait (timeout_ns <= 0 restores the default
+ * of 10 s) and a skew. In the backward the skew is added to every awaited dQ ordinal; in
+ * the forward a skew > 0 makes the kernel load no K/V tiles. Either way no wait on them
+ * can be satisfied: each one runs out its limit, the kernel records DASH_ERR_SYNC_TIMEOUT
+ * (backward: in the workspace; forward: in dash_attn_fwd_ex's status word) and returns,
+ * and the CUDA context stays usable. Not thread-safe against concurrent calls.
  */
 void dash_debug_set_sync(long long timeout_ns, int ordinal_skew);
 
 /*
  * Tracing hook. When device_counters is not NULL, later dash_attn_bwd main kernels add,
  * per CTA, the clock cycles spent in each of their waits into
- * device_counters[cta * 24 + site] (uint64). Sites with a fixed meaning in both kernels:
+ * device_counters[cta * 32 + site] (uint64). Sites with a fixed meaning in both kernels:
  *   15 : waiting for a dQ block's turn (the ordered mode's semaphore wait),
  *   16 : adding a dQ partial into the accumulator and handing the turn on,
  *   19 : the CTA's total cycles.
  * The other sites (producer, MMA-issue and softmax-gradient waits) are listed in the
- * library's sources. The buffer must hold 24 counters per SM of the device, zeroed by
+ * library's sources. The buffer must hold 32 counters per SM of the device, zeroed by
  * the caller. NULL turns tracing off.
  */
 void dash_debug_set_trace(void* device_counters);

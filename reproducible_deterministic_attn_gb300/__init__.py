@@ -11,7 +11,7 @@ from .dash_attn import (  # noqa: F401
     MASKS, SCHED_ASCENDING, SCHED_DESCENDING, SCHED_SHIFT, SCHED_SYMMETRIC_SHIFT, SCHEDULES,
     DashError, attn_backward, attn_forward, dash_attn_bwd, dash_attn_bwd_static,
     dash_attn_bwd_workspace_size,
-    dash_attn_fwd, dash_attn_get_status, dash_attn_shutdown, dash_debug_set_sync,
+    dash_attn_fwd, dash_attn_fwd_ex, dash_attn_get_status, dash_attn_shutdown, dash_debug_set_sync,
     dash_debug_set_trace,
     dash_last_error, dash_profile_enable, dash_profile_read, dash_sched_num_slots, dash_sched_simulate, dash_sched_simulate_ex, dash_sched_select,
     dash_sched_table, dash_sched_dealt_table, dash_gemm_splitk, dash_gemm_splitk_workspace_size, gemm_splitk,

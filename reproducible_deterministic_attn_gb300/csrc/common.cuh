@@ -40,6 +40,9 @@ struct FwdParams {
   float scale;
   int causal;
   float scale_log2;          // scale * log2(e)
+  int* status;               // optional: set to kStatusSyncTimeout when a wait runs out
+  long long timeout_ns;      // bound on one pipeline wait
+  int withhold_kv;           // testing hook: load no K/V tiles, so the waits for them run out
 };
 
 struct BwdParams {
@@ -83,7 +86,7 @@ enum : int {
   TR_MMA_DP_EMPTY, TR_MMA_P_FULL, TR_MMA_ACC_EMPTY, TR_MMA_DS_FULL, TR_MMA_DQ_EMPTY,
   TR_SG_S_FULL, TR_SG_P_EMPTY, TR_SG_DP_FULL, TR_SG_DS_EMPTY, TR_DQ_FULL, TR_DQ_SEM,
   TR_DQ_REDUCE, TR_DQ_ACC_FULL, TR_DQ_STAGE, TR_TOTAL, TR_ISSUE_S, TR_ISSUE_DP, TR_ISSUE_DV,
-  TR_ISSUE_DKDQ, TR_SITES = 24
+  TR_ISSUE_DKDQ, TR_X0, TR_X1, TR_X2, TR_X3, TR_X4, TR_X5, TR_X6, TR_X7, TR_SITES = 32
 };
 
 __device__ __forceinline__ long long global_timer_ns() {

@@ -189,6 +189,10 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Forgets the static scratch's cached device addresses and table images (defined with
+// dash_attn_bwd_static below; the caller holds g_mu).
+void reset_static_state_locked();
+
 // Profiling hook state: a pool of event pairs recorded around the main kernel.
 constexpr int kProfPairs = 1024;
 std::mutex g_prof_mu;
@@ -322,6 +326,7 @@ void dash_attn_shutdown(void) {
   g_dealt.clear();
   g_host_dealt.clear();
   g_deadlock_free.clear();
+  reset_static_state_locked();
 }
 
 size_t dash_attn_bwd_workspace_size(int B, int S, int H, int D) {
@@ -329,9 +334,9 @@ size_t dash_attn_bwd_workspace_size(int B, int S, int H, int D) {
   return ws_layout(B, S, H, D).total;
 }
 
-dash_status_t dash_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-                            int B, int S, int H, int D, float scale, int mask,
-                            cudaStream_t stream) {
+dash_status_t dash_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                               int B, int S, int H, int D, float scale, int mask, int* status,
+                               cudaStream_t stream) {
   if (!q || !k || !v || !o || !lse) return DASH_ERR_INVALID_ARG;
   if (B < 1 || S < 1 || H < 1 || D < 1) return DASH_ERR_INVALID_ARG;
   if (mask != DASH_MASK_FULL && mask != DASH_MASK_CAUSAL) return DASH_ERR_INVALID_ARG;
@@ -339,9 +344,10 @@ dash_status_t dash_attn_fwd(const void* q, const void* k, const void* v, void* o
   if (!shape_ok(B, S, H, D)) return DASH_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return DASH_ERR_INVALID_ARG;
+  if (status && ((uintptr_t)status & 3u)) return DASH_ERR_INVALID_ARG;
   dash::FwdParams p{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v,
                     (__nv_bfloat16*)o, lse, B, S, H, D, scale, mask == DASH_MASK_CAUSAL,
-                    scale * dash::kLog2e};
+                    scale * dash::kLog2e, status, g_timeout_ns, g_ordinal_skew > 0 ? 1 : 0};
   if (!encoder()) {
     g_last_error = "cuTensorMapEncodeTiled is not available from the driver";
     return DASH_ERR_CUDA;
@@ -358,9 +364,16 @@ dash_status_t dash_attn_fwd(const void* q, const void* k, const void* v, void* o
   void* kfn = D == 64 ? (void*)dash::tc::fwd_tc_kernel<64> : (void*)dash::tc::fwd_tc_kernel<128>;
   const size_t smem = D == 64 ? dash::tc::FwdL<64>::ALLOC : dash::tc::FwdL<128>::ALLOC;
   DASH_CUDA(cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  if (status) DASH_CUDA(cudaMemsetAsync(status, 0, sizeof(int), stream));
   void* args[] = {&p, &maps};
   DASH_CUDA(cudaLaunchKernel(kfn, grid, dim3(dash::tc::kFwdThreads), args, smem, stream));
   return DASH_OK;
+}
+
+dash_status_t dash_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int S, int H, int D, float scale, int mask,
+                            cudaStream_t stream) {
+  return dash_attn_fwd_ex(q, k, v, o, lse, B, S, H, D, scale, mask, nullptr, stream);
 }
 
 dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const void* o,
@@ -714,7 +727,8 @@ std::mutex g_static_mu;
 unsigned char* g_static_ptr[kMaxDevices] = {};
 
 // Device address of the scratch array on `dev` (the current device). Looked up once per
-// device with that device current; later calls reuse it.
+// device with that device current; later calls reuse it until dash_attn_shutdown, which
+// forgets it (a device reset reloads the module, so the address must be looked up again).
 dash_status_t static_scratch(int dev, unsigned char** out) {
   if (dev < 0 || dev >= kMaxDevices) {
     g_last_error = "dash_attn_bwd_static: device index out of range";
@@ -732,6 +746,51 @@ dash_status_t static_scratch(int dev, unsigned char** out) {
 }
 
 __global__ void copy_status_kernel(const int* header, int* out) { *out = header[dash::WS_STATUS]; }
+
+// Host image of the schedule tables that follow the workspace in the static scratch, in
+// the scratch's own layout (offsets relative to the workspace's end), so that one copy
+// moves all of them. Entries live until dash_attn_shutdown: a queued copy never reads
+// host memory that has been freed.
+struct StaticTables {
+  std::vector<int32_t> image;
+  size_t task_off, ord_off, cnt_off;   // byte offsets of the task, order, count tables
+  int num_slots;
+};
+std::map<std::tuple<int, int, int, int, int>, std::shared_ptr<const StaticTables>> g_static_tables;
+
+dash_status_t static_tables(int mask, int schedule, int n, int heads, int grid,
+                            std::shared_ptr<const StaticTables>* out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto key = std::make_tuple(mask, schedule, n, heads, grid);
+  auto it = g_static_tables.find(key);
+  if (it == g_static_tables.end()) {
+    dash::Schedule sc;
+    const int rc = dash::build_schedule(mask, schedule, n, &sc);
+    if (rc) return (dash_status_t)rc;
+    std::shared_ptr<const std::vector<int32_t>> dealt;
+    if (dash::arrival_ordered(sc)) dealt = host_dealt_locked(sc, heads, grid);
+    const std::vector<int32_t>& ord = dealt ? *dealt : sc.ord;
+    auto t = std::make_shared<StaticTables>();
+    t->num_slots = sc.num_slots;
+    t->task_off = round_up(sc.slot_off.size() * 4, 256);
+    t->ord_off = round_up(t->task_off + sc.tasks.size() * 4, 256);
+    t->cnt_off = round_up(t->ord_off + ord.size() * 4, 256);
+    t->image.assign(round_up(t->cnt_off + sc.cnt.size() * 4, 256) / 4, 0);
+    std::memcpy(t->image.data(), sc.slot_off.data(), sc.slot_off.size() * 4);
+    std::memcpy(t->image.data() + t->task_off / 4, sc.tasks.data(), sc.tasks.size() * 4);
+    std::memcpy(t->image.data() + t->ord_off / 4, ord.data(), ord.size() * 4);
+    std::memcpy(t->image.data() + t->cnt_off / 4, sc.cnt.data(), sc.cnt.size() * 4);
+    it = g_static_tables.emplace(key, std::move(t)).first;
+  }
+  *out = it->second;
+  return DASH_OK;
+}
+
+void reset_static_state_locked() {
+  g_static_tables.clear();
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  for (auto& ptr : g_static_ptr) ptr = nullptr;
+}
 
 }  // namespace
 
@@ -753,30 +812,27 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
                           (const void*)dv})
     if (!aligned16(ptr)) return DASH_ERR_INVALID_ARG;
   const int n = S / dash::kTile;
-  dash::Schedule sc;
-  int rc = dash::build_schedule(mask, schedule, n, &sc);
-  if (rc) return (dash_status_t)rc;
+  {
+    dash::Schedule probe;
+    const int rc = dash::build_schedule(mask, schedule, n, &probe);
+    if (rc) return (dash_status_t)rc;
+  }
   int dev = 0, sms = 0;
   DASH_CUDA(cudaGetDevice(&dev));
   DASH_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  const int units = B * H * sc.num_slots;
+  const int slots = dash_sched_num_slots(mask, schedule, n);
+  const int units = B * H * slots;
   const int grid = sms < units ? sms : units;
   // the dQ orders of this grid (per head for shift and symmetric shift), as the regular
-  // entry point uses them; the per-head table is built once per shape (host memory)
-  std::shared_ptr<const std::vector<int32_t>> dealt;
-  if (dash::arrival_ordered(sc)) {
-    std::lock_guard<std::mutex> lk(g_mu);
-    dealt = host_dealt_locked(sc, B * H, grid);
-  }
-  const std::vector<int32_t>& ord = dealt ? *dealt : sc.ord;
+  // entry point uses them, with the other tables: built once per shape in host memory
+  std::shared_ptr<const StaticTables> tb;
+  dash_status_t st = static_tables(mask, schedule, n, B * H, grid, &tb);
+  if (st != DASH_OK) return st;
 
   // scratch layout: the backward workspace, then the schedule tables
   const WsLayout wl = ws_layout(B, S, H, D);
   const size_t t_off = wl.total;
-  const size_t t_task = round_up(t_off + sc.slot_off.size() * 4, 256);
-  const size_t t_ord = round_up(t_task + sc.tasks.size() * 4, 256);
-  const size_t t_cnt = round_up(t_ord + ord.size() * 4, 256);
-  const size_t need = round_up(t_cnt + sc.cnt.size() * 4, 256);
+  const size_t need = t_off + tb->image.size() * 4;
   if (need > kStaticScratchBytes) {
     char buf[200];
     snprintf(buf, sizeof(buf),
@@ -787,18 +843,8 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
     return DASH_ERR_WORKSPACE_TOO_SMALL;
   }
   unsigned char* ws = nullptr;
-  dash_status_t st = static_scratch(dev, &ws);
+  st = static_scratch(dev, &ws);
   if (st != DASH_OK) return st;
-
-  // Tables are written for every call: the array keeps whatever the last call left.
-  DASH_CUDA(cudaMemcpyAsync(ws + t_off, sc.slot_off.data(), sc.slot_off.size() * 4,
-                            cudaMemcpyHostToDevice, stream));
-  DASH_CUDA(cudaMemcpyAsync(ws + t_task, sc.tasks.data(), sc.tasks.size() * 4,
-                            cudaMemcpyHostToDevice, stream));
-  DASH_CUDA(cudaMemcpyAsync(ws + t_ord, ord.data(), ord.size() * 4,
-                            cudaMemcpyHostToDevice, stream));
-  DASH_CUDA(cudaMemcpyAsync(ws + t_cnt, sc.cnt.data(), sc.cnt.size() * 4,
-                            cudaMemcpyHostToDevice, stream));
 
   dash::BwdParams p;
   p.q = (const __nv_bfloat16*)q;
@@ -816,17 +862,18 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
   p.dq_acc = (float*)(ws + wl.dq_acc);
   p.sems = (int*)(ws + wl.sems);
   p.slot_off = (const int32_t*)(ws + t_off);
-  p.tasks = (const int32_t*)(ws + t_task);
-  p.ord = (const int32_t*)(ws + t_ord);
-  p.ord_stride = dash::arrival_ordered(sc) ? (long long)n * n : 0;
-  p.cnt = (const int32_t*)(ws + t_cnt);
+  p.tasks = (const int32_t*)(ws + t_off + tb->task_off);
+  p.ord = (const int32_t*)(ws + t_off + tb->ord_off);
+  p.ord_stride = (schedule == DASH_SCHED_SHIFT || schedule == DASH_SCHED_SYMMETRIC_SHIFT)
+                     ? (long long)n * n : 0;
+  p.cnt = (const int32_t*)(ws + t_off + tb->cnt_off);
   p.B = B;
   p.S = S;
   p.H = H;
   p.D = D;
   p.n = n;
-  p.num_slots = sc.num_slots;
-  p.num_units = B * H * sc.num_slots;
+  p.num_slots = tb->num_slots;
+  p.num_units = B * H * tb->num_slots;
   p.scale = scale;
   p.scale_log2 = scale * dash::kLog2e;
   p.causal = mask == DASH_MASK_CAUSAL;
@@ -837,6 +884,8 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
   p.trace = nullptr;
   p.num_sems = B * H * n * dash::kDqChains;
 
+  // Every refusal comes before the first queued operation: a refused call leaves the
+  // stream and the scratch untouched.
   if (!encoder()) {
     g_last_error = "cuTensorMapEncodeTiled is not available from the driver";
     return DASH_ERR_CUDA;
@@ -859,9 +908,18 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
     return DASH_ERR_CUDA;
   }
   DASH_CUDA(cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  int per_sm = 0;
+  DASH_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, threads, smem));
+  if (per_sm < 1) {
+    g_last_error = "backward kernel does not fit on one SM";
+    return DASH_ERR_CUDA;
+  }
   if (deterministic && !deadlock_free(mask, schedule, n, B * H, grid))
     return DASH_ERR_DEADLOCK_RISK;
 
+  // Tables are written for every call: the array keeps whatever the last call left.
+  DASH_CUDA(cudaMemcpyAsync(ws + t_off, tb->image.data(), tb->image.size() * 4,
+                            cudaMemcpyHostToDevice, stream));
   dash::bwd_preprocess_kernel<<<sms * 4, 256, 0, stream>>>(p);
   DASH_CUDA(cudaGetLastError());
   void* args[] = {&p, &maps};

@@ -13,8 +13,8 @@
 //
 // Warp roles (256 threads): 0 = TMA producer (Q once, K and V in two stages), 1 = MMA
 // issuer, 2..3 idle, 4..7 = softmax (thread = one Q row = one TMEM lane). Every wait is
-// bounded; a CTA that gives up writes NaN into its LSE rows so the failure cannot pass
-// unnoticed.
+// bounded; a CTA that gives up writes NaN into its LSE rows and, when the caller passed a
+// status word, records DASH_ERR_SYNC_TIMEOUT there, so the failure cannot pass unnoticed.
 #pragma once
 
 #include "kernels_tc.cuh"
@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   uint32_t* tmem_slot = (uint32_t*)(sm + L::BAR_OFF + 8 * F_COUNT);
   volatile int* abort_flag = (volatile int*)(sm + L::BAR_OFF + 8 * F_COUNT + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long tmo = 2000000000ll;   // 2 s per wait: far beyond any legitimate wait
+  const long long tmo = p.timeout_ns;   // per wait: far beyond any legitimate wait
 
   const int n = p.S / kTile;
   const int qt = n - 1 - (int)blockIdx.x;          // longest causal rows first
@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ptx::tma_load_3d(sm + L::Q_OFF + cb * kTile * 128, &maps.q, cb * 64, h, b * p.S + q0,
                          bars + F_Q_FULL);
       int j = 0;
-      for (; j < nt; ++j) {
+      for (; j < (p.withhold_kv ? 0 : nt); ++j) {
         const int s = j & 1;
         if (j >= 2 && !ptx::mbar_wait(bars + F_KV_EMPTY + s, ((j >> 1) - 1) & 1, abort_flag, tmo))
           break;
@@ -257,6 +257,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);
   }
+  if (threadIdx.x == 0 && *abort_flag && p.status) atomicCAS(p.status, 0, kStatusSyncTimeout);
 }
 
 }  // namespace tc

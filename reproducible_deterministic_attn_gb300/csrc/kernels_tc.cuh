@@ -143,8 +143,56 @@ struct Walk {
 struct Trace {
   unsigned long long* c;   // shared counters, null when tracing is off
   __device__ __forceinline__ long long t0() const { return c ? clock64() : 0; }
+  // a shared-memory reduction, so the tracing thread never waits for the old value
   __device__ __forceinline__ void add(int site, long long start) const {
-    if (c) c[site] += (unsigned long long)(clock64() - start);
+    if (c) atomicAdd(c + site, (unsigned long long)(clock64() - start));
+  }
+};
+
+// Gap-free variant of the trace for one thread: every cycle between two marks is charged
+// to the site of the later mark, so the sites add up to the thread's whole loop time. The
+// counters live in registers (site indices are compile-time constants) and are added to the
+// shared counters once, by flush().
+template <int N>
+struct SegTrace {
+  unsigned long long* c;   // shared counters, null when tracing is off
+  uint32_t acc[N];
+  long long last;
+  __device__ __forceinline__ SegTrace(unsigned long long* counters) : c(counters), last(0) {
+#pragma unroll
+    for (int k = 0; k < N; ++k) acc[k] = 0;
+    if (c) last = clock64();
+  }
+  // charge the cycles since the previous mark to slot k
+  __device__ __forceinline__ void mark(int k) {
+    if (c) {
+      const long long now = clock64();
+      acc[k] += (uint32_t)(now - last);
+      last = now;
+    }
+  }
+  __device__ __forceinline__ void flush(const int (&sites)[N]) const {
+    if (c) {
+#pragma unroll
+      for (int k = 0; k < N; ++k) atomicAdd(c + sites[k], (unsigned long long)acc[k]);
+    }
+  }
+};
+
+// Gap-free trace kept in the shared counters directly (no registers beyond the last
+// timestamp): mark(site) adds the cycles since the previous mark to the site.
+struct SegTraceShared {
+  unsigned long long* c;   // shared counters, null when tracing is off
+  long long last;
+  __device__ __forceinline__ SegTraceShared(unsigned long long* counters) : c(counters), last(0) {
+    if (c) last = clock64();
+  }
+  __device__ __forceinline__ void mark(int site) {
+    if (c) {
+      const long long now = clock64();
+      atomicAdd(c + site, (unsigned long long)(now - last));
+      last = now;
+    }
   }
 };
 

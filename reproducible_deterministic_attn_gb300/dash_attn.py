@@ -39,6 +39,8 @@ _dblp = ctypes.POINTER(ctypes.c_double)
 _SIGNATURES = {
     "dash_attn_fwd": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_float,
                                _c_int, _vp]),
+    "dash_attn_fwd_ex": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                                  _c_float, _c_int, _vp, _vp]),
     "dash_attn_bwd_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
     "dash_attn_bwd": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_size,
                                _c_int, _c_int, _c_int, _c_int, _c_float, _c_int, _c_int, _c_int,
@@ -119,6 +121,17 @@ def dash_attn_fwd(q, k, v, o, lse, scale: float, mask: int, stream=None) -> None
                                 _stream(q, stream)), "dash_attn_fwd")
 
 
+def dash_attn_fwd_ex(q, k, v, o, lse, scale: float, mask: int, status=None, stream=None) -> None:
+    """dash_attn_fwd with a device status word (an int32 CUDA tensor of one element, or
+    None): cleared by the call, set to DASH_ERR_SYNC_TIMEOUT by the kernel if a wait ran
+    out."""
+    B, S, H, D = _shape(q)
+    _check(load().dash_attn_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr(), B, S, H, D, float(scale), int(mask),
+                                   status.data_ptr() if status is not None else None,
+                                   _stream(q, stream)), "dash_attn_fwd_ex")
+
+
 def dash_attn_bwd_workspace_size(B: int, S: int, H: int, D: int) -> int:
     return int(load().dash_attn_bwd_workspace_size(B, S, H, D))
 
@@ -170,14 +183,14 @@ def dash_debug_set_sync(timeout_ns: int, ordinal_skew: int) -> None:
 
 
 # dash_debug_set_trace sites with a fixed meaning (include/dash_attn.h)
-TRACE_SITES = 24
+TRACE_SITES = 32
 TRACE_DQ_TURN_WAIT = 15     # waiting for a dQ block's turn (ordered mode)
 TRACE_DQ_ADD = 16           # adding a dQ partial and handing the turn on
 TRACE_TOTAL = 19            # the CTA's total cycles
 
 
 def dash_debug_set_trace(counters) -> None:
-    """counters: a zeroed uint64 CUDA tensor of 24 * SM-count entries, or None to stop."""
+    """counters: a zeroed uint64 CUDA tensor of 32 * SM-count entries, or None to stop."""
     load().dash_debug_set_trace(None if counters is None else counters.data_ptr())
 
 

@@ -3,6 +3,8 @@
 * every ordered-reduction wait is bounded: with a skew on the awaited ordinals no wait
   can be satisfied, the kernel records DASH_ERR_SYNC_TIMEOUT and returns, and the context
   stays usable for a normal call right after;
+* the forward's waits are bounded the same way, and its status word reports a wait that
+  ran out (the testing hook withholds the K/V tiles);
 * a head spread over many rounds of the persistent grid -- where a fixed per-schedule
   dQ order would wait on itself -- runs to the end, because shift's order is the order
   of arrival on the dealt grid.
@@ -47,6 +49,32 @@ def test_sync_timeout_is_reported_and_context_survives(D, det):
     again = da.attn_backward(q, k, v, o, do, lse, scale, False, "shift", det, workspace=ws)
     for a, b in zip(again, ref):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_forward_timeout_is_reported_and_context_survives(D):
+    """The forward's waits are bounded too: with the K/V tiles withheld (the testing hook)
+    every wait for them runs out, the status word says so and the LSE rows are NaN; the
+    next call, without the hook, computes the normal result."""
+    B, S, H = 1, 512, 2
+    x = make_inputs(B, S, H, D, 5)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    scale = 1 / math.sqrt(D)
+    o_ref, lse_ref = da.attn_forward(q, k, v, scale, True)
+    status = torch.full((1,), -7, dtype=torch.int32, device="cuda")
+    o, lse = torch.empty_like(q), torch.empty_like(lse_ref)
+    try:
+        da.dash_debug_set_sync(50_000_000, 1)          # 50 ms per wait, K/V withheld
+        da.dash_attn_fwd_ex(q, k, v, o, lse, scale, da.MASK_CAUSAL, status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == da.DASH_ERR_SYNC_TIMEOUT
+        assert bool(torch.isnan(lse).all())
+    finally:
+        da.dash_debug_set_sync(0, 0)
+    da.dash_attn_fwd_ex(q, k, v, o, lse, scale, da.MASK_CAUSAL, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == da.DASH_OK
+    assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
 
 
 def test_head_spread_over_many_rounds_of_the_grid_runs():

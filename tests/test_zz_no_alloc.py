@@ -70,13 +70,44 @@ def test_static_matches_regular_on_two_calls_in_a_row(case):
                 assert torch.equal(got, want), (call, name)
 
 
-def test_static_rejects_shapes_beyond_the_scratch():
-    B, S, H, D = 2, 8192, 16, 128      # 134 MB of fp32 dQ accumulator alone
-    q = torch.zeros((1, 128, 1, 128), dtype=torch.bfloat16, device="cuda")
-    lse = torch.zeros((1, 1, 128), dtype=torch.float32, device="cuda")
+def _static_call(lib, t, status, B, S, H, D, mask, sched, det):
+    q, k, v, o, do, lse, dq, dk, dv = t
+    return lib.dash_attn_bwd_static(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                    do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                    dv.data_ptr(), status.data_ptr(), B, S, H, D,
+                                    ctypes.c_float(1.0 / math.sqrt(D)), mask, sched, det,
+                                    torch.cuda.current_stream().cuda_stream)
+
+
+def _buffers(B, S, H, D):
+    """Inputs and sentinel-filled outputs of the full claimed size, so that no refusal
+    test could read or write out of bounds even if the call went ahead."""
+    def bf():
+        return torch.zeros((B, S, H, D), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((B, H, S), dtype=torch.float32, device="cuda")
+    outs = [torch.full((B, S, H, D), 7.0, dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    return [bf(), bf(), bf(), bf(), bf(), lse] + outs
+
+
+@pytest.mark.parametrize("refusal", ["beyond_scratch", "unsupported_pair"])
+def test_static_refusal_queues_nothing(refusal):
+    """A refused call returns its error before anything is queued: the outputs and the
+    status word keep the values they had."""
+    if refusal == "beyond_scratch":
+        B, S, H, D, mask, sched = 2, 8192, 16, 128, da.MASK_FULL, da.SCHEDULES["shift"]
+        want = da.DASH_ERR_WORKSPACE_TOO_SMALL
+    else:
+        B, S, H, D, mask, sched = 1, 256, 2, 64, da.MASK_CAUSAL, da.SCHEDULES["shift"]
+        want = da.DASH_ERR_UNSUPPORTED
+    t = _buffers(B, S, H, D)
+    status = torch.full((1,), 12345, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
     lib = da.load()
-    p = q.data_ptr()
-    st = lib.dash_attn_bwd_static(p, p, p, p, p, lse.data_ptr(), p, p, p, None, B, S, H, D,
-                                  ctypes.c_float(0.1), 0, 0, 1, None)
-    assert st == da.DASH_ERR_WORKSPACE_TOO_SMALL
-    assert "static scratch" in da.dash_last_error()
+    st = _static_call(lib, t, status, B, S, H, D, mask, sched, 1)
+    assert st == want
+    if refusal == "beyond_scratch":
+        assert "static scratch" in da.dash_last_error()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 12345
+    for out in t[6:]:
+        assert bool((out == 7.0).all())
