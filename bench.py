@@ -45,6 +45,8 @@ WORKLOADS = {
     "causal-1x16384x32x128": dict(mask="causal", B=1, S=16384, H=32, D=128),
     # smaller full-mask case for kernel profiles (inputs still larger than L2)
     "full-2x4096x16x128": dict(mask="full", B=2, S=4096, H=16, D=128),
+    # long full-mask sequence: where the pages see Shift fall behind the baseline order
+    "full-1x16384x16x128": dict(mask="full", B=1, S=16384, H=16, D=128),
 }
 # the transformer-block sweep: causal, 16384 tokens (B * S), 32 heads, D = 64 and 128
 for _s in (1024, 2048, 4096, 8192, 16384):
