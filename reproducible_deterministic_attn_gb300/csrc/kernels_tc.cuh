@@ -143,9 +143,8 @@ struct Walk {
 struct Trace {
   unsigned long long* c;   // shared counters, null when tracing is off
   __device__ __forceinline__ long long t0() const { return c ? clock64() : 0; }
-  // a shared-memory reduction, so the tracing thread never waits for the old value
   __device__ __forceinline__ void add(int site, long long start) const {
-    if (c) atomicAdd(c + site, (unsigned long long)(clock64() - start));
+    if (c) c[site] += (unsigned long long)(clock64() - start);
   }
 };
 
