@@ -247,7 +247,7 @@ def workload_config(args, w):
             "deterministic": True,
             "l2": ("inputs larger than L2 (%.0f MB read per step vs 129 MB L2)"
                    % (input_bytes(w) / 2**20)) if input_bytes(w) > L2_BYTES else
-                  "L2 flushed between steps (256 MB write)"}
+                  "L2 flushed before every step (256 MB write, outside the step's own CUDA events)"}
 
 
 # ---------------------------------------------------------------------------------------
@@ -331,6 +331,27 @@ def run_gpu(args, w, rank, world, local_rank):
             flush.fill_(1)
         da.dash_attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, scale, mask, s, det)
 
+    def timed_steps(n_steps, det, s):
+        """Device time of n_steps backward calls in ms. With the L2 flush, each call is
+        bracketed by its own event pair after its flush, so the flush is not timed."""
+        if flush is None:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(n_steps):
+                step(det, s)
+            e1.record()
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n_steps)]
+        for a, b in ev:
+            flush.fill_(1)
+            a.record()
+            da.dash_attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, scale, mask, s, det)
+            b.record()
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev)
+
     def barrier():
         torch.cuda.synchronize()
         if world > 1:
@@ -341,13 +362,8 @@ def run_gpu(args, w, rank, world, local_rank):
         if profile:
             da.dash_profile_enable(True)
             da.dash_profile_read()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(n_steps):
-            step(det, s)
-        e1.record()
+        ms = timed_steps(n_steps, det, s)
         barrier()
-        ms = e0.elapsed_time(e1)
         main = None
         if profile:
             tot, cnt = da.dash_profile_read()
