@@ -7,9 +7,21 @@
 
 namespace dash {
 
+// x as hi + mid + lo, each rounded to bf16 in turn (their sum equals x to ~2^-24 |x|),
+// packed as K columns 0, 1, 2 of a row of the score-offset block; columns 3..7 zero.
+__device__ __forceinline__ uint4 split3_bf16(float x) {
+  const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+  const float r1 = x - __bfloat162float(hi);
+  const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+  return make_uint4((uint32_t)__bfloat16_as_ushort(hi) | ((uint32_t)__bfloat16_as_ushort(mid) << 16),
+                    (uint32_t)__bfloat16_as_ushort(lo), 0u, 0u);
+}
+
 // ---------------------------------------------------------------------------------
-// Preprocess: D = rowsum(dO * O) and -LSE*log2(e) per row; clear the semaphores, the
-// status header and the fp32 dQ accumulator copies in use. A row of D elements is read
+// Preprocess: D = rowsum(dO * O) and -LSE*log2(e) per row (and, for head dimension 128,
+// the score-offset blocks of -LSE/scale and -D); clear the semaphores, the status header
+// and the fp32 dQ accumulator copies in use. A row of D elements is read
 // by D/8 consecutive lanes of one warp, 8 bf16 (16 bytes) of dO and of O each; each lane
 // sums its 8 products in order, then a fixed shuffle tree over the row's lanes
 // (deterministic).
@@ -47,6 +59,18 @@ __global__ void bwd_preprocess_kernel(BwdParams p) {
     if (r < rows && sub == 0) {
       p.Dsum[r] = acc;
       p.nlse2[r] = -p.lse[r] * kLog2e;
+      if (p.qx) {
+        // row rr of 128-row tile t of head bh; 8-row group g, K columns 0..7 at byte
+        // 256 g + 16 (rr % 8), K columns 8..15 128 bytes further (all zero)
+        const int s = r % p.S, bh = r / p.S;
+        const int rr = s % kTile;
+        const size_t off = (((size_t)bh * (p.S / kTile) + s / kTile) * 4096 +
+                            (size_t)(rr >> 3) * 256 + (rr & 7) * 16) / sizeof(uint4);
+        reinterpret_cast<uint4*>(p.qx)[off] = split3_bf16(-p.lse[r] / p.scale);
+        reinterpret_cast<uint4*>(p.qx)[off + 8] = make_uint4(0u, 0u, 0u, 0u);
+        reinterpret_cast<uint4*>(p.dox)[off] = split3_bf16(-acc);
+        reinterpret_cast<uint4*>(p.dox)[off + 8] = make_uint4(0u, 0u, 0u, 0u);
+      }
     }
   }
   for (int e = tid; e < p.num_sems; e += nth) p.sems[e] = 0;

@@ -58,6 +58,11 @@ struct BwdParams {
   int* ws_header;            // status words
   float* Dsum;               // [B, H, S] rowsum(dO * O)
   float* nlse2;              // [B, H, S] -LSE * log2(e) (the exponent offset of P in base 2)
+  // Head dimension 128 only (else null): per (b*H + h, 128-row tile) a 4096-byte block of
+  // 128 rows x 16 bf16 in the tensor core's no-swizzle K-major layout, holding in columns
+  // 0..2 the three-term bf16 split of -LSE/scale (qx) and of -Dsum (dox); zero elsewhere.
+  __nv_bfloat16* qx;
+  __nv_bfloat16* dox;
   float* dq_acc;             // [B, H, S, D] fp32
   int* sems;                 // [B, H, n]: one per 128-row dQ block
   int num_sems;               // B * H * n * kDqChains

@@ -138,18 +138,23 @@ struct MainKernel {
   size_t smem;
   int br;   // Q/dO rows per TMA box and dQ accumulator box height
 };
-MainKernel main_kernel(int D) {
+// `traced`: the head-dim-128 kernel is compiled twice, with and without its wait-cycle
+// trace; the traced build is launched only while a trace buffer is set.
+MainKernel main_kernel(int D, bool traced) {
   if (D == 64)
     return {(void*)dash::tc::bwd_tc_kernel<64>, (size_t)dash::tc::Smem<64>::ALLOC,
             dash::tc::Cfg<64>::BR};
-  return {(void*)dash::tc::bwd_tc128_kernel, (size_t)dash::tc::L128::ALLOC, dash::kTile};
+  return {traced ? (void*)dash::tc::bwd_tc128_kernel<true> : (void*)dash::tc::bwd_tc128_kernel<false>,
+          (size_t)dash::tc::L128::ALLOC, dash::kTile};
 }
 
 // The D = 128 kernel moves registers between warpgroups (setmaxnreg); its split adds up to
 // exactly the per-thread count it is launched with, so any other count is refused here
 // (a larger request than the pool holds would never be granted).
 bool launch_regs_ok(const MainKernel& mk) {
-  if (mk.fn != (void*)dash::tc::bwd_tc128_kernel) return true;
+  if (mk.fn != (void*)dash::tc::bwd_tc128_kernel<false> &&
+      mk.fn != (void*)dash::tc::bwd_tc128_kernel<true>)
+    return true;
   cudaFuncAttributes fa;
   if (cudaFuncGetAttributes(&fa, mk.fn) != cudaSuccess) return false;
   return fa.numRegs == dash::tc::L128::REGS_LAUNCH;
@@ -267,7 +272,7 @@ bool map_rows_k(CUtensorMap* m, const void* ptr, int rows, int K, int box_rows) 
 }
 
 struct WsLayout {
-  size_t dsum, nlse2, dq_acc, sems, total;
+  size_t dsum, nlse2, qx, dox, dq_acc, sems, total;
 };
 
 WsLayout ws_layout(int B, int S, int H, int D) {
@@ -275,7 +280,10 @@ WsLayout ws_layout(int B, int S, int H, int D) {
   const size_t rows = (size_t)B * H * S;
   w.dsum = dash::kWsHeaderBytes;
   w.nlse2 = round_up(w.dsum + rows * sizeof(float), 256);
-  w.dq_acc = round_up(w.nlse2 + rows * sizeof(float), 256);
+  // score-offset blocks of the head-dim-128 kernel: 16 bf16 per row each
+  w.qx = round_up(w.nlse2 + rows * sizeof(float), 256);
+  w.dox = round_up(w.qx + (D == 128 ? rows * 32 : 0), 256);
+  w.dq_acc = round_up(w.dox + (D == 128 ? rows * 32 : 0), 256);
   w.sems = round_up(w.dq_acc + dash::kDqChains * rows * D * sizeof(float), 256);   // k copies
   w.total = round_up(w.sems + (size_t)B * H * (S / dash::kTile) * dash::kDqChains * sizeof(int),
                      256);
@@ -422,6 +430,8 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
   p.ws_header = (int*)ws;
   p.Dsum = (float*)(ws + wl.dsum);
   p.nlse2 = (float*)(ws + wl.nlse2);
+  p.qx = D == 128 ? (__nv_bfloat16*)(ws + wl.qx) : nullptr;
+  p.dox = D == 128 ? (__nv_bfloat16*)(ws + wl.dox) : nullptr;
   p.dq_acc = (float*)(ws + wl.dq_acc);
   p.sems = (int*)(ws + wl.sems);
   p.slot_off = tb.slot_off;
@@ -453,7 +463,7 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
     return DASH_ERR_CUDA;
   }
   dash::tc::TmaMaps maps;
-  const MainKernel mk = main_kernel(D);
+  const MainKernel mk = main_kernel(D, g_trace != nullptr);
   const int br = mk.br;
   if (!map_bshd(&maps.q, q, B, S, H, D, br) || !map_bshd(&maps.dO, dO, B, S, H, D, br) ||
       !map_bshd(&maps.k, k, B, S, H, D, dash::kTile) ||
@@ -859,6 +869,8 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
   p.ws_header = (int*)ws;
   p.Dsum = (float*)(ws + wl.dsum);
   p.nlse2 = (float*)(ws + wl.nlse2);
+  p.qx = D == 128 ? (__nv_bfloat16*)(ws + wl.qx) : nullptr;
+  p.dox = D == 128 ? (__nv_bfloat16*)(ws + wl.dox) : nullptr;
   p.dq_acc = (float*)(ws + wl.dq_acc);
   p.sems = (int*)(ws + wl.sems);
   p.slot_off = (const int32_t*)(ws + t_off);
@@ -891,7 +903,7 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
     return DASH_ERR_CUDA;
   }
   dash::tc::TmaMaps maps;
-  const MainKernel mk = main_kernel(D);
+  const MainKernel mk = main_kernel(D, false);
   const int br = mk.br;
   if (!map_bshd(&maps.q, q, B, S, H, D, br) || !map_bshd(&maps.dO, dO, B, S, H, D, br) ||
       !map_bshd(&maps.k, k, B, S, H, D, dash::kTile) ||

@@ -1,42 +1,36 @@
-// Backward main kernel for head dimension 128: whole 128 x 128 tasks, software-pipelined.
+// Backward main kernel for head dimension 128: whole 128 x 128 tasks with the KV rows in
+// the TMEM lanes.
 //
 // Same persistent grid, units, schedule walk and ordered dQ reduction as the general
 // kernel (kernels_tc.cuh); what differs is how one task (KV_i, Q_j) maps onto the SM:
 //
-//   S    = Q K^T        M = 128 q, N = 128 kv, K = 128 d     TMEM cols [0, 128)
-//   P    = exp2(S * scale*log2e - LSE*log2e)                 smem bf16 [q][kv]
-//   dP   = dO V^T       M = 128 q, N = 128 kv, K = 128 d     TMEM cols [0, 128) again
-//   dS   = P * (dP - Dsum)                                   smem bf16 [q][kv], P's buffer
-//   dV  += P^T dO       M = 128 kv, N = 128 d, K = 128 q     TMEM cols [256, 384)
-//   dK  += dS^T Q       M = 128 kv, N = 128 d, K = 128 q     TMEM cols [384, 512)
-//   dQ^T = K^T dS^T     M = 128 d, N = 128 q, K = 128 kv     TMEM cols [128, 256)
+//   S''^T  = K Q^T - LSE/scale  M = 128 kv, N = 128 q, K = 128 d + 16   TMEM cols [0, 128)
+//   P^T    = exp2(S''^T * scale*log2e)                 bf16, TMEM, over S''^T's columns
+//   dP''^T = V dO^T - Dsum      M = 128 kv, N = 128 q, K = 128 d + 16   TMEM cols [128, 256)
+//   dS^T   = P^T * dP''^T                              bf16, TMEM over S''^T, and smem [kv][q]
+//   dV    += P^T dO             M = 128 kv, N = 128 d, K = 128 q, A from TMEM  [256, 384)
+//   dK    += dS^T Q             M = 128 kv, N = 128 d, K = 128 q, A from TMEM  [384, 512)
+//   dQ^T   = K^T dS^T           M = 128 d,  N = 128 q, K = 128 kv       TMEM cols [128, 256)
 //
-// S and dP have the query rows in the TMEM lanes, so each softmax-gradient thread owns one
-// query row: its -LSE*log2e and Dsum are two scalars, and forming P and dS needs no
-// shared-memory reads at all. P^T and dS^T are read by the tensor core as MN-major views
-// of the [q][kv] tiles.
+// The per-query offsets -LSE/scale and -Dsum enter the two score products as one extra
+// K step of 16: the A side holds ones in K columns 0..2 (a constant block), the B side the
+// offset split into three bf16 terms hi + mid + lo (exact to ~2^-24 of the offset; the
+// preprocess kernel writes these blocks). The softmax-gradient threads therefore need no
+// per-column data at all: P = exp2(S'' * scale*log2e), dS = P * dP''.
 //
-// Every MMA is 128 x 128 x 16 per instruction; measured on GB300 each such instruction
-// takes ~65 cycles whatever the operand majors, i.e. the tensor core's full rate, so a
-// task's five products need ~2600 cycles of tensor time. The kernel is laid out so that
-// the tensor pipe never waits for the softmax-gradient warps: one thread issues the
-// products in the fixed order
+// P^T and dS^T stay in TMEM as the A operand of dV and dK (the MMA reads A from TMEM, so
+// those products leave the shared-memory data path to the other traffic); dS^T is also
+// stored to shared memory as the B operand of dQ^T. Each softmax-gradient thread owns one
+// kv row and 64 query columns (half h: columns [64h, 64h + 64)); it writes its P^T into
+// packed bf16 columns [64h, 64h + 32) and its dS^T into [64h + 32, 64h + 64), columns of
+// S''^T it has already loaded.
 //
-//   S(t), dK(t-1), dQ^T(t-1), dP(t), dV(t)
-//
-// so that between any product and the softmax-gradient result it needs there is at
-// least one other product already queued:
-//   - dP(t) reuses S's columns; it waits only for the softmax-gradient warps to have
-//     loaded S(t) (dK(t-1) and dQ^T(t-1) run meanwhile);
-//   - dV(t) waits for P(t), which the exponentials produce while dK(t-1), dQ^T(t-1)
-//     and dP(t) run;
-//   - S(t+1) reuses the columns again once dP(t) has been loaded (dV(t) runs meanwhile);
-//   - dK(t) and dQ^T(t) wait for dS(t), formed while dV(t) and S(t+1) run.
-// P and dS share one shared-memory tile: dS(t) is stored once dV(t) has read P(t), and
-// P(t+1) once dQ^T(t) has read dS(t). Q and dO are double-buffered by task
-// parity: Q(t+2) loads once dK(t) has run, dO(t+2) once dV(t) has. At the end of a KV
-// tile the pending dK/dQ^T are issued before the next tile's S^T (they still read the old
-// K), and K, V reload after them.
+// One thread issues, per task t: S(t), dP(t), dV(t), dK(t), dQ^T(t). S(t+1) waits for
+// dK(t) to have completed (it overwrites P^T and dS^T), which the dQ^T(t) products cover;
+// dP(t+1) waits for the read-out to have taken dQ^T(t) out of the columns the two share;
+// dQ^T(t) waits for dS^T(t), stored after dP(t) was loaded. Q is double-buffered by task
+// parity (its last reader dK(t) runs after S(t+1) has been waited for), dO single-buffered
+// (its last reader is dV(t); dP(t+1) is three products later).
 //
 // The dQ^T columns are read into registers by the read-out warpgroup and handed back at
 // once; the partial is then added into the fp32 dQ accumulator with coalesced red.global
@@ -44,11 +38,11 @@
 // 128-byte line). In deterministic mode the adds of a 128-row block wait for the block's
 // turn and the turn is handed on after they have been performed.
 //
-// Shared memory (1024-aligned base, checked): K, V, Q x 2, dO x 2, P^T/dS^T, -LSE*log2e
-// and Dsum per Q buffer, barriers, trace: 231,936 bytes.
+// Shared memory (1024-aligned base, checked): K, V, Q x 2, dO, dS^T, the offset blocks of
+// Q x 2 and dO, the ones block, barriers, trace.
 //
 // Warp roles (512 threads): 0 = TMA producer, 1 = MMA issuer, 2, 3 = idle,
-// 4..11 = softmax-gradient (quarter = TMEM lanes = query rows, half = 64 kv columns),
+// 4..11 = softmax-gradient (quarter = TMEM lanes = kv rows, half = 64 query columns),
 // 12..15 = dQ read-out and reduction, and the dK/dV epilogue.
 #pragma once
 
@@ -60,19 +54,21 @@ namespace tc {
 struct L128 {
   static constexpr int D = 128;
   static constexpr int TILE_BYTES = kTile * D * 2;            // one 128 x 128 bf16 tile
+  static constexpr int EXT_BYTES = kTile * 16 * 2;            // 128 rows x 16 bf16, no swizzle
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = K_OFF + TILE_BYTES;
   static constexpr int Q_OFF = V_OFF + TILE_BYTES;            // two Q buffers
-  static constexpr int DO_OFF = Q_OFF + 2 * TILE_BYTES;       // two dO buffers
-  static constexpr int PDS_OFF = DO_OFF + 2 * TILE_BYTES;     // P, then dS [q][kv]
-  static constexpr int LD_OFF = PDS_OFF + TILE_BYTES;         // per Q buffer: -LSE*log2e, Dsum
-  static constexpr int LD_BYTES = 2 * kTile * 4;
-  static constexpr int BAR_OFF = LD_OFF + 2 * LD_BYTES;
+  static constexpr int DO_OFF = Q_OFF + 2 * TILE_BYTES;       // one dO buffer
+  static constexpr int DS_OFF = DO_OFF + TILE_BYTES;          // dS^T [kv][q]
+  static constexpr int QX_OFF = DS_OFF + TILE_BYTES;          // two Q offset blocks
+  static constexpr int DOX_OFF = QX_OFF + 2 * EXT_BYTES;      // dO offset block
+  static constexpr int ONES_OFF = DOX_OFF + EXT_BYTES;        // ones in K columns 0..2
+  static constexpr int BAR_OFF = ONES_OFF + EXT_BYTES;
   static constexpr int TRACE_OFF = BAR_OFF + 320;
   static constexpr int ALLOC = TRACE_OFF + 8 * TR_SITES;
   static_assert(ALLOC <= 232448, "shared memory budget");
   // TMEM columns
-  static constexpr int T_SP = 0, T_DQ = 128, T_DV = 256, T_DK = 384;
+  static constexpr int T_SP = 0, T_DPQ = 128, T_DV = 256, T_DK = 384;
   // registers per thread after the re-split (launch: 128 x 512 threads)
   static constexpr int REGS_LAUNCH = 128, REGS_SINGLE = 88, REGS_READOUT = 168;
   static_assert(REGS_SINGLE + 2 * REGS_LAUNCH + REGS_READOUT == 4 * REGS_LAUNCH,
@@ -81,9 +77,8 @@ struct L128 {
 
 enum {
   E_KV_FULL = 0, E_KV_EMPTY, E_Q_FULL, E_Q_EMPTY = E_Q_FULL + 2, E_DO_FULL = E_Q_EMPTY + 2,
-  E_DO_EMPTY = E_DO_FULL + 2, E_S_FULL = E_DO_EMPTY + 2, E_S_LOADED, E_P_FULL, E_DP_FULL,
-  E_DP_LOADED, E_P_READ, E_DS_FULL, E_DS_READ, E_DQ_FULL, E_DQ_EMPTY, E_ACC_FULL,
-  E_ACC_EMPTY, E_DRAIN, E_TURN, E_REDS, E_COUNT
+  E_DO_EMPTY, E_S_FULL, E_SP_FREE, E_P_FULL, E_DP_FULL, E_DS_FULL, E_DS_READ, E_DQ_FULL,
+  E_DQ_EMPTY, E_ACC_FULL, E_ACC_EMPTY, E_DRAIN, E_TURN, E_REDS, E_COUNT
 };
 static_assert(8 * E_COUNT + 8 <= 320, "barrier area");
 
@@ -92,50 +87,87 @@ static_assert(8 * E_COUNT + 8 <= 320, "barrier area");
 enum : int {
   K_PROD_Q_EMPTY = TR_PROD_STAGE_EMPTY,   // producer: a Q buffer is free
   K_PROD_KV_EMPTY = TR_PROD_KV_EMPTY,     // producer: K and V are free
-  K_PROD_DO_EMPTY = TR_MMA_DQ_EMPTY,      // producer: a dO buffer is free
+  K_PROD_DO_EMPTY = TR_MMA_DQ_EMPTY,      // producer: the dO buffer is free
   K_X_KV_FULL = TR_MMA_KV_FULL,           // issuer: K and V landed
   K_X_Q_FULL = TR_MMA_STAGE_FULL,         // issuer: Q landed
-  K_X_DP_LOADED = TR_MMA_S_EMPTY,         // issuer: previous dP^T loaded out of TMEM
-  K_X_DO_S_LOADED = TR_MMA_DP_EMPTY,      // issuer: dO landed, S^T loaded out of TMEM
-  K_X_P_FULL = TR_MMA_P_FULL,             // issuer: P^T stored
+  K_X_SP_FREE = TR_MMA_S_EMPTY,           // issuer: dK(t-1) done, S's columns free
+  K_X_DO_FULL = TR_MMA_DP_EMPTY,          // issuer: dO landed
+  K_X_P_FULL = TR_MMA_P_FULL,             // issuer: P^T in TMEM
   K_X_ACC_EMPTY = TR_MMA_ACC_EMPTY,       // issuer: dK/dV accumulators read out
-  K_X_DS_FULL = TR_MMA_DS_FULL,           // issuer: dS^T stored
+  K_X_DS_FULL = TR_MMA_DS_FULL,           // issuer: dS^T in TMEM and shared memory
   K_X_DQ_EMPTY = TR_SG_DS_EMPTY,          // issuer: previous dQ^T read out
-  K_SG_S_FULL = TR_SG_S_FULL,             // softmax-gradient: S^T ready
-  K_SG_P_COMPUTE = TR_DQ_FULL,            // softmax-gradient: exp2 of the scores
-  K_SG_DP_FULL = TR_SG_DP_FULL,           // softmax-gradient: dP^T ready
-  K_SG_BUF = TR_DQ_STAGE,                 // softmax-gradient: the P^T/dS^T tile is free
-  K_SG_DS_COMPUTE = TR_SG_P_EMPTY,        // softmax-gradient: dP^T load and dS^T
-  K_SG_S_LOAD = TR_X1,                    // softmax-gradient: S^T out of TMEM
-  K_SG_P_STORE = TR_X2,                   // softmax-gradient: P^T into shared memory
-  K_SG_DS_STORE = TR_X3,                  // softmax-gradient: dS^T into shared memory
+  K_SG_S_FULL = TR_SG_S_FULL,             // softmax-gradient: S''^T ready
+  K_SG_P_COMPUTE = TR_DQ_FULL,            // softmax-gradient: exp2 and P^T into TMEM
+  K_SG_DP_FULL = TR_SG_DP_FULL,           // softmax-gradient: dP''^T ready
+  K_SG_BUF = TR_DQ_STAGE,                 // softmax-gradient: the dS^T tile is free
+  K_SG_DS_COMPUTE = TR_SG_P_EMPTY,        // softmax-gradient: dP''^T loads, dS^T stores
+  K_SG_S_LOAD = TR_X1,                    // softmax-gradient: S''^T out of TMEM
+  K_SG_P_STORE = TR_X2,                   // softmax-gradient: P^T stores complete
+  K_SG_DS_STORE = TR_X3,                  // softmax-gradient: dS^T stores complete
   K_X_WALK = TR_X0,                       // issuer: stepping the task walk
   K_RO_DQ_LOAD = TR_X4,                   // read-out: dQ^T out of TMEM
   K_RO_EPILOGUE = TR_X5,                  // read-out: dK/dV out of TMEM to global memory
-  K_RO_DQ_FULL = TR_ISSUE_DP,             // read-out: dQ^T ready
+  K_RO_DQ_FULL = TR_X6,                   // read-out: dQ^T ready
   K_RO_SEM = TR_DQ_SEM,                   // read-out: the block's turn (deterministic)
   K_RO_REDUCE = TR_DQ_REDUCE,             // read-out: adds and hand-off
   K_RO_ACC_FULL = TR_DQ_ACC_FULL,         // read-out: dK/dV accumulators final
-  K_ISSUE_SDP = TR_ISSUE_S,               // issuer: issuing S^T and dP^T
+  K_ISSUE_S = TR_ISSUE_S,                 // issuer: issuing S''^T
+  K_ISSUE_DP = TR_ISSUE_DP,               // issuer: issuing dP''^T
   K_ISSUE_DV = TR_ISSUE_DV,               // issuer: issuing dV
-  K_ISSUE_DQDK = TR_ISSUE_DKDQ            // issuer: issuing dK and dQ^T
+  K_ISSUE_DKDQ = TR_ISSUE_DKDQ            // issuer: issuing dK and dQ^T
 };
 
 // K-major step ks of a [128 rows][128] bf16 tile in 64-column blocks, in 16-byte units;
 // an MN-major step is 16 rows of 128 bytes.
-__device__ __forceinline__ uint32_t kstep128(int ks) {
-  return ((ks >> 2) * kTile * 128 + (ks & 3) * 32) >> 4;
-}
+// The issue loops step running descriptors: from step ks to ks + 1 a K-major operand moves
+// 32 bytes, or to the next 64-column block after step 3; an MN-major operand moves 16 rows.
+constexpr uint32_t kKStep = 32 >> 4, kKBlockStep = (kTile * 128 - 3 * 32) >> 4;
 constexpr uint32_t kMnStep = 2048 >> 4;
+template <int KS>
+__device__ __forceinline__ uint32_t next_k(uint32_t d) {
+  return KS == 3 ? ptx::step_add<kKBlockStep>(d) : ptx::step_add<kKStep>(d);
+}
+// P^T (base column 0) and dS^T (base column 32) in TMEM: step ks reads 8 packed columns at
+// 64 * (ks / 4) + 8 * (ks % 4) from the base
+template <int KS>
+__device__ __forceinline__ uint32_t next_ts(uint32_t t) {
+  return KS == 3 ? ptx::step_add<64 - 24>(t) : ptx::step_add<8>(t);
+}
+
+// The 8 K steps of one 128 x 128 x 128 product: A and B both shared-memory descriptors
+// (K-major or MN-major each), or A in TMEM.
+template <bool A_MN, bool B_MN>
+__device__ __forceinline__ void issue_ss(uint32_t d, uint32_t a, uint32_t b, uint32_t id,
+                                         uint32_t acc0) {
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    ptx::mma_lo(d, a, b, id, ks > 0 ? 1u : acc0);
+    if (ks < 7) {
+      a = A_MN ? ptx::step_add<kMnStep>(a) : (ks == 3 ? next_k<3>(a) : next_k<0>(a));
+      b = B_MN ? ptx::step_add<kMnStep>(b) : (ks == 3 ? next_k<3>(b) : next_k<0>(b));
+    }
+  }
+}
+__device__ __forceinline__ void issue_ts(uint32_t d, uint32_t a_tmem, uint32_t b_mn, uint32_t id,
+                                         uint32_t acc0) {
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    ptx::mma_ts(d, a_tmem, b_mn, id, ks > 0 ? 1u : acc0);
+    if (ks < 7) {
+      a_tmem = ks == 3 ? next_ts<3>(a_tmem) : next_ts<0>(a_tmem);
+      b_mn = ptx::step_add<kMnStep>(b_mn);
+    }
+  }
+}
 
 // Slots of the MMA issuer's gap-free trace and the shared trace sites they are added to.
 enum : int {
-  X_WALK = 0, X_KV_FULL, X_Q_FULL, X_DP_LOADED, X_ISSUE_SDP, X_DS_FULL, X_ISSUE_DKDQ,
-  X_DQ_EMPTY, X_DO_S_LOADED, X_P_FULL, X_ACC_EMPTY, X_ISSUE_DV, X_SLOTS
+  X_WALK = 0, X_KV_FULL, X_Q_FULL, X_SP_FREE, X_ISSUE_S, X_DO_FULL, X_DQ_EMPTY, X_ISSUE_DP,
+  X_P_FULL, X_ACC_EMPTY, X_ISSUE_DV, X_DS_FULL, X_ISSUE_DKDQ, X_SLOTS
 };
 __device__ constexpr int kIssuerSites[X_SLOTS] = {
-    K_X_WALK, K_X_KV_FULL, K_X_Q_FULL, K_X_DP_LOADED, K_ISSUE_SDP, K_X_DS_FULL, K_ISSUE_DQDK,
-    K_X_DQ_EMPTY, K_X_DO_S_LOADED, K_X_P_FULL, K_X_ACC_EMPTY, K_ISSUE_DV};
+    K_X_WALK, K_X_KV_FULL, K_X_Q_FULL, K_X_SP_FREE, K_ISSUE_S, K_X_DO_FULL, K_X_DQ_EMPTY,
+    K_ISSUE_DP, K_X_P_FULL, K_X_ACC_EMPTY, K_ISSUE_DV, K_X_DS_FULL, K_ISSUE_DKDQ};
 using IssuerTrace = SegTrace<X_SLOTS>;
 
 // Sites of the softmax-gradient warps' gap-free trace (one thread: warp 4, lane 0).
@@ -145,70 +177,15 @@ enum : int {
   G_DS_STORE = K_SG_DS_STORE
 };
 
-// Issues S(t) = Q(t) K^T into the S/dP columns once Q(t) has landed and the
-// softmax-gradient warps have loaded dP(t-1) out of those columns.
-__device__ __forceinline__ bool issue_s128(uint64_t* bars, volatile int* abort_flag, long long tmo,
-                                           IssuerTrace& tr, uint32_t tmem, uint32_t dQ_k,
-                                           uint32_t dK_k, int t) {
-  constexpr uint32_t ID_S = ptx::idesc_bf16(128, 128, 0, 0);
-  bool good = ptx::mbar_wait(bars + E_Q_FULL + (t & 1), (t >> 1) & 1, abort_flag, tmo);
-  tr.mark(X_Q_FULL);
-  if (good && t > 0) good = ptx::mbar_wait(bars + E_DP_LOADED, (t - 1) & 1, abort_flag, tmo);
-  tr.mark(X_DP_LOADED);
-  if (!good) return false;
-  ptx::tc_fence_after();
-#pragma unroll
-  for (int ks = 0; ks < 128 / 16; ++ks)
-    ptx::mma_lo(tmem + L128::T_SP, dQ_k + kstep128(ks), dK_k + kstep128(ks), ID_S, ks > 0);
-  ptx::mma_commit(bars + E_S_FULL);
-  tr.mark(X_ISSUE_SDP);
-  return true;
+// Writes 8 values of kv row r (16-byte chunk `chunk` of the row's 128 query columns) as
+// bf16 into a [kv][q] tile at sTile (128-byte swizzle).
+__device__ __forceinline__ void store_chunk8(uint32_t sTile, int r, int chunk, const uint32_t* u) {
+  ptx::st_shared_v4(sTile + sw_chunk(r, chunk, kTile), u[0], u[1], u[2], u[3]);
 }
 
-// Issues dK(t) += dS^T Q(t) once dS(t) is stored, then dQ^T(t) = K^T dS^T once the
-// read-out has taken dQ^T(t-1) out of its columns.
-__device__ __forceinline__ bool issue_dk_dq128(uint64_t* bars, volatile int* abort_flag,
-                                               long long tmo, IssuerTrace& tr, uint32_t tmem,
-                                               uint32_t dQ_mn, uint32_t dPDS_mn, uint32_t dK_mn,
-                                               uint32_t dDS_k, int t, bool first) {
-  constexpr uint32_t ID_ACC = ptx::idesc_bf16(128, 128, 1, 1);  // dK
-  constexpr uint32_t ID_DQT = ptx::idesc_bf16(128, 128, 1, 0);  // dQ^T = K^T dS^T
-  bool good = ptx::mbar_wait(bars + E_DS_FULL, t & 1, abort_flag, tmo);
-  tr.mark(X_DS_FULL);
-  if (!good) return false;
-  ptx::tc_fence_after();
-  // dK += dS^T Q: A = dS^T (MN-major over kv), B = Q (MN-major over d)
-#pragma unroll
-  for (int ks = 0; ks < kTile / 16; ++ks)
-    ptx::mma_lo(tmem + L128::T_DK, dPDS_mn + ks * kMnStep, dQ_mn + ks * kMnStep, ID_ACC,
-                (ks > 0 || !first) ? 1u : 0u);
-  ptx::mma_commit(bars + E_Q_EMPTY + (t & 1));       // Q(t)'s last reader
-  tr.mark(X_ISSUE_DKDQ);
-  if (t > 0) good = ptx::mbar_wait(bars + E_DQ_EMPTY, (t - 1) & 1, abort_flag, tmo);
-  tr.mark(X_DQ_EMPTY);
-  if (!good) return false;
-  ptx::tc_fence_after();
-  // dQ^T = K^T dS^T: A = K^T (MN-major over d), B = dS^T (K-major over kv)
-#pragma unroll
-  for (int ks = 0; ks < kTile / 16; ++ks)
-    ptx::mma_lo(tmem + L128::T_DQ, dK_mn + ks * kMnStep, dDS_k + kstep128(ks), ID_DQT, ks > 0);
-  ptx::mma_commit(bars + E_DS_READ);                 // dK(t) and dQ^T(t) have read dS(t)
-  ptx::mma_commit(bars + E_DQ_FULL);
-  tr.mark(X_ISSUE_DKDQ);
-  return true;
-}
-
-// Writes 64 values of query row r (kv columns col0..col0+63) as bf16 into the [q][kv] tile
-// at sPDS (128-byte swizzle), then makes them visible to the tensor core.
-__device__ __forceinline__ void store_row128(uint32_t sPDS, int r, int col0, const float (&v)[64]) {
-#pragma unroll
-  for (int k = 0; k < 8; ++k)
-    ptx::st_shared_v4(sPDS + sw_chunk(r, (col0 >> 3) + k, kTile),
-                      ptx::pack_bf16(v[8 * k], v[8 * k + 1]), ptx::pack_bf16(v[8 * k + 2], v[8 * k + 3]),
-                      ptx::pack_bf16(v[8 * k + 4], v[8 * k + 5]), ptx::pack_bf16(v[8 * k + 6], v[8 * k + 7]));
-  ptx::fence_proxy_async_smem();
-}
-
+// kTrace: compiled with the optional wait-cycle trace (launched only while a trace buffer
+// is set); without it the trace code and its registers are absent.
+template <bool kTrace>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc128_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ TmaMaps maps) {
   using L = L128;
@@ -216,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem128[];
   uint8_t* sm = smem128;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // The layout fills the opt-in maximum, so there is no room to realign the base.
+  // The layout fills most of the opt-in maximum, so there is no room to realign the base.
   if (ptx::smem_u32(sm) & 1023u) {
     if (threadIdx.x == 0) atomicCAS(p.ws_header + WS_STATUS, 0, kStatusSmemLayout);
     return;
@@ -232,15 +209,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(bars + E_Q_FULL + b, 1);
       ptx::mbar_init(bars + E_Q_EMPTY + b, 1);
-      ptx::mbar_init(bars + E_DO_FULL + b, 1);
-      ptx::mbar_init(bars + E_DO_EMPTY + b, 1);
     }
+    ptx::mbar_init(bars + E_DO_FULL, 1);
+    ptx::mbar_init(bars + E_DO_EMPTY, 1);
     ptx::mbar_init(bars + E_S_FULL, 1);
-    ptx::mbar_init(bars + E_S_LOADED, 8);
+    ptx::mbar_init(bars + E_SP_FREE, 1);
     ptx::mbar_init(bars + E_P_FULL, 8);
     ptx::mbar_init(bars + E_DP_FULL, 1);
-    ptx::mbar_init(bars + E_DP_LOADED, 8);
-    ptx::mbar_init(bars + E_P_READ, 1);
     ptx::mbar_init(bars + E_DS_FULL, 8);
     ptx::mbar_init(bars + E_DS_READ, 1);
     ptx::mbar_init(bars + E_DQ_FULL, 1);
@@ -253,6 +228,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
+  // The ones block: row r, K column k < 3 is 1.0, everything else 0 (threads 0..255 write
+  // one 16-byte core-matrix row each: row t / 2, K half t % 2).
+  if (threadIdx.x < 2 * kTile) {
+    const int row = threadIdx.x >> 1, kh = threadIdx.x & 1;
+    const uint32_t one = 0x3F80u;   // bf16 1.0
+    const uint4 v = kh == 0 ? make_uint4(one | (one << 16), one, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
+    *(uint4*)(sm + L::ONES_OFF + (row >> 3) * 256 + kh * 128 + (row & 7) * 16) = v;
+  }
+  ptx::fence_proxy_async_smem();
   unsigned long long* trace_s = (unsigned long long*)(sm + L::TRACE_OFF);
   if (threadIdx.x < TR_SITES) trace_s[threadIdx.x] = 0;
   const long long t_start = clock64();
@@ -270,26 +254,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::regs_dec<L::REGS_SINGLE>();
     if (warp == 0 && lane == 0) {
       // ===================================== TMA producer =====================================
-      const Trace tr{p.trace ? trace_s : nullptr};
+      const Trace tr{(kTrace && p.trace) ? trace_s : nullptr};
+      const uint8_t* qx = (const uint8_t*)p.qx;
+      const uint8_t* dox = (const uint8_t*)p.dox;
       Walk w(p);
       int it = 0, tl = 0;
       bool ok = true;
       while (ok && w.next()) {
         const int b = w.bh / p.H, h = w.bh % p.H;
         const int q0 = w.j * kTile, qb = it & 1;
-        // Q_j with its -LSE*log2e and Dsum rows into Q buffer qb (free once dK of task it-2
-        // has run)
+        const size_t blk = ((size_t)w.bh * p.n + w.j) * L::EXT_BYTES;   // this Q tile's offsets
+        // Q_j and its offset block into Q buffer qb (free once dK of task it-2 has run)
         long long t0 = tr.t0();
         if (it >= 2 && !(ok = ptx::mbar_wait(bars + E_Q_EMPTY + qb, ((it >> 1) - 1) & 1, abort_flag, tmo)))
           break;
         tr.add(K_PROD_Q_EMPTY, t0);
-        uint8_t* qs = sm + L::Q_OFF + qb * L::TILE_BYTES;
-        uint8_t* ld = sm + L::LD_OFF + qb * L::LD_BYTES;
-        ptx::mbar_expect_tx(bars + E_Q_FULL + qb, L::TILE_BYTES + L::LD_BYTES);
+        ptx::mbar_expect_tx(bars + E_Q_FULL + qb, L::TILE_BYTES + L::EXT_BYTES);
         for (int cb = 0; cb < 2; ++cb)
-          ptx::tma_load_3d(qs + cb * kTile * 128, &maps.q, cb * 64, h, b * p.S + q0, bars + E_Q_FULL + qb);
-        ptx::bulk_load(ld, p.nlse2 + (size_t)w.bh * p.S + q0, kTile * 4, bars + E_Q_FULL + qb);
-        ptx::bulk_load(ld + kTile * 4, p.Dsum + (size_t)w.bh * p.S + q0, kTile * 4, bars + E_Q_FULL + qb);
+          ptx::tma_load_3d(sm + L::Q_OFF + qb * L::TILE_BYTES + cb * kTile * 128, &maps.q, cb * 64,
+                           h, b * p.S + q0, bars + E_Q_FULL + qb);
+        ptx::bulk_load(sm + L::QX_OFF + qb * L::EXT_BYTES, qx + blk, L::EXT_BYTES, bars + E_Q_FULL + qb);
         // K and V of a new KV tile, once the previous tile's last MMAs have read them
         if (w.first_of_tile) {
           t0 = tr.t0();
@@ -304,87 +288,85 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ++tl;
         }
-        // dO_j into dO buffer qb (free once dV of task it-2 has run)
+        // dO_j and its offset block (free once dV of task it-1 has run)
         t0 = tr.t0();
-        if (it >= 2 && !(ok = ptx::mbar_wait(bars + E_DO_EMPTY + qb, ((it >> 1) - 1) & 1, abort_flag, tmo)))
+        if (it >= 1 && !(ok = ptx::mbar_wait(bars + E_DO_EMPTY, (it - 1) & 1, abort_flag, tmo)))
           break;
         tr.add(K_PROD_DO_EMPTY, t0);
-        ptx::mbar_expect_tx(bars + E_DO_FULL + qb, L::TILE_BYTES);
+        ptx::mbar_expect_tx(bars + E_DO_FULL, L::TILE_BYTES + L::EXT_BYTES);
         for (int cb = 0; cb < 2; ++cb)
-          ptx::tma_load_3d(sm + L::DO_OFF + qb * L::TILE_BYTES + cb * kTile * 128, &maps.dO, cb * 64,
-                           h, b * p.S + q0, bars + E_DO_FULL + qb);
+          ptx::tma_load_3d(sm + L::DO_OFF + cb * kTile * 128, &maps.dO, cb * 64, h, b * p.S + q0,
+                           bars + E_DO_FULL);
+        ptx::bulk_load(sm + L::DOX_OFF, dox + blk, L::EXT_BYTES, bars + E_DO_FULL);
         ++it;
       }
       // drain: every issued load has landed before the CTA may exit
-      for (int k = (it > 2 ? it - 2 : 0); k < it; ++k) {
+      for (int k = (it > 2 ? it - 2 : 0); k < it; ++k)
         ptx::mbar_drain(bars + E_Q_FULL + (k & 1), (k >> 1) & 1, 100000000ll);
-        ptx::mbar_drain(bars + E_DO_FULL + (k & 1), (k >> 1) & 1, 100000000ll);
-      }
+      if (it > 0) ptx::mbar_drain(bars + E_DO_FULL, (it - 1) & 1, 100000000ll);
       if (tl > 0) ptx::mbar_drain(bars + E_KV_FULL, (tl - 1) & 1, 100000000ll);
     } else if (warp == 1 && lane == 0) {
       // ===================================== MMA issuer =======================================
-      IssuerTrace tr(p.trace ? trace_s : nullptr);
+      IssuerTrace tr((kTrace && p.trace) ? trace_s : nullptr);
       const uint32_t sK = ptx::smem_u32(sm + L::K_OFF), sV = ptx::smem_u32(sm + L::V_OFF);
       const uint32_t sQ = ptx::smem_u32(sm + L::Q_OFF), sdO = ptx::smem_u32(sm + L::DO_OFF);
-      const uint32_t sPDS = ptx::smem_u32(sm + L::PDS_OFF);
+      const uint32_t sDS = ptx::smem_u32(sm + L::DS_OFF);
       const uint32_t dK_k = ptx::sdesc_lo(sK, 16), dV_k = ptx::sdesc_lo(sV, 16);
       const uint32_t dK_mn = ptx::sdesc_lo(sK, kTile * 128);
-      // P / dS [q][kv]: P^T and dS^T as MN-major A operands of dV and dK; dS^T as the
-      // K-major B operand of dQ^T
-      const uint32_t dPDS_mn = ptx::sdesc_lo(sPDS, kTile * 128), dDS_k = ptx::sdesc_lo(sPDS, 16);
       const uint32_t dQ_k0 = ptx::sdesc_lo(sQ, 16), dQ_mn0 = ptx::sdesc_lo(sQ, kTile * 128);
-      const uint32_t ddO_k0 = ptx::sdesc_lo(sdO, 16), ddO_mn0 = ptx::sdesc_lo(sdO, kTile * 128);
-      constexpr uint32_t ID_S = ptx::idesc_bf16(128, 128, 0, 0);    // dP
-      constexpr uint32_t ID_ACC = ptx::idesc_bf16(128, 128, 1, 1);  // dV
-      constexpr uint32_t BUF_STEP = L::TILE_BYTES >> 4;             // next Q / dO buffer
+      const uint32_t ddO_k = ptx::sdesc_lo(sdO, 16), ddO_mn = ptx::sdesc_lo(sdO, kTile * 128);
+      // dS^T [kv][q] as the MN-major B operand of dQ^T (K = kv rows, N = q contiguous)
+      const uint32_t dDS_mn = ptx::sdesc_lo(sDS, kTile * 128);
+      // the offset step: ones (A) against the Q / dO offset blocks (B), no swizzle
+      // (no swizzle: 8-row x 16-byte core matrices, K halves 128 bytes apart, 8-row groups
+      // 256 bytes apart)
+      const uint32_t dOnes = ptx::sdesc_lo(ptx::smem_u32(sm + L::ONES_OFF), 128);
+      const uint32_t dQx0 = ptx::sdesc_lo(ptx::smem_u32(sm + L::QX_OFF), 128);
+      const uint32_t dDOx = ptx::sdesc_lo(ptx::smem_u32(sm + L::DOX_OFF), 128);
+      constexpr uint32_t ID_S = ptx::idesc_bf16(128, 128, 0, 0);    // S''^T, dP''^T
+      constexpr uint32_t ID_TS = ptx::idesc_bf16(128, 128, 0, 1);   // dV, dK (A in TMEM)
+      constexpr uint32_t ID_DQT = ptx::idesc_bf16(128, 128, 1, 1);  // dQ^T = K^T dS^T
+      constexpr uint32_t BUF_STEP = L::TILE_BYTES >> 4;             // next Q buffer
+      constexpr uint32_t XBUF_STEP = L::EXT_BYTES >> 4;             // next Q offset block
       Walk w(p);
       int it = 0, tile = -1;
-      bool ok = true, pend = false, pend_first = false;   // task it-1's dK/dQ^T not yet issued
-      bool have = w.next();
+      bool ok = true;
       tr.mark(X_WALK);
-      while (ok) {
-        // At the end of a KV tile the pending dK/dQ^T still read the old K: they go before
-        // the next tile's S. Within a tile S(it) goes first.
-        const bool boundary = !have || w.first_of_tile;
-        if (have && !boundary)
-          if (!(ok = issue_s128(bars, abort_flag, tmo, tr, tmem, dQ_k0 + (it & 1) * BUF_STEP, dK_k, it)))
-            break;
-        if (pend) {
-          if (!(ok = issue_dk_dq128(bars, abort_flag, tmo, tr, tmem,
-                                    dQ_mn0 + ((it - 1) & 1) * BUF_STEP, dPDS_mn, dK_mn, dDS_k,
-                                    it - 1, pend_first)))
-            break;
-          if (boundary) {
-            ptx::mma_commit(bars + E_ACC_FULL);
-            ptx::mma_commit(bars + E_KV_EMPTY);
-          }
-          pend = false;
-        }
-        if (!have) break;
-        if (boundary) {
+      while (ok && w.next()) {
+        tr.mark(X_WALK);
+        const int qb = it & 1;
+        if (w.first_of_tile) {
           ++tile;
           ok = ptx::mbar_wait(bars + E_KV_FULL, tile & 1, abort_flag, tmo);
           tr.mark(X_KV_FULL);
           if (!ok) break;
-          if (!(ok = issue_s128(bars, abort_flag, tmo, tr, tmem, dQ_k0 + (it & 1) * BUF_STEP, dK_k, it)))
-            break;
         }
-        // ---- dP(it) = dO V^T into the S/dP columns, once S(it) has been loaded
-        ok = ptx::mbar_wait(bars + E_DO_FULL + (it & 1), (it >> 1) & 1, abort_flag, tmo);
-        if (ok) ok = ptx::mbar_wait(bars + E_S_LOADED, it & 1, abort_flag, tmo);
-        tr.mark(X_DO_S_LOADED);
+        // ---- S''^T(it) = [K | ones] [Q | Qx]^T, once Q(it) has landed and dK(it-1) has
+        // released the P^T / dS^T columns
+        ok = ptx::mbar_wait(bars + E_Q_FULL + qb, (it >> 1) & 1, abort_flag, tmo);
+        tr.mark(X_Q_FULL);
+        if (ok && it > 0) ok = ptx::mbar_wait(bars + E_SP_FREE, (it - 1) & 1, abort_flag, tmo);
+        tr.mark(X_SP_FREE);
         if (!ok) break;
         ptx::tc_fence_after();
-        {
-          const uint32_t ddO_k = ddO_k0 + (it & 1) * BUF_STEP;
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks)
-            ptx::mma_lo(tmem + L::T_SP, ddO_k + kstep128(ks), dV_k + kstep128(ks), ID_S, ks > 0);
-        }
+        issue_ss<false, false>(tmem + L::T_SP, dK_k, dQ_k0 + qb * BUF_STEP, ID_S, 0u);
+        ptx::mma_lo_noswz(tmem + L::T_SP, dOnes, dQx0 + qb * XBUF_STEP, ID_S, 1u);
+        ptx::mma_commit(bars + E_S_FULL);
+        tr.mark(X_ISSUE_S);
+        // ---- dP''^T(it) = [V | ones] [dO | dOx]^T, once dO(it) has landed and the read-out
+        // has taken dQ^T(it-1) out of the columns the two share
+        ok = ptx::mbar_wait(bars + E_DO_FULL, it & 1, abort_flag, tmo);
+        tr.mark(X_DO_FULL);
+        if (ok && it > 0) ok = ptx::mbar_wait(bars + E_DQ_EMPTY, (it - 1) & 1, abort_flag, tmo);
+        tr.mark(X_DQ_EMPTY);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_ss<false, false>(tmem + L::T_DPQ, dV_k, ddO_k, ID_S, 0u);
+        ptx::mma_lo_noswz(tmem + L::T_DPQ, dOnes, dDOx, ID_S, 1u);
         ptx::mma_commit(bars + E_DP_FULL);
-        tr.mark(X_ISSUE_SDP);
-        // ---- dV(it) += P^T dO, once P(it) is stored (and, for a new tile, the previous
-        // tile's accumulators have been read out)
+        tr.mark(X_ISSUE_DP);
+        // ---- dV += P^T dO (A = P^T from TMEM), once P^T(it) is stored and, for a new tile,
+        // the previous tile's accumulators have been read out
         ok = ptx::mbar_wait(bars + E_P_FULL, it & 1, abort_flag, tmo);
         tr.mark(X_P_FULL);
         if (ok && w.first_of_tile && tile > 0)
@@ -392,22 +374,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         tr.mark(X_ACC_EMPTY);
         if (!ok) break;
         ptx::tc_fence_after();
-        {
-          const uint32_t ddO_mn = ddO_mn0 + (it & 1) * BUF_STEP;
-          const uint32_t acc0 = w.first_of_tile ? 0u : 1u;
-#pragma unroll
-          for (int ks = 0; ks < kTile / 16; ++ks)
-            ptx::mma_lo(tmem + L::T_DV, dPDS_mn + ks * kMnStep, ddO_mn + ks * kMnStep, ID_ACC,
-                        ks > 0 ? 1u : acc0);
-        }
-        ptx::mma_commit(bars + E_DO_EMPTY + (it & 1));   // dO(it)'s last reader
-        ptx::mma_commit(bars + E_P_READ);
+        const uint32_t acc0 = w.first_of_tile ? 0u : 1u;
+        issue_ts(tmem + L::T_DV, tmem + L::T_SP, ddO_mn, ID_TS, acc0);
+        ptx::mma_commit(bars + E_DO_EMPTY);              // dO(it)'s last reader
         tr.mark(X_ISSUE_DV);
-        pend = true;
-        pend_first = w.first_of_tile;
+        // ---- dK += dS^T Q (A = dS^T from TMEM), then dQ^T = K^T dS^T, once dS^T(it) is
+        // stored (which also means dP''^T(it) has left the columns dQ^T overwrites)
+        ok = ptx::mbar_wait(bars + E_DS_FULL, it & 1, abort_flag, tmo);
+        tr.mark(X_DS_FULL);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_ts(tmem + L::T_DK, tmem + L::T_SP + 32, dQ_mn0 + qb * BUF_STEP, ID_TS, acc0);
+        ptx::mma_commit(bars + E_Q_EMPTY + qb);          // Q(it)'s last reader
+        ptx::mma_commit(bars + E_SP_FREE);               // P^T and dS^T have been read
+        issue_ss<true, true>(tmem + L::T_DPQ, dK_mn, dDS_mn, ID_DQT, 0u);
+        ptx::mma_commit(bars + E_DS_READ);               // the dS^T tile may be rewritten
+        ptx::mma_commit(bars + E_DQ_FULL);
+        if (w.last_of_tile) {
+          ptx::mma_commit(bars + E_ACC_FULL);
+          ptx::mma_commit(bars + E_KV_EMPTY);
+        }
+        tr.mark(X_ISSUE_DKDQ);
         ++it;
-        have = w.next();
-        tr.mark(X_WALK);
       }
       tr.flush(kIssuerSites);
       // drain: no MMA may be in flight when TMEM is released
@@ -417,70 +405,73 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < 12) {
     // =============================== softmax-gradient warps =================================
     const int quarter = warp & 3, half = (warp - 4) >> 2;
-    const int r = quarter * 32 + lane;         // query row within the tile
-    const int col0 = half * 64;                // this thread's 64 kv columns
+    const int r = quarter * 32 + lane;         // kv row within the tile (TMEM lane)
+    const int col0 = half * 64;                // this thread's 64 query columns
     const uint32_t lane_addr = ((uint32_t)(quarter * 32) << 16);
-    const uint32_t sPDS = ptx::smem_u32(sm + L::PDS_OFF);
-    SegTraceShared trs((p.trace && warp == 4 && lane == 0) ? trace_s : nullptr);
+    const uint32_t sDS = ptx::smem_u32(sm + L::DS_OFF);
+    SegTraceShared trs((kTrace && p.trace && warp == 4 && lane == 0) ? trace_s : nullptr);
     Walk w(p);
     int it = 0;
     bool ok = true;
     while (ok && w.next()) {
-      const int qb = it & 1;
-      const float* ld_s = (const float*)(sm + L::LD_OFF + qb * L::LD_BYTES);
-      ok = ptx::warp_wait(bars + E_Q_FULL + qb, (it >> 1) & 1, abort_flag, tmo);
-      // this row's -LSE*log2e and Dsum
-      const float nlse = ld_s[r], dsum = ld_s[kTile + r];
-      if (ok) ok = ptx::warp_wait(bars + E_S_FULL, it & 1, abort_flag, tmo);
+      ok = ptx::warp_wait(bars + E_S_FULL, it & 1, abort_flag, tmo);
       trs.mark(G_S_FULL);
       if (!ok) break;
       ptx::tc_fence_after();
       float pv[64];
       ptx::tmem_ld64(tmem + lane_addr + L::T_SP + col0, pv);
-      // S is in registers: dP(it) may overwrite its columns
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bars + E_S_LOADED);
       trs.mark(G_S_LOAD);
+      // P^T = exp2(S'' * scale*log2e), 16 columns at a time into packed bf16 TMEM columns
+      // [col0, col0 + 32). Diagonal tile: query c is visible to key r iff c >= r.
+      const bool diag = p.causal && w.i == w.j;
+      const int lim = r - col0;                // first visible column of this thread
 #pragma unroll
-      for (int c = 0; c < 64; ++c) pv[c] = ptx::ex2(fmaf(pv[c], p.scale_log2, nlse));
-      if (p.causal && w.i == w.j) {
-        // diagonal tile: keys after the query are masked out
-        const int lim = r - col0;              // the last visible column of this thread
+      for (int g = 0; g < 4; ++g) {
+        uint32_t u[8];
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (c > lim) pv[c] = 0.f;
+        for (int c = 16 * g; c < 16 * g + 16; ++c) pv[c] = ptx::ex2(pv[c] * p.scale_log2);
+        if (diag) {
+#pragma unroll
+          for (int c = 16 * g; c < 16 * g + 16; ++c)
+            if (c < lim) pv[c] = 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) u[k] = ptx::pack_bf16(pv[16 * g + 2 * k], pv[16 * g + 2 * k + 1]);
+        ptx::tmem_st8(tmem + lane_addr + L::T_SP + col0 + 8 * g, u);
       }
       trs.mark(G_EXP);
-      // P(it) replaces dS(it-1) in the shared tile: dK(it-1) and dQ^T(it-1) must have read it
-      if (it > 0) ok = ptx::warp_wait(bars + E_DS_READ, (it - 1) & 1, abort_flag, tmo);
-      trs.mark(G_BUF);
-      if (!ok) break;
-      store_row128(sPDS, r, col0, pv);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bars + E_P_FULL);
       trs.mark(G_P_STORE);
       ok = ptx::warp_wait(bars + E_DP_FULL, it & 1, abort_flag, tmo);
       trs.mark(G_DP_FULL);
-      if (!ok) break;
-      ptx::tc_fence_after();
-#pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        float dp[32];
-        ptx::tmem_ld32(tmem + lane_addr + L::T_SP + col0 + c0, dp);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) pv[c0 + c] *= dp[c] - dsum;
-      }
-      // dP is in registers: S(it+1) may overwrite its columns
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bars + E_DP_LOADED);
-      trs.mark(G_DS);
-      // dS(it) replaces P(it): dV(it) must have read it
-      ok = ptx::warp_wait(bars + E_P_READ, it & 1, abort_flag, tmo);
+      // dS^T(it) replaces dS^T(it-1) in shared memory, which dQ^T(it-1) has read (issued
+      // before dP(it), so this wait returns at once)
+      if (ok && it > 0) ok = ptx::warp_wait(bars + E_DS_READ, (it - 1) & 1, abort_flag, tmo);
       trs.mark(G_BUF);
       if (!ok) break;
-      store_row128(sPDS, r, col0, pv);
+      ptx::tc_fence_after();
+      // dS^T = P^T * dP'', 16 columns per TMEM load (P^T is held in fp32 registers, so the
+      // loads stay small enough not to spill); each 16 columns go to packed TMEM columns
+      // [col0 + 32, col0 + 64) and to the shared [kv][q] tile
+#pragma unroll
+      for (int c0 = 0; c0 < 64; c0 += 16) {
+        float dp[16];
+        ptx::tmem_ld16(tmem + lane_addr + L::T_DPQ + col0 + c0, dp);
+        uint32_t u[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          u[k] = ptx::pack_bf16(pv[c0 + 2 * k] * dp[2 * k], pv[c0 + 2 * k + 1] * dp[2 * k + 1]);
+        ptx::tmem_st8(tmem + lane_addr + L::T_SP + col0 + 32 + c0 / 2, u);
+        store_chunk8(sDS, r, (col0 + c0) / 8, u);
+        store_chunk8(sDS, r, (col0 + c0) / 8 + 1, u + 4);
+      }
+      trs.mark(G_DS);
+      ptx::tmem_wait_st();
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bars + E_DS_FULL);
       trs.mark(G_DS_STORE);
@@ -492,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;       // d column of dQ^T; kv row of dK/dV
     const uint32_t lane_addr = ((uint32_t)(quarter * 32) << 16);
-    const Trace trq{(p.trace && warp == 12 && lane == 0) ? trace_s : nullptr};
+    const Trace trq{(kTrace && p.trace && warp == 12 && lane == 0) ? trace_s : nullptr};
     Walk w(p);
     int it = 0, tl = 0;
     bool ok = true;
@@ -508,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c0 = 0; c0 < 128; c0 += 32) {
         float t[32];
-        ptx::tmem_ld32(tmem + lane_addr + L::T_DQ + c0, t);
+        ptx::tmem_ld32(tmem + lane_addr + L::T_DPQ + c0, t);
 #pragma unroll
         for (int c = 0; c < 32; ++c) v[c0 + c] = t[c];
       }
@@ -618,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __threadfence();
     }
   }
-  if (p.trace) {
+  if (kTrace && p.trace) {
     if (threadIdx.x == 0) trace_s[TR_TOTAL] = (unsigned long long)(clock64() - t_start);
     __syncthreads();
     if (threadIdx.x < TR_SITES) p.trace[(size_t)blockIdx.x * TR_SITES + threadIdx.x] = trace_s[threadIdx.x];

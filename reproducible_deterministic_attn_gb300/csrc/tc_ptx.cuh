@@ -218,6 +218,27 @@ __device__ __forceinline__ void mma_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t 
       : "memory");
 }
 
+// The same for two no-swizzle K-major operands whose 8-row groups are 256 bytes apart:
+// the descriptors' high words are the constant kDescHiNoSwz.
+constexpr uint32_t kDescHiNoSwz = (256u >> 4) | (1u << 14);
+__device__ __forceinline__ void mma_lo_noswz(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; .reg .b64 da, db; setp.ne.b32 p, %4, 0; mov.b64 da, {%1, %5}; "
+      "mov.b64 db, {%2, %5}; tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p; }" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kDescHiNoSwz)
+      : "memory");
+}
+
+// x + c computed in place (an opaque add), so that a fully unrolled issue loop steps one
+// running descriptor instead of keeping every step's descriptor live in a register.
+template <uint32_t C>
+__device__ __forceinline__ uint32_t step_add(uint32_t x) {
+  uint32_t y;
+  asm volatile("add.u32 %0, %1, %2;" : "=r"(y) : "r"(x), "n"(C));
+  return y;
+}
+
 // MMA whose A operand sits in TMEM (128 lanes = M rows; a K step of 16 bf16 elements is
 // 8 columns of packed pairs); B is a shared-memory descriptor given as its low word.
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
@@ -252,6 +273,22 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
+}
+
+// 32 lanes x 16 columns of 32-bit: thread t of the warp gets lane (base + t), columns
+// [col, col + 16).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int k = 0; k < 16; ++k) v[k] = __uint_as_float(r[k]);
 }
 
 // 32 lanes x 64 columns of 32-bit in one load: thread t of the warp gets lane (base + t),
@@ -295,6 +332,18 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Stores 8 columns of 32-bit values for the warp's 32 lanes (thread t -> lane base + t);
+// tmem_wait_st() waits until this thread's TMEM stores have been performed.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+               "r"(r[7])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Register re-split between warpgroups (executed by every thread of a warpgroup).
 template <int N>
 __device__ __forceinline__ void regs_dec() {
@@ -320,10 +369,6 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
-}
-
-__device__ __forceinline__ float2 unpack_bf16(uint32_t v) {
-  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
