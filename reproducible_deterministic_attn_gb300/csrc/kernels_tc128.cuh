@@ -41,7 +41,8 @@
 // Shared memory (1024-aligned base, checked): K, V, Q x 2, dO, dS^T, the offset blocks of
 // Q x 2 and dO, the ones block, barriers, trace.
 //
-// Warp roles (512 threads): 0 = TMA producer, 1 = MMA issuer, 2, 3 = idle,
+// Warp roles (512 threads): 0 = TMA producer, 1 = MMA issuer, 2 = dQ hand-off
+// (deterministic mode), 3 = idle,
 // 4..11 = softmax-gradient (quarter = TMEM lanes = kv rows, half = 64 query columns),
 // 12..15 = dQ read-out and reduction, and the dK/dV epilogue.
 #pragma once
@@ -77,8 +78,8 @@ struct L128 {
 
 enum {
   E_KV_FULL = 0, E_KV_EMPTY, E_Q_FULL, E_Q_EMPTY = E_Q_FULL + 2, E_DO_FULL = E_Q_EMPTY + 2,
-  E_DO_EMPTY, E_S_FULL, E_SP_FREE, E_P_FULL, E_DP_FULL, E_DS_FULL, E_DS_READ, E_DQ_FULL,
-  E_DQ_EMPTY, E_ACC_FULL, E_ACC_EMPTY, E_DRAIN, E_TURN, E_REDS, E_COUNT
+  E_DO_EMPTY, E_S_FULL, E_SP_FREE, E_P_FULL, E_DP_FULL, E_DS_FULL, E_DQ_FULL,
+  E_DQ_EMPTY, E_ACC_FULL, E_ACC_EMPTY, E_DRAIN, E_TURN, E_REDS, E_RELD, E_COUNT
 };
 static_assert(8 * E_COUNT + 8 <= 320, "barrier area");
 
@@ -177,6 +178,12 @@ enum : int {
   G_DS_STORE = K_SG_DS_STORE
 };
 
+// P = exp2(S'' * scale*log2e) for 32 of a thread's 64 columns, in place.
+__device__ __forceinline__ void exp_half(float (&pv)[64], int c0, float scale_log2) {
+#pragma unroll
+  for (int c = 0; c < 32; ++c) pv[c0 + c] = ptx::ex2(pv[c0 + c] * scale_log2);
+}
+
 // Writes 8 values of kv row r (16-byte chunk `chunk` of the row's 128 query columns) as
 // bf16 into a [kv][q] tile at sTile (128-byte swizzle).
 __device__ __forceinline__ void store_chunk8(uint32_t sTile, int r, int chunk, const uint32_t* u) {
@@ -217,14 +224,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(bars + E_P_FULL, 8);
     ptx::mbar_init(bars + E_DP_FULL, 1);
     ptx::mbar_init(bars + E_DS_FULL, 8);
-    ptx::mbar_init(bars + E_DS_READ, 1);
     ptx::mbar_init(bars + E_DQ_FULL, 1);
     ptx::mbar_init(bars + E_DQ_EMPTY, 4);
     ptx::mbar_init(bars + E_ACC_FULL, 1);
     ptx::mbar_init(bars + E_ACC_EMPTY, 4);
     ptx::mbar_init(bars + E_DRAIN, 1);
     ptx::mbar_init(bars + E_TURN, 1);
-    ptx::mbar_init(bars + E_REDS, 3);
+    ptx::mbar_init(bars + E_REDS, 4);
+    ptx::mbar_init(bars + E_RELD, 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -305,6 +312,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_drain(bars + E_Q_FULL + (k & 1), (k >> 1) & 1, 100000000ll);
       if (it > 0) ptx::mbar_drain(bars + E_DO_FULL, (it - 1) & 1, 100000000ll);
       if (tl > 0) ptx::mbar_drain(bars + E_KV_FULL, (tl - 1) & 1, 100000000ll);
+    } else if (warp == 2 && lane == 0 && p.deterministic) {
+      // ================================ dQ hand-off (deterministic) ===========================
+      // Once all four read-out warps have issued task it's adds (E_REDS: their arrivals
+      // release them at CTA scope, this wait acquires them), the releasing store orders
+      // every one of those adds before the block's new ordinal at GPU scope; it waits for
+      // them to be performed, which the read-out no longer does. E_RELD tells warp 12 the
+      // hand-off is done; it grants the next turn only after that, so E_REDS never runs a
+      // phase ahead of this wait.
+      Walk w(p);
+      int it = 0;
+      bool ok = true;
+      while (ok && w.next()) {
+        if (!(ok = ptx::mbar_wait(bars + E_REDS, it & 1, abort_flag, tmo))) break;
+        const int ord = __ldg(p.ord + w.bh * p.ord_stride + w.i * p.n + w.j);
+        const int chain = ord % p.chains, o = ord / p.chains;
+        st_release_gpu(p.sems + (w.bh * p.n + w.j) * kDqChains + chain, o + 1 + p.ordinal_skew);
+        ptx::mbar_arrive(bars + E_RELD);
+        ++it;
+      }
     } else if (warp == 1 && lane == 0) {
       // ===================================== MMA issuer =======================================
       IssuerTrace tr((kTrace && p.trace) ? trace_s : nullptr);
@@ -388,7 +414,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mma_commit(bars + E_Q_EMPTY + qb);          // Q(it)'s last reader
         ptx::mma_commit(bars + E_SP_FREE);               // P^T and dS^T have been read
         issue_ss<true, true>(tmem + L::T_DPQ, dK_mn, dDS_mn, ID_DQT, 0u);
-        ptx::mma_commit(bars + E_DS_READ);               // the dS^T tile may be rewritten
         ptx::mma_commit(bars + E_DQ_FULL);
         if (w.last_of_tile) {
           ptx::mma_commit(bars + E_ACC_FULL);
@@ -418,18 +443,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       trs.mark(G_S_FULL);
       if (!ok) break;
       ptx::tc_fence_after();
+      // S''^T in two 32-column loads: the second is in flight while the first half's
+      // exponentials run
       float pv[64];
-      ptx::tmem_ld64(tmem + lane_addr + L::T_SP + col0, pv);
-      trs.mark(G_S_LOAD);
-      // P^T = exp2(S'' * scale*log2e), 16 columns at a time into packed bf16 TMEM columns
-      // [col0, col0 + 32). Diagonal tile: query c is visible to key r iff c >= r.
+      {
+        uint32_t a[32], b[32];
+        ptx::tmem_ld32_issue(tmem + lane_addr + L::T_SP + col0, a);
+        ptx::tmem_ld32_wait(a);
+        ptx::tmem_ld32_issue(tmem + lane_addr + L::T_SP + col0 + 32, b);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) pv[c] = __uint_as_float(a[c]);
+        trs.mark(G_S_LOAD);
+        exp_half(pv, 0, p.scale_log2);
+        ptx::tmem_ld32_wait(b);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) pv[32 + c] = __uint_as_float(b[c]);
+        exp_half(pv, 32, p.scale_log2);
+      }
+      // P^T, 16 columns at a time into packed bf16 TMEM columns [col0, col0 + 32). Diagonal
+      // tile: query c is visible to key r iff c >= r.
       const bool diag = p.causal && w.i == w.j;
       const int lim = r - col0;                // first visible column of this thread
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         uint32_t u[8];
-#pragma unroll
-        for (int c = 16 * g; c < 16 * g + 16; ++c) pv[c] = ptx::ex2(pv[c] * p.scale_log2);
         if (diag) {
 #pragma unroll
           for (int c = 16 * g; c < 16 * g + 16; ++c)
@@ -445,12 +482,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bars + E_P_FULL);
       trs.mark(G_P_STORE);
+      // dP''^T(it) is complete. Its commit tracks every MMA issued before it, so dQ^T(it-1)
+      // -- the last reader of the shared dS^T tile -- has completed too, and dS^T(it) may
+      // replace it.
       ok = ptx::warp_wait(bars + E_DP_FULL, it & 1, abort_flag, tmo);
       trs.mark(G_DP_FULL);
-      // dS^T(it) replaces dS^T(it-1) in shared memory, which dQ^T(it-1) has read (issued
-      // before dP(it), so this wait returns at once)
-      if (ok && it > 0) ok = ptx::warp_wait(bars + E_DS_READ, (it - 1) & 1, abort_flag, tmo);
-      trs.mark(G_BUF);
       if (!ok) break;
       ptx::tc_fence_after();
       // dS^T = P^T * dP'', 16 columns per TMEM load (P^T is held in fp32 registers, so the
@@ -513,14 +549,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int chain = ord % p.chains, o = ord / p.chains;
       const int sem_idx = (w.bh * p.n + w.j) * kDqChains + chain;
       if (p.deterministic) {
-        // The 128-row block's turn: lane 0 of warp 12 polls the semaphore and signals
-        // E_TURN; the other read-out warps wait on it (bounded, like every wait here).
+        // The 128-row block's turn: lane 0 of warp 12 polls the semaphore, then waits until
+        // the releasing warp has handed on the previous task's block (so that every read-out
+        // warp has passed its wait for the previous turn), and signals E_TURN; the other
+        // read-out warps wait on it (bounded, like every wait here). The poll's round trip
+        // overlaps the previous hand-off's wait for its adds.
         t0 = trq.t0();
         int got = 1;
         if (warp == 12) {
           if (lane == 0) {
             got = wait_turn(p.sems + sem_idx, o + p.ordinal_skew, p.ws_header, p.timeout_ns,
                             w.bh, w.j) ? 1 : 0;
+            if (got && it > 0) got = ptx::mbar_wait(bars + E_RELD, (it - 1) & 1, abort_flag, tmo) ? 1 : 0;
             if (got) ptx::mbar_arrive(bars + E_TURN);
             else *abort_flag = 1;
           }
@@ -537,23 +577,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 128; ++c) ptx::red_add_f32(dst + (size_t)c * D, v[c]);
       if (p.deterministic) {
-        // Hand the turn on once every read-out thread's adds are ordered before it: warps
-        // 13..15 arrive on E_REDS (release), warp 12's lane 0 waits on it (acquire), then
-        // the releasing store.
+        // Every read-out warp arrives on E_REDS once its adds are issued (release); warp 2
+        // hands the turn on (below).
         __syncwarp();
-        int done = 1;
-        if (warp != 12) {
-          if (lane == 0) ptx::mbar_arrive(bars + E_REDS);
-        } else {
-          if (lane == 0) {
-            done = ptx::mbar_wait(bars + E_REDS, it & 1, abort_flag, tmo) ? 1 : 0;
-            if (done)   // release store: orders every add above (this warp's via __syncwarp,
-                        // the others' via E_REDS) before the new ordinal at gpu scope
-              st_release_gpu(p.sems + sem_idx, o + 1 + p.ordinal_skew);
-          }
-          done = __shfl_sync(0xffffffffu, done, 0);
-        }
-        if (!done) break;
+        if (lane == 0) ptx::mbar_arrive(bars + E_REDS);
       }
       trq.add(K_RO_REDUCE, t0);
       // ---- dK/dV epilogue after the tile's last task ----
