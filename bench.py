@@ -271,9 +271,9 @@ def traffic_from_profile(w, sched):
     return float(ent) if ent is not None else None
 
 
-# the sources the main head-dim-128 kernel is compiled from (the file and its includes):
+# the sources the main kernel is compiled from (the file and its includes):
 # the traffic record stays valid while none of them changes
-MAIN_KERNEL_SOURCES = ("common.cuh", "kernels_tc.cuh", "kernels_tc128.cuh", "tc_ptx.cuh")
+MAIN_KERNEL_SOURCES = ("common.cuh", "tc_shared.cuh", "bwd_main.cuh", "tc_ptx.cuh")
 
 
 def kernel_source_hash():

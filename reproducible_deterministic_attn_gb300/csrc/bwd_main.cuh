@@ -1,8 +1,11 @@
-// Backward main kernel for head dimension 128: whole 128 x 128 tasks with the KV rows in
-// the TMEM lanes.
+// Backward main kernel (head dimension 64 or 128): whole 128 x 128 tasks with the KV rows
+// in the TMEM lanes.
 //
-// Same persistent grid, units, schedule walk and ordered dQ reduction as the general
-// kernel (kernels_tc.cuh); what differs is how one task (KV_i, Q_j) maps onto the SM:
+// One persistent CTA per SM. A unit is one schedule chain (slot) of one (batch, head); CTA
+// c runs units c, c + grid, ... Each schedule task (KV_i, Q_j) covers a 128 x 128 tile of
+// the score matrix; KV_i's K and V stay in shared memory for all its tasks and its dK/dV
+// accumulate in TMEM (DASH keeps a KV tile's dK/dV on one SM). One task maps onto the SM
+// as (shown for D = 128):
 //
 //   S''^T  = K Q^T - LSE/scale  M = 128 kv, N = 128 q, K = 128 d + 16   TMEM cols [0, 128)
 //   P^T    = exp2(S''^T * scale*log2e)                 bf16, TMEM, over S''^T's columns
@@ -11,6 +14,10 @@
 //   dV    += P^T dO             M = 128 kv, N = 128 d, K = 128 q, A from TMEM  [256, 384)
 //   dK    += dS^T Q             M = 128 kv, N = 128 d, K = 128 q, A from TMEM  [384, 512)
 //   dQ^T   = K^T dS^T           M = 128 d,  N = 128 q, K = 128 kv       TMEM cols [128, 256)
+//
+// At D = 64 the score products take 4 + 1 K steps, dV and dK are 64 wide (TMEM [256, 320)
+// and [320, 384)), and dQ = dS K (M = 128 q, N = 64 d) is formed instead of dQ^T, with the
+// query rows in the TMEM lanes; its read-out adds each row's 64 values 16 bytes at a time.
 //
 // The per-query offsets -LSE/scale and -Dsum enter the two score products as one extra
 // K step of 16: the A side holds ones in K columns 0..2 (a constant block), the B side the
@@ -39,7 +46,7 @@
 // turn and the turn is handed on after they have been performed.
 //
 // Shared memory (1024-aligned base, checked): K, V, Q x 2, dO, dS^T, the offset blocks of
-// Q x 2 and dO, the ones block, barriers, trace.
+// Q x 2 and dO, the ones block, barriers, trace (213.6 KB at D = 128, 131 KB at D = 64).
 //
 // Warp roles (512 threads): 0 = TMA producer, 1 = MMA issuer, 2 = dQ hand-off
 // (deterministic mode), 3 = idle,
@@ -47,34 +54,38 @@
 // 12..15 = dQ read-out and reduction, and the dK/dV epilogue.
 #pragma once
 
-#include "kernels_tc.cuh"
+#include "tc_shared.cuh"
 
 namespace dash {
 namespace tc {
 
-struct L128 {
-  static constexpr int D = 128;
-  static constexpr int TILE_BYTES = kTile * D * 2;            // one 128 x 128 bf16 tile
+template <int D_>
+struct LTc {
+  static constexpr int D = D_;
+  static_assert(D == 64 || D == 128, "head dimension 64 or 128");
+  static constexpr int TILE_BYTES = kTile * D * 2;            // one 128-row bf16 tile of Q/K/V/dO
+  static constexpr int DS_BYTES = kTile * kTile * 2;          // dS^T [kv][q]
   static constexpr int EXT_BYTES = kTile * 16 * 2;            // 128 rows x 16 bf16, no swizzle
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = K_OFF + TILE_BYTES;
   static constexpr int Q_OFF = V_OFF + TILE_BYTES;            // two Q buffers
   static constexpr int DO_OFF = Q_OFF + 2 * TILE_BYTES;       // one dO buffer
   static constexpr int DS_OFF = DO_OFF + TILE_BYTES;          // dS^T [kv][q]
-  static constexpr int QX_OFF = DS_OFF + TILE_BYTES;          // two Q offset blocks
+  static constexpr int QX_OFF = DS_OFF + DS_BYTES;            // two Q offset blocks
   static constexpr int DOX_OFF = QX_OFF + 2 * EXT_BYTES;      // dO offset block
   static constexpr int ONES_OFF = DOX_OFF + EXT_BYTES;        // ones in K columns 0..2
   static constexpr int BAR_OFF = ONES_OFF + EXT_BYTES;
   static constexpr int TRACE_OFF = BAR_OFF + 320;
   static constexpr int ALLOC = TRACE_OFF + 8 * TR_SITES;
   static_assert(ALLOC <= 232448, "shared memory budget");
-  // TMEM columns
-  static constexpr int T_SP = 0, T_DPQ = 128, T_DV = 256, T_DK = 384;
+  // TMEM columns: S''^T (then P^T, dS^T), dP''^T (then dQ), dV, dK
+  static constexpr int T_SP = 0, T_DPQ = 128, T_DV = 256, T_DK = 256 + D;
   // registers per thread after the re-split (launch: 128 x 512 threads)
   static constexpr int REGS_LAUNCH = 128, REGS_SINGLE = 88, REGS_READOUT = 168;
   static_assert(REGS_SINGLE + 2 * REGS_LAUNCH + REGS_READOUT == 4 * REGS_LAUNCH,
                 "the four warpgroups must share exactly the launch's registers");
 };
+using L128 = LTc<128>;
 
 enum {
   E_KV_FULL = 0, E_KV_EMPTY, E_Q_FULL, E_Q_EMPTY = E_Q_FULL + 2, E_DO_FULL = E_Q_EMPTY + 2,
@@ -135,15 +146,15 @@ __device__ __forceinline__ uint32_t next_ts(uint32_t t) {
   return KS == 3 ? ptx::step_add<64 - 24>(t) : ptx::step_add<8>(t);
 }
 
-// The 8 K steps of one 128 x 128 x 128 product: A and B both shared-memory descriptors
-// (K-major or MN-major each), or A in TMEM.
-template <bool A_MN, bool B_MN>
+// The NK K steps (of 16) of one product: A and B both shared-memory descriptors (K-major or
+// MN-major each), or A in TMEM (always 8 steps: K = 128 query rows).
+template <bool A_MN, bool B_MN, int NK = 8>
 __device__ __forceinline__ void issue_ss(uint32_t d, uint32_t a, uint32_t b, uint32_t id,
                                          uint32_t acc0) {
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
+  for (int ks = 0; ks < NK; ++ks) {
     ptx::mma_lo(d, a, b, id, ks > 0 ? 1u : acc0);
-    if (ks < 7) {
+    if (ks < NK - 1) {
       a = A_MN ? ptx::step_add<kMnStep>(a) : (ks == 3 ? next_k<3>(a) : next_k<0>(a));
       b = B_MN ? ptx::step_add<kMnStep>(b) : (ks == 3 ? next_k<3>(b) : next_k<0>(b));
     }
@@ -192,11 +203,10 @@ __device__ __forceinline__ void store_chunk8(uint32_t sTile, int r, int chunk, c
 
 // kTrace: compiled with the optional wait-cycle trace (launched only while a trace buffer
 // is set); without it the trace code and its registers are absent.
-template <bool kTrace>
+template <int D, bool kTrace>
 __global__ void __launch_bounds__(kThreads, 1)
-    bwd_tc128_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ TmaMaps maps) {
-  using L = L128;
-  constexpr int D = 128;
+    bwd_main_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ TmaMaps maps) {
+  using L = LTc<D>;
   extern __shared__ __align__(1024) uint8_t smem128[];
   uint8_t* sm = smem128;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -277,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         tr.add(K_PROD_Q_EMPTY, t0);
         ptx::mbar_expect_tx(bars + E_Q_FULL + qb, L::TILE_BYTES + L::EXT_BYTES);
-        for (int cb = 0; cb < 2; ++cb)
+        for (int cb = 0; cb < D / 64; ++cb)
           ptx::tma_load_3d(sm + L::Q_OFF + qb * L::TILE_BYTES + cb * kTile * 128, &maps.q, cb * 64,
                            h, b * p.S + q0, bars + E_Q_FULL + qb);
         ptx::bulk_load(sm + L::QX_OFF + qb * L::EXT_BYTES, qx + blk, L::EXT_BYTES, bars + E_Q_FULL + qb);
@@ -287,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (tl > 0 && !(ok = ptx::mbar_wait(bars + E_KV_EMPTY, (tl - 1) & 1, abort_flag, tmo))) break;
           tr.add(K_PROD_KV_EMPTY, t0);
           ptx::mbar_expect_tx(bars + E_KV_FULL, 2 * L::TILE_BYTES);
-          for (int cb = 0; cb < 2; ++cb) {
+          for (int cb = 0; cb < D / 64; ++cb) {
             ptx::tma_load_3d(sm + L::K_OFF + cb * kTile * 128, &maps.k, cb * 64, h,
                              b * p.S + w.i * kTile, bars + E_KV_FULL);
             ptx::tma_load_3d(sm + L::V_OFF + cb * kTile * 128, &maps.v, cb * 64, h,
@@ -301,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         tr.add(K_PROD_DO_EMPTY, t0);
         ptx::mbar_expect_tx(bars + E_DO_FULL, L::TILE_BYTES + L::EXT_BYTES);
-        for (int cb = 0; cb < 2; ++cb)
+        for (int cb = 0; cb < D / 64; ++cb)
           ptx::tma_load_3d(sm + L::DO_OFF + cb * kTile * 128, &maps.dO, cb * 64, h, b * p.S + q0,
                            bars + E_DO_FULL);
         ptx::bulk_load(sm + L::DOX_OFF, dox + blk, L::EXT_BYTES, bars + E_DO_FULL);
@@ -350,8 +360,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t dQx0 = ptx::sdesc_lo(ptx::smem_u32(sm + L::QX_OFF), 128);
       const uint32_t dDOx = ptx::sdesc_lo(ptx::smem_u32(sm + L::DOX_OFF), 128);
       constexpr uint32_t ID_S = ptx::idesc_bf16(128, 128, 0, 0);    // S''^T, dP''^T
-      constexpr uint32_t ID_TS = ptx::idesc_bf16(128, 128, 0, 1);   // dV, dK (A in TMEM)
-      constexpr uint32_t ID_DQT = ptx::idesc_bf16(128, 128, 1, 1);  // dQ^T = K^T dS^T
+      constexpr uint32_t ID_TS = ptx::idesc_bf16(128, D, 0, 1);     // dV, dK (A in TMEM)
+      // D = 128: dQ^T = K^T dS^T (M = d); D = 64: dQ = dS K (M = q, N = 64 d)
+      constexpr uint32_t ID_DQ = ptx::idesc_bf16(128, D == 128 ? 128 : 64, 1, 1);
       constexpr uint32_t BUF_STEP = L::TILE_BYTES >> 4;             // next Q buffer
       constexpr uint32_t XBUF_STEP = L::EXT_BYTES >> 4;             // next Q offset block
       Walk w(p);
@@ -375,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tr.mark(X_SP_FREE);
         if (!ok) break;
         ptx::tc_fence_after();
-        issue_ss<false, false>(tmem + L::T_SP, dK_k, dQ_k0 + qb * BUF_STEP, ID_S, 0u);
+        issue_ss<false, false, D / 16>(tmem + L::T_SP, dK_k, dQ_k0 + qb * BUF_STEP, ID_S, 0u);
         ptx::mma_lo_noswz(tmem + L::T_SP, dOnes, dQx0 + qb * XBUF_STEP, ID_S, 1u);
         ptx::mma_commit(bars + E_S_FULL);
         tr.mark(X_ISSUE_S);
@@ -387,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tr.mark(X_DQ_EMPTY);
         if (!ok) break;
         ptx::tc_fence_after();
-        issue_ss<false, false>(tmem + L::T_DPQ, dV_k, ddO_k, ID_S, 0u);
+        issue_ss<false, false, D / 16>(tmem + L::T_DPQ, dV_k, ddO_k, ID_S, 0u);
         ptx::mma_lo_noswz(tmem + L::T_DPQ, dOnes, dDOx, ID_S, 1u);
         ptx::mma_commit(bars + E_DP_FULL);
         tr.mark(X_ISSUE_DP);
@@ -413,7 +424,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_ts(tmem + L::T_DK, tmem + L::T_SP + 32, dQ_mn0 + qb * BUF_STEP, ID_TS, acc0);
         ptx::mma_commit(bars + E_Q_EMPTY + qb);          // Q(it)'s last reader
         ptx::mma_commit(bars + E_SP_FREE);               // P^T and dS^T have been read
-        issue_ss<true, true>(tmem + L::T_DPQ, dK_mn, dDS_mn, ID_DQT, 0u);
+        if (D == 128)
+          issue_ss<true, true>(tmem + L::T_DPQ, dK_mn, dDS_mn, ID_DQ, 0u);
+        else   // A = dS (MN-major over q: the [kv][q] tile), B = K (MN-major over d)
+          issue_ss<true, true>(tmem + L::T_DPQ, dDS_mn, dK_mn, ID_DQ, 0u);
         ptx::mma_commit(bars + E_DQ_FULL);
         if (w.last_of_tile) {
           ptx::mma_commit(bars + E_ACC_FULL);
@@ -517,7 +531,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ============== dQ read-out and reduction into the accumulator + dK/dV epilogue ===========
     ptx::regs_inc<L::REGS_READOUT>();
     const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;       // d column of dQ^T; kv row of dK/dV
+    const int row = quarter * 32 + lane;       // TMEM lane: d (D = 128) or query row (D = 64) of
+                                               // the dQ partial; kv row of dK/dV
     const uint32_t lane_addr = ((uint32_t)(quarter * 32) << 16);
     const Trace trq{(kTrace && p.trace && warp == 12 && lane == 0) ? trace_s : nullptr};
     Walk w(p);
@@ -531,9 +546,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       ptx::tc_fence_after();
       t0 = trq.t0();
-      float v[128];                            // dQ[q0 + c][row], c = 0..127
+      // D = 128: dQ^T, this thread's lane is d and its 128 columns the query rows;
+      // D = 64: dQ, this thread's lane is query row q0 + row and its 64 columns d
+      constexpr int NV = D == 128 ? 128 : 64;
+      float v[NV];
 #pragma unroll
-      for (int c0 = 0; c0 < 128; c0 += 32) {
+      for (int c0 = 0; c0 < NV; c0 += 32) {
         float t[32];
         ptx::tmem_ld32(tmem + lane_addr + L::T_DPQ + c0, t);
 #pragma unroll
@@ -572,10 +590,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!got) break;
       }
       t0 = trq.t0();
-      float* dst = p.dq_acc + (size_t)chain * p.B * p.H * p.S * D +
-                   ((size_t)w.bh * p.S + (size_t)w.j * kTile) * D + row;
+      if (D == 128) {
+        // lane = d: one warp instruction adds 32 consecutive d of one query row (128 bytes)
+        float* dst = p.dq_acc + (size_t)chain * p.B * p.H * p.S * D +
+                     ((size_t)w.bh * p.S + (size_t)w.j * kTile) * D + row;
 #pragma unroll
-      for (int c = 0; c < 128; ++c) ptx::red_add_f32(dst + (size_t)c * D, v[c]);
+        for (int c = 0; c < NV; ++c) ptx::red_add_f32(dst + (size_t)c * D, v[c]);
+      } else {
+        // lane = query row: each thread adds its row's 64 d, 16 bytes at a time
+        float* dst = p.dq_acc + (size_t)chain * p.B * p.H * p.S * D +
+                     ((size_t)w.bh * p.S + (size_t)w.j * kTile + row) * D;
+#pragma unroll
+        for (int c = 0; c < NV; c += 4) ptx::red_add_v4_f32(dst + c, v[c], v[c + 1], v[c + 2], v[c + 3]);
+      }
       if (p.deterministic) {
         // Every read-out warp arrives on E_REDS once its adds are issued (release); warp 2
         // hands the turn on (below).

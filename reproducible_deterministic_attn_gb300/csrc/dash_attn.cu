@@ -16,8 +16,8 @@
 
 #include "common.cuh"
 #include "bwd_aux.cuh"
-#include "kernels_tc.cuh"
-#include "kernels_tc128.cuh"
+#include "tc_shared.cuh"
+#include "bwd_main.cuh"
 #include "fwd_tc.cuh"
 #include "gemm_splitk.cuh"
 #include "sched.h"
@@ -138,23 +138,21 @@ struct MainKernel {
   size_t smem;
   int br;   // Q/dO rows per TMA box and dQ accumulator box height
 };
-// `traced`: the head-dim-128 kernel is compiled twice, with and without its wait-cycle
-// trace; the traced build is launched only while a trace buffer is set.
+// `traced`: the main kernel is compiled twice per head dimension, with and without its
+// wait-cycle trace; the traced build is launched only while a trace buffer is set.
 MainKernel main_kernel(int D, bool traced) {
+  using namespace dash::tc;
   if (D == 64)
-    return {(void*)dash::tc::bwd_tc_kernel<64>, (size_t)dash::tc::Smem<64>::ALLOC,
-            dash::tc::Cfg<64>::BR};
-  return {traced ? (void*)dash::tc::bwd_tc128_kernel<true> : (void*)dash::tc::bwd_tc128_kernel<false>,
-          (size_t)dash::tc::L128::ALLOC, dash::kTile};
+    return {traced ? (void*)bwd_main_kernel<64, true> : (void*)bwd_main_kernel<64, false>,
+            (size_t)LTc<64>::ALLOC, dash::kTile};
+  return {traced ? (void*)bwd_main_kernel<128, true> : (void*)bwd_main_kernel<128, false>,
+          (size_t)LTc<128>::ALLOC, dash::kTile};
 }
 
-// The D = 128 kernel moves registers between warpgroups (setmaxnreg); its split adds up to
+// The main kernel moves registers between warpgroups (setmaxnreg); its split adds up to
 // exactly the per-thread count it is launched with, so any other count is refused here
 // (a larger request than the pool holds would never be granted).
 bool launch_regs_ok(const MainKernel& mk) {
-  if (mk.fn != (void*)dash::tc::bwd_tc128_kernel<false> &&
-      mk.fn != (void*)dash::tc::bwd_tc128_kernel<true>)
-    return true;
   cudaFuncAttributes fa;
   if (cudaFuncGetAttributes(&fa, mk.fn) != cudaSuccess) return false;
   return fa.numRegs == dash::tc::L128::REGS_LAUNCH;
@@ -246,18 +244,6 @@ bool map_bshd(CUtensorMap* m, const void* ptr, int B, int S, int H, int D, int r
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2D view [B*H*S][D] of the fp32 dQ accumulator; box = 32 columns x `rows` rows.
-bool map_acc(CUtensorMap* m, float* ptr, long long rows_total, int D, int rows) {
-  const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows_total};
-  const cuuint64_t strides[1] = {(cuuint64_t)D * 4};
-  const cuuint32_t box[2] = {32, (cuuint32_t)rows};
-  const cuuint32_t es[2] = {1, 1};
-  return encoder()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // 2D view [rows][K] of a row-major bf16 matrix; box = 64 K-columns x 128 rows, 128-byte
 // swizzle.
 bool map_rows_k(CUtensorMap* m, const void* ptr, int rows, int K, int box_rows) {
@@ -280,10 +266,10 @@ WsLayout ws_layout(int B, int S, int H, int D) {
   const size_t rows = (size_t)B * H * S;
   w.dsum = dash::kWsHeaderBytes;
   w.nlse2 = round_up(w.dsum + rows * sizeof(float), 256);
-  // score-offset blocks of the head-dim-128 kernel: 16 bf16 per row each
+  // score-offset blocks of the main kernel: 16 bf16 per row each
   w.qx = round_up(w.nlse2 + rows * sizeof(float), 256);
-  w.dox = round_up(w.qx + (D == 128 ? rows * 32 : 0), 256);
-  w.dq_acc = round_up(w.dox + (D == 128 ? rows * 32 : 0), 256);
+  w.dox = round_up(w.qx + rows * 32, 256);
+  w.dq_acc = round_up(w.dox + rows * 32, 256);
   w.sems = round_up(w.dq_acc + dash::kDqChains * rows * D * sizeof(float), 256);   // k copies
   w.total = round_up(w.sems + (size_t)B * H * (S / dash::kTile) * dash::kDqChains * sizeof(int),
                      256);
@@ -430,8 +416,8 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
   p.ws_header = (int*)ws;
   p.Dsum = (float*)(ws + wl.dsum);
   p.nlse2 = (float*)(ws + wl.nlse2);
-  p.qx = D == 128 ? (__nv_bfloat16*)(ws + wl.qx) : nullptr;
-  p.dox = D == 128 ? (__nv_bfloat16*)(ws + wl.dox) : nullptr;
+  p.qx = (__nv_bfloat16*)(ws + wl.qx);
+  p.dox = (__nv_bfloat16*)(ws + wl.dox);
   p.dq_acc = (float*)(ws + wl.dq_acc);
   p.sems = (int*)(ws + wl.sems);
   p.slot_off = tb.slot_off;
@@ -467,8 +453,7 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
   const int br = mk.br;
   if (!map_bshd(&maps.q, q, B, S, H, D, br) || !map_bshd(&maps.dO, dO, B, S, H, D, br) ||
       !map_bshd(&maps.k, k, B, S, H, D, dash::kTile) ||
-      !map_bshd(&maps.v, v, B, S, H, D, dash::kTile) ||
-      !map_acc(&maps.acc, p.dq_acc, (long long)dash::kDqChains * B * H * S, D, br)) {
+      !map_bshd(&maps.v, v, B, S, H, D, dash::kTile)) {
     g_last_error = "cuTensorMapEncodeTiled rejected a tensor";
     return DASH_ERR_CUDA;
   }
@@ -869,8 +854,8 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
   p.ws_header = (int*)ws;
   p.Dsum = (float*)(ws + wl.dsum);
   p.nlse2 = (float*)(ws + wl.nlse2);
-  p.qx = D == 128 ? (__nv_bfloat16*)(ws + wl.qx) : nullptr;
-  p.dox = D == 128 ? (__nv_bfloat16*)(ws + wl.dox) : nullptr;
+  p.qx = (__nv_bfloat16*)(ws + wl.qx);
+  p.dox = (__nv_bfloat16*)(ws + wl.dox);
   p.dq_acc = (float*)(ws + wl.dq_acc);
   p.sems = (int*)(ws + wl.sems);
   p.slot_off = (const int32_t*)(ws + t_off);
@@ -907,8 +892,7 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
   const int br = mk.br;
   if (!map_bshd(&maps.q, q, B, S, H, D, br) || !map_bshd(&maps.dO, dO, B, S, H, D, br) ||
       !map_bshd(&maps.k, k, B, S, H, D, dash::kTile) ||
-      !map_bshd(&maps.v, v, B, S, H, D, dash::kTile) ||
-      !map_acc(&maps.acc, p.dq_acc, (long long)dash::kDqChains * B * H * S, D, br)) {
+      !map_bshd(&maps.v, v, B, S, H, D, dash::kTile)) {
     g_last_error = "cuTensorMapEncodeTiled rejected a tensor";
     return DASH_ERR_CUDA;
   }

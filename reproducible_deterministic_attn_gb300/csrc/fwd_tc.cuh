@@ -17,7 +17,7 @@
 // status word, records DASH_ERR_SYNC_TIMEOUT there, so the failure cannot pass unnoticed.
 #pragma once
 
-#include "kernels_tc.cuh"
+#include "tc_shared.cuh"
 
 namespace dash {
 namespace tc {

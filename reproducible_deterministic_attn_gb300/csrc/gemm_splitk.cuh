@@ -23,7 +23,7 @@
 // read out.
 #pragma once
 
-#include "kernels_tc.cuh"
+#include "tc_shared.cuh"
 
 namespace dash {
 namespace tc {

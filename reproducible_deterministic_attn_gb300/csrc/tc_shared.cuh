@@ -1,0 +1,123 @@
+// Pieces shared by the tcgen05 kernels (backward main kernel, forward, split-K GEMM):
+// launch shape and TMEM size, the TMA tensor maps, the 128-byte swizzle of a bf16 tile, the
+// persistent grid's task walk and the optional wait-cycle trace helpers.
+#pragma once
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace dash {
+namespace tc {
+
+constexpr int kThreads = 512;
+constexpr int kTmemCols = 512;
+
+struct TmaMaps {
+  CUtensorMap q, k, v, dO;   // 3D bf16 [B*S][H][D], boxes {64, 1, rows}
+};
+
+// byte offset of (row, 8-column chunk) in a bf16 tile of 128-byte rows, 64-column blocks
+// of `rows` rows each, 128-byte swizzle
+__device__ __forceinline__ uint32_t sw_chunk(int row, int chunk, int rows) {
+  return (uint32_t)((chunk >> 3) * rows * 128 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+}
+
+// Iterates this CTA's (unit, task) sequence; every role walks the same sequence. The
+// task table is read two entries ahead so its load latency hides behind the work.
+struct Walk {
+  const BwdParams& p;
+  int u, t, t_end, bh, i, j;
+  int32_t prev_tk, cur_tk, nxt_tk, nxt2_tk;
+  bool first_of_tile, last_of_tile;
+  __device__ Walk(const BwdParams& pp)
+      : p(pp), u((int)blockIdx.x - (int)gridDim.x), t(0), t_end(0) {}
+  __device__ __forceinline__ int32_t task_at(int k) const {
+    return k < t_end ? __ldg(p.tasks + k) : -1;
+  }
+  __device__ bool next() {
+    ++t;
+    if (t >= t_end) {
+      do {
+        u += gridDim.x;
+        if (u >= p.num_units) return false;
+        const int slot = u % p.num_slots;
+        bh = u / p.num_slots;
+        t = __ldg(p.slot_off + slot);
+        t_end = __ldg(p.slot_off + slot + 1);
+      } while (t >= t_end);
+      prev_tk = -1;
+      cur_tk = task_at(t);
+      nxt_tk = task_at(t + 1);
+    } else {
+      prev_tk = cur_tk;
+      cur_tk = nxt_tk;
+      nxt_tk = nxt2_tk;
+    }
+    nxt2_tk = task_at(t + 2);
+    i = cur_tk >> 16;
+    j = cur_tk & 0xffff;
+    first_of_tile = prev_tk < 0 || (prev_tk >> 16) != i;
+    last_of_tile = nxt_tk < 0 || (nxt_tk >> 16) != i;
+    return true;
+  }
+};
+
+// Optional wait-cycle trace: one writer per site, counters in shared memory, copied to
+// p.trace[cta * TR_SITES + site] at exit.
+struct Trace {
+  unsigned long long* c;   // shared counters, null when tracing is off
+  __device__ __forceinline__ long long t0() const { return c ? clock64() : 0; }
+  __device__ __forceinline__ void add(int site, long long start) const {
+    if (c) c[site] += (unsigned long long)(clock64() - start);
+  }
+};
+
+// Gap-free variant of the trace for one thread: every cycle between two marks is charged
+// to the site of the later mark, so the sites add up to the thread's whole loop time. The
+// counters live in registers (site indices are compile-time constants) and are added to the
+// shared counters once, by flush().
+template <int N>
+struct SegTrace {
+  unsigned long long* c;   // shared counters, null when tracing is off
+  uint32_t acc[N];
+  long long last;
+  __device__ __forceinline__ SegTrace(unsigned long long* counters) : c(counters), last(0) {
+#pragma unroll
+    for (int k = 0; k < N; ++k) acc[k] = 0;
+    if (c) last = clock64();
+  }
+  // charge the cycles since the previous mark to slot k
+  __device__ __forceinline__ void mark(int k) {
+    if (c) {
+      const long long now = clock64();
+      acc[k] += (uint32_t)(now - last);
+      last = now;
+    }
+  }
+  __device__ __forceinline__ void flush(const int (&sites)[N]) const {
+    if (c) {
+#pragma unroll
+      for (int k = 0; k < N; ++k) atomicAdd(c + sites[k], (unsigned long long)acc[k]);
+    }
+  }
+};
+
+// Gap-free trace kept in the shared counters directly (no registers beyond the last
+// timestamp): mark(site) adds the cycles since the previous mark to the site.
+struct SegTraceShared {
+  unsigned long long* c;   // shared counters, null when tracing is off
+  long long last;
+  __device__ __forceinline__ SegTraceShared(unsigned long long* counters) : c(counters), last(0) {
+    if (c) last = clock64();
+  }
+  __device__ __forceinline__ void mark(int site) {
+    if (c) {
+      const long long now = clock64();
+      atomicAdd(c + site, (unsigned long long)(now - last));
+      last = now;
+    }
+  }
+};
+
+}  // namespace tc
+}  // namespace dash
