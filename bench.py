@@ -310,12 +310,12 @@ def run_gpu(args, w, rank, world, local_rank):
     sched = da.SCHEDULES[args.schedule]
     # deterministic mode: 1 = one fixed chain per dQ block (the pages' order as one serial
     # chain), 2 = the same order as two interleaved chains. Measured on GB300 the second is
-    # faster at head dim 128 from S = 2048 on (full 2x8192x16x128: 942 vs 811 TF/s; causal
-    # 1x16384x32x128: 933 vs 841; causal 4x4096x32x128: 769 vs 703) and slower at S = 1024
-    # (causal 16x1024x32x128: 432 vs 459), where chains are short and zeroing and summing the
-    # second fp32 copy costs more than the shorter waits save; at head dim 64 one chain.
-    DET = ((2 if D == 128 and S >= 2048 else 1) if args.dq_chains == "auto"
-           else int(args.dq_chains))
+    # faster from S = 2048 on (full 2x8192x16x128: 942 vs 811 TF/s; causal 1x16384x32x128:
+    # 933 vs 841; causal 4x4096x32x128: 769 vs 703; causal 1x16384x32x64: 460 vs 428; causal
+    # 4x2048x16x64: 325 vs 308) and slower at S = 1024 (causal 16x1024x32x128: 432 vs 459),
+    # where chains are short and zeroing and summing the second fp32 copy costs more than
+    # the shorter waits save.
+    DET = ((2 if S >= 2048 else 1) if args.dq_chains == "auto" else int(args.dq_chains))
 
     x = make_inputs(B, S, H, D, seed=rank)
     q, k, v, do = (x[nm].to(dev) for nm in ("q", "k", "v", "do"))

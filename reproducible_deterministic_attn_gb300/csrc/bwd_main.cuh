@@ -15,9 +15,10 @@
 //   dK    += dS^T Q             M = 128 kv, N = 128 d, K = 128 q, A from TMEM  [384, 512)
 //   dQ^T   = K^T dS^T           M = 128 d,  N = 128 q, K = 128 kv       TMEM cols [128, 256)
 //
-// At D = 64 the score products take 4 + 1 K steps, dV and dK are 64 wide (TMEM [256, 320)
-// and [320, 384)), and dQ = dS K (M = 128 q, N = 64 d) is formed instead of dQ^T, with the
-// query rows in the TMEM lanes; its read-out adds each row's 64 values 16 bytes at a time.
+// At D = 64 the score products take 4 + 1 K steps and dV and dK are 64 wide (TMEM [256, 320)
+// and [320, 384)). dQ^T stays an M = 128 product: K^T is padded with a zero block to 128
+// rows, so the partial lands with d in TMEM lanes 0..63 and is added in whole 128-byte
+// lines like at D = 128 (by read-out warps 12 and 13).
 //
 // The per-query offsets -LSE/scale and -Dsum enter the two score products as one extra
 // K step of 16: the A side holds ones in K columns 0..2 (a constant block), the B side the
@@ -74,7 +75,12 @@ struct LTc {
   static constexpr int QX_OFF = DS_OFF + DS_BYTES;            // two Q offset blocks
   static constexpr int DOX_OFF = QX_OFF + 2 * EXT_BYTES;      // dO offset block
   static constexpr int ONES_OFF = DOX_OFF + EXT_BYTES;        // ones in K columns 0..2
-  static constexpr int BAR_OFF = ONES_OFF + EXT_BYTES;
+  // D = 64: a zero block after which K^T is padded to 128 rows, so that dQ^T = K^T dS^T
+  // can be an M = 128 product (its rows 64..127 are zero and unused)
+  static constexpr int ZERO_OFF = ONES_OFF + EXT_BYTES;
+  static constexpr int ZERO_BYTES = D == 64 ? TILE_BYTES : 0;
+  static_assert(ZERO_OFF % 1024 == 0, "swizzled block alignment");
+  static constexpr int BAR_OFF = ZERO_OFF + ZERO_BYTES;
   static constexpr int TRACE_OFF = BAR_OFF + 320;
   static constexpr int ALLOC = TRACE_OFF + 8 * TR_SITES;
   static_assert(ALLOC <= 232448, "shared memory budget");
@@ -253,6 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint4 v = kh == 0 ? make_uint4(one | (one << 16), one, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
     *(uint4*)(sm + L::ONES_OFF + (row >> 3) * 256 + kh * 128 + (row & 7) * 16) = v;
   }
+  for (int e = threadIdx.x; e < L::ZERO_BYTES / 16; e += blockDim.x)
+    *(uint4*)(sm + L::ZERO_OFF + 16 * e) = make_uint4(0u, 0u, 0u, 0u);
   ptx::fence_proxy_async_smem();
   unsigned long long* trace_s = (unsigned long long*)(sm + L::TRACE_OFF);
   if (threadIdx.x < TR_SITES) trace_s[threadIdx.x] = 0;
@@ -349,6 +357,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sDS = ptx::smem_u32(sm + L::DS_OFF);
       const uint32_t dK_k = ptx::sdesc_lo(sK, 16), dV_k = ptx::sdesc_lo(sV, 16);
       const uint32_t dK_mn = ptx::sdesc_lo(sK, kTile * 128);
+      // K^T as the MN-major A operand of dQ^T (M = d): at D = 64 its second 64-row block is
+      // the zero block
+      const uint32_t dKt_mn = D == 128 ? dK_mn : ptx::sdesc_lo(sK, L::ZERO_OFF - L::K_OFF);
       const uint32_t dQ_k0 = ptx::sdesc_lo(sQ, 16), dQ_mn0 = ptx::sdesc_lo(sQ, kTile * 128);
       const uint32_t ddO_k = ptx::sdesc_lo(sdO, 16), ddO_mn = ptx::sdesc_lo(sdO, kTile * 128);
       // dS^T [kv][q] as the MN-major B operand of dQ^T (K = kv rows, N = q contiguous)
@@ -361,8 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t dDOx = ptx::sdesc_lo(ptx::smem_u32(sm + L::DOX_OFF), 128);
       constexpr uint32_t ID_S = ptx::idesc_bf16(128, 128, 0, 0);    // S''^T, dP''^T
       constexpr uint32_t ID_TS = ptx::idesc_bf16(128, D, 0, 1);     // dV, dK (A in TMEM)
-      // D = 128: dQ^T = K^T dS^T (M = d); D = 64: dQ = dS K (M = q, N = 64 d)
-      constexpr uint32_t ID_DQ = ptx::idesc_bf16(128, D == 128 ? 128 : 64, 1, 1);
+      // dQ^T = K^T dS^T: M = 128 (d, padded with zero rows at D = 64), N = 128 q, K = 128 kv
+      constexpr uint32_t ID_DQ = ptx::idesc_bf16(128, 128, 1, 1);
       constexpr uint32_t BUF_STEP = L::TILE_BYTES >> 4;             // next Q buffer
       constexpr uint32_t XBUF_STEP = L::EXT_BYTES >> 4;             // next Q offset block
       Walk w(p);
@@ -424,10 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_ts(tmem + L::T_DK, tmem + L::T_SP + 32, dQ_mn0 + qb * BUF_STEP, ID_TS, acc0);
         ptx::mma_commit(bars + E_Q_EMPTY + qb);          // Q(it)'s last reader
         ptx::mma_commit(bars + E_SP_FREE);               // P^T and dS^T have been read
-        if (D == 128)
-          issue_ss<true, true>(tmem + L::T_DPQ, dK_mn, dDS_mn, ID_DQ, 0u);
-        else   // A = dS (MN-major over q: the [kv][q] tile), B = K (MN-major over d)
-          issue_ss<true, true>(tmem + L::T_DPQ, dDS_mn, dK_mn, ID_DQ, 0u);
+        issue_ss<true, true>(tmem + L::T_DPQ, dKt_mn, dDS_mn, ID_DQ, 0u);
         ptx::mma_commit(bars + E_DQ_FULL);
         if (w.last_of_tile) {
           ptx::mma_commit(bars + E_ACC_FULL);
@@ -531,8 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ============== dQ read-out and reduction into the accumulator + dK/dV epilogue ===========
     ptx::regs_inc<L::REGS_READOUT>();
     const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;       // TMEM lane: d (D = 128) or query row (D = 64) of
-                                               // the dQ partial; kv row of dK/dV
+    const int row = quarter * 32 + lane;       // d column of dQ^T; kv row of dK/dV
     const uint32_t lane_addr = ((uint32_t)(quarter * 32) << 16);
     const Trace trq{(kTrace && p.trace && warp == 12 && lane == 0) ? trace_s : nullptr};
     Walk w(p);
@@ -546,12 +553,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       ptx::tc_fence_after();
       t0 = trq.t0();
-      // D = 128: dQ^T, this thread's lane is d and its 128 columns the query rows;
-      // D = 64: dQ, this thread's lane is query row q0 + row and its 64 columns d
-      constexpr int NV = D == 128 ? 128 : 64;
-      float v[NV];
+      // dQ^T: this thread's lane is d and its 128 columns the query rows. At D = 64 only
+      // warps 12 and 13 hold d rows (lanes 64..127 are the zero padding).
+      const bool holds_d = D == 128 || warp < 14;
+      float v[128];
 #pragma unroll
-      for (int c0 = 0; c0 < NV; c0 += 32) {
+      for (int c0 = 0; c0 < 128; c0 += 32) {
         float t[32];
         ptx::tmem_ld32(tmem + lane_addr + L::T_DPQ + c0, t);
 #pragma unroll
@@ -590,18 +597,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!got) break;
       }
       t0 = trq.t0();
-      if (D == 128) {
+      if (holds_d) {
         // lane = d: one warp instruction adds 32 consecutive d of one query row (128 bytes)
         float* dst = p.dq_acc + (size_t)chain * p.B * p.H * p.S * D +
                      ((size_t)w.bh * p.S + (size_t)w.j * kTile) * D + row;
 #pragma unroll
-        for (int c = 0; c < NV; ++c) ptx::red_add_f32(dst + (size_t)c * D, v[c]);
-      } else {
-        // lane = query row: each thread adds its row's 64 d, 16 bytes at a time
-        float* dst = p.dq_acc + (size_t)chain * p.B * p.H * p.S * D +
-                     ((size_t)w.bh * p.S + (size_t)w.j * kTile + row) * D;
-#pragma unroll
-        for (int c = 0; c < NV; c += 4) ptx::red_add_v4_f32(dst + c, v[c], v[c + 1], v[c + 2], v[c + 3]);
+        for (int c = 0; c < 128; ++c) ptx::red_add_f32(dst + (size_t)c * D, v[c]);
       }
       if (p.deterministic) {
         // Every read-out warp arrives on E_REDS once its adds are issued (release); warp 2
