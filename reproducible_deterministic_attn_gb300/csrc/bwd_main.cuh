@@ -69,11 +69,12 @@ struct LTc {
   static constexpr int EXT_BYTES = kTile * 16 * 2;            // 128 rows x 16 bf16, no swizzle
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = K_OFF + TILE_BYTES;
-  static constexpr int Q_OFF = V_OFF + TILE_BYTES;            // two Q buffers
-  static constexpr int DO_OFF = Q_OFF + 2 * TILE_BYTES;       // one dO buffer
+  static constexpr int NQ = D == 64 ? 3 : 2;                  // Q buffers (task t: t % NQ)
+  static constexpr int Q_OFF = V_OFF + TILE_BYTES;
+  static constexpr int DO_OFF = Q_OFF + NQ * TILE_BYTES;      // one dO buffer
   static constexpr int DS_OFF = DO_OFF + TILE_BYTES;          // dS^T [kv][q]
-  static constexpr int QX_OFF = DS_OFF + DS_BYTES;            // two Q offset blocks
-  static constexpr int DOX_OFF = QX_OFF + 2 * EXT_BYTES;      // dO offset block
+  static constexpr int QX_OFF = DS_OFF + DS_BYTES;            // the Q buffers' offset blocks
+  static constexpr int DOX_OFF = QX_OFF + NQ * EXT_BYTES;     // dO offset block
   static constexpr int ONES_OFF = DOX_OFF + EXT_BYTES;        // ones in K columns 0..2
   // D = 64: a zero block after which K^T is padded to 128 rows, so that dQ^T = K^T dS^T
   // can be an M = 128 product (its rows 64..127 are zero and unused)
@@ -94,7 +95,7 @@ struct LTc {
 using L128 = LTc<128>;
 
 enum {
-  E_KV_FULL = 0, E_KV_EMPTY, E_Q_FULL, E_Q_EMPTY = E_Q_FULL + 2, E_DO_FULL = E_Q_EMPTY + 2,
+  E_KV_FULL = 0, E_KV_EMPTY, E_Q_FULL, E_Q_EMPTY = E_Q_FULL + 3, E_DO_FULL = E_Q_EMPTY + 3,
   E_DO_EMPTY, E_S_FULL, E_SP_FREE, E_P_FULL, E_DP_FULL, E_DS_FULL, E_DQ_FULL,
   E_DQ_EMPTY, E_ACC_FULL, E_ACC_EMPTY, E_DRAIN, E_TURN, E_REDS, E_RELD, E_COUNT
 };
@@ -229,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     ptx::mbar_init(bars + E_KV_FULL, 1);
     ptx::mbar_init(bars + E_KV_EMPTY, 1);
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < L::NQ; ++b) {
       ptx::mbar_init(bars + E_Q_FULL + b, 1);
       ptx::mbar_init(bars + E_Q_EMPTY + b, 1);
     }
@@ -287,11 +288,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       while (ok && w.next()) {
         const int b = w.bh / p.H, h = w.bh % p.H;
-        const int q0 = w.j * kTile, qb = it & 1;
+        const int q0 = w.j * kTile, qb = it % L::NQ;
         const size_t blk = ((size_t)w.bh * p.n + w.j) * L::EXT_BYTES;   // this Q tile's offsets
-        // Q_j and its offset block into Q buffer qb (free once dK of task it-2 has run)
+        // Q_j and its offset block into Q buffer qb (free once dK of task it-NQ has run)
         long long t0 = tr.t0();
-        if (it >= 2 && !(ok = ptx::mbar_wait(bars + E_Q_EMPTY + qb, ((it >> 1) - 1) & 1, abort_flag, tmo)))
+        if (it >= L::NQ &&
+            !(ok = ptx::mbar_wait(bars + E_Q_EMPTY + qb, (it / L::NQ - 1) & 1, abort_flag, tmo)))
           break;
         tr.add(K_PROD_Q_EMPTY, t0);
         ptx::mbar_expect_tx(bars + E_Q_FULL + qb, L::TILE_BYTES + L::EXT_BYTES);
@@ -326,8 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++it;
       }
       // drain: every issued load has landed before the CTA may exit
-      for (int k = (it > 2 ? it - 2 : 0); k < it; ++k)
-        ptx::mbar_drain(bars + E_Q_FULL + (k & 1), (k >> 1) & 1, 100000000ll);
+      for (int k = (it > L::NQ ? it - L::NQ : 0); k < it; ++k)
+        ptx::mbar_drain(bars + E_Q_FULL + k % L::NQ, (k / L::NQ) & 1, 100000000ll);
       if (it > 0) ptx::mbar_drain(bars + E_DO_FULL, (it - 1) & 1, 100000000ll);
       if (tl > 0) ptx::mbar_drain(bars + E_KV_FULL, (tl - 1) & 1, 100000000ll);
     } else if (warp == 2 && lane == 0 && p.deterministic) {
@@ -376,14 +378,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t ID_DQ = ptx::idesc_bf16(128, 128, 1, 1);
       constexpr uint32_t BUF_STEP = L::TILE_BYTES >> 4;             // next Q buffer
       constexpr uint32_t XBUF_STEP = L::EXT_BYTES >> 4;             // next Q offset block
+      // The walk is stepped to the next task right after dV is issued, so that its table
+      // loads overlap the wait for dS; this task's tile flags are kept in locals.
       Walk w(p);
       int it = 0, tile = -1;
       bool ok = true;
+      bool have = w.next();
       tr.mark(X_WALK);
-      while (ok && w.next()) {
-        tr.mark(X_WALK);
-        const int qb = it & 1;
-        if (w.first_of_tile) {
+      while (ok && have) {
+        const bool first = w.first_of_tile, last = w.last_of_tile;
+        const int qb = it % L::NQ;
+        if (first) {
           ++tile;
           ok = ptx::mbar_wait(bars + E_KV_FULL, tile & 1, abort_flag, tmo);
           tr.mark(X_KV_FULL);
@@ -391,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // ---- S''^T(it) = [K | ones] [Q | Qx]^T, once Q(it) has landed and dK(it-1) has
         // released the P^T / dS^T columns
-        ok = ptx::mbar_wait(bars + E_Q_FULL + qb, (it >> 1) & 1, abort_flag, tmo);
+        ok = ptx::mbar_wait(bars + E_Q_FULL + qb, (it / L::NQ) & 1, abort_flag, tmo);
         tr.mark(X_Q_FULL);
         if (ok && it > 0) ok = ptx::mbar_wait(bars + E_SP_FREE, (it - 1) & 1, abort_flag, tmo);
         tr.mark(X_SP_FREE);
@@ -417,15 +422,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the previous tile's accumulators have been read out
         ok = ptx::mbar_wait(bars + E_P_FULL, it & 1, abort_flag, tmo);
         tr.mark(X_P_FULL);
-        if (ok && w.first_of_tile && tile > 0)
+        if (ok && first && tile > 0)
           ok = ptx::mbar_wait(bars + E_ACC_EMPTY, (tile - 1) & 1, abort_flag, tmo);
         tr.mark(X_ACC_EMPTY);
         if (!ok) break;
         ptx::tc_fence_after();
-        const uint32_t acc0 = w.first_of_tile ? 0u : 1u;
+        const uint32_t acc0 = first ? 0u : 1u;
         issue_ts(tmem + L::T_DV, tmem + L::T_SP, ddO_mn, ID_TS, acc0);
         ptx::mma_commit(bars + E_DO_EMPTY);              // dO(it)'s last reader
         tr.mark(X_ISSUE_DV);
+        have = w.next();
+        tr.mark(X_WALK);
         // ---- dK += dS^T Q (A = dS^T from TMEM), then dQ^T = K^T dS^T, once dS^T(it) is
         // stored (which also means dP''^T(it) has left the columns dQ^T overwrites)
         ok = ptx::mbar_wait(bars + E_DS_FULL, it & 1, abort_flag, tmo);
@@ -437,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mma_commit(bars + E_SP_FREE);               // P^T and dS^T have been read
         issue_ss<true, true>(tmem + L::T_DPQ, dKt_mn, dDS_mn, ID_DQ, 0u);
         ptx::mma_commit(bars + E_DQ_FULL);
-        if (w.last_of_tile) {
+        if (last) {
           ptx::mma_commit(bars + E_ACC_FULL);
           ptx::mma_commit(bars + E_KV_EMPTY);
         }
