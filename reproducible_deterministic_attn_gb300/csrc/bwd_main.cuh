@@ -70,6 +70,8 @@ struct LTc {
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = K_OFF + TILE_BYTES;
   static constexpr int NQ = D == 64 ? 3 : 2;                  // Q buffers (task t: t % NQ)
+  // issue S(t+1) between dK(t) and dQ^T(t) (measured faster at D = 64 only)
+  static constexpr bool kEarlyS = D == 64;
   static constexpr int Q_OFF = V_OFF + TILE_BYTES;
   static constexpr int DO_OFF = Q_OFF + NQ * TILE_BYTES;      // one dO buffer
   static constexpr int DS_OFF = DO_OFF + TILE_BYTES;          // dS^T [kv][q]
@@ -177,6 +179,17 @@ __device__ __forceinline__ void issue_ts(uint32_t d, uint32_t a_tmem, uint32_t b
       b_mn = ptx::step_add<kMnStep>(b_mn);
     }
   }
+}
+
+// S''^T = [K | ones] [Q | Qx]^T: the D / 16 K steps of the scores and the offset step, then
+// the commit that signals it.
+template <int D>
+__device__ __forceinline__ void issue_s_mmas(uint32_t tmem, uint32_t dK_k, uint32_t dQ_k,
+                                             uint32_t dOnes, uint32_t dQx, uint64_t* bar) {
+  constexpr uint32_t ID_S = ptx::idesc_bf16(128, 128, 0, 0);
+  issue_ss<false, false, D / 16>(tmem + LTc<D>::T_SP, dK_k, dQ_k, ID_S, 0u);
+  ptx::mma_lo_noswz(tmem + LTc<D>::T_SP, dOnes, dQx, ID_S, 1u);
+  ptx::mma_commit(bar);
 }
 
 // Slots of the MMA issuer's gap-free trace and the shared trace sites they are added to.
@@ -383,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       Walk w(p);
       int it = 0, tile = -1;
       bool ok = true;
-      bool have = w.next();
+      bool have = w.next(), s_done = false;   // s_done: S(it) was issued ahead
       tr.mark(X_WALK);
       while (ok && have) {
         const bool first = w.first_of_tile, last = w.last_of_tile;
@@ -395,17 +408,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
         }
         // ---- S''^T(it) = [K | ones] [Q | Qx]^T, once Q(it) has landed and dK(it-1) has
-        // released the P^T / dS^T columns
-        ok = ptx::mbar_wait(bars + E_Q_FULL + qb, (it / L::NQ) & 1, abort_flag, tmo);
-        tr.mark(X_Q_FULL);
-        if (ok && it > 0) ok = ptx::mbar_wait(bars + E_SP_FREE, (it - 1) & 1, abort_flag, tmo);
-        tr.mark(X_SP_FREE);
-        if (!ok) break;
-        ptx::tc_fence_after();
-        issue_ss<false, false, D / 16>(tmem + L::T_SP, dK_k, dQ_k0 + qb * BUF_STEP, ID_S, 0u);
-        ptx::mma_lo_noswz(tmem + L::T_SP, dOnes, dQx0 + qb * XBUF_STEP, ID_S, 1u);
-        ptx::mma_commit(bars + E_S_FULL);
-        tr.mark(X_ISSUE_S);
+        // released the P^T / dS^T columns (unless it was issued ahead, below)
+        if (!s_done) {
+          ok = ptx::mbar_wait(bars + E_Q_FULL + qb, (it / L::NQ) & 1, abort_flag, tmo);
+          tr.mark(X_Q_FULL);
+          if (ok && it > 0) ok = ptx::mbar_wait(bars + E_SP_FREE, (it - 1) & 1, abort_flag, tmo);
+          tr.mark(X_SP_FREE);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          issue_s_mmas<D>(tmem, dK_k, dQ_k0 + qb * BUF_STEP, dOnes, dQx0 + qb * XBUF_STEP, bars + E_S_FULL);
+          tr.mark(X_ISSUE_S);
+        }
         // ---- dP''^T(it) = [V | ones] [dO | dOx]^T, once dO(it) has landed and the read-out
         // has taken dQ^T(it-1) out of the columns the two share
         ok = ptx::mbar_wait(bars + E_DO_FULL, it & 1, abort_flag, tmo);
@@ -442,6 +455,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_ts(tmem + L::T_DK, tmem + L::T_SP + 32, dQ_mn0 + qb * BUF_STEP, ID_TS, acc0);
         ptx::mma_commit(bars + E_Q_EMPTY + qb);          // Q(it)'s last reader
         ptx::mma_commit(bars + E_SP_FREE);               // P^T and dS^T have been read
+        tr.mark(X_ISSUE_DKDQ);
+        // ---- D = 64: S''^T(it+1) ahead of dQ^T(it) when task it+1 uses the same K, once
+        // dK(it) has completed (S overwrites the dS^T it reads), so the softmax-gradient
+        // warps get it a whole product earlier
+        s_done = L::kEarlyS && have && !w.first_of_tile;
+        if (s_done) {
+          const int qn = (it + 1) % L::NQ;
+          ok = ptx::mbar_wait(bars + E_Q_FULL + qn, ((it + 1) / L::NQ) & 1, abort_flag, tmo);
+          tr.mark(X_Q_FULL);
+          if (ok) ok = ptx::mbar_wait(bars + E_SP_FREE, it & 1, abort_flag, tmo);
+          tr.mark(X_SP_FREE);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          issue_s_mmas<D>(tmem, dK_k, dQ_k0 + qn * BUF_STEP, dOnes, dQx0 + qn * XBUF_STEP, bars + E_S_FULL);
+          tr.mark(X_ISSUE_S);
+        }
         issue_ss<true, true>(tmem + L::T_DPQ, dKt_mn, dDS_mn, ID_DQ, 0u);
         ptx::mma_commit(bars + E_DQ_FULL);
         if (last) {
