@@ -99,8 +99,9 @@ dash_status_t dash_attn_fwd_ex(const void* q, const void* k, const void* v, void
  * Bytes of scratch dash_attn_bwd needs for this shape: a status header, D = rowsum(dO*O)
  * and -LSE*log2(e) (two fp32 [B,H,S] arrays), two score-offset block arrays (-LSE/scale
  * and -D as three bf16 terms each, 32 bytes per row), two copies of the fp32 dQ accumulator
- * [2,B,H,S,D] (deterministic = 2 uses both) and two int32 semaphores per 128-row dQ block,
- * one per chain [B,H,S/128,2]. Returns 0 for an unsupported shape.
+ * [2,B,H,S,D] (deterministic = 2 uses both) and one 128-byte line of int32 semaphores per
+ * 128-row dQ block, one semaphore per chain [B,H,S/128,32]. Returns 0 for an unsupported
+ * shape.
  */
 size_t dash_attn_bwd_workspace_size(int B, int S, int H, int D);
 

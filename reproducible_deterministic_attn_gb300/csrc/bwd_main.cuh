@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = ptx::mbar_wait(bars + E_REDS, it & 1, abort_flag, tmo))) break;
         const int ord = __ldg(p.ord + w.bh * p.ord_stride + w.i * p.n + w.j);
         const int chain = ord % p.chains, o = ord / p.chains;
-        st_release_gpu(p.sems + (w.bh * p.n + w.j) * kDqChains + chain, o + 1 + p.ordinal_skew);
+        st_release_gpu(p.sems + (w.bh * p.n + w.j) * kSemStride + chain, o + 1 + p.ordinal_skew);
         ptx::mbar_arrive(bars + E_RELD);
         ++it;
       }
@@ -608,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // for o - chains, in chain o % chains, adding into accumulator copy o % chains.
       const int ord = __ldg(p.ord + w.bh * p.ord_stride + w.i * p.n + w.j);
       const int chain = ord % p.chains, o = ord / p.chains;
-      const int sem_idx = (w.bh * p.n + w.j) * kDqChains + chain;
+      const int sem_idx = (w.bh * p.n + w.j) * kSemStride + chain;
       if (p.deterministic) {
         // The 128-row block's turn: lane 0 of warp 12 polls the semaphore, then waits until
         // the releasing warp has handed on the previous task's block (so that every read-out

@@ -23,11 +23,15 @@ constexpr int kStatusSyncTimeout = 5;
 // The fixed dQ order of a block runs as k = deterministic interleaved chains (1 <= k <=
 // kDqChains): contribution o adds, in order, into accumulator copy o % k after
 // contribution o - k, so k = 1 is one serial chain; the convert adds the copies in index
-// order. Semaphore of (bh, block j, chain c): sems[(bh * n + j) * kDqChains + c]; copy c
-// of the accumulator starts at dq_acc + c * B*H*S*D. Measured on GB300 (full 2x8192x16x128,
-// shift): k = 1, 2, 3, 4 give 588, 687, 666, 675 TFLOP/s -- beyond two chains the extra
-// copies cost more than the shorter waits save, so two is the maximum.
+// order. Semaphore of (bh, block j, chain c): sems[(bh * n + j) * kSemStride + c] -- each
+// block's semaphores sit in a 128-byte line of their own, so the polls and releasing stores
+// of different blocks do not meet on one L2 line; copy c of the accumulator starts at
+// dq_acc + c * B*H*S*D. Measured on GB300 (full 2x8192x16x128, shift): beyond two chains
+// the extra copies cost more than the shorter waits save (the first kernel: k = 1, 2, 3, 4
+// gave 588, 687, 666, 675 TFLOP/s; the current one 811, 964, 942, 939), so two is the
+// maximum.
 constexpr int kDqChains = 2;
+constexpr int kSemStride = 32;
 constexpr int kStatusSmemLayout = 4;   // reported as DASH_ERR_CUDA: unusable shared-memory base
 
 struct FwdParams {
@@ -64,8 +68,8 @@ struct BwdParams {
   __nv_bfloat16* qx;
   __nv_bfloat16* dox;
   float* dq_acc;             // [B, H, S, D] fp32
-  int* sems;                 // [B, H, n]: one per 128-row dQ block
-  int num_sems;               // B * H * n * kDqChains
+  int* sems;                 // [B, H, n, kSemStride]: per 128-row dQ block, one per chain
+  int num_sems;               // B * H * n * kSemStride
   int chains;                 // interleaved dQ chains, 1..kDqChains (deterministic mode)
   const int32_t* slot_off;   // schedule: chain offsets
   const int32_t* tasks;      // schedule: (kv << 16) | q

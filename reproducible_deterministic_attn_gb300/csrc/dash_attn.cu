@@ -271,7 +271,7 @@ WsLayout ws_layout(int B, int S, int H, int D) {
   w.dox = round_up(w.qx + rows * 32, 256);
   w.dq_acc = round_up(w.dox + rows * 32, 256);
   w.sems = round_up(w.dq_acc + dash::kDqChains * rows * D * sizeof(float), 256);   // k copies
-  w.total = round_up(w.sems + (size_t)B * H * (S / dash::kTile) * dash::kDqChains * sizeof(int),
+  w.total = round_up(w.sems + (size_t)B * H * (S / dash::kTile) * dash::kSemStride * sizeof(int),
                      256);
   return w;
 }
@@ -440,7 +440,7 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
   p.ordinal_skew = g_ordinal_skew;
   p.trace = g_trace;
 
-  p.num_sems = B * H * n * dash::kDqChains;
+  p.num_sems = B * H * n * dash::kSemStride;
 
   // Persistent grid, one CTA per SM: every CTA must be resident at once (the ordered
   // reduction waits on other CTAs), so the launch is cooperative.
@@ -879,7 +879,7 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
   p.timeout_ns = g_timeout_ns;
   p.ordinal_skew = g_ordinal_skew;
   p.trace = nullptr;
-  p.num_sems = B * H * n * dash::kDqChains;
+  p.num_sems = B * H * n * dash::kSemStride;
 
   // Every refusal comes before the first queued operation: a refused call leaves the
   // stream and the scratch untouched.
