@@ -252,15 +252,35 @@ int dash_sched_table(int mask, int schedule, int n, int32_t* slot_offsets, int32
                      int cap, int32_t* ordinals);
 
 /*
- * The dQ orders dash_attn_bwd follows when `heads` (= B * H) heads' chains are dealt round
- * robin, head-major, onto `grid` persistent CTAs:
+ * How dash_attn_bwd spreads `heads` (= B * H) heads' chains over `grid` persistent CTAs.
+ * Round robin -- unit u (head u / num_slots, chain slot u % num_slots) whole to CTA
+ * u % grid -- unless the schedule orders dQ by arrival (SHIFT, SYMMETRIC_SHIFT) and the
+ * units overrun whole rounds of the grid (more units than CTAs, not a multiple of them).
+ * Then every chain is cut where its KV tile changes and the pieces are dealt longest
+ * first (equal lengths in head-major chain order), each to the CTA with the least work
+ * dealt so far (the lower index on a tie); each CTA runs its pieces in the order dealt.
+ * This balancing is the library's own (the pages study one head on n SMs); it keeps every
+ * KV tile whole on one CTA. Outputs:
+ *   cta_offsets : int32[grid + 1]; CTA c runs pieces cta_offsets[c] .. cta_offsets[c + 1]
+ *   pieces      : int32[3 * cap]; piece k = (head, first task, end task), the tasks being
+ *                 indices into dash_sched_table's task table
+ * Returns the number of pieces, or a negative dash_status_t value (heads or grid < 1, null
+ * outputs, cap too small: -DASH_ERR_INVALID_ARG; an unsupported (mask, schedule, n): the
+ * schedule's error).
+ */
+int dash_sched_deal(int mask, int schedule, int n, int heads, int grid, int32_t* cta_offsets,
+                    int32_t* pieces, int cap);
+
+/*
+ * The dQ orders dash_attn_bwd follows when `heads` (= B * H) heads' chains are dealt onto
+ * `grid` persistent CTAs as dash_sched_deal describes:
  *   ordinals : int32[heads * n * n]; ordinals[(h * n + i) * n + j] = position of KV_i's
  *              partial in head h's dQ_j order, -1 where the mask removes the task.
  * ASCENDING and DESCENDING: ascending KV index in every head. SHIFT and SYMMETRIC_SHIFT
  * (whose order the pages define as the order of arrival): a partial's place in its
- * CTA's task sequence -- the tasks of the CTA's earlier units, then its step in the chain
- * -- the lower KV index first on a tie. With whole heads per round of the grid this is
- * dash_sched_table's order; when the grid splits a head over two rounds, the chains run
+ * CTA's task sequence -- the tasks of the CTA's earlier pieces, then its step in the
+ * piece -- the lower KV index first on a tie. With whole heads per round of the grid this
+ * is dash_sched_table's order; when the grid splits a head over two rounds, the chains run
  * in the earlier round come first, so no partial waits for a chain that has not started.
  * Returns DASH_OK, DASH_ERR_INVALID_ARG (heads or grid < 1, null ordinals), or the
  * schedule's error for an unsupported (mask, schedule, n).
@@ -273,8 +293,7 @@ dash_status_t dash_sched_dealt_table(int mask, int schedule, int n, int heads, i
  * every task is a compute phase of cost c then a reduce phase of cost r; one SM runs its
  * tasks back to back; reductions into one dQ block follow the orders the kernel uses on a
  * grid of num_sms CTAs (dash_sched_dealt_table(mask, schedule, n, heads, num_sms)). `heads`
- * heads' chains are dealt round robin, head-major, onto `num_sms` SMs (the kernel's own
- * dealing). Writes the makespan and, if sm_end is not NULL, each SM's finish time
+ * heads' chains are dealt onto `num_sms` SMs as the kernel deals them (dash_sched_deal). Writes the makespan and, if sm_end is not NULL, each SM's finish time
  * (double[num_sms]). Returns DASH_ERR_DEADLOCK_RISK when the waits form a cycle.
  */
 dash_status_t dash_sched_simulate(int mask, int schedule, int n, int heads, int num_sms,

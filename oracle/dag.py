@@ -49,6 +49,14 @@ Readings where the pages are silent (listed in the design notes as well):
   SMs: a partial arrives when its SM has run all the tasks dealt to it before this one
   (the lower KV index first on a tie). Where a head's chains all start together this is
   the fixed order above; ascending and descending keep ascending KV index either way.
+* Balanced dealing (``dealt=True`` only; this library's own choice, the pages study one
+  head on n SMs): when the units do not fill whole rounds of the SMs (and there are more
+  units than SMs), round robin leaves some SMs a whole unit more work than others. Shift
+  and symmetric shift then cut every chain where its KV tile changes and deal the pieces
+  longest first, each to the SM with the least work dealt so far (the lower SM index on
+  a tie; pieces of equal length in head-major chain order); every SM runs its pieces in
+  the order dealt. Each KV tile still runs on one SM, in its chain's order. Equal-length
+  pieces (shift) are dealt exactly as round robin deals them.
 """
 
 from __future__ import annotations
@@ -59,6 +67,8 @@ __all__ = [
     "SCHEDULES",
     "chains",
     "reduction_order",
+    "pieces",
+    "deal",
     "dealt_reduction_order",
     "schedule_dag",
     "longest_path",
@@ -144,24 +154,59 @@ def longest_path(n_vertices: int, edges: list[tuple[int, int, float]]):
     return depth if seen == n_vertices else None
 
 
-def dealt_reduction_order(mask: str, sched: str, n: int, m: int, num_sms: int):
+def pieces(chain: list[tuple[int, int]]) -> list[list[tuple[int, int]]]:
+    """A chain cut where its KV tile changes: its runs of one KV tile, in chain order."""
+    out: list[list[tuple[int, int]]] = []
+    for task in chain:
+        if out and out[-1][-1][0] == task[0]:
+            out[-1].append(task)
+        else:
+            out.append([task])
+    return out
+
+
+def deal(mask: str, sched: str, n: int, m: int, num_sms: int, balanced: bool = True):
+    """Per SM, the runs of tasks it executes, in order: lists of (head, [(i, j), ...]).
+
+    Round robin deals the units (head, chain slot) head-major, unit u to SM u mod P.
+    ``balanced`` deals as the library's kernels do (the module docstring): round robin
+    unless the schedule orders dQ by arrival and the units overrun whole rounds of the
+    SMs, in which case the chains' KV-tile pieces go longest first to the least-loaded SM.
+    """
+    ch = chains(mask, sched, n)
+    units = [(h, slot) for h in range(m) for slot in range(len(ch))]
+    per_sm: list[list[tuple[int, list[tuple[int, int]]]]] = [[] for _ in range(num_sms)]
+    full_rounds, rest = divmod(len(units), num_sms)
+    if (not balanced or sched in ("ascending", "descending") or rest == 0
+            or full_rounds == 0):
+        for u, (h, slot) in enumerate(units):
+            per_sm[u % num_sms].append((h, list(ch[slot])))
+        return per_sm
+    runs = [(h, run) for (h, slot) in units for run in pieces(ch[slot])]
+    load = [0] * num_sms
+    for k in sorted(range(len(runs)), key=lambda k: (-len(runs[k][1]), k)):
+        sm = min(range(num_sms), key=lambda s: (load[s], s))
+        per_sm[sm].append(runs[k])
+        load[sm] += len(runs[k][1])
+    return per_sm
+
+
+def dealt_reduction_order(mask: str, sched: str, n: int, m: int, num_sms: int,
+                          balanced: bool = True):
     """For each (head, dQ block j), the KV tiles that reduce into it, in the order the
-    dealt SMs produce them (the ``dealt=True`` reading in the module docstring)."""
+    dealt SMs produce them (the ``dealt=True`` reading in the module docstring); with
+    ``balanced`` false, on SMs dealt round robin."""
     if sched in ("ascending", "descending"):
         fixed = reduction_order(mask, sched, n)
         return {(h, j): list(fixed[j]) for h in range(m) for j in range(n)}
-    ch = chains(mask, sched, n)
-    done = [0] * num_sms                     # tasks each SM has run so far
     arrivals: dict[tuple[int, int], list[tuple[int, int]]] = {
         (h, j): [] for h in range(m) for j in range(n)}
-    unit = 0
-    for h in range(m):
-        for chain in ch:
-            sm = unit % num_sms
-            for (i, j) in chain:
-                arrivals[(h, j)].append((done[sm], i))
-                done[sm] += 1
-            unit += 1
+    for runs in deal(mask, sched, n, m, num_sms, balanced):
+        place = 0                            # tasks this SM has run so far
+        for h, run in runs:
+            for (i, j) in run:
+                arrivals[(h, j)].append((place, i))
+                place += 1
     return {key: [i for _, i in sorted(lst)] for key, lst in arrivals.items()}
 
 
@@ -173,6 +218,24 @@ def _orders(mask: str, sched: str, n: int, m: int, num_sms: int, dealt: bool):
     return {(h, j): fixed[j] for h in range(m) for j in fixed}
 
 
+def _dealt_tasks(mask: str, sched: str, n: int, m: int, num_sms: int, dealt: bool):
+    """Number the tasks SM by SM in run order: (per_sm task lists, tasks, sm_of_task,
+    index). ``dealt`` deals as the kernels do (balanced), else round robin."""
+    per_sm: list[list[int]] = [[] for _ in range(num_sms)]
+    tasks: list[tuple[int, int, int]] = []
+    sm_of_task: list[int] = []
+    index: dict[tuple[int, int, int], int] = {}
+    for sm, runs in enumerate(deal(mask, sched, n, m, num_sms, balanced=dealt)):
+        for hd, run in runs:
+            for (i, j) in run:
+                k = len(tasks)
+                tasks.append((hd, i, j))
+                sm_of_task.append(sm)
+                index[(hd, i, j)] = k
+                per_sm[sm].append(k)
+    return per_sm, tasks, sm_of_task, index
+
+
 def schedule_dag(mask: str, sched: str, n: int, m: int, num_sms: int, c: float, r: float,
                  dealt: bool = False):
     """Build the explicit DAG of m heads' tasks dealt onto ``num_sms`` SMs.
@@ -181,21 +244,8 @@ def schedule_dag(mask: str, sched: str, n: int, m: int, num_sms: int, c: float, 
     Returns (n_vertices, edges, tasks, sm_of_task) where tasks[k] = (head, i, j) and task k
     owns vertices 4k..4k+3.
     """
-    ch = chains(mask, sched, n)
     order = _orders(mask, sched, n, m, num_sms, dealt)
-    units = [(h, slot) for h in range(m) for slot in range(len(ch))]   # head-major deal
-    per_sm: list[list[int]] = [[] for _ in range(num_sms)]
-    tasks: list[tuple[int, int, int]] = []
-    sm_of_task: list[int] = []
-    index: dict[tuple[int, int, int], int] = {}
-    for u, (h, slot) in enumerate(units):
-        sm = u % num_sms
-        for (i, j) in ch[slot]:
-            k = len(tasks)
-            tasks.append((h, i, j))
-            sm_of_task.append(sm)
-            index[(h, i, j)] = k
-            per_sm[sm].append(k)
+    per_sm, tasks, sm_of_task, index = _dealt_tasks(mask, sched, n, m, num_sms, dealt)
     edges: list[tuple[int, int, float]] = []
     for k in range(len(tasks)):
         cs, ce, rs, re = 4 * k, 4 * k + 1, 4 * k + 2, 4 * k + 3
@@ -251,21 +301,8 @@ def schedule_dag_ex(mask: str, sched: str, n: int, m: int, num_sms: int, c: floa
 
     Same vertex numbering and return value as schedule_dag.
     """
-    ch = chains(mask, sched, n)
     order = _orders(mask, sched, n, m, num_sms, dealt)
-    units = [(hd, slot) for hd in range(m) for slot in range(len(ch))]   # head-major deal
-    per_sm: list[list[int]] = [[] for _ in range(num_sms)]
-    tasks: list[tuple[int, int, int]] = []
-    sm_of_task: list[int] = []
-    index: dict[tuple[int, int, int], int] = {}
-    for u, (hd, slot) in enumerate(units):
-        sm = u % num_sms
-        for (i, j) in ch[slot]:
-            k = len(tasks)
-            tasks.append((hd, i, j))
-            sm_of_task.append(sm)
-            index[(hd, i, j)] = k
-            per_sm[sm].append(k)
+    per_sm, tasks, sm_of_task, index = _dealt_tasks(mask, sched, n, m, num_sms, dealt)
     edges: list[tuple[int, int, float]] = []
     for k in range(len(tasks)):
         cs, ce, rs, re = 4 * k, 4 * k + 1, 4 * k + 2, 4 * k + 3

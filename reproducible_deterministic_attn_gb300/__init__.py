@@ -14,7 +14,7 @@ from .dash_attn import (  # noqa: F401
     dash_attn_fwd, dash_attn_fwd_ex, dash_attn_get_status, dash_attn_shutdown, dash_debug_set_sync,
     dash_debug_set_trace,
     dash_last_error, dash_profile_enable, dash_profile_read, dash_sched_num_slots, dash_sched_simulate, dash_sched_simulate_ex, dash_sched_select,
-    dash_sched_table, dash_sched_dealt_table, dash_gemm_splitk, dash_gemm_splitk_workspace_size, gemm_splitk,
+    dash_sched_table, dash_sched_deal, dash_sched_dealt_table, dash_gemm_splitk, dash_gemm_splitk_workspace_size, gemm_splitk,
     dash_status_string, load, new_workspace, TRACE_SITES, TRACE_DQ_TURN_WAIT, TRACE_DQ_ADD,
     TRACE_TOTAL,
 )

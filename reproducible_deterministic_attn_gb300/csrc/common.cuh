@@ -71,15 +71,14 @@ struct BwdParams {
   int* sems;                 // [B, H, n, kSemStride]: per 128-row dQ block, one per chain
   int num_sems;               // B * H * n * kSemStride
   int chains;                 // interleaved dQ chains, 1..kDqChains (deterministic mode)
-  const int32_t* slot_off;   // schedule: chain offsets
+  const int32_t* cta_off;    // dealing: CTA c runs pieces [cta_off[c], cta_off[c + 1])
+  const int32_t* pieces;     // dealing: 4 words per piece: head, first task, end task, 0
   const int32_t* tasks;      // schedule: (kv << 16) | q
   const int32_t* ord;        // schedule: ordinals, ord[bh * ord_stride + i * n + j]
   long long ord_stride;      // n * n when every head has its own order, else 0
   const int32_t* cnt;        // schedule: contributors per dQ block
   int B, S, H, D;
   int n;                     // tiles per head
-  int num_slots;             // chains per head
-  int num_units;             // B * H * num_slots
   float scale;
   float scale_log2;          // scale * log2(e)
   int causal;

@@ -44,7 +44,6 @@ dash_status_t cuda_fail(cudaError_t e, const char* what) {
   } while (0)
 
 struct DeviceTables {
-  int32_t* slot_off = nullptr;
   int32_t* tasks = nullptr;
   int32_t* ord = nullptr;
   int32_t* cnt = nullptr;
@@ -54,8 +53,22 @@ struct DeviceTables {
 std::mutex g_mu;
 std::map<std::tuple<int, int, int, int>, DeviceTables> g_tables;        // (dev, mask, sched, n)
 std::map<std::tuple<int, int, int, int, int>, bool> g_deadlock_free;    // (mask, sched, n, heads, grid)
-// per-head dQ orders of the arrival-ordered schedules, (dev, mask, sched, n, heads, grid)
-std::map<std::tuple<int, int, int, int, int, int>, int32_t*> g_dealt;
+// What one grid follows, per (dev, mask, sched, n, heads, grid): each CTA's pieces of work
+// (dash::deal) and, for the arrival-ordered schedules, the per-head dQ orders.
+struct DealtTables {
+  int32_t* ord = nullptr;       // [heads][n][n]; null: the schedule's own order
+  int32_t* cta_off = nullptr;   // [grid + 1]
+  int32_t* pieces = nullptr;    // [pieces][4]: head, first task, end task, 0
+};
+std::map<std::tuple<int, int, int, int, int, int>, DealtTables> g_dealt;
+
+// The pieces in the kernel's 16-byte form: (head, first task, end task, 0).
+std::vector<int32_t> piece_words(const dash::Dealing& dl) {
+  std::vector<int32_t> w;
+  w.reserve(4 * dl.pieces.size());
+  for (const dash::Piece& pc : dl.pieces) w.insert(w.end(), {pc.head, pc.t_begin, pc.t_end, 0});
+  return w;
+}
 // their host copies, (mask, sched, n, heads, grid): building one sorts every task of the
 // shape, so it is done once per shape
 std::map<std::tuple<int, int, int, int, int>, std::shared_ptr<const std::vector<int32_t>>> g_host_dealt;
@@ -92,7 +105,6 @@ dash_status_t get_tables(int dev, int mask, int sched, int n, DeviceTables* out)
     if (e != cudaSuccess) return e;
     return cudaMemcpy(*dst, v.data(), v.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
   };
-  DASH_CUDA(upload(sc.slot_off, &t.slot_off));
   DASH_CUDA(upload(sc.tasks, &t.tasks));
   DASH_CUDA(upload(sc.ord, &t.ord));
   DASH_CUDA(upload(sc.cnt, &t.cnt));
@@ -101,14 +113,24 @@ dash_status_t get_tables(int dev, int mask, int sched, int n, DeviceTables* out)
   return DASH_OK;
 }
 
-// Points p->ord at the dQ orders the kernel follows on a grid of `grid` CTAs: the
-// schedule's own table for ascending/descending (one order for all heads), the per-head
-// arrival orders of dash::dealt_orders for shift and symmetric shift (cached per shape).
-dash_status_t set_orders(int dev, int mask, int sched, int n, int heads, int grid,
-                         const DeviceTables& tb, dash::BwdParams* p) {
-  p->ord = tb.ord;
-  p->ord_stride = 0;
-  if (sched != dash::SCHED_SHIFT && sched != dash::SCHED_SYMMETRIC_SHIFT) return DASH_OK;
+// Copies a host table to a new device allocation (freed with the caches).
+cudaError_t upload_new(const std::vector<int32_t>& v, int32_t** dst) {
+  cudaError_t e = cudaMalloc(dst, v.size() * sizeof(int32_t));
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpy(*dst, v.data(), v.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    cudaFree(*dst);
+    *dst = nullptr;
+  }
+  return e;
+}
+
+// Points p at what a grid of `grid` CTAs follows: each CTA's pieces (dash::deal) and the
+// dQ orders -- the schedule's own table for ascending/descending (one order for all
+// heads), the per-head arrival orders of dash::dealt_orders for shift and symmetric shift
+// (cached per shape).
+dash_status_t set_dealing(int dev, int mask, int sched, int n, int heads, int grid,
+                          const DeviceTables& tb, dash::BwdParams* p) {
   std::lock_guard<std::mutex> lk(g_mu);
   auto key = std::make_tuple(dev, mask, sched, n, heads, grid);
   auto it = g_dealt.find(key);
@@ -116,18 +138,25 @@ dash_status_t set_orders(int dev, int mask, int sched, int n, int heads, int gri
     dash::Schedule sc;
     int rc = dash::build_schedule(mask, sched, n, &sc);
     if (rc) return (dash_status_t)rc;
-    const std::vector<int32_t>& ord = *host_dealt_locked(sc, heads, grid);
-    int32_t* d = nullptr;
-    DASH_CUDA(cudaMalloc(&d, ord.size() * sizeof(int32_t)));
-    cudaError_t e = cudaMemcpy(d, ord.data(), ord.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
+    dash::Dealing dl;
+    dash::deal(sc, heads, grid, &dl);
+    DealtTables d;
+    cudaError_t e = upload_new(dl.cta_off, &d.cta_off);
+    if (e == cudaSuccess) e = upload_new(piece_words(dl), &d.pieces);
+    if (e == cudaSuccess && dash::arrival_ordered(sc))
+      e = upload_new(*host_dealt_locked(sc, heads, grid), &d.ord);
     if (e != cudaSuccess) {
-      cudaFree(d);
-      return cuda_fail(e, "cudaMemcpy(dQ orders)");
+      cudaFree(d.cta_off);
+      cudaFree(d.pieces);
+      cudaFree(d.ord);
+      return cuda_fail(e, "uploading the dealing tables");
     }
     it = g_dealt.emplace(key, d).first;
   }
-  p->ord = it->second;
-  p->ord_stride = (long long)n * n;
+  p->ord = it->second.ord ? it->second.ord : tb.ord;
+  p->ord_stride = it->second.ord ? (long long)n * n : 0;
+  p->cta_off = it->second.cta_off;
+  p->pieces = it->second.pieces;
   return DASH_OK;
 }
 
@@ -306,14 +335,15 @@ void dash_attn_shutdown(void) {
   cudaGetDevice(&cur);
   for (auto& kv : g_tables) {
     cudaSetDevice(std::get<0>(kv.first));
-    cudaFree(kv.second.slot_off);
     cudaFree(kv.second.tasks);
     cudaFree(kv.second.ord);
     cudaFree(kv.second.cnt);
   }
   for (auto& kv : g_dealt) {
     cudaSetDevice(std::get<0>(kv.first));
-    cudaFree(kv.second);
+    cudaFree(kv.second.ord);
+    cudaFree(kv.second.cta_off);
+    cudaFree(kv.second.pieces);
   }
   if (cur >= 0) cudaSetDevice(cur);
   g_tables.clear();
@@ -420,7 +450,6 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
   p.dox = (__nv_bfloat16*)(ws + wl.dox);
   p.dq_acc = (float*)(ws + wl.dq_acc);
   p.sems = (int*)(ws + wl.sems);
-  p.slot_off = tb.slot_off;
   p.tasks = tb.tasks;
   p.ord = tb.ord;
   p.cnt = tb.cnt;
@@ -429,8 +458,7 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
   p.H = H;
   p.D = D;
   p.n = n;
-  p.num_slots = tb.num_slots;
-  p.num_units = B * H * tb.num_slots;
+  const int units = B * H * tb.num_slots;
   p.scale = scale;
   p.scale_log2 = scale * dash::kLog2e;
   p.causal = mask == DASH_MASK_CAUSAL;
@@ -473,10 +501,10 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
     return DASH_ERR_CUDA;
   }
   int grid = sms;                      // one CTA per SM (512 TMEM columns each)
-  if (grid > p.num_units) grid = p.num_units;
+  if (grid > units) grid = units;
   if (deterministic && !deadlock_free(mask, schedule, n, B * H, grid))
     return DASH_ERR_DEADLOCK_RISK;
-  st = set_orders(dev, mask, schedule, n, B * H, grid, tb, &p);
+  st = set_dealing(dev, mask, schedule, n, B * H, grid, tb, &p);
   if (st != DASH_OK) return st;
 
   dash::bwd_preprocess_kernel<<<sms * 4, 256, 0, stream>>>(p);
@@ -580,6 +608,24 @@ dash_status_t dash_sched_dealt_table(int mask, int schedule, int n, int heads, i
   dash::dealt_orders(sc, heads, grid, &ord);
   std::memcpy(ordinals, ord.data(), ord.size() * sizeof(int32_t));
   return DASH_OK;
+}
+
+int dash_sched_deal(int mask, int schedule, int n, int heads, int grid, int32_t* cta_offsets,
+                    int32_t* pieces, int cap) {
+  if (heads < 1 || grid < 1 || !cta_offsets || !pieces || cap < 0) return -DASH_ERR_INVALID_ARG;
+  dash::Schedule sc;
+  int rc = dash::build_schedule(mask, schedule, n, &sc);
+  if (rc) return -rc;
+  dash::Dealing dl;
+  dash::deal(sc, heads, grid, &dl);
+  if ((size_t)cap < dl.pieces.size()) return -DASH_ERR_INVALID_ARG;
+  std::memcpy(cta_offsets, dl.cta_off.data(), dl.cta_off.size() * sizeof(int32_t));
+  for (size_t k = 0; k < dl.pieces.size(); ++k) {
+    pieces[3 * k] = dl.pieces[k].head;
+    pieces[3 * k + 1] = dl.pieces[k].t_begin;
+    pieces[3 * k + 2] = dl.pieces[k].t_end;
+  }
+  return (int)dl.pieces.size();
 }
 
 dash_status_t dash_sched_simulate(int mask, int schedule, int n, int heads, int num_sms,
@@ -748,8 +794,8 @@ __global__ void copy_status_kernel(const int* header, int* out) { *out = header[
 // host memory that has been freed.
 struct StaticTables {
   std::vector<int32_t> image;
-  size_t task_off, ord_off, cnt_off;   // byte offsets of the task, order, count tables
-  int num_slots;
+  // byte offsets of the piece, task, order and count tables (the CTA offsets come first)
+  size_t piece_off, task_off, ord_off, cnt_off;
 };
 std::map<std::tuple<int, int, int, int, int>, std::shared_ptr<const StaticTables>> g_static_tables;
 
@@ -765,13 +811,17 @@ dash_status_t static_tables(int mask, int schedule, int n, int heads, int grid,
     std::shared_ptr<const std::vector<int32_t>> dealt;
     if (dash::arrival_ordered(sc)) dealt = host_dealt_locked(sc, heads, grid);
     const std::vector<int32_t>& ord = dealt ? *dealt : sc.ord;
+    dash::Dealing dl;
+    dash::deal(sc, heads, grid, &dl);
+    const std::vector<int32_t> words = piece_words(dl);
     auto t = std::make_shared<StaticTables>();
-    t->num_slots = sc.num_slots;
-    t->task_off = round_up(sc.slot_off.size() * 4, 256);
+    t->piece_off = round_up(dl.cta_off.size() * 4, 256);
+    t->task_off = round_up(t->piece_off + words.size() * 4, 256);
     t->ord_off = round_up(t->task_off + sc.tasks.size() * 4, 256);
     t->cnt_off = round_up(t->ord_off + ord.size() * 4, 256);
     t->image.assign(round_up(t->cnt_off + sc.cnt.size() * 4, 256) / 4, 0);
-    std::memcpy(t->image.data(), sc.slot_off.data(), sc.slot_off.size() * 4);
+    std::memcpy(t->image.data(), dl.cta_off.data(), dl.cta_off.size() * 4);
+    std::memcpy(t->image.data() + t->piece_off / 4, words.data(), words.size() * 4);
     std::memcpy(t->image.data() + t->task_off / 4, sc.tasks.data(), sc.tasks.size() * 4);
     std::memcpy(t->image.data() + t->ord_off / 4, ord.data(), ord.size() * 4);
     std::memcpy(t->image.data() + t->cnt_off / 4, sc.cnt.data(), sc.cnt.size() * 4);
@@ -858,7 +908,8 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
   p.dox = (__nv_bfloat16*)(ws + wl.dox);
   p.dq_acc = (float*)(ws + wl.dq_acc);
   p.sems = (int*)(ws + wl.sems);
-  p.slot_off = (const int32_t*)(ws + t_off);
+  p.cta_off = (const int32_t*)(ws + t_off);
+  p.pieces = (const int32_t*)(ws + t_off + tb->piece_off);
   p.tasks = (const int32_t*)(ws + t_off + tb->task_off);
   p.ord = (const int32_t*)(ws + t_off + tb->ord_off);
   p.ord_stride = (schedule == DASH_SCHED_SHIFT || schedule == DASH_SCHED_SYMMETRIC_SHIFT)
@@ -869,8 +920,6 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
   p.H = H;
   p.D = D;
   p.n = n;
-  p.num_slots = tb->num_slots;
-  p.num_units = B * H * tb->num_slots;
   p.scale = scale;
   p.scale_log2 = scale * dash::kLog2e;
   p.causal = mask == DASH_MASK_CAUSAL;

@@ -16,6 +16,8 @@
 #include "sched.h"
 
 #include <algorithm>
+#include <functional>
+#include <queue>
 
 namespace dash {
 
@@ -100,6 +102,51 @@ int build_schedule(int mask, int sched, int n, Schedule* out) {
   return 0;
 }
 
+void deal(const Schedule& sc, int heads, int grid, Dealing* out) {
+  out->cta_off.assign(grid + 1, 0);
+  out->pieces.clear();
+  const long long units = (long long)heads * sc.num_slots;
+  std::vector<std::vector<Piece>> per_cta(grid);
+  if (!arrival_ordered(sc) || units % grid == 0 || units < grid) {
+    // round robin: unit u = (head u / slots, slot u % slots) to CTA u % grid
+    for (long long u = 0; u < units; ++u) {
+      const int slot = (int)(u % sc.num_slots);
+      per_cta[u % grid].push_back(
+          {(int32_t)(u / sc.num_slots), sc.slot_off[slot], sc.slot_off[slot + 1]});
+    }
+  } else {
+    // the chains cut where the KV tile changes, in head-major chain order
+    std::vector<Piece> runs;
+    for (int h = 0; h < heads; ++h)
+      for (int slot = 0; slot < sc.num_slots; ++slot) {
+        int b = sc.slot_off[slot];
+        for (int t = b + 1; t <= sc.slot_off[slot + 1]; ++t)
+          if (t == sc.slot_off[slot + 1] || (sc.tasks[t] >> 16) != (sc.tasks[b] >> 16)) {
+            runs.push_back({h, b, t});
+            b = t;
+          }
+      }
+    // longest first (stable: equal lengths keep the head-major order), each to the CTA
+    // with the least work so far, the lower index on a tie
+    std::stable_sort(runs.begin(), runs.end(), [](const Piece& a, const Piece& b) {
+      return a.t_end - a.t_begin > b.t_end - b.t_begin;
+    });
+    using Load = std::pair<long long, int>;   // (tasks dealt, CTA)
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> least;
+    for (int c = 0; c < grid; ++c) least.push({0, c});
+    for (const Piece& pc : runs) {
+      Load l = least.top();
+      least.pop();
+      per_cta[l.second].push_back(pc);
+      least.push({l.first + (pc.t_end - pc.t_begin), l.second});
+    }
+  }
+  for (int c = 0; c < grid; ++c) {
+    out->cta_off[c + 1] = out->cta_off[c] + (int32_t)per_cta[c].size();
+    out->pieces.insert(out->pieces.end(), per_cta[c].begin(), per_cta[c].end());
+  }
+}
+
 void dealt_orders(const Schedule& sc, int heads, int grid, std::vector<int32_t>* out) {
   const int n = sc.n;
   out->assign((size_t)heads * n * n, -1);
@@ -109,18 +156,18 @@ void dealt_orders(const Schedule& sc, int heads, int grid, std::vector<int32_t>*
     return;
   }
   // (place in the CTA's task sequence, kv) of every partial, per (head, dQ block)
+  Dealing dl;
+  deal(sc, heads, grid, &dl);
   std::vector<std::vector<std::pair<long long, int>>> arrivals((size_t)heads * n);
-  std::vector<long long> place(grid, 0);
-  const long long units = (long long)heads * sc.num_slots;
-  for (long long u = 0; u < units; ++u) {
-    const int cta = (int)(u % grid);
-    const int head = (int)(u / sc.num_slots), slot = (int)(u % sc.num_slots);
-    const int beg = sc.slot_off[slot], len = sc.slot_off[slot + 1] - beg;
-    for (int t = 0; t < len; ++t) {
-      const int32_t tk = sc.tasks[beg + t];
-      arrivals[(size_t)head * n + (tk & 0xffff)].push_back({place[cta] + t, tk >> 16});
+  for (int cta = 0; cta < grid; ++cta) {
+    long long place = 0;
+    for (int k = dl.cta_off[cta]; k < dl.cta_off[cta + 1]; ++k) {
+      const Piece& pc = dl.pieces[k];
+      for (int t = pc.t_begin; t < pc.t_end; ++t, ++place) {
+        const int32_t tk = sc.tasks[t];
+        arrivals[(size_t)pc.head * n + (tk & 0xffff)].push_back({place, tk >> 16});
+      }
     }
-    place[cta] += len;
   }
   for (size_t hj = 0; hj < arrivals.size(); ++hj) {
     auto& a = arrivals[hj];
@@ -139,9 +186,10 @@ bool simulate(const Schedule& sc, int heads, int num_sms, double c, double r,
 bool simulate_ex(const Schedule& sc, int heads, int num_sms, double c, double r, double h,
                  bool overlapped, double* makespan, std::vector<double>* sm_end) {
   const int n = sc.n;
-  const long long units = (long long)heads * sc.num_slots;
   std::vector<int32_t> ord;
   dealt_orders(sc, heads, num_sms, &ord);
+  Dealing dl;
+  deal(sc, heads, num_sms, &dl);
   // who reduces at position k of head h's dQ_j: inv[(h * n + j) * n + k] = kv tile
   std::vector<int32_t> inv((size_t)heads * n * n, -1);
   for (int hd = 0; hd < heads; ++hd)
@@ -151,10 +199,12 @@ bool simulate_ex(const Schedule& sc, int heads, int num_sms, double c, double r,
         if (o >= 0) inv[((size_t)hd * n + j) * n + o] = i;
       }
 
-  // per SM: the list of units in dealing order; progress = (unit index, task index)
-  std::vector<std::vector<long long>> sm_units(num_sms);
-  for (long long u = 0; u < units; ++u) sm_units[u % num_sms].push_back(u);
-  std::vector<size_t> unit_pos(num_sms, 0), task_pos(num_sms, 0);
+  // per SM: progress = (piece index into dl.pieces, task index into sc.tasks)
+  std::vector<int> piece_pos(num_sms), task_pos(num_sms);
+  for (int sm = 0; sm < num_sms; ++sm) {
+    piece_pos[sm] = dl.cta_off[sm];
+    task_pos[sm] = piece_pos[sm] < dl.cta_off[sm + 1] ? dl.pieces[piece_pos[sm]].t_begin : 0;
+  }
   // per SM: end of its last C phase, of its last R phase and of the R phase before that
   std::vector<double> c_last(num_sms, 0.0), r_last(num_sms, 0.0), r_prev(num_sms, 0.0);
   // reduce-end time and SM of (head, kv, q); sentinel -1 = not yet done
@@ -165,11 +215,10 @@ bool simulate_ex(const Schedule& sc, int heads, int num_sms, double c, double r,
   while (remaining > 0) {
     bool progress = false;
     for (int sm = 0; sm < num_sms; ++sm) {
-      while (unit_pos[sm] < sm_units[sm].size()) {
-        const long long u = sm_units[sm][unit_pos[sm]];
-        const int head = (int)(u / sc.num_slots), slot = (int)(u % sc.num_slots);
-        const int beg = sc.slot_off[slot], len = sc.slot_off[slot + 1] - beg;
-        const int32_t tk = sc.tasks[beg + task_pos[sm]];
+      while (piece_pos[sm] < dl.cta_off[sm + 1]) {
+        const Piece& pc = dl.pieces[piece_pos[sm]];
+        const int head = pc.head;
+        const int32_t tk = sc.tasks[task_pos[sm]];
         const int i = tk >> 16, j = tk & 0xffff;
         const int o = ord[((size_t)head * n + i) * n + j];
         double pred_ready = 0.0;
@@ -195,10 +244,8 @@ bool simulate_ex(const Schedule& sc, int heads, int num_sms, double c, double r,
         r_last[sm] = r_end;
         --remaining;
         progress = true;
-        if (++task_pos[sm] == (size_t)len) {
-          task_pos[sm] = 0;
-          ++unit_pos[sm];
-        }
+        if (++task_pos[sm] == pc.t_end && ++piece_pos[sm] < dl.cta_off[sm + 1])
+          task_pos[sm] = dl.pieces[piece_pos[sm]].t_begin;
       }
     }
     if (!progress) return false;

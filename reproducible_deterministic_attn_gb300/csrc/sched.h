@@ -26,12 +26,40 @@ struct Schedule {
 // Returns 0 and fills `out`, or a positive dash_status_t code.
 int build_schedule(int mask, int sched, int n, Schedule* out);
 
-// The dQ order the kernels follow when `heads` heads' chains are dealt round robin,
-// head-major, onto `grid` persistent CTAs: out[(h * n + i) * n + j] = position of KV_i's
-// partial in head h's dQ_j order (-1 where the mask removes the task).
+// True when the schedule orders dQ by arrival (its order depends on the dealing).
+inline bool arrival_ordered(const Schedule& sc) {
+  return sc.sched == SCHED_SHIFT || sc.sched == SCHED_SYMMETRIC_SHIFT;
+}
+
+// A run of one head's chain: tasks[t_begin, t_end) of the schedule, for head `head`.
+struct Piece {
+  int32_t head, t_begin, t_end;
+};
+
+// The work of each persistent CTA, in run order: CTA c runs
+// pieces[cta_off[c] .. cta_off[c + 1]).
+struct Dealing {
+  std::vector<int32_t> cta_off;      // grid + 1
+  std::vector<Piece> pieces;
+};
+
+// How the kernels spread `heads` heads' chains over `grid` persistent CTAs. Round robin
+// -- unit u = (head u / num_slots, chain slot u % num_slots) whole to CTA u % grid --
+// unless the schedule orders dQ by arrival and the units overrun whole rounds of the grid
+// (units % grid != 0 and units > grid). Then round robin would leave some CTAs a whole
+// unit more work than the rest, and the chains are instead cut where the KV tile changes
+// and the pieces dealt longest first (equal lengths in head-major chain order), each to
+// the CTA with the least work dealt so far (the lower index on a tie); a CTA runs its
+// pieces in the order dealt. Every KV tile still runs whole on one CTA, in chain order.
+// Pieces of equal length (shift) are dealt exactly as round robin deals them.
+void deal(const Schedule& sc, int heads, int grid, Dealing* out);
+
+// The dQ order the kernels follow when `heads` heads' chains are dealt onto `grid`
+// persistent CTAs (deal above): out[(h * n + i) * n + j] = position of KV_i's partial in
+// head h's dQ_j order (-1 where the mask removes the task).
 //   ascending, descending  -- ascending KV index in every head (`ord` repeated);
 //   shift, symmetric shift -- order of arrival: a partial's place in its CTA's task
-//                             sequence (the tasks of the CTA's earlier units, then its
+//                             sequence (the tasks of the CTA's earlier pieces, then its
 //                             step), the lower KV index first on a tie.
 // When every chain of a head starts together (the pages' setting: one head on n SMs,
 // or whole heads per round of the grid) the arrival order is the step order of `ord`.
@@ -41,15 +69,10 @@ int build_schedule(int mask, int sched, int n, Schedule* out);
 // and each CTA runs its tasks in increasing place, so these orders cannot deadlock.
 void dealt_orders(const Schedule& sc, int heads, int grid, std::vector<int32_t>* out);
 
-// True when the schedule orders dQ by arrival (its order depends on the dealing).
-inline bool arrival_ordered(const Schedule& sc) {
-  return sc.sched == SCHED_SHIFT || sc.sched == SCHED_SYMMETRIC_SHIFT;
-}
-
-// Event-driven critical path of `heads` heads dealt round robin (head-major) onto
-// `num_sms` SMs, with the dQ orders of dealt_orders(sc, heads, num_sms) -- the orders the
-// kernels follow on a grid of num_sms CTAs. Returns false on a cycle (deadlock). sm_end
-// may be null.
+// Event-driven critical path of `heads` heads dealt onto `num_sms` SMs as the kernels
+// deal them (deal above), with the dQ orders of dealt_orders(sc, heads, num_sms) -- the
+// orders the kernels follow on a grid of num_sms CTAs. Returns false on a cycle
+// (deadlock). sm_end may be null.
 bool simulate(const Schedule& sc, int heads, int num_sms, double c, double r,
               double* makespan, std::vector<double>* sm_end);
 

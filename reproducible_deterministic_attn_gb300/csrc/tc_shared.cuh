@@ -22,15 +22,18 @@ __device__ __forceinline__ uint32_t sw_chunk(int row, int chunk, int rows) {
   return (uint32_t)((chunk >> 3) * rows * 128 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
 }
 
-// Iterates this CTA's (unit, task) sequence; every role walks the same sequence. The
-// task table is read two entries ahead so its load latency hides behind the work.
+// Iterates this CTA's (piece, task) sequence; every role walks the same sequence. A piece
+// is a run of one head's chain that covers whole KV tiles, so a new piece always starts a
+// new tile. The task table is read two entries ahead so its load latency hides behind
+// the work.
 struct Walk {
   const BwdParams& p;
-  int u, t, t_end, bh, i, j;
+  int k, k_end, t, t_end, bh, i, j;
   int32_t prev_tk, cur_tk, nxt_tk, nxt2_tk;
   bool first_of_tile, last_of_tile;
   __device__ Walk(const BwdParams& pp)
-      : p(pp), u((int)blockIdx.x - (int)gridDim.x), t(0), t_end(0) {}
+      : p(pp), k(__ldg(pp.cta_off + blockIdx.x) - 1), k_end(__ldg(pp.cta_off + blockIdx.x + 1)),
+        t(0), t_end(0) {}
   __device__ __forceinline__ int32_t task_at(int k) const {
     return k < t_end ? __ldg(p.tasks + k) : -1;
   }
@@ -38,12 +41,11 @@ struct Walk {
     ++t;
     if (t >= t_end) {
       do {
-        u += gridDim.x;
-        if (u >= p.num_units) return false;
-        const int slot = u % p.num_slots;
-        bh = u / p.num_slots;
-        t = __ldg(p.slot_off + slot);
-        t_end = __ldg(p.slot_off + slot + 1);
+        if (++k >= k_end) return false;
+        const int4 pc = __ldg(reinterpret_cast<const int4*>(p.pieces) + k);
+        bh = pc.x;
+        t = pc.y;
+        t_end = pc.z;
       } while (t >= t_end);
       prev_tk = -1;
       cur_tk = task_at(t);

@@ -59,6 +59,7 @@ _SIGNATURES = {
     "dash_sched_num_slots": (_c_int, [_c_int, _c_int, _c_int]),
     "dash_sched_table": (_c_int, [_c_int, _c_int, _c_int, _i32p, _i32p, _c_int, _i32p]),
     "dash_sched_dealt_table": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _i32p]),
+    "dash_sched_deal": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _i32p, _i32p, _c_int]),
     "dash_sched_simulate": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_double, _c_double,
                                      _dblp, _dblp]),
     "dash_sched_simulate_ex": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_double,
@@ -223,6 +224,21 @@ def dash_sched_table(mask: int, schedule: int, n: int):
         raise DashError(-cnt, "dash_sched_table")
     pairs = [(tasks[k] >> 16, tasks[k] & 0xFFFF) for k in range(cnt)]
     return list(off), pairs, [list(ords[i * n:(i + 1) * n]) for i in range(n)]
+
+
+def dash_sched_deal(mask: int, schedule: int, n: int, heads: int, grid: int):
+    """Each CTA's work in run order: per CTA a list of (head, [(kv, q), ...]) pieces."""
+    _, pairs, _ = dash_sched_table(mask, schedule, n)
+    slots = dash_sched_num_slots(mask, schedule, n)
+    cap = 2 * heads * slots              # a chain has at most two KV tiles
+    off = (ctypes.c_int32 * (grid + 1))()
+    pieces = (ctypes.c_int32 * (3 * cap))()
+    cnt = load().dash_sched_deal(int(mask), int(schedule), int(n), int(heads), int(grid),
+                                 off, pieces, cap)
+    if cnt < 0:
+        raise DashError(-cnt, "dash_sched_deal")
+    return [[(pieces[3 * k], pairs[pieces[3 * k + 1]:pieces[3 * k + 2]])
+             for k in range(off[c], off[c + 1])] for c in range(grid)]
 
 
 def dash_sched_dealt_table(mask: int, schedule: int, n: int, heads: int, grid: int):

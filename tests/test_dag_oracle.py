@@ -283,7 +283,7 @@ def _dealt_rows(kind):
 def test_dealt_worked_examples_orders():
     from oracle.dag import dealt_reduction_order
     rows = _dealt_rows("ORDER")
-    assert len(rows) == 8
+    assert len(rows) == 14
     for mask, sched, n, m, sms, head, j, want in rows:
         got = dealt_reduction_order(mask, sched, int(n), int(m), int(sms))[(int(head), int(j))]
         assert got == [int(x) for x in want.split()], (mask, sched, j)
@@ -300,7 +300,71 @@ def test_dealt_worked_examples_makespans():
         assert simulate(mask, sched, int(n), int(m), int(sms), float(c), float(r))["makespan"] is None
 
 
+def test_balanced_worked_example_deal_and_makespan():
+    from oracle.dag import deal
+    rows = _dealt_rows("DEAL")
+    assert len(rows) == 4
+    for mask, sched, n, m, sms, sm, want in rows:
+        got = deal(mask, sched, int(n), int(m), int(sms))[int(sm)]
+        runs = []
+        for piece in want.split(";"):
+            h, kv, *qs = (int(x) for x in piece.split())
+            runs.append((h, [(kv, q) for q in qs]))
+        assert got == runs, (sm, got)
+    rows = _dealt_rows("BALANCED")
+    assert len(rows) == 1
+    for mask, sched, n, m, sms, c, r, want, ends in rows:
+        res = simulate(mask, sched, int(n), int(m), int(sms), float(c), float(r), dealt=True)
+        assert res["makespan"] == float(want)
+        assert res["sm_end"] == [float(x) for x in ends.split()]
+        # round robin gives two SMs two whole units (10 tasks, makespan 30)
+        rr = deal(mask, sched, int(n), int(m), int(sms), balanced=False)
+        assert max(sum(len(run) for _, run in runs) for runs in rr) == 10
+
+
+def test_balanced_deal_invariants():
+    from oracle.dag import deal
+    for mask, sched in [("full", "ascending"), ("full", "shift"), ("causal", "descending"),
+                        ("causal", "symmetric_shift")]:
+        for n in (2, 4, 6, 8):
+            ch = chains(mask, sched, n)
+            longest = max(len(c) for c in ch)
+            for m in (1, 2, 3, 5):
+                for sms in range(1, 3 * n + 2):
+                    per_sm = deal(mask, sched, n, m, sms)
+                    rr = deal(mask, sched, n, m, sms, balanced=False)
+                    units = m * len(ch)
+                    if (sched in ("ascending", "descending") or units % sms == 0
+                            or units < sms or sched == "shift"):
+                        # fixed-order schedules, whole rounds, a single partial round and
+                        # equal-length chains: exactly round robin
+                        assert per_sm == rr, (mask, sched, n, m, sms)
+                        continue
+                    seen = {}
+                    for sm, runs in enumerate(per_sm):
+                        for h, run in runs:
+                            assert len({i for i, _ in run}) == 1       # one KV tile per piece
+                            i = run[0][0]
+                            assert (h, i) not in seen                  # a KV tile on one SM
+                            seen[(h, i)] = sm
+                            chain = next(c for c in ch if (i, run[0][1]) in c)
+                            k = chain.index(run[0])                    # contiguous, in order
+                            assert chain[k:k + len(run)] == run
+                    tasks = sorted((h, i, j) for runs in per_sm for h, run in runs
+                                   for (i, j) in run)
+                    assert tasks == sorted((h, i, j) for h in range(m) for c in ch
+                                           for (i, j) in c)
+                    # greedy list scheduling: the last piece dealt to the busiest SM started
+                    # on the least load, at most the mean of the rest
+                    loads = [sum(len(run) for _, run in runs) for runs in per_sm]
+                    total = sum(loads)
+                    assert max(loads) <= total / sms + longest * (1 - 1 / sms) + 1e-9
+                    assert max(loads) <= max(sum(len(run) for _, run in runs) for runs in rr)
+
+
 def test_dealt_equals_the_pages_order_when_heads_start_together():
+    # the pages' setting on round-robin SMs (balanced dealing cuts chains only when the
+    # units overrun whole rounds, which a head-per-round grid never does)
     from oracle.dag import dealt_reduction_order
     for mask, sched in [("full", "ascending"), ("full", "descending"), ("full", "shift"),
                         ("causal", "ascending"), ("causal", "descending"),
@@ -313,7 +377,7 @@ def test_dealt_equals_the_pages_order_when_heads_start_together():
                 if sched in ("ascending", "descending"):
                     sms_list += [1, 3, 5]          # their order ignores the dealing
                 for sms in sms_list:
-                    got = dealt_reduction_order(mask, sched, n, m, sms)
+                    got = dealt_reduction_order(mask, sched, n, m, sms, balanced=False)
                     for h in range(m):
                         for j in range(n):
                             assert got[(h, j)] == fixed[j], (mask, sched, n, m, sms, h, j)

@@ -61,6 +61,39 @@ def test_dealt_tables_match_oracle(seed):
             assert masked == (0 if mask == 0 else n * (n - 1) // 2)
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_deal_matches_oracle(seed):
+    rng = random.Random(800 + seed)
+    for _ in range(20):
+        mask, sched = rng.choice([(0, 0), (0, 1), (0, 2), (1, 0), (1, 1), (1, 3)])
+        n = rng.choice([1, 2, 3, 4, 6, 8, 12]) if sched != 3 else rng.choice([2, 4, 6, 8, 12])
+        m, grid = rng.randint(1, 6), rng.randint(1, 3 * n + 2)
+        got = da.dash_sched_deal(mask, sched, n, m, grid)
+        want = dag.deal(MASKS[mask], NAMES[sched], n, m, grid)
+        assert got == [[(h, list(run)) for h, run in runs] for runs in want], (mask, sched, n, m, grid)
+
+
+def test_deal_at_the_kernel_sizes():
+    # 152 CTAs. Causal 4x16 heads of n = 16 (512 units of 17 tasks) and 1x32 heads of
+    # n = 128 (2048 units of 129) overrun whole rounds: pieces dealt longest first bring
+    # the busiest CTA to the mean (57.3 and 1738.1 tasks) instead of a whole unit above
+    # it. Full 2x16 heads of n = 64: equal units, dealt round robin.
+    for mask, sched, n, heads, rr_max, max_load in [(1, 3, 16, 64, 68, 58),
+                                                   (1, 3, 128, 32, 1806, 1739),
+                                                   (0, 2, 64, 32, 14 * 64, 14 * 64)]:
+        got = da.dash_sched_deal(mask, sched, n, heads, 152)
+        want = dag.deal(MASKS[mask], NAMES[sched], n, heads, 152)
+        assert got == [[(h, list(run)) for h, run in runs] for runs in want]
+        loads = [sum(len(run) for _, run in runs) for runs in got]
+        assert max(loads) == max_load
+        rr = dag.deal(MASKS[mask], NAMES[sched], n, heads, 152, balanced=False)
+        assert max(sum(len(run) for _, run in runs) for runs in rr) == rr_max
+    with pytest.raises(da.DashError):
+        da.dash_sched_deal(1, 3, 8, 0, 4)
+    with pytest.raises(da.DashError):
+        da.dash_sched_deal(1, 3, 7, 1, 4)             # symmetric shift needs even n
+
+
 def test_dealt_tables_at_the_kernel_sizes():
     # 152 CTAs: full 2x16 heads of n = 64 and causal 32 heads of n = 128 split heads over
     # two rounds of the grid; the per-head orders still follow the dealing
