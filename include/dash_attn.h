@@ -99,9 +99,11 @@ dash_status_t dash_attn_fwd_ex(const void* q, const void* k, const void* v, void
  * Bytes of scratch dash_attn_bwd needs for this shape: a status header, D = rowsum(dO*O)
  * and -LSE*log2(e) (two fp32 [B,H,S] arrays), two score-offset block arrays (-LSE/scale
  * and -D as three bf16 terms each, 32 bytes per row), two copies of the fp32 dQ accumulator
- * [2,B,H,S,D] (deterministic = 2 uses both) and one 128-byte line of int32 semaphores per
- * 128-row dQ block, one semaphore per chain [B,H,S/128,32]. Returns 0 for an unsupported
- * shape.
+ * [2,B,H,S,D] (deterministic = 2 uses both), one 128-byte line of int32 semaphores per
+ * 128-row dQ block, one semaphore per chain [B,H,S/128,32], 256 x 4 int32 split-tile flags
+ * and the fp32 dK/dV partials of the KV tiles a grid may split over two CTAs
+ * (dash_sched_deal): min(B*H*S/128 / 2, 256) tiles of [2][128][D]. Returns 0 for an
+ * unsupported shape.
  */
 size_t dash_attn_bwd_workspace_size(int B, int S, int H, int D);
 
@@ -259,11 +261,16 @@ int dash_sched_table(int mask, int schedule, int n, int32_t* slot_offsets, int32
  * Then every chain is cut where its KV tile changes and the pieces are dealt longest
  * first (equal lengths in head-major chain order), each to the CTA with the least work
  * dealt so far (the lower index on a tie); each CTA runs its pieces in the order dealt.
- * This balancing is the library's own (the pages study one head on n SMs); it keeps every
- * KV tile whole on one CTA. Outputs:
+ * Shift's units are single KV tiles of one length, dealt round robin all the same; there,
+ * when the last partial round holds r units with 2 r <= grid (r <= 256), each of those r
+ * KV tiles is split in two halves (the first ceil(len / 2) tasks, then the rest): split
+ * k's first half runs on CTA k and its second half on CTA r + k, after their whole units. The first half hands its fp32 dK/dV
+ * partial to the second, which adds its own (in that order) and writes dK/dV. This balancing is the library's own (the pages study one head
+ * on n SMs). Outputs:
  *   cta_offsets : int32[grid + 1]; CTA c runs pieces cta_offsets[c] .. cta_offsets[c + 1]
- *   pieces      : int32[3 * cap]; piece k = (head, first task, end task), the tasks being
- *                 indices into dash_sched_table's task table
+ *   pieces      : int32[5 * cap]; piece k = (head, first task, end task, part, split), the
+ *                 tasks being indices into dash_sched_table's task table; part 0 = whole
+ *                 KV tiles, 1 / 2 = first / second half of split tile `split` (0 for part 0)
  * Returns the number of pieces, or a negative dash_status_t value (heads or grid < 1, null
  * outputs, cap too small: -DASH_ERR_INVALID_ARG; an unsupported (mask, schedule, n): the
  * schedule's error).

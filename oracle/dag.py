@@ -56,7 +56,12 @@ Readings where the pages are silent (listed in the design notes as well):
   longest first, each to the SM with the least work dealt so far (the lower SM index on
   a tie; pieces of equal length in head-major chain order); every SM runs its pieces in
   the order dealt. Each KV tile still runs on one SM, in its chain's order. Equal-length
-  pieces (shift) are dealt exactly as round robin deals them.
+  pieces (shift) are dealt exactly as round robin deals them, except that when the last
+  partial round holds r units with 2 r <= P (and r <= MAX_SPLIT_TILES), each of those r
+  KV tiles is split into two halves (the first ceil(len / 2) tasks, then the rest): split
+  k's first half goes to SM k and its second half to SM r + k, after their whole units.
+  The second half's last reduction ends no earlier than the first half's last one (it
+  adds the first half's dK/dV partial before writing dK/dV).
 """
 
 from __future__ import annotations
@@ -78,6 +83,7 @@ __all__ = [
 ]
 
 SCHEDULES = ("ascending", "descending", "shift", "symmetric_shift")
+MAX_SPLIT_TILES = 256          # most KV tiles one balanced dealing splits in two
 
 
 def _keys(mask: str, i: int, n: int) -> list[int]:
@@ -166,27 +172,43 @@ def pieces(chain: list[tuple[int, int]]) -> list[list[tuple[int, int]]]:
 
 
 def deal(mask: str, sched: str, n: int, m: int, num_sms: int, balanced: bool = True):
-    """Per SM, the runs of tasks it executes, in order: lists of (head, [(i, j), ...]).
+    """Per SM, the runs of tasks it executes, in order: lists of (head, [(i, j), ...],
+    part, split) -- part 0 for whole KV tiles, 1 and 2 for the first and second half of
+    split tile ``split`` (0 where part is 0).
 
     Round robin deals the units (head, chain slot) head-major, unit u to SM u mod P.
     ``balanced`` deals as the library's kernels do (the module docstring): round robin
     unless the schedule orders dQ by arrival and the units overrun whole rounds of the
-    SMs, in which case the chains' KV-tile pieces go longest first to the least-loaded SM.
+    SMs, in which case the chains' KV-tile pieces go longest first to the least-loaded SM
+    (shift: its last partial round halved where there is room).
     """
     ch = chains(mask, sched, n)
     units = [(h, slot) for h in range(m) for slot in range(len(ch))]
-    per_sm: list[list[tuple[int, list[tuple[int, int]]]]] = [[] for _ in range(num_sms)]
+    per_sm: list[list[tuple[int, list[tuple[int, int]], int, int]]] = [
+        [] for _ in range(num_sms)]
     full_rounds, rest = divmod(len(units), num_sms)
     if (not balanced or sched in ("ascending", "descending") or rest == 0
             or full_rounds == 0):
         for u, (h, slot) in enumerate(units):
-            per_sm[u % num_sms].append((h, list(ch[slot])))
+            per_sm[u % num_sms].append((h, list(ch[slot]), 0, 0))
+        return per_sm
+    if (sched == "shift" and 2 * rest <= num_sms and rest <= MAX_SPLIT_TILES
+            and max(len(c) for c in ch) >= 2):
+        whole = len(units) - rest
+        for u in range(whole):
+            h, slot = units[u]
+            per_sm[u % num_sms].append((h, list(ch[slot]), 0, 0))
+        for k in range(rest):
+            h, slot = units[whole + k]
+            cut = (len(ch[slot]) + 1) // 2
+            per_sm[k].append((h, list(ch[slot][:cut]), 1, k))
+            per_sm[rest + k].append((h, list(ch[slot][cut:]), 2, k))
         return per_sm
     runs = [(h, run) for (h, slot) in units for run in pieces(ch[slot])]
     load = [0] * num_sms
     for k in sorted(range(len(runs)), key=lambda k: (-len(runs[k][1]), k)):
         sm = min(range(num_sms), key=lambda s: (load[s], s))
-        per_sm[sm].append(runs[k])
+        per_sm[sm].append((runs[k][0], runs[k][1], 0, 0))
         load[sm] += len(runs[k][1])
     return per_sm
 
@@ -203,7 +225,7 @@ def dealt_reduction_order(mask: str, sched: str, n: int, m: int, num_sms: int,
         (h, j): [] for h in range(m) for j in range(n)}
     for runs in deal(mask, sched, n, m, num_sms, balanced):
         place = 0                            # tasks this SM has run so far
-        for h, run in runs:
+        for h, run, _part, _split in runs:
             for (i, j) in run:
                 arrivals[(h, j)].append((place, i))
                 place += 1
@@ -220,20 +242,25 @@ def _orders(mask: str, sched: str, n: int, m: int, num_sms: int, dealt: bool):
 
 def _dealt_tasks(mask: str, sched: str, n: int, m: int, num_sms: int, dealt: bool):
     """Number the tasks SM by SM in run order: (per_sm task lists, tasks, sm_of_task,
-    index). ``dealt`` deals as the kernels do (balanced), else round robin."""
+    index, halves). ``dealt`` deals as the kernels do (balanced), else round robin;
+    halves lists (last task of a first half, last task of its second half)."""
     per_sm: list[list[int]] = [[] for _ in range(num_sms)]
     tasks: list[tuple[int, int, int]] = []
     sm_of_task: list[int] = []
     index: dict[tuple[int, int, int], int] = {}
+    last_of: dict[tuple[int, int], int] = {}
     for sm, runs in enumerate(deal(mask, sched, n, m, num_sms, balanced=dealt)):
-        for hd, run in runs:
+        for hd, run, part, split in runs:
             for (i, j) in run:
                 k = len(tasks)
                 tasks.append((hd, i, j))
                 sm_of_task.append(sm)
                 index[(hd, i, j)] = k
                 per_sm[sm].append(k)
-    return per_sm, tasks, sm_of_task, index
+            if part:
+                last_of[(split, part)] = len(tasks) - 1
+    halves = [(last_of[(s, 1)], last_of[(s, 2)]) for (s, p) in sorted(last_of) if p == 1]
+    return per_sm, tasks, sm_of_task, index, halves
 
 
 def schedule_dag(mask: str, sched: str, n: int, m: int, num_sms: int, c: float, r: float,
@@ -245,7 +272,7 @@ def schedule_dag(mask: str, sched: str, n: int, m: int, num_sms: int, c: float, 
     owns vertices 4k..4k+3.
     """
     order = _orders(mask, sched, n, m, num_sms, dealt)
-    per_sm, tasks, sm_of_task, index = _dealt_tasks(mask, sched, n, m, num_sms, dealt)
+    per_sm, tasks, sm_of_task, index, halves = _dealt_tasks(mask, sched, n, m, num_sms, dealt)
     edges: list[tuple[int, int, float]] = []
     for k in range(len(tasks)):
         cs, ce, rs, re = 4 * k, 4 * k + 1, 4 * k + 2, 4 * k + 3
@@ -256,6 +283,8 @@ def schedule_dag(mask: str, sched: str, n: int, m: int, num_sms: int, c: float, 
     for (h, j), kv in order.items():                 # fixed dQ reduction order
         for a, b in zip(kv, kv[1:]):
             edges.append((4 * index[(h, a, j)] + 3, 4 * index[(h, b, j)] + 2, 0.0))
+    for ka, kb in halves:                            # a second half adds its first's dK/dV
+        edges.append((4 * ka + 3, 4 * kb + 3, 0.0))
     return 4 * len(tasks), edges, tasks, sm_of_task
 
 
@@ -302,7 +331,7 @@ def schedule_dag_ex(mask: str, sched: str, n: int, m: int, num_sms: int, c: floa
     Same vertex numbering and return value as schedule_dag.
     """
     order = _orders(mask, sched, n, m, num_sms, dealt)
-    per_sm, tasks, sm_of_task, index = _dealt_tasks(mask, sched, n, m, num_sms, dealt)
+    per_sm, tasks, sm_of_task, index, halves = _dealt_tasks(mask, sched, n, m, num_sms, dealt)
     edges: list[tuple[int, int, float]] = []
     for k in range(len(tasks)):
         cs, ce, rs, re = 4 * k, 4 * k + 1, 4 * k + 2, 4 * k + 3
@@ -322,6 +351,8 @@ def schedule_dag_ex(mask: str, sched: str, n: int, m: int, num_sms: int, c: floa
             ka, kb = index[(hd, a, j)], index[(hd, b, j)]
             w = 0.0 if sm_of_task[ka] == sm_of_task[kb] else h
             edges.append((4 * ka + 3, 4 * kb + 2, w))
+    for ka, kb in halves:
+        edges.append((4 * ka + 3, 4 * kb + 3, 0.0))
     return 4 * len(tasks), edges, tasks, sm_of_task
 
 

@@ -20,8 +20,8 @@ __device__ __forceinline__ uint4 split3_bf16(float x) {
 
 // ---------------------------------------------------------------------------------
 // Preprocess: D = rowsum(dO * O) and -LSE*log2(e) per row (and, for head dimension 128,
-// the score-offset blocks of -LSE/scale and -D); clear the semaphores, the status header
-// and the fp32 dQ accumulator copies in use. A row of D elements is read
+// the score-offset blocks of -LSE/scale and -D); clear the semaphores, the split-tile
+// flags, the status header and the fp32 dQ accumulator copies in use. A row of D elements is read
 // by D/8 consecutive lanes of one warp, 8 bf16 (16 bytes) of dO and of O each; each lane
 // sums its 8 products in order, then a fixed shuffle tree over the row's lanes
 // (deterministic).
@@ -74,6 +74,7 @@ __global__ void bwd_preprocess_kernel(BwdParams p) {
     }
   }
   for (int e = tid; e < p.num_sems; e += nth) p.sems[e] = 0;
+  for (int e = tid; e < kSplitTiles * kSplitFlags; e += nth) p.split_flags[e] = 0;
   if (tid < (int)(kWsHeaderBytes / sizeof(int))) p.ws_header[tid] = 0;
   const long long nacc4 = (long long)p.chains * p.B * p.H * p.S * p.D / 4;   // copies in use
   float4* acc4 = reinterpret_cast<float4*>(p.dq_acc);

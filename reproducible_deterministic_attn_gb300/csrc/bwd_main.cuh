@@ -222,8 +222,10 @@ __device__ __forceinline__ void store_chunk8(uint32_t sTile, int r, int chunk, c
 }
 
 // kTrace: compiled with the optional wait-cycle trace (launched only while a trace buffer
-// is set); without it the trace code and its registers are absent.
-template <int D, bool kTrace>
+// is set); without it the trace code and its registers are absent. kSplit: compiled with
+// the epilogue of KV tiles split over two CTAs (launched only for a dealing that splits
+// one); without it the epilogue is the whole-tile one alone.
+template <int D, bool kTrace, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ TmaMaps maps) {
   using L = LTc<D>;
@@ -656,30 +658,84 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         t0 = trq.t0();
         const size_t g = ((size_t)b * p.S + (size_t)w.i * kTile + row) * rs + (size_t)h * D;
+        // A KV tile split over two CTAs: the first half stores its fp32 partials (dK
+        // unscaled) for the second, which adds them to its own before writing dK/dV.
+        const int part = kSplit ? (w.tag & 3) : 0;
+        float* half_acc = p.split_acc + ((size_t)(w.tag >> 2) * 2 * kTile + row) * D;
+        int* half_flag = p.split_flags + (w.tag >> 2) * kSplitFlags + quarter;
+        if (part == 2) {
+          int got = 1;
+          if (lane == 0) got = wait_at_least(half_flag, 1, p.ws_header, p.timeout_ns, w.bh, w.i) ? 1 : 0;
+          if (!__shfl_sync(0xffffffffu, got, 0)) {
+            if (lane == 0) *abort_flag = 1;
+            break;
+          }
+          __syncwarp();
+        }
+        if (part == 1) {
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          float a[32];
-          ptx::tmem_ld32(tmem + lane_addr + L::T_DV + c0, a);
-          uint4* dst4 = (uint4*)(p.dv + g + c0);
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            float a[32];
+            ptx::tmem_ld32(tmem + lane_addr + L::T_DK + c0, a);
+            float4* dk4 = (float4*)(half_acc + c0);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            dst4[k] = make_uint4(ptx::pack_bf16(a[8 * k], a[8 * k + 1]),
-                                 ptx::pack_bf16(a[8 * k + 2], a[8 * k + 3]),
-                                 ptx::pack_bf16(a[8 * k + 4], a[8 * k + 5]),
-                                 ptx::pack_bf16(a[8 * k + 6], a[8 * k + 7]));
-          ptx::tmem_ld32(tmem + lane_addr + L::T_DK + c0, a);
-          dst4 = (uint4*)(p.dk + g + c0);
-          const float sc = p.scale;
+            for (int k = 0; k < 8; ++k) dk4[k] = make_float4(a[4 * k], a[4 * k + 1], a[4 * k + 2], a[4 * k + 3]);
+            ptx::tmem_ld32(tmem + lane_addr + L::T_DV + c0, a);
+            float4* dv4 = (float4*)(half_acc + kTile * D + c0);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            dst4[k] = make_uint4(ptx::pack_bf16(sc * a[8 * k], sc * a[8 * k + 1]),
-                                 ptx::pack_bf16(sc * a[8 * k + 2], sc * a[8 * k + 3]),
-                                 ptx::pack_bf16(sc * a[8 * k + 4], sc * a[8 * k + 5]),
-                                 ptx::pack_bf16(sc * a[8 * k + 6], sc * a[8 * k + 7]));
+            for (int k = 0; k < 8; ++k) dv4[k] = make_float4(a[4 * k], a[4 * k + 1], a[4 * k + 2], a[4 * k + 3]);
+          }
+        } else {
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            float a[32];
+            ptx::tmem_ld32(tmem + lane_addr + L::T_DV + c0, a);
+            if (part == 2) {
+              const float4* hv4 = (const float4*)(half_acc + kTile * D + c0);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const float4 x = hv4[k];
+                a[4 * k] = x.x + a[4 * k];
+                a[4 * k + 1] = x.y + a[4 * k + 1];
+                a[4 * k + 2] = x.z + a[4 * k + 2];
+                a[4 * k + 3] = x.w + a[4 * k + 3];
+              }
+            }
+            uint4* dst4 = (uint4*)(p.dv + g + c0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              dst4[k] = make_uint4(ptx::pack_bf16(a[8 * k], a[8 * k + 1]),
+                                   ptx::pack_bf16(a[8 * k + 2], a[8 * k + 3]),
+                                   ptx::pack_bf16(a[8 * k + 4], a[8 * k + 5]),
+                                   ptx::pack_bf16(a[8 * k + 6], a[8 * k + 7]));
+            ptx::tmem_ld32(tmem + lane_addr + L::T_DK + c0, a);
+            if (part == 2) {
+              const float4* hk4 = (const float4*)(half_acc + c0);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const float4 x = hk4[k];
+                a[4 * k] = x.x + a[4 * k];
+                a[4 * k + 1] = x.y + a[4 * k + 1];
+                a[4 * k + 2] = x.z + a[4 * k + 2];
+                a[4 * k + 3] = x.w + a[4 * k + 3];
+              }
+            }
+            dst4 = (uint4*)(p.dk + g + c0);
+            const float sc = p.scale;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              dst4[k] = make_uint4(ptx::pack_bf16(sc * a[8 * k], sc * a[8 * k + 1]),
+                                   ptx::pack_bf16(sc * a[8 * k + 2], sc * a[8 * k + 3]),
+                                   ptx::pack_bf16(sc * a[8 * k + 4], sc * a[8 * k + 5]),
+                                   ptx::pack_bf16(sc * a[8 * k + 6], sc * a[8 * k + 7]));
+          }
         }
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bars + E_ACC_EMPTY);
+        if (lane == 0) {
+          ptx::mbar_arrive(bars + E_ACC_EMPTY);
+          if (part == 1) st_release_gpu(half_flag, 1);   // this quarter's partial is stored
+        }
         trq.add(K_RO_EPILOGUE, t0);
         ++tl;
       }

@@ -32,6 +32,10 @@ constexpr int kStatusSyncTimeout = 5;
 // maximum.
 constexpr int kDqChains = 2;
 constexpr int kSemStride = 32;
+// A KV tile split over two CTAs hands its first half's fp32 dK/dV partial to the second
+// half through the workspace, one ready flag per 32-row quarter (a read-out warp's rows).
+constexpr int kSplitTiles = 256;     // most split tiles in one launch
+constexpr int kSplitFlags = 4;       // flags per split tile
 constexpr int kStatusSmemLayout = 4;   // reported as DASH_ERR_CUDA: unusable shared-memory base
 
 struct FwdParams {
@@ -68,11 +72,14 @@ struct BwdParams {
   __nv_bfloat16* qx;
   __nv_bfloat16* dox;
   float* dq_acc;             // [B, H, S, D] fp32
+  float* split_acc;          // [split tile][2][128][D] fp32: first half's dK, dV partials
+  int* split_flags;          // [split tile][kSplitFlags]: 1 once that quarter is stored
   int* sems;                 // [B, H, n, kSemStride]: per 128-row dQ block, one per chain
   int num_sems;               // B * H * n * kSemStride
   int chains;                 // interleaved dQ chains, 1..kDqChains (deterministic mode)
   const int32_t* cta_off;    // dealing: CTA c runs pieces [cta_off[c], cta_off[c + 1])
-  const int32_t* pieces;     // dealing: 4 words per piece: head, first task, end task, 0
+  const int32_t* pieces;     // dealing: 4 words per piece: head, first task, end task,
+                             // (split tile << 2) | part (0 whole, 1 / 2 first / second half)
   const int32_t* tasks;      // schedule: (kv << 16) | q
   const int32_t* ord;        // schedule: ordinals, ord[bh * ord_stride + i * n + j]
   long long ord_stride;      // n * n when every head has its own order, else 0

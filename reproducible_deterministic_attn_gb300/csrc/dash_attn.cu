@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
 #include <map>
@@ -58,15 +59,16 @@ std::map<std::tuple<int, int, int, int, int>, bool> g_deadlock_free;    // (mask
 struct DealtTables {
   int32_t* ord = nullptr;       // [heads][n][n]; null: the schedule's own order
   int32_t* cta_off = nullptr;   // [grid + 1]
-  int32_t* pieces = nullptr;    // [pieces][4]: head, first task, end task, 0
+  int32_t* pieces = nullptr;    // [pieces][4]: head, first task, end task, split/part
 };
 std::map<std::tuple<int, int, int, int, int, int>, DealtTables> g_dealt;
 
-// The pieces in the kernel's 16-byte form: (head, first task, end task, 0).
+// The pieces in the kernel's 16-byte form: (head, first task, end task, (split << 2) | part).
 std::vector<int32_t> piece_words(const dash::Dealing& dl) {
   std::vector<int32_t> w;
   w.reserve(4 * dl.pieces.size());
-  for (const dash::Piece& pc : dl.pieces) w.insert(w.end(), {pc.head, pc.t_begin, pc.t_end, 0});
+  for (const dash::Piece& pc : dl.pieces)
+    w.insert(w.end(), {pc.head, pc.t_begin, pc.t_end, (pc.split << 2) | pc.part});
   return w;
 }
 // their host copies, (mask, sched, n, heads, grid): building one sorts every task of the
@@ -169,12 +171,18 @@ struct MainKernel {
 };
 // `traced`: the main kernel is compiled twice per head dimension, with and without its
 // wait-cycle trace; the traced build is launched only while a trace buffer is set.
-MainKernel main_kernel(int D, bool traced) {
+// `split`: the dealing splits a KV tile over two CTAs (its epilogue is compiled only into
+// those instances; the traced build always has it).
+MainKernel main_kernel(int D, bool traced, bool split) {
   using namespace dash::tc;
   if (D == 64)
-    return {traced ? (void*)bwd_main_kernel<64, true> : (void*)bwd_main_kernel<64, false>,
+    return {traced  ? (void*)bwd_main_kernel<64, true, true>
+            : split ? (void*)bwd_main_kernel<64, false, true>
+                    : (void*)bwd_main_kernel<64, false, false>,
             (size_t)LTc<64>::ALLOC, dash::kTile};
-  return {traced ? (void*)bwd_main_kernel<128, true> : (void*)bwd_main_kernel<128, false>,
+  return {traced  ? (void*)bwd_main_kernel<128, true, true>
+          : split ? (void*)bwd_main_kernel<128, false, true>
+                  : (void*)bwd_main_kernel<128, false, false>,
           (size_t)LTc<128>::ALLOC, dash::kTile};
 }
 
@@ -287,8 +295,10 @@ bool map_rows_k(CUtensorMap* m, const void* ptr, int rows, int K, int box_rows) 
 }
 
 struct WsLayout {
-  size_t dsum, nlse2, qx, dox, dq_acc, sems, total;
+  size_t dsum, nlse2, qx, dox, dq_acc, sems, split_flags, split_acc, total;
 };
+
+static_assert(dash::kSplitTiles == dash::kMaxSplitTiles, "split tiles: one bound");
 
 WsLayout ws_layout(int B, int S, int H, int D) {
   WsLayout w;
@@ -300,8 +310,13 @@ WsLayout ws_layout(int B, int S, int H, int D) {
   w.dox = round_up(w.qx + rows * 32, 256);
   w.dq_acc = round_up(w.dox + rows * 32, 256);
   w.sems = round_up(w.dq_acc + dash::kDqChains * rows * D * sizeof(float), 256);   // k copies
-  w.total = round_up(w.sems + (size_t)B * H * (S / dash::kTile) * dash::kSemStride * sizeof(int),
-                     256);
+  w.split_flags = round_up(
+      w.sems + (size_t)B * H * (S / dash::kTile) * dash::kSemStride * sizeof(int), 256);
+  // split KV tiles: only a grid's last partial round, with room for two halves per tile,
+  // so fewer than half the units (B * H * S / 128 bounds them for every schedule)
+  const size_t splits = std::min<size_t>((size_t)B * H * (S / dash::kTile) / 2, dash::kSplitTiles);
+  w.split_acc = round_up(w.split_flags + dash::kSplitTiles * dash::kSplitFlags * sizeof(int), 256);
+  w.total = round_up(w.split_acc + splits * 2 * dash::kTile * D * sizeof(float), 256);
   return w;
 }
 
@@ -450,6 +465,8 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
   p.dox = (__nv_bfloat16*)(ws + wl.dox);
   p.dq_acc = (float*)(ws + wl.dq_acc);
   p.sems = (int*)(ws + wl.sems);
+  p.split_flags = (int*)(ws + wl.split_flags);
+  p.split_acc = (float*)(ws + wl.split_acc);
   p.tasks = tb.tasks;
   p.ord = tb.ord;
   p.cnt = tb.cnt;
@@ -477,7 +494,12 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
     return DASH_ERR_CUDA;
   }
   dash::tc::TmaMaps maps;
-  const MainKernel mk = main_kernel(D, g_trace != nullptr);
+  int sms = 0;
+  DASH_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  int grid = sms;                      // one CTA per SM (512 TMEM columns each)
+  if (grid > units) grid = units;
+  const MainKernel mk =
+      main_kernel(D, g_trace != nullptr, dash::split_tiles(schedule, n, units, grid) > 0);
   const int br = mk.br;
   if (!map_bshd(&maps.q, q, B, S, H, D, br) || !map_bshd(&maps.dO, dO, B, S, H, D, br) ||
       !map_bshd(&maps.k, k, B, S, H, D, dash::kTile) ||
@@ -493,15 +515,12 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
     return DASH_ERR_CUDA;
   }
   DASH_CUDA(cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-  int per_sm = 0, sms = 0;
+  int per_sm = 0;
   DASH_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, threads, smem));
-  DASH_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   if (per_sm < 1) {
     g_last_error = "backward kernel does not fit on one SM";
     return DASH_ERR_CUDA;
   }
-  int grid = sms;                      // one CTA per SM (512 TMEM columns each)
-  if (grid > units) grid = units;
   if (deterministic && !deadlock_free(mask, schedule, n, B * H, grid))
     return DASH_ERR_DEADLOCK_RISK;
   st = set_dealing(dev, mask, schedule, n, B * H, grid, tb, &p);
@@ -621,9 +640,9 @@ int dash_sched_deal(int mask, int schedule, int n, int heads, int grid, int32_t*
   if ((size_t)cap < dl.pieces.size()) return -DASH_ERR_INVALID_ARG;
   std::memcpy(cta_offsets, dl.cta_off.data(), dl.cta_off.size() * sizeof(int32_t));
   for (size_t k = 0; k < dl.pieces.size(); ++k) {
-    pieces[3 * k] = dl.pieces[k].head;
-    pieces[3 * k + 1] = dl.pieces[k].t_begin;
-    pieces[3 * k + 2] = dl.pieces[k].t_end;
+    const dash::Piece& pc = dl.pieces[k];
+    const int32_t w[5] = {pc.head, pc.t_begin, pc.t_end, pc.part, pc.split};
+    std::memcpy(pieces + 5 * k, w, sizeof(w));
   }
   return (int)dl.pieces.size();
 }
@@ -908,6 +927,8 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
   p.dox = (__nv_bfloat16*)(ws + wl.dox);
   p.dq_acc = (float*)(ws + wl.dq_acc);
   p.sems = (int*)(ws + wl.sems);
+  p.split_flags = (int*)(ws + wl.split_flags);
+  p.split_acc = (float*)(ws + wl.split_acc);
   p.cta_off = (const int32_t*)(ws + t_off);
   p.pieces = (const int32_t*)(ws + t_off + tb->piece_off);
   p.tasks = (const int32_t*)(ws + t_off + tb->task_off);
@@ -937,7 +958,7 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
     return DASH_ERR_CUDA;
   }
   dash::tc::TmaMaps maps;
-  const MainKernel mk = main_kernel(D, false);
+  const MainKernel mk = main_kernel(D, false, dash::split_tiles(schedule, n, units, grid) > 0);
   const int br = mk.br;
   if (!map_bshd(&maps.q, q, B, S, H, D, br) || !map_bshd(&maps.dO, dO, B, S, H, D, br) ||
       !map_bshd(&maps.k, k, B, S, H, D, dash::kTile) ||

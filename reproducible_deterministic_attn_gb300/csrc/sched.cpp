@@ -106,13 +106,36 @@ void deal(const Schedule& sc, int heads, int grid, Dealing* out) {
   out->cta_off.assign(grid + 1, 0);
   out->pieces.clear();
   const long long units = (long long)heads * sc.num_slots;
+  const long long rem = units % grid;
   std::vector<std::vector<Piece>> per_cta(grid);
-  if (!arrival_ordered(sc) || units % grid == 0 || units < grid) {
+  auto unit_piece = [&](long long u) {
+    const int slot = (int)(u % sc.num_slots);
+    Piece pc;
+    pc.head = (int32_t)(u / sc.num_slots);
+    pc.t_begin = sc.slot_off[slot];
+    pc.t_end = sc.slot_off[slot + 1];
+    return pc;
+  };
+  if (!arrival_ordered(sc) || rem == 0 || units < grid) {
     // round robin: unit u = (head u / slots, slot u % slots) to CTA u % grid
-    for (long long u = 0; u < units; ++u) {
-      const int slot = (int)(u % sc.num_slots);
-      per_cta[u % grid].push_back(
-          {(int32_t)(u / sc.num_slots), sc.slot_off[slot], sc.slot_off[slot + 1]});
+    for (long long u = 0; u < units; ++u) per_cta[u % grid].push_back(unit_piece(u));
+  } else if (sc.sched == SCHED_SHIFT) {
+    // one KV tile per unit, all of one length: round robin, with the last partial round's
+    // tiles halved over two CTAs where there is room
+    // (Holding back the highest slots of every head instead, so that the halves spread
+    // over the heads, measured slower in deterministic mode on GB300: it lengthens the
+    // turn waits of the earlier rounds more than the last head's denser dQ order costs.)
+    const long long splits = split_tiles(sc.sched, sc.n, units, grid);
+    const long long whole = units - splits;
+    for (long long u = 0; u < whole; ++u) per_cta[u % grid].push_back(unit_piece(u));
+    for (long long k = 0; k < splits; ++k) {
+      Piece a = unit_piece(whole + k), b = a;
+      a.t_end = b.t_begin = a.t_begin + (a.t_end - a.t_begin + 1) / 2;
+      a.part = 1;
+      b.part = 2;
+      a.split = b.split = (int32_t)k;
+      per_cta[k].push_back(a);
+      per_cta[splits + k].push_back(b);
     }
   } else {
     // the chains cut where the KV tile changes, in head-major chain order
@@ -228,6 +251,15 @@ bool simulate_ex(const Schedule& sc, int heads, int num_sms, double c, double r,
           if (rend[pk] < 0) break;                              // predecessor not done
           pred_ready = rend[pk] + (rsm[pk] == sm ? 0.0 : h);
         }
+        // the second half of a split tile ends after its first half (which ends at the
+        // task before it in the chain): it adds the first half's dK/dV partial
+        double half_ready = 0.0;
+        if (pc.part == 2 && task_pos[sm] == pc.t_end - 1) {
+          const int32_t ta = sc.tasks[pc.t_begin - 1];
+          const size_t ak = ((size_t)head * n + (ta >> 16)) * n + (ta & 0xffff);
+          if (rend[ak] < 0) break;
+          half_ready = rend[ak];
+        }
         double c_end, r_end;
         if (overlapped) {
           c_end = std::max(c_last[sm], r_prev[sm]) + c;
@@ -236,6 +268,7 @@ bool simulate_ex(const Schedule& sc, int heads, int num_sms, double c, double r,
           c_end = r_last[sm] + c;
           r_end = std::max(c_end, pred_ready) + r;
         }
+        r_end = std::max(r_end, half_ready);
         const size_t k = ((size_t)head * n + i) * n + j;
         rend[k] = r_end;
         rsm[k] = sm;

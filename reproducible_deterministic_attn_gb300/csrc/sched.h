@@ -32,9 +32,27 @@ inline bool arrival_ordered(const Schedule& sc) {
 }
 
 // A run of one head's chain: tasks[t_begin, t_end) of the schedule, for head `head`.
+// part 0 covers whole KV tiles; part 1 and 2 are the first and second half of one KV
+// tile split over two CTAs (split tile `split`): the first half hands its fp32 dK/dV
+// partial to the second, which adds its own and writes dK/dV.
 struct Piece {
   int32_t head, t_begin, t_end;
+  int32_t part = 0, split = 0;
 };
+
+// Most KV tiles one grid splits (bounds the workspace of the split partials).
+constexpr int kMaxSplitTiles = 256;
+
+// How many KV tiles deal() splits over two CTAs for `units` units of schedule `sched` (n
+// KV tiles per head) on `grid` CTAs: shift's last partial round, r = units mod grid
+// units, when 2 r <= grid (and r <= kMaxSplitTiles); otherwise none.
+inline long long split_tiles(int sched, int n, long long units, int grid) {
+  const long long rem = units % grid;
+  if (sched != SCHED_SHIFT || units < grid || rem == 0 || 2 * rem > grid ||
+      rem > kMaxSplitTiles || n < 2)
+    return 0;
+  return rem;
+}
 
 // The work of each persistent CTA, in run order: CTA c runs
 // pieces[cta_off[c] .. cta_off[c + 1]).
@@ -51,7 +69,12 @@ struct Dealing {
 // and the pieces dealt longest first (equal lengths in head-major chain order), each to
 // the CTA with the least work dealt so far (the lower index on a tie); a CTA runs its
 // pieces in the order dealt. Every KV tile still runs whole on one CTA, in chain order.
-// Pieces of equal length (shift) are dealt exactly as round robin deals them.
+// Pieces of equal length (shift) are dealt exactly as round robin deals them; there,
+// when the last partial round has r units and 2 r <= grid (r <= kMaxSplitTiles), each of
+// those r KV tiles is instead split in two halves (the first ceil(len / 2) tasks, then
+// the rest): split k's first half runs on CTA k and its second half on CTA r + k, after
+// their whole units, so the busiest CTA runs half a unit less and no first half ever
+// waits behind a second half.
 void deal(const Schedule& sc, int heads, int grid, Dealing* out);
 
 // The dQ order the kernels follow when `heads` heads' chains are dealt onto `grid`

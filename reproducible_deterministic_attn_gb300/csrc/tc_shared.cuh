@@ -29,6 +29,7 @@ __device__ __forceinline__ uint32_t sw_chunk(int row, int chunk, int rows) {
 struct Walk {
   const BwdParams& p;
   int k, k_end, t, t_end, bh, i, j;
+  int tag;                    // this piece's (split tile << 2) | part
   int32_t prev_tk, cur_tk, nxt_tk, nxt2_tk;
   bool first_of_tile, last_of_tile;
   __device__ Walk(const BwdParams& pp)
@@ -46,6 +47,7 @@ struct Walk {
         bh = pc.x;
         t = pc.y;
         t_end = pc.z;
+        tag = pc.w;
       } while (t >= t_end);
       prev_tk = -1;
       cur_tk = task_at(t);

@@ -227,18 +227,19 @@ def dash_sched_table(mask: int, schedule: int, n: int):
 
 
 def dash_sched_deal(mask: int, schedule: int, n: int, heads: int, grid: int):
-    """Each CTA's work in run order: per CTA a list of (head, [(kv, q), ...]) pieces."""
+    """Each CTA's work in run order: per CTA a list of (head, [(kv, q), ...], part, split)
+    pieces (part 0: whole KV tiles; 1 / 2: first / second half of split tile `split`)."""
     _, pairs, _ = dash_sched_table(mask, schedule, n)
     slots = dash_sched_num_slots(mask, schedule, n)
     cap = 2 * heads * slots              # a chain has at most two KV tiles
     off = (ctypes.c_int32 * (grid + 1))()
-    pieces = (ctypes.c_int32 * (3 * cap))()
+    pieces = (ctypes.c_int32 * (5 * cap))()
     cnt = load().dash_sched_deal(int(mask), int(schedule), int(n), int(heads), int(grid),
                                  off, pieces, cap)
     if cnt < 0:
         raise DashError(-cnt, "dash_sched_deal")
-    return [[(pieces[3 * k], pairs[pieces[3 * k + 1]:pieces[3 * k + 2]])
-             for k in range(off[c], off[c + 1])] for c in range(grid)]
+    return [[(pieces[5 * k], pairs[pieces[5 * k + 1]:pieces[5 * k + 2]], pieces[5 * k + 3],
+              pieces[5 * k + 4]) for k in range(off[c], off[c + 1])] for c in range(grid)]
 
 
 def dash_sched_dealt_table(mask: int, schedule: int, n: int, heads: int, grid: int):

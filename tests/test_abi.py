@@ -47,10 +47,13 @@ def test_workspace_size(lib):
     B, S, H, D = 2, 256, 3, 64
     ws = da.dash_attn_bwd_workspace_size(B, S, H, D)
     # header, D and -LSE*log2e rows, the two score-offset block arrays (32 bytes per row
-    # each), two fp32 dQ accumulator copies, one 128-byte line of semaphores per dQ block
+    # each), two fp32 dQ accumulator copies, one 128-byte line of semaphores per dQ block,
+    # 256 x 4 split-tile flags and the split tiles' fp32 dK/dV partials (at most half the
+    # B * H * S / 128 KV tiles, at most 256)
+    splits = min(B * H * (S // 128) // 2, 256)
     need = (256 + 2 * B * H * S * 4 + 2 * B * H * S * 32 + 2 * B * H * S * D * 4
-            + B * H * (S // 128) * 128)
-    assert need <= ws <= need + 6 * 256 and ws % 256 == 0
+            + B * H * (S // 128) * 128 + 256 * 4 * 4 + splits * 2 * 128 * D * 4)
+    assert need <= ws <= need + 8 * 256 and ws % 256 == 0
     assert da.dash_attn_bwd_workspace_size(1, 100, 1, 64) == 0      # S not a multiple of 128
     assert da.dash_attn_bwd_workspace_size(1, 128, 1, 96) == 0      # unsupported head dim
 

@@ -309,7 +309,7 @@ def test_balanced_worked_example_deal_and_makespan():
         runs = []
         for piece in want.split(";"):
             h, kv, *qs = (int(x) for x in piece.split())
-            runs.append((h, [(kv, q) for q in qs]))
+            runs.append((h, [(kv, q) for q in qs], 0, 0))
         assert got == runs, (sm, got)
     rows = _dealt_rows("BALANCED")
     assert len(rows) == 1
@@ -319,7 +319,7 @@ def test_balanced_worked_example_deal_and_makespan():
         assert res["sm_end"] == [float(x) for x in ends.split()]
         # round robin gives two SMs two whole units (10 tasks, makespan 30)
         rr = deal(mask, sched, int(n), int(m), int(sms), balanced=False)
-        assert max(sum(len(run) for _, run in runs) for runs in rr) == 10
+        assert max(sum(len(run) for _, run, _, _ in runs) for runs in rr) == 10
 
 
 def test_balanced_deal_invariants():
@@ -334,32 +334,53 @@ def test_balanced_deal_invariants():
                     per_sm = deal(mask, sched, n, m, sms)
                     rr = deal(mask, sched, n, m, sms, balanced=False)
                     units = m * len(ch)
-                    if (sched in ("ascending", "descending") or units % sms == 0
-                            or units < sms or sched == "shift"):
+                    rest = units % sms
+                    halved = sched == "shift" and units > sms and 0 < 2 * rest <= sms
+                    if (sched in ("ascending", "descending") or rest == 0
+                            or units < sms or (sched == "shift" and not halved)):
                         # fixed-order schedules, whole rounds, a single partial round and
-                        # equal-length chains: exactly round robin
+                        # equal-length chains without room to halve: exactly round robin
                         assert per_sm == rr, (mask, sched, n, m, sms)
                         continue
                     seen = {}
+                    halves = {}
                     for sm, runs in enumerate(per_sm):
-                        for h, run in runs:
+                        for h, run, part, split in runs:
                             assert len({i for i, _ in run}) == 1       # one KV tile per piece
                             i = run[0][0]
-                            assert (h, i) not in seen                  # a KV tile on one SM
-                            seen[(h, i)] = sm
                             chain = next(c for c in ch if (i, run[0][1]) in c)
                             k = chain.index(run[0])                    # contiguous, in order
                             assert chain[k:k + len(run)] == run
-                    tasks = sorted((h, i, j) for runs in per_sm for h, run in runs
+                            if part:
+                                assert halved
+                                halves.setdefault(split, {})[part] = (sm, h, run)
+                                continue
+                            assert (h, i) not in seen                  # a KV tile on one SM
+                            seen[(h, i)] = sm
+                    if halved:
+                        # split k: first ceil(len / 2) tasks on SM k, the rest on SM rest + k,
+                        # each the last piece of its SM
+                        assert sorted(halves) == list(range(rest))
+                        for k, pr in halves.items():
+                            (sa, ha, ra), (sb, hb, rb) = pr[1], pr[2]
+                            assert (sa, sb, ha) == (k, rest + k, hb)
+                            assert len(ra) == (len(ra) + len(rb) + 1) // 2
+                            assert per_sm[sa][-1][2] == 1 and per_sm[sb][-1][2] == 2
+                    tasks = sorted((h, i, j) for runs in per_sm for h, run, _, _ in runs
                                    for (i, j) in run)
                     assert tasks == sorted((h, i, j) for h in range(m) for c in ch
                                            for (i, j) in c)
-                    # greedy list scheduling: the last piece dealt to the busiest SM started
-                    # on the least load, at most the mean of the rest
-                    loads = [sum(len(run) for _, run in runs) for runs in per_sm]
+                    loads = [sum(len(run) for _, run, _, _ in runs) for runs in per_sm]
                     total = sum(loads)
-                    assert max(loads) <= total / sms + longest * (1 - 1 / sms) + 1e-9
-                    assert max(loads) <= max(sum(len(run) for _, run in runs) for runs in rr)
+                    if halved:
+                        # whole rounds plus at most one half of a unit
+                        assert max(loads) == (units // sms) * longest + (longest + 1) // 2
+                    else:
+                        # greedy list scheduling: the last piece dealt to the busiest SM
+                        # started on the least load, at most the mean of the rest
+                        assert max(loads) <= total / sms + longest * (1 - 1 / sms) + 1e-9
+                    assert max(loads) <= max(sum(len(run) for _, run, _, _ in runs)
+                                             for runs in rr)
 
 
 def test_dealt_equals_the_pages_order_when_heads_start_together():

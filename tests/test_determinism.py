@@ -58,6 +58,8 @@ HEADLINE = [
     ((1, 16384, 32, 128), True, "descending", 2),
     ((2, 2048, 8, 128), True, "symmetric_shift", 1),
     ((2, 2048, 8, 128), True, "descending", 1),
+    # full shift, 160 units on 152 CTAs: the last partial round's KV tiles split in two
+    ((1, 2048, 10, 128), False, "shift", 2),
 ]
 
 

@@ -6,6 +6,8 @@ sampled slices. Tolerance: max |gpu - ref| <= 2e-2 * max |ref| per tensor; LSE 1
 import pytest
 import torch
 
+import reproducible_deterministic_attn_gb300 as da
+
 from tests._lib import ensure_built, has_gpu
 from tests.gpu_common import assert_within, check_against_oracle, run_case
 
@@ -42,6 +44,23 @@ def test_small_shapes(shape, mask, sched, det):
     causal = mask == "causal"
     res = run_case(B, S, H, D, causal, sched, det, seed=1)
     assert_within(check_against_oracle(res, causal))
+
+
+# Full mask, shift, more KV tiles than CTAs: 160 units on a 152-SM grid leave 8 in the
+# last partial round, and each of those tiles is split over two CTAs whose dK/dV
+# partials are combined (first half's fp32 partial + second half's, then bf16). Every
+# head is checked.
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("det", [1, 0, 2])
+def test_split_tiles_full_shift(D, det):
+    B, S, H = 1, 2048, 10
+    units = B * H * (S // 128)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    dealt = da.dash_sched_deal(0, da.SCHED_SHIFT, S // 128, B * H, min(sms, units))
+    if not any(pc[2] == 1 for runs in dealt for pc in runs):
+        pytest.skip("this GPU's grid splits no KV tile at this shape")
+    res = run_case(B, S, H, D, False, "shift", det, seed=3)
+    assert_within(check_against_oracle(res, False))
 
 
 def test_config1_full_256_d64():

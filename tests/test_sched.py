@@ -70,24 +70,26 @@ def test_deal_matches_oracle(seed):
         m, grid = rng.randint(1, 6), rng.randint(1, 3 * n + 2)
         got = da.dash_sched_deal(mask, sched, n, m, grid)
         want = dag.deal(MASKS[mask], NAMES[sched], n, m, grid)
-        assert got == [[(h, list(run)) for h, run in runs] for runs in want], (mask, sched, n, m, grid)
+        assert got == want, (mask, sched, n, m, grid)
 
 
 def test_deal_at_the_kernel_sizes():
     # 152 CTAs. Causal 4x16 heads of n = 16 (512 units of 17 tasks) and 1x32 heads of
     # n = 128 (2048 units of 129) overrun whole rounds: pieces dealt longest first bring
     # the busiest CTA to the mean (57.3 and 1738.1 tasks) instead of a whole unit above
-    # it. Full 2x16 heads of n = 64: equal units, dealt round robin.
-    for mask, sched, n, heads, rr_max, max_load in [(1, 3, 16, 64, 68, 58),
-                                                   (1, 3, 128, 32, 1806, 1739),
-                                                   (0, 2, 64, 32, 14 * 64, 14 * 64)]:
+    # it. Full 2x16 heads of n = 64 (2048 units of 64, 72 in the last round): those 72 KV
+    # tiles are halved over 144 CTAs, so the busiest runs 13.5 units (mean 13.47).
+    for mask, sched, n, heads, rr_max, max_load, splits in [(1, 3, 16, 64, 68, 58, 0),
+                                                           (1, 3, 128, 32, 1806, 1739, 0),
+                                                           (0, 2, 64, 32, 896, 864, 72)]:
         got = da.dash_sched_deal(mask, sched, n, heads, 152)
         want = dag.deal(MASKS[mask], NAMES[sched], n, heads, 152)
-        assert got == [[(h, list(run)) for h, run in runs] for runs in want]
-        loads = [sum(len(run) for _, run in runs) for runs in got]
+        assert got == want
+        loads = [sum(len(run) for _, run, _, _ in runs) for runs in got]
         assert max(loads) == max_load
+        assert sum(1 for runs in got for pc in runs if pc[2] == 1) == splits
         rr = dag.deal(MASKS[mask], NAMES[sched], n, heads, 152, balanced=False)
-        assert max(sum(len(run) for _, run in runs) for runs in rr) == rr_max
+        assert max(sum(len(run) for _, run, _, _ in runs) for runs in rr) == rr_max
     with pytest.raises(da.DashError):
         da.dash_sched_deal(1, 3, 8, 0, 4)
     with pytest.raises(da.DashError):
