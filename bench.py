@@ -45,6 +45,9 @@ WORKLOADS = {
     "causal-1x16384x32x128": dict(mask="causal", B=1, S=16384, H=32, D=128),
     # smaller full-mask case for kernel profiles (inputs still larger than L2)
     "full-2x4096x16x128": dict(mask="full", B=2, S=4096, H=16, D=128),
+    # the same with a last partial round of 16 units on 152 CTAs, whose KV tiles the
+    # dealing splits over two CTAs (the kernel instance with the split-tile epilogue)
+    "full-3x4096x16x128": dict(mask="full", B=3, S=4096, H=16, D=128),
     # long full-mask sequence: where the pages see Shift fall behind the baseline order
     "full-1x16384x16x128": dict(mask="full", B=1, S=16384, H=16, D=128),
 }
@@ -271,9 +274,11 @@ def traffic_from_profile(w, sched):
     return float(ent) if ent is not None else None
 
 
-# the sources the main kernel is compiled from (the file and its includes):
-# the traffic record stays valid while none of them changes
-MAIN_KERNEL_SOURCES = ("common.cuh", "tc_shared.cuh", "bwd_main.cuh", "tc_ptx.cuh")
+# the sources the main kernel is compiled from (the file and its includes) and the
+# dealing that spreads its work over the CTAs: the traffic record stays valid while none
+# of them changes
+MAIN_KERNEL_SOURCES = ("common.cuh", "tc_shared.cuh", "bwd_main.cuh", "tc_ptx.cuh",
+                       "sched.h", "sched.cpp")
 
 
 def kernel_source_hash():
