@@ -309,7 +309,7 @@ def run_gpu(args, w, rank, world, local_rank):
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         choice, _ = da.dash_sched_select(mask, S // 128, B * H, sms, SELECT_COSTS["c"],
                                          SELECT_COSTS["r"], SELECT_COSTS["h"],
-                                         SELECT_COSTS["overlapped"])
+                                         SELECT_COSTS["overlapped"], head_dim=D)
         args.schedule = {v: k for k, v in da.SCHEDULES.items()}[choice]
         selected_by = "dash_sched_select, costs " + json.dumps(SELECT_COSTS)
     sched = da.SCHEDULES[args.schedule]

@@ -254,33 +254,37 @@ int dash_sched_table(int mask, int schedule, int n, int32_t* slot_offsets, int32
                      int cap, int32_t* ordinals);
 
 /*
- * How dash_attn_bwd spreads `heads` (= B * H) heads' chains over `grid` persistent CTAs.
- * Round robin -- unit u (head u / num_slots, chain slot u % num_slots) whole to CTA
- * u % grid -- unless the schedule orders dQ by arrival (SHIFT, SYMMETRIC_SHIFT) and the
- * units overrun whole rounds of the grid (more units than CTAs, not a multiple of them).
- * Then every chain is cut where its KV tile changes and the pieces are dealt longest
- * first (equal lengths in head-major chain order), each to the CTA with the least work
- * dealt so far (the lower index on a tie); each CTA runs its pieces in the order dealt.
- * Shift's units are single KV tiles of one length, dealt round robin all the same; there,
- * when the last partial round holds r units with 2 r <= grid (r <= 256), each of those r
- * KV tiles is split in two halves (the first ceil(len / 2) tasks, then the rest): split
- * k's first half runs on CTA k and its second half on CTA r + k, after their whole units. The first half hands its fp32 dK/dV
- * partial to the second, which adds its own (in that order) and writes dK/dV. This balancing is the library's own (the pages study one head
- * on n SMs). Outputs:
+ * How dash_attn_bwd spreads `heads` (= B * H) heads' chains over `grid` persistent CTAs
+ * at head dimension `head_dim` (64 or 128). Round robin -- unit u (head u / num_slots,
+ * chain slot u % num_slots) whole to CTA u % grid -- unless the schedule orders dQ by
+ * arrival (SHIFT, SYMMETRIC_SHIFT) and the units overrun whole rounds of the grid (more
+ * units than CTAs, not a multiple of them). Then chains are cut where their KV tile
+ * changes and the pieces dealt longest first (equal lengths in head-major chain order),
+ * each to the CTA with the least work dealt so far (the lower index on a tie); each CTA
+ * runs its pieces in the order dealt. At head dimension 64 every unit is cut this way; at
+ * 128 the first q - 1 of the q whole rounds stay round robin (whole units, keeping each
+ * head's chains on concurrent CTAs and its tiles in L2) and only the units after them are
+ * cut. Shift's units are single KV tiles of one length, dealt round robin all the same;
+ * there, when the last partial round holds r units with 2 r <= grid (r <= 256), each of
+ * those r KV tiles is split in two halves (the first ceil(len / 2) tasks, then the rest):
+ * split k's first half runs on CTA k and its second half on CTA r + k, after their whole
+ * units. The first half hands its fp32 dK/dV partial to the second, which adds its own (in
+ * that order) and writes dK/dV. This balancing is the library's own (the pages study one
+ * head on n SMs). Outputs:
  *   cta_offsets : int32[grid + 1]; CTA c runs pieces cta_offsets[c] .. cta_offsets[c + 1]
  *   pieces      : int32[5 * cap]; piece k = (head, first task, end task, part, split), the
  *                 tasks being indices into dash_sched_table's task table; part 0 = whole
  *                 KV tiles, 1 / 2 = first / second half of split tile `split` (0 for part 0)
- * Returns the number of pieces, or a negative dash_status_t value (heads or grid < 1, null
- * outputs, cap too small: -DASH_ERR_INVALID_ARG; an unsupported (mask, schedule, n): the
- * schedule's error).
+ * Returns the number of pieces, or a negative dash_status_t value (heads or grid < 1,
+ * head_dim not 64 or 128, null outputs, cap too small: -DASH_ERR_INVALID_ARG; an
+ * unsupported (mask, schedule, n): the schedule's error).
  */
-int dash_sched_deal(int mask, int schedule, int n, int heads, int grid, int32_t* cta_offsets,
-                    int32_t* pieces, int cap);
+int dash_sched_deal(int mask, int schedule, int n, int heads, int grid, int head_dim,
+                    int32_t* cta_offsets, int32_t* pieces, int cap);
 
 /*
- * The dQ orders dash_attn_bwd follows when `heads` (= B * H) heads' chains are dealt onto
- * `grid` persistent CTAs as dash_sched_deal describes:
+ * The dQ orders dash_attn_bwd follows at head dimension `head_dim` when `heads` (= B * H)
+ * heads' chains are dealt onto `grid` persistent CTAs as dash_sched_deal describes:
  *   ordinals : int32[heads * n * n]; ordinals[(h * n + i) * n + j] = position of KV_i's
  *              partial in head h's dQ_j order, -1 where the mask removes the task.
  * ASCENDING and DESCENDING: ascending KV index in every head. SHIFT and SYMMETRIC_SHIFT
@@ -289,22 +293,26 @@ int dash_sched_deal(int mask, int schedule, int n, int heads, int grid, int32_t*
  * piece -- the lower KV index first on a tie. With whole heads per round of the grid this
  * is dash_sched_table's order; when the grid splits a head over two rounds, the chains run
  * in the earlier round come first, so no partial waits for a chain that has not started.
- * Returns DASH_OK, DASH_ERR_INVALID_ARG (heads or grid < 1, null ordinals), or the
- * schedule's error for an unsupported (mask, schedule, n).
+ * Returns DASH_OK, DASH_ERR_INVALID_ARG (heads or grid < 1, head_dim not 64 or 128, null
+ * ordinals), or the schedule's error for an unsupported (mask, schedule, n).
  */
 dash_status_t dash_sched_dealt_table(int mask, int schedule, int n, int heads, int grid,
-                                     int32_t* ordinals);
+                                     int head_dim, int32_t* ordinals);
 
 /*
  * Critical path of the compute/reduce DAG (Pith review, "What carries the argument"):
  * every task is a compute phase of cost c then a reduce phase of cost r; one SM runs its
  * tasks back to back; reductions into one dQ block follow the orders the kernel uses on a
- * grid of num_sms CTAs (dash_sched_dealt_table(mask, schedule, n, heads, num_sms)). `heads`
- * heads' chains are dealt onto `num_sms` SMs as the kernel deals them (dash_sched_deal). Writes the makespan and, if sm_end is not NULL, each SM's finish time
- * (double[num_sms]). Returns DASH_ERR_DEADLOCK_RISK when the waits form a cycle.
+ * grid of num_sms CTAs (dash_sched_dealt_table(mask, schedule, n, heads, num_sms,
+ * head_dim)). `heads` heads' chains are dealt onto `num_sms` SMs as the kernel deals them
+ * at head dimension `head_dim` (dash_sched_deal); the second half of a split KV tile ends
+ * no earlier than its first half. Writes the makespan and, if sm_end is not NULL, each SM's
+ * finish time (double[num_sms]). Returns DASH_ERR_DEADLOCK_RISK when the waits form a
+ * cycle, DASH_ERR_INVALID_ARG for bad arguments (head_dim not 64 or 128).
  */
 dash_status_t dash_sched_simulate(int mask, int schedule, int n, int heads, int num_sms,
-                                  double c, double r, double* makespan, double* sm_end);
+                                  int head_dim, double c, double r, double* makespan,
+                                  double* sm_end);
 
 /*
  * The same critical path with synchronisation cost (the Pith review's "Where Pith is
@@ -322,22 +330,22 @@ dash_status_t dash_sched_simulate(int mask, int schedule, int n, int heads, int 
  * not in {0, 1}.
  */
 dash_status_t dash_sched_simulate_ex(int mask, int schedule, int n, int heads, int num_sms,
-                                     double c, double r, double h, int overlapped,
+                                     int head_dim, double c, double r, double h, int overlapped,
                                      double* makespan, double* sm_end);
 
 /*
  * Run-time schedule selector: among the schedules defined for `mask` and n (ascending and
  * descending always; shift for the full mask; symmetric shift for the causal mask and even
  * n) whose waits are acyclic on `num_sms` SMs, the one with the smallest
- * dash_sched_simulate_ex makespan (ties: the lower enum value). Writes it to
- * *schedule_out and, if makespan_out is not NULL, its makespan. The pages pick schedules by
- * configuration (Descending vs Symmetric Shift at d = 128, Shift vs the baseline at long
- * sequences); this makes that choice from the cost model. Costs measured on GB300 with
- * this library (head dim 128, cycles per 128x128 task): c ~ 6900, r ~ 5600, h ~ 3000,
- * overlapped = 1. Returns DASH_ERR_INVALID_ARG for bad arguments.
+ * dash_sched_simulate_ex makespan at head dimension `head_dim` (ties: the lower enum
+ * value). Writes it to *schedule_out and, if makespan_out is not NULL, its makespan. The
+ * pages pick schedules by configuration (Descending vs Symmetric Shift at d = 128, Shift vs
+ * the baseline at long sequences); this makes that choice from the cost model. Costs
+ * measured on GB300 with this library (head dim 128, cycles per 128x128 task): c ~ 6900,
+ * r ~ 5600, h ~ 3000, overlapped = 1. Returns DASH_ERR_INVALID_ARG for bad arguments.
  */
-dash_status_t dash_sched_select(int mask, int n, int heads, int num_sms, double c, double r,
-                                double h, int overlapped, int* schedule_out,
+dash_status_t dash_sched_select(int mask, int n, int heads, int num_sms, int head_dim, double c,
+                                double r, double h, int overlapped, int* schedule_out,
                                 double* makespan_out);
 
 /*

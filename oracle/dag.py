@@ -55,7 +55,10 @@ Readings where the pages are silent (listed in the design notes as well):
   and symmetric shift then cut every chain where its KV tile changes and deal the pieces
   longest first, each to the SM with the least work dealt so far (the lower SM index on
   a tie; pieces of equal length in head-major chain order); every SM runs its pieces in
-  the order dealt. Each KV tile still runs on one SM, in its chain's order. Equal-length
+  the order dealt. At head dimension 128 the first q - 1 of the q whole rounds stay round
+  robin (whole units) and only the units after them are cut and dealt that way (their
+  twice larger tiles need the L2 locality a round-robin round keeps; measured on GB300);
+  at head dimension 64 every unit is. Each KV tile still runs on one SM, in its chain's order. Equal-length
   pieces (shift) are dealt exactly as round robin deals them, except that when the last
   partial round holds r units with 2 r <= P (and r <= MAX_SPLIT_TILES), each of those r
   KV tiles is split into two halves (the first ceil(len / 2) tasks, then the rest): split
@@ -171,7 +174,8 @@ def pieces(chain: list[tuple[int, int]]) -> list[list[tuple[int, int]]]:
     return out
 
 
-def deal(mask: str, sched: str, n: int, m: int, num_sms: int, balanced: bool = True):
+def deal(mask: str, sched: str, n: int, m: int, num_sms: int, balanced: bool = True,
+         head_dim: int = 128):
     """Per SM, the runs of tasks it executes, in order: lists of (head, [(i, j), ...],
     part, split) -- part 0 for whole KV tiles, 1 and 2 for the first and second half of
     split tile ``split`` (0 where part is 0).
@@ -204,8 +208,12 @@ def deal(mask: str, sched: str, n: int, m: int, num_sms: int, balanced: bool = T
             per_sm[k].append((h, list(ch[slot][:cut]), 1, k))
             per_sm[rest + k].append((h, list(ch[slot][cut:]), 2, k))
         return per_sm
-    runs = [(h, run) for (h, slot) in units for run in pieces(ch[slot])]
-    load = [0] * num_sms
+    lead = (full_rounds - 1) * num_sms if head_dim >= 128 else 0
+    for u in range(lead):
+        h, slot = units[u]
+        per_sm[u % num_sms].append((h, list(ch[slot]), 0, 0))
+    runs = [(h, run) for (h, slot) in units[lead:] for run in pieces(ch[slot])]
+    load = [0] * num_sms                     # the round-robin rounds loaded every SM alike
     for k in sorted(range(len(runs)), key=lambda k: (-len(runs[k][1]), k)):
         sm = min(range(num_sms), key=lambda s: (load[s], s))
         per_sm[sm].append((runs[k][0], runs[k][1], 0, 0))
@@ -214,7 +222,7 @@ def deal(mask: str, sched: str, n: int, m: int, num_sms: int, balanced: bool = T
 
 
 def dealt_reduction_order(mask: str, sched: str, n: int, m: int, num_sms: int,
-                          balanced: bool = True):
+                          balanced: bool = True, head_dim: int = 128):
     """For each (head, dQ block j), the KV tiles that reduce into it, in the order the
     dealt SMs produce them (the ``dealt=True`` reading in the module docstring); with
     ``balanced`` false, on SMs dealt round robin."""
@@ -223,7 +231,7 @@ def dealt_reduction_order(mask: str, sched: str, n: int, m: int, num_sms: int,
         return {(h, j): list(fixed[j]) for h in range(m) for j in range(n)}
     arrivals: dict[tuple[int, int], list[tuple[int, int]]] = {
         (h, j): [] for h in range(m) for j in range(n)}
-    for runs in deal(mask, sched, n, m, num_sms, balanced):
+    for runs in deal(mask, sched, n, m, num_sms, balanced, head_dim):
         place = 0                            # tasks this SM has run so far
         for h, run, _part, _split in runs:
             for (i, j) in run:
@@ -232,15 +240,17 @@ def dealt_reduction_order(mask: str, sched: str, n: int, m: int, num_sms: int,
     return {key: [i for _, i in sorted(lst)] for key, lst in arrivals.items()}
 
 
-def _orders(mask: str, sched: str, n: int, m: int, num_sms: int, dealt: bool):
+def _orders(mask: str, sched: str, n: int, m: int, num_sms: int, dealt: bool,
+            head_dim: int = 128):
     """(head, j) -> dQ_j order of that head, fixed per schedule or dealt."""
     if dealt:
-        return dealt_reduction_order(mask, sched, n, m, num_sms)
+        return dealt_reduction_order(mask, sched, n, m, num_sms, head_dim=head_dim)
     fixed = reduction_order(mask, sched, n)
     return {(h, j): fixed[j] for h in range(m) for j in fixed}
 
 
-def _dealt_tasks(mask: str, sched: str, n: int, m: int, num_sms: int, dealt: bool):
+def _dealt_tasks(mask: str, sched: str, n: int, m: int, num_sms: int, dealt: bool,
+                 head_dim: int = 128):
     """Number the tasks SM by SM in run order: (per_sm task lists, tasks, sm_of_task,
     index, halves). ``dealt`` deals as the kernels do (balanced), else round robin;
     halves lists (last task of a first half, last task of its second half)."""
@@ -249,7 +259,8 @@ def _dealt_tasks(mask: str, sched: str, n: int, m: int, num_sms: int, dealt: boo
     sm_of_task: list[int] = []
     index: dict[tuple[int, int, int], int] = {}
     last_of: dict[tuple[int, int], int] = {}
-    for sm, runs in enumerate(deal(mask, sched, n, m, num_sms, balanced=dealt)):
+    for sm, runs in enumerate(deal(mask, sched, n, m, num_sms, balanced=dealt,
+                                   head_dim=head_dim)):
         for hd, run, part, split in runs:
             for (i, j) in run:
                 k = len(tasks)
@@ -264,15 +275,16 @@ def _dealt_tasks(mask: str, sched: str, n: int, m: int, num_sms: int, dealt: boo
 
 
 def schedule_dag(mask: str, sched: str, n: int, m: int, num_sms: int, c: float, r: float,
-                 dealt: bool = False):
+                 dealt: bool = False, head_dim: int = 128):
     """Build the explicit DAG of m heads' tasks dealt onto ``num_sms`` SMs.
 
     Every task (head, i, j) owns four vertices: compute start/end and reduce start/end.
     Returns (n_vertices, edges, tasks, sm_of_task) where tasks[k] = (head, i, j) and task k
     owns vertices 4k..4k+3.
     """
-    order = _orders(mask, sched, n, m, num_sms, dealt)
-    per_sm, tasks, sm_of_task, index, halves = _dealt_tasks(mask, sched, n, m, num_sms, dealt)
+    order = _orders(mask, sched, n, m, num_sms, dealt, head_dim)
+    per_sm, tasks, sm_of_task, index, halves = _dealt_tasks(mask, sched, n, m, num_sms, dealt,
+                                                            head_dim)
     edges: list[tuple[int, int, float]] = []
     for k in range(len(tasks)):
         cs, ce, rs, re = 4 * k, 4 * k + 1, 4 * k + 2, 4 * k + 3
@@ -289,13 +301,14 @@ def schedule_dag(mask: str, sched: str, n: int, m: int, num_sms: int, c: float, 
 
 
 def simulate(mask: str, sched: str, n: int, m: int, num_sms: int, c: float, r: float,
-             dealt: bool = False):
+             dealt: bool = False, head_dim: int = 128):
     """Critical path of the schedule DAG.
 
     Returns a dict with ``makespan`` (None on a cycle, i.e. a deadlock), ``sm_end`` (finish
     time per SM) and ``sm_idle`` (finish time minus busy time per SM).
     """
-    nv, edges, tasks, sm_of_task = schedule_dag(mask, sched, n, m, num_sms, c, r, dealt)
+    nv, edges, tasks, sm_of_task = schedule_dag(mask, sched, n, m, num_sms, c, r, dealt,
+                                                head_dim)
     depth = longest_path(nv, edges)
     if depth is None:
         return {"makespan": None, "sm_end": None, "sm_idle": None}
@@ -325,13 +338,14 @@ def simulate(mask: str, sched: str, n: int, m: int, num_sms: int, c: float, r: f
 # With h = 0 and overlapped = False this is exactly schedule_dag / simulate above.
 # ---------------------------------------------------------------------------------------
 def schedule_dag_ex(mask: str, sched: str, n: int, m: int, num_sms: int, c: float, r: float,
-                    h: float, overlapped: bool, dealt: bool = False):
+                    h: float, overlapped: bool, dealt: bool = False, head_dim: int = 128):
     """The schedule DAG with hand-off cost ``h`` and, optionally, the two-engine SM.
 
     Same vertex numbering and return value as schedule_dag.
     """
-    order = _orders(mask, sched, n, m, num_sms, dealt)
-    per_sm, tasks, sm_of_task, index, halves = _dealt_tasks(mask, sched, n, m, num_sms, dealt)
+    order = _orders(mask, sched, n, m, num_sms, dealt, head_dim)
+    per_sm, tasks, sm_of_task, index, halves = _dealt_tasks(mask, sched, n, m, num_sms, dealt,
+                                                            head_dim)
     edges: list[tuple[int, int, float]] = []
     for k in range(len(tasks)):
         cs, ce, rs, re = 4 * k, 4 * k + 1, 4 * k + 2, 4 * k + 3
@@ -357,10 +371,11 @@ def schedule_dag_ex(mask: str, sched: str, n: int, m: int, num_sms: int, c: floa
 
 
 def simulate_ex(mask: str, sched: str, n: int, m: int, num_sms: int, c: float, r: float,
-                h: float = 0.0, overlapped: bool = False, dealt: bool = False):
+                h: float = 0.0, overlapped: bool = False, dealt: bool = False,
+                head_dim: int = 128):
     """Critical path of schedule_dag_ex; same return value as simulate."""
     nv, edges, tasks, sm_of_task = schedule_dag_ex(mask, sched, n, m, num_sms, c, r, h,
-                                                   overlapped, dealt)
+                                                   overlapped, dealt, head_dim)
     depth = longest_path(nv, edges)
     if depth is None:
         return {"makespan": None, "sm_end": None, "sm_idle": None}

@@ -53,15 +53,17 @@ struct DeviceTables {
 
 std::mutex g_mu;
 std::map<std::tuple<int, int, int, int>, DeviceTables> g_tables;        // (dev, mask, sched, n)
-std::map<std::tuple<int, int, int, int, int>, bool> g_deadlock_free;    // (mask, sched, n, heads, grid)
-// What one grid follows, per (dev, mask, sched, n, heads, grid): each CTA's pieces of work
-// (dash::deal) and, for the arrival-ordered schedules, the per-head dQ orders.
+// (mask, sched, n, heads, grid, head dim)
+std::map<std::tuple<int, int, int, int, int, int>, bool> g_deadlock_free;
+// What one grid follows, per (dev, mask, sched, n, heads, grid, head dim): each CTA's
+// pieces of work (dash::deal) and, for the arrival-ordered schedules, the per-head dQ
+// orders.
 struct DealtTables {
   int32_t* ord = nullptr;       // [heads][n][n]; null: the schedule's own order
   int32_t* cta_off = nullptr;   // [grid + 1]
   int32_t* pieces = nullptr;    // [pieces][4]: head, first task, end task, split/part
 };
-std::map<std::tuple<int, int, int, int, int, int>, DealtTables> g_dealt;
+std::map<std::tuple<int, int, int, int, int, int, int>, DealtTables> g_dealt;
 
 // The pieces in the kernel's 16-byte form: (head, first task, end task, (split << 2) | part).
 std::vector<int32_t> piece_words(const dash::Dealing& dl) {
@@ -73,17 +75,19 @@ std::vector<int32_t> piece_words(const dash::Dealing& dl) {
 }
 // their host copies, (mask, sched, n, heads, grid): building one sorts every task of the
 // shape, so it is done once per shape
-std::map<std::tuple<int, int, int, int, int>, std::shared_ptr<const std::vector<int32_t>>> g_host_dealt;
+std::map<std::tuple<int, int, int, int, int, int>, std::shared_ptr<const std::vector<int32_t>>>
+    g_host_dealt;
 
-// Host copy of the per-head dQ orders of an arrival-ordered schedule on `grid` CTAs
-// (cached; the caller holds g_mu).
+// Host copy of the per-head dQ orders of an arrival-ordered schedule on `grid` CTAs at
+// head dimension `head_dim` (cached; the caller holds g_mu).
 std::shared_ptr<const std::vector<int32_t>> host_dealt_locked(const dash::Schedule& sc,
-                                                              int heads, int grid) {
-  auto key = std::make_tuple(sc.mask, sc.sched, sc.n, heads, grid);
+                                                              int heads, int grid,
+                                                              int head_dim) {
+  auto key = std::make_tuple(sc.mask, sc.sched, sc.n, heads, grid, head_dim);
   auto it = g_host_dealt.find(key);
   if (it == g_host_dealt.end()) {
     auto v = std::make_shared<std::vector<int32_t>>();
-    dash::dealt_orders(sc, heads, grid, v.get());
+    dash::dealt_orders(sc, heads, grid, head_dim, v.get());
     it = g_host_dealt.emplace(key, std::move(v)).first;
   }
   return it->second;
@@ -132,21 +136,21 @@ cudaError_t upload_new(const std::vector<int32_t>& v, int32_t** dst) {
 // heads), the per-head arrival orders of dash::dealt_orders for shift and symmetric shift
 // (cached per shape).
 dash_status_t set_dealing(int dev, int mask, int sched, int n, int heads, int grid,
-                          const DeviceTables& tb, dash::BwdParams* p) {
+                          int head_dim, const DeviceTables& tb, dash::BwdParams* p) {
   std::lock_guard<std::mutex> lk(g_mu);
-  auto key = std::make_tuple(dev, mask, sched, n, heads, grid);
+  auto key = std::make_tuple(dev, mask, sched, n, heads, grid, head_dim);
   auto it = g_dealt.find(key);
   if (it == g_dealt.end()) {
     dash::Schedule sc;
     int rc = dash::build_schedule(mask, sched, n, &sc);
     if (rc) return (dash_status_t)rc;
     dash::Dealing dl;
-    dash::deal(sc, heads, grid, &dl);
+    dash::deal(sc, heads, grid, head_dim, &dl);
     DealtTables d;
     cudaError_t e = upload_new(dl.cta_off, &d.cta_off);
     if (e == cudaSuccess) e = upload_new(piece_words(dl), &d.pieces);
     if (e == cudaSuccess && dash::arrival_ordered(sc))
-      e = upload_new(*host_dealt_locked(sc, heads, grid), &d.ord);
+      e = upload_new(*host_dealt_locked(sc, heads, grid, head_dim), &d.ord);
     if (e != cudaSuccess) {
       cudaFree(d.cta_off);
       cudaFree(d.pieces);
@@ -195,9 +199,10 @@ bool launch_regs_ok(const MainKernel& mk) {
   return fa.numRegs == dash::tc::L128::REGS_LAUNCH;
 }
 
-// True when the schedule's waits are acyclic for `heads` heads on `grid` persistent CTAs.
-bool deadlock_free(int mask, int sched, int n, int heads, int grid) {
-  auto key = std::make_tuple(mask, sched, n, heads, grid);
+// True when the schedule's waits are acyclic for `heads` heads on `grid` persistent CTAs
+// dealt at head dimension `head_dim`.
+bool deadlock_free(int mask, int sched, int n, int heads, int grid, int head_dim) {
+  auto key = std::make_tuple(mask, sched, n, heads, grid, head_dim);
   {
     std::lock_guard<std::mutex> lk(g_mu);
     auto it = g_deadlock_free.find(key);
@@ -209,7 +214,7 @@ bool deadlock_free(int mask, int sched, int n, int heads, int grid) {
     dash::Schedule sc;
     if (dash::build_schedule(mask, sched, n, &sc) != 0) return false;
     double mk = 0;
-    ok = dash::simulate(sc, heads, grid, 1.0, 0.1, &mk, nullptr);
+    ok = dash::simulate(sc, heads, grid, head_dim, 1.0, 0.1, &mk, nullptr);
   }
   std::lock_guard<std::mutex> lk(g_mu);
   g_deadlock_free[key] = ok;
@@ -521,9 +526,9 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
     g_last_error = "backward kernel does not fit on one SM";
     return DASH_ERR_CUDA;
   }
-  if (deterministic && !deadlock_free(mask, schedule, n, B * H, grid))
+  if (deterministic && !deadlock_free(mask, schedule, n, B * H, grid, D))
     return DASH_ERR_DEADLOCK_RISK;
-  st = set_dealing(dev, mask, schedule, n, B * H, grid, tb, &p);
+  st = set_dealing(dev, mask, schedule, n, B * H, grid, D, tb, &p);
   if (st != DASH_OK) return st;
 
   dash::bwd_preprocess_kernel<<<sms * 4, 256, 0, stream>>>(p);
@@ -618,25 +623,28 @@ int dash_sched_table(int mask, int schedule, int n, int32_t* slot_offsets, int32
 }
 
 dash_status_t dash_sched_dealt_table(int mask, int schedule, int n, int heads, int grid,
-                                    int32_t* ordinals) {
-  if (heads < 1 || grid < 1 || !ordinals) return DASH_ERR_INVALID_ARG;
+                                    int head_dim, int32_t* ordinals) {
+  if (heads < 1 || grid < 1 || !ordinals || (head_dim != 64 && head_dim != 128))
+    return DASH_ERR_INVALID_ARG;
   dash::Schedule sc;
   int rc = dash::build_schedule(mask, schedule, n, &sc);
   if (rc) return (dash_status_t)rc;
   std::vector<int32_t> ord;
-  dash::dealt_orders(sc, heads, grid, &ord);
+  dash::dealt_orders(sc, heads, grid, head_dim, &ord);
   std::memcpy(ordinals, ord.data(), ord.size() * sizeof(int32_t));
   return DASH_OK;
 }
 
-int dash_sched_deal(int mask, int schedule, int n, int heads, int grid, int32_t* cta_offsets,
-                    int32_t* pieces, int cap) {
-  if (heads < 1 || grid < 1 || !cta_offsets || !pieces || cap < 0) return -DASH_ERR_INVALID_ARG;
+int dash_sched_deal(int mask, int schedule, int n, int heads, int grid, int head_dim,
+                    int32_t* cta_offsets, int32_t* pieces, int cap) {
+  if (heads < 1 || grid < 1 || !cta_offsets || !pieces || cap < 0 ||
+      (head_dim != 64 && head_dim != 128))
+    return -DASH_ERR_INVALID_ARG;
   dash::Schedule sc;
   int rc = dash::build_schedule(mask, schedule, n, &sc);
   if (rc) return -rc;
   dash::Dealing dl;
-  dash::deal(sc, heads, grid, &dl);
+  dash::deal(sc, heads, grid, head_dim, &dl);
   if ((size_t)cap < dl.pieces.size()) return -DASH_ERR_INVALID_ARG;
   std::memcpy(cta_offsets, dl.cta_off.data(), dl.cta_off.size() * sizeof(int32_t));
   for (size_t k = 0; k < dl.pieces.size(); ++k) {
@@ -648,13 +656,17 @@ int dash_sched_deal(int mask, int schedule, int n, int heads, int grid, int32_t*
 }
 
 dash_status_t dash_sched_simulate(int mask, int schedule, int n, int heads, int num_sms,
-                                  double c, double r, double* makespan, double* sm_end) {
-  if (heads < 1 || num_sms < 1 || !makespan || !(c >= 0) || !(r >= 0)) return DASH_ERR_INVALID_ARG;
+                                  int head_dim, double c, double r, double* makespan,
+                                  double* sm_end) {
+  if (heads < 1 || num_sms < 1 || !makespan || !(c >= 0) || !(r >= 0) ||
+      (head_dim != 64 && head_dim != 128))
+    return DASH_ERR_INVALID_ARG;
   dash::Schedule sc;
   int rc = dash::build_schedule(mask, schedule, n, &sc);
   if (rc) return (dash_status_t)rc;
   std::vector<double> ends;
-  if (!dash::simulate(sc, heads, num_sms, c, r, makespan, &ends)) return DASH_ERR_DEADLOCK_RISK;
+  if (!dash::simulate(sc, heads, num_sms, head_dim, c, r, makespan, &ends))
+    return DASH_ERR_DEADLOCK_RISK;
   if (sm_end) std::memcpy(sm_end, ends.data(), ends.size() * sizeof(double));
   return DASH_OK;
 }
@@ -722,26 +734,27 @@ dash_status_t dash_gemm_splitk(const void* a, const void* b, float* c, void* wor
 }
 
 dash_status_t dash_sched_simulate_ex(int mask, int schedule, int n, int heads, int num_sms,
-                                     double c, double r, double h, int overlapped,
+                                     int head_dim, double c, double r, double h, int overlapped,
                                      double* makespan, double* sm_end) {
   if (heads < 1 || num_sms < 1 || !makespan || !(c >= 0) || !(r >= 0) || !(h >= 0) ||
-      (overlapped != 0 && overlapped != 1))
+      (overlapped != 0 && overlapped != 1) || (head_dim != 64 && head_dim != 128))
     return DASH_ERR_INVALID_ARG;
   dash::Schedule sc;
   int rc = dash::build_schedule(mask, schedule, n, &sc);
   if (rc) return (dash_status_t)rc;
   std::vector<double> ends;
-  if (!dash::simulate_ex(sc, heads, num_sms, c, r, h, overlapped != 0, makespan, &ends))
+  if (!dash::simulate_ex(sc, heads, num_sms, head_dim, c, r, h, overlapped != 0, makespan,
+                         &ends))
     return DASH_ERR_DEADLOCK_RISK;
   if (sm_end) std::memcpy(sm_end, ends.data(), ends.size() * sizeof(double));
   return DASH_OK;
 }
 
-dash_status_t dash_sched_select(int mask, int n, int heads, int num_sms, double c, double r,
-                                double h, int overlapped, int* schedule_out,
+dash_status_t dash_sched_select(int mask, int n, int heads, int num_sms, int head_dim, double c,
+                                double r, double h, int overlapped, int* schedule_out,
                                 double* makespan_out) {
   if (!schedule_out || heads < 1 || num_sms < 1 || !(c >= 0) || !(r >= 0) || !(h >= 0) ||
-      (overlapped != 0 && overlapped != 1))
+      (overlapped != 0 && overlapped != 1) || (head_dim != 64 && head_dim != 128))
     return DASH_ERR_INVALID_ARG;
   if (mask != DASH_MASK_FULL && mask != DASH_MASK_CAUSAL) return DASH_ERR_INVALID_ARG;
   int best = -1;
@@ -752,7 +765,8 @@ dash_status_t dash_sched_select(int mask, int n, int heads, int num_sms, double 
     if (rc == DASH_ERR_UNSUPPORTED) continue;          // schedule not defined for this mask/n
     if (rc) return (dash_status_t)rc;
     double mk = 0.0;
-    if (!dash::simulate_ex(sc, heads, num_sms, c, r, h, overlapped != 0, &mk, nullptr))
+    if (!dash::simulate_ex(sc, heads, num_sms, head_dim, c, r, h, overlapped != 0, &mk,
+                           nullptr))
       continue;                                        // its waits would deadlock this grid
     if (best < 0 || mk < best_mk) {                    // ties keep the lower enum value
       best = s;
@@ -816,22 +830,23 @@ struct StaticTables {
   // byte offsets of the piece, task, order and count tables (the CTA offsets come first)
   size_t piece_off, task_off, ord_off, cnt_off;
 };
-std::map<std::tuple<int, int, int, int, int>, std::shared_ptr<const StaticTables>> g_static_tables;
+std::map<std::tuple<int, int, int, int, int, int>, std::shared_ptr<const StaticTables>>
+    g_static_tables;
 
-dash_status_t static_tables(int mask, int schedule, int n, int heads, int grid,
+dash_status_t static_tables(int mask, int schedule, int n, int heads, int grid, int head_dim,
                             std::shared_ptr<const StaticTables>* out) {
   std::lock_guard<std::mutex> lk(g_mu);
-  auto key = std::make_tuple(mask, schedule, n, heads, grid);
+  auto key = std::make_tuple(mask, schedule, n, heads, grid, head_dim);
   auto it = g_static_tables.find(key);
   if (it == g_static_tables.end()) {
     dash::Schedule sc;
     const int rc = dash::build_schedule(mask, schedule, n, &sc);
     if (rc) return (dash_status_t)rc;
     std::shared_ptr<const std::vector<int32_t>> dealt;
-    if (dash::arrival_ordered(sc)) dealt = host_dealt_locked(sc, heads, grid);
+    if (dash::arrival_ordered(sc)) dealt = host_dealt_locked(sc, heads, grid, head_dim);
     const std::vector<int32_t>& ord = dealt ? *dealt : sc.ord;
     dash::Dealing dl;
-    dash::deal(sc, heads, grid, &dl);
+    dash::deal(sc, heads, grid, head_dim, &dl);
     const std::vector<int32_t> words = piece_words(dl);
     auto t = std::make_shared<StaticTables>();
     t->piece_off = round_up(dl.cta_off.size() * 4, 256);
@@ -890,7 +905,7 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
   // the dQ orders of this grid (per head for shift and symmetric shift), as the regular
   // entry point uses them, with the other tables: built once per shape in host memory
   std::shared_ptr<const StaticTables> tb;
-  dash_status_t st = static_tables(mask, schedule, n, B * H, grid, &tb);
+  dash_status_t st = static_tables(mask, schedule, n, B * H, grid, D, &tb);
   if (st != DASH_OK) return st;
 
   // scratch layout: the backward workspace, then the schedule tables
@@ -980,7 +995,7 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
     g_last_error = "backward kernel does not fit on one SM";
     return DASH_ERR_CUDA;
   }
-  if (deterministic && !deadlock_free(mask, schedule, n, B * H, grid))
+  if (deterministic && !deadlock_free(mask, schedule, n, B * H, grid, D))
     return DASH_ERR_DEADLOCK_RISK;
 
   // Tables are written for every call: the array keeps whatever the last call left.

@@ -102,7 +102,7 @@ int build_schedule(int mask, int sched, int n, Schedule* out) {
   return 0;
 }
 
-void deal(const Schedule& sc, int heads, int grid, Dealing* out) {
+void deal(const Schedule& sc, int heads, int grid, int head_dim, Dealing* out) {
   out->cta_off.assign(grid + 1, 0);
   out->pieces.clear();
   const long long units = (long long)heads * sc.num_slots;
@@ -138,19 +138,23 @@ void deal(const Schedule& sc, int heads, int grid, Dealing* out) {
       per_cta[splits + k].push_back(b);
     }
   } else {
-    // the chains cut where the KV tile changes, in head-major chain order
+    // head dimension 128: whole rounds but the last stay round robin
+    const long long lead = head_dim >= 128 ? (units / grid - 1) * grid : 0;
+    for (long long u = 0; u < lead; ++u) per_cta[u % grid].push_back(unit_piece(u));
+    // the other units' chains cut where the KV tile changes, in head-major chain order
     std::vector<Piece> runs;
-    for (int h = 0; h < heads; ++h)
-      for (int slot = 0; slot < sc.num_slots; ++slot) {
-        int b = sc.slot_off[slot];
-        for (int t = b + 1; t <= sc.slot_off[slot + 1]; ++t)
-          if (t == sc.slot_off[slot + 1] || (sc.tasks[t] >> 16) != (sc.tasks[b] >> 16)) {
-            runs.push_back({h, b, t});
-            b = t;
-          }
-      }
+    for (long long u = lead; u < units; ++u) {
+      const int h = (int)(u / sc.num_slots), slot = (int)(u % sc.num_slots);
+      int b = sc.slot_off[slot];
+      for (int t = b + 1; t <= sc.slot_off[slot + 1]; ++t)
+        if (t == sc.slot_off[slot + 1] || (sc.tasks[t] >> 16) != (sc.tasks[b] >> 16)) {
+          runs.push_back({h, b, t});
+          b = t;
+        }
+    }
     // longest first (stable: equal lengths keep the head-major order), each to the CTA
-    // with the least work so far, the lower index on a tie
+    // with the least work so far (the round-robin rounds gave every CTA the same), the
+    // lower index on a tie
     std::stable_sort(runs.begin(), runs.end(), [](const Piece& a, const Piece& b) {
       return a.t_end - a.t_begin > b.t_end - b.t_begin;
     });
@@ -170,7 +174,8 @@ void deal(const Schedule& sc, int heads, int grid, Dealing* out) {
   }
 }
 
-void dealt_orders(const Schedule& sc, int heads, int grid, std::vector<int32_t>* out) {
+void dealt_orders(const Schedule& sc, int heads, int grid, int head_dim,
+                  std::vector<int32_t>* out) {
   const int n = sc.n;
   out->assign((size_t)heads * n * n, -1);
   if (!arrival_ordered(sc)) {
@@ -180,7 +185,7 @@ void dealt_orders(const Schedule& sc, int heads, int grid, std::vector<int32_t>*
   }
   // (place in the CTA's task sequence, kv) of every partial, per (head, dQ block)
   Dealing dl;
-  deal(sc, heads, grid, &dl);
+  deal(sc, heads, grid, head_dim, &dl);
   std::vector<std::vector<std::pair<long long, int>>> arrivals((size_t)heads * n);
   for (int cta = 0; cta < grid; ++cta) {
     long long place = 0;
@@ -201,18 +206,18 @@ void dealt_orders(const Schedule& sc, int heads, int grid, std::vector<int32_t>*
   }
 }
 
-bool simulate(const Schedule& sc, int heads, int num_sms, double c, double r,
+bool simulate(const Schedule& sc, int heads, int num_sms, int head_dim, double c, double r,
               double* makespan, std::vector<double>* sm_end) {
-  return simulate_ex(sc, heads, num_sms, c, r, 0.0, false, makespan, sm_end);
+  return simulate_ex(sc, heads, num_sms, head_dim, c, r, 0.0, false, makespan, sm_end);
 }
 
-bool simulate_ex(const Schedule& sc, int heads, int num_sms, double c, double r, double h,
-                 bool overlapped, double* makespan, std::vector<double>* sm_end) {
+bool simulate_ex(const Schedule& sc, int heads, int num_sms, int head_dim, double c, double r,
+                 double h, bool overlapped, double* makespan, std::vector<double>* sm_end) {
   const int n = sc.n;
   std::vector<int32_t> ord;
-  dealt_orders(sc, heads, num_sms, &ord);
+  dealt_orders(sc, heads, num_sms, head_dim, &ord);
   Dealing dl;
-  deal(sc, heads, num_sms, &dl);
+  deal(sc, heads, num_sms, head_dim, &dl);
   // who reduces at position k of head h's dQ_j: inv[(h * n + j) * n + k] = kv tile
   std::vector<int32_t> inv((size_t)heads * n * n, -1);
   for (int hd = 0; hd < heads; ++hd)

@@ -69,17 +69,22 @@ struct Dealing {
 // and the pieces dealt longest first (equal lengths in head-major chain order), each to
 // the CTA with the least work dealt so far (the lower index on a tie); a CTA runs its
 // pieces in the order dealt. Every KV tile still runs whole on one CTA, in chain order.
+// At head dimension 128 the first q - 1 of the q whole rounds stay round robin (whole
+// units, head-major) and only the units after them are cut and dealt longest first: a
+// round-robin round keeps each head's chains on concurrent CTAs, so its Q/dO tiles and
+// dQ accumulator blocks stay in L2, which the twice larger tiles need (at head dimension
+// 64 dealing every unit's pieces longest first measured faster).
 // Pieces of equal length (shift) are dealt exactly as round robin deals them; there,
 // when the last partial round has r units and 2 r <= grid (r <= kMaxSplitTiles), each of
 // those r KV tiles is instead split in two halves (the first ceil(len / 2) tasks, then
 // the rest): split k's first half runs on CTA k and its second half on CTA r + k, after
 // their whole units, so the busiest CTA runs half a unit less and no first half ever
 // waits behind a second half.
-void deal(const Schedule& sc, int heads, int grid, Dealing* out);
+void deal(const Schedule& sc, int heads, int grid, int head_dim, Dealing* out);
 
-// The dQ order the kernels follow when `heads` heads' chains are dealt onto `grid`
-// persistent CTAs (deal above): out[(h * n + i) * n + j] = position of KV_i's partial in
-// head h's dQ_j order (-1 where the mask removes the task).
+// The dQ order the kernels follow at head dimension `head_dim` when `heads` heads' chains
+// are dealt onto `grid` persistent CTAs (deal above): out[(h * n + i) * n + j] = position
+// of KV_i's partial in head h's dQ_j order (-1 where the mask removes the task).
 //   ascending, descending  -- ascending KV index in every head (`ord` repeated);
 //   shift, symmetric shift -- order of arrival: a partial's place in its CTA's task
 //                             sequence (the tasks of the CTA's earlier pieces, then its
@@ -90,13 +95,14 @@ void deal(const Schedule& sc, int heads, int grid, Dealing* out);
 // that run in the earlier round come first, so no partial waits for a chain that has not
 // started. An arrival-ordered wait always points to a strictly earlier (place, KV index)
 // and each CTA runs its tasks in increasing place, so these orders cannot deadlock.
-void dealt_orders(const Schedule& sc, int heads, int grid, std::vector<int32_t>* out);
+void dealt_orders(const Schedule& sc, int heads, int grid, int head_dim,
+                  std::vector<int32_t>* out);
 
 // Event-driven critical path of `heads` heads dealt onto `num_sms` SMs as the kernels
-// deal them (deal above), with the dQ orders of dealt_orders(sc, heads, num_sms) -- the
-// orders the kernels follow on a grid of num_sms CTAs. Returns false on a cycle
-// (deadlock). sm_end may be null.
-bool simulate(const Schedule& sc, int heads, int num_sms, double c, double r,
+// deal them at head dimension `head_dim` (deal above), with the dQ orders of
+// dealt_orders(sc, heads, num_sms, head_dim) -- the orders the kernels follow on a grid of
+// num_sms CTAs. Returns false on a cycle (deadlock). sm_end may be null.
+bool simulate(const Schedule& sc, int heads, int num_sms, int head_dim, double c, double r,
               double* makespan, std::vector<double>* sm_end);
 
 // The same with synchronisation cost and the two-engine SM (the Pith review's "Where Pith
@@ -107,7 +113,7 @@ bool simulate(const Schedule& sc, int heads, int num_sms, double c, double r,
 //                 accumulator reuse of a kernel that reads one partial out while the
 //                 next is computed); false = C then R, task after task.
 // h = 0, overlapped = false is simulate() above.
-bool simulate_ex(const Schedule& sc, int heads, int num_sms, double c, double r, double h,
-                 bool overlapped, double* makespan, std::vector<double>* sm_end);
+bool simulate_ex(const Schedule& sc, int heads, int num_sms, int head_dim, double c, double r,
+                 double h, bool overlapped, double* makespan, std::vector<double>* sm_end);
 
 }  // namespace dash

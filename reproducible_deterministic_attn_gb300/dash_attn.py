@@ -58,13 +58,14 @@ _SIGNATURES = {
     "dash_profile_read": (_c_int, [_dblp, ctypes.POINTER(_c_int)]),
     "dash_sched_num_slots": (_c_int, [_c_int, _c_int, _c_int]),
     "dash_sched_table": (_c_int, [_c_int, _c_int, _c_int, _i32p, _i32p, _c_int, _i32p]),
-    "dash_sched_dealt_table": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _i32p]),
-    "dash_sched_deal": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _i32p, _i32p, _c_int]),
-    "dash_sched_simulate": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_double, _c_double,
-                                     _dblp, _dblp]),
-    "dash_sched_simulate_ex": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_double,
-                                        _c_double, _c_double, _c_int, _dblp, _dblp]),
-    "dash_sched_select": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_double, _c_double,
+    "dash_sched_dealt_table": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _i32p]),
+    "dash_sched_deal": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _i32p, _i32p,
+                                 _c_int]),
+    "dash_sched_simulate": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_double,
+                                     _c_double, _dblp, _dblp]),
+    "dash_sched_simulate_ex": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                        _c_double, _c_double, _c_double, _c_int, _dblp, _dblp]),
+    "dash_sched_select": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_double, _c_double,
                                    _c_double, _c_int, ctypes.POINTER(_c_int), _dblp]),
     "dash_gemm_splitk_workspace_size": (ctypes.c_size_t, [_c_int, _c_int]),
     "dash_gemm_splitk": (_c_int, [_vp, _vp, _vp, _vp, ctypes.c_size_t, _c_int, _c_int, _c_int,
@@ -226,38 +227,43 @@ def dash_sched_table(mask: int, schedule: int, n: int):
     return list(off), pairs, [list(ords[i * n:(i + 1) * n]) for i in range(n)]
 
 
-def dash_sched_deal(mask: int, schedule: int, n: int, heads: int, grid: int):
-    """Each CTA's work in run order: per CTA a list of (head, [(kv, q), ...], part, split)
-    pieces (part 0: whole KV tiles; 1 / 2: first / second half of split tile `split`)."""
+def dash_sched_deal(mask: int, schedule: int, n: int, heads: int, grid: int,
+                    head_dim: int = 128):
+    """Each CTA's work in run order at head dimension `head_dim`: per CTA a list of
+    (head, [(kv, q), ...], part, split) pieces (part 0: whole KV tiles; 1 / 2: first /
+    second half of split tile `split`)."""
     _, pairs, _ = dash_sched_table(mask, schedule, n)
     slots = dash_sched_num_slots(mask, schedule, n)
     cap = 2 * heads * slots              # a chain has at most two KV tiles
     off = (ctypes.c_int32 * (grid + 1))()
     pieces = (ctypes.c_int32 * (5 * cap))()
     cnt = load().dash_sched_deal(int(mask), int(schedule), int(n), int(heads), int(grid),
-                                 off, pieces, cap)
+                                 int(head_dim), off, pieces, cap)
     if cnt < 0:
         raise DashError(-cnt, "dash_sched_deal")
     return [[(pieces[5 * k], pairs[pieces[5 * k + 1]:pieces[5 * k + 2]], pieces[5 * k + 3],
               pieces[5 * k + 4]) for k in range(off[c], off[c + 1])] for c in range(grid)]
 
 
-def dash_sched_dealt_table(mask: int, schedule: int, n: int, heads: int, grid: int):
-    """The dQ orders the backward follows on `grid` CTAs: ords[h][i][j] (-1 = masked)."""
+def dash_sched_dealt_table(mask: int, schedule: int, n: int, heads: int, grid: int,
+                           head_dim: int = 128):
+    """The dQ orders the backward follows on `grid` CTAs at head dimension `head_dim`:
+    ords[h][i][j] (-1 = masked)."""
     ords = (ctypes.c_int32 * (heads * n * n))()
     _check(load().dash_sched_dealt_table(int(mask), int(schedule), int(n), int(heads),
-                                         int(grid), ords), "dash_sched_dealt_table")
+                                         int(grid), int(head_dim), ords),
+           "dash_sched_dealt_table")
     return [[list(ords[(h * n + i) * n:(h * n + i + 1) * n]) for i in range(n)]
             for h in range(heads)]
 
 
 def dash_sched_simulate(mask: int, schedule: int, n: int, heads: int, num_sms: int,
-                        c: float, r: float):
+                        c: float, r: float, head_dim: int = 128):
     """Returns (makespan, per-SM finish times), or (None, None) on a deadlock."""
     mk = ctypes.c_double(0.0)
     ends = (ctypes.c_double * num_sms)()
     st = load().dash_sched_simulate(int(mask), int(schedule), int(n), int(heads), int(num_sms),
-                                    float(c), float(r), ctypes.byref(mk), ends)
+                                    int(head_dim), float(c), float(r), ctypes.byref(mk), ends)
     if st == DASH_ERR_DEADLOCK_RISK:
         return None, None
     _check(st, "dash_sched_simulate")
@@ -265,13 +271,13 @@ def dash_sched_simulate(mask: int, schedule: int, n: int, heads: int, num_sms: i
 
 
 def dash_sched_simulate_ex(mask: int, schedule: int, n: int, heads: int, num_sms: int,
-                           c: float, r: float, h: float, overlapped: int):
+                           c: float, r: float, h: float, overlapped: int, head_dim: int = 128):
     """Returns (makespan, per-SM finish times), or (None, None) on a deadlock."""
     mk = ctypes.c_double(0.0)
     ends = (ctypes.c_double * num_sms)()
     st = load().dash_sched_simulate_ex(int(mask), int(schedule), int(n), int(heads),
-                                       int(num_sms), float(c), float(r), float(h),
-                                       int(overlapped), ctypes.byref(mk), ends)
+                                       int(num_sms), int(head_dim), float(c), float(r),
+                                       float(h), int(overlapped), ctypes.byref(mk), ends)
     if st == DASH_ERR_DEADLOCK_RISK:
         return None, None
     _check(st, "dash_sched_simulate_ex")
@@ -279,13 +285,13 @@ def dash_sched_simulate_ex(mask: int, schedule: int, n: int, heads: int, num_sms
 
 
 def dash_sched_select(mask: int, n: int, heads: int, num_sms: int, c: float, r: float,
-                      h: float, overlapped: int):
+                      h: float, overlapped: int, head_dim: int = 128):
     """Returns (schedule, makespan) chosen by the library's cost model."""
     sched = _c_int(-1)
     mk = ctypes.c_double(0.0)
-    st = load().dash_sched_select(int(mask), int(n), int(heads), int(num_sms), float(c),
-                                  float(r), float(h), int(overlapped), ctypes.byref(sched),
-                                  ctypes.byref(mk))
+    st = load().dash_sched_select(int(mask), int(n), int(heads), int(num_sms), int(head_dim),
+                                  float(c), float(r), float(h), int(overlapped),
+                                  ctypes.byref(sched), ctypes.byref(mk))
     _check(st, "dash_sched_select")
     return sched.value, mk.value
 

@@ -329,9 +329,9 @@ def test_balanced_deal_invariants():
         for n in (2, 4, 6, 8):
             ch = chains(mask, sched, n)
             longest = max(len(c) for c in ch)
-            for m in (1, 2, 3, 5):
+            for m, hd in itertools.product((1, 2, 3, 5, 9), (64, 128)):
                 for sms in range(1, 3 * n + 2):
-                    per_sm = deal(mask, sched, n, m, sms)
+                    per_sm = deal(mask, sched, n, m, sms, head_dim=hd)
                     rr = deal(mask, sched, n, m, sms, balanced=False)
                     units = m * len(ch)
                     rest = units % sms
@@ -342,21 +342,27 @@ def test_balanced_deal_invariants():
                         # equal-length chains without room to halve: exactly round robin
                         assert per_sm == rr, (mask, sched, n, m, sms)
                         continue
+                    if not halved and hd >= 128:
+                        # head dim 128: all whole rounds but the last stay round robin
+                        lead = units // sms - 1
+                        assert all(per_sm[x][:lead] == rr[x][:lead] for x in range(sms))
                     seen = {}
                     halves = {}
                     for sm, runs in enumerate(per_sm):
                         for h, run, part, split in runs:
-                            assert len({i for i, _ in run}) == 1       # one KV tile per piece
-                            i = run[0][0]
-                            chain = next(c for c in ch if (i, run[0][1]) in c)
+                            chain = next(c for c in ch if run[0] in c)
                             k = chain.index(run[0])                    # contiguous, in order
                             assert chain[k:k + len(run)] == run
                             if part:
                                 assert halved
                                 halves.setdefault(split, {})[part] = (sm, h, run)
                                 continue
-                            assert (h, i) not in seen                  # a KV tile on one SM
-                            seen[(h, i)] = sm
+                            kvs = {i for i, _ in run}
+                            # a round-robin unit, or one KV tile of a cut chain
+                            assert run == chain or len(kvs) == 1
+                            for i in kvs:
+                                assert (h, i) not in seen              # a KV tile on one SM
+                                seen[(h, i)] = sm
                     if halved:
                         # split k: first ceil(len / 2) tasks on SM k, the rest on SM rest + k,
                         # each the last piece of its SM

@@ -51,8 +51,9 @@ def test_dealt_tables_match_oracle(seed):
         mask, sched = rng.choice([(0, 0), (0, 1), (0, 2), (1, 0), (1, 1), (1, 3)])
         n = rng.choice([1, 2, 3, 4, 6, 8, 12]) if sched != 3 else rng.choice([2, 4, 6, 8, 12])
         m, grid = rng.randint(1, 5), rng.randint(1, 3 * n + 2)
-        got = da.dash_sched_dealt_table(mask, sched, n, m, grid)
-        want = dag.dealt_reduction_order(MASKS[mask], NAMES[sched], n, m, grid)
+        hd = rng.choice([64, 128])
+        got = da.dash_sched_dealt_table(mask, sched, n, m, grid, hd)
+        want = dag.dealt_reduction_order(MASKS[mask], NAMES[sched], n, m, grid, head_dim=hd)
         for h in range(m):
             for j in range(n):
                 for pos, i in enumerate(want[(h, j)]):
@@ -67,23 +68,26 @@ def test_deal_matches_oracle(seed):
     for _ in range(20):
         mask, sched = rng.choice([(0, 0), (0, 1), (0, 2), (1, 0), (1, 1), (1, 3)])
         n = rng.choice([1, 2, 3, 4, 6, 8, 12]) if sched != 3 else rng.choice([2, 4, 6, 8, 12])
-        m, grid = rng.randint(1, 6), rng.randint(1, 3 * n + 2)
-        got = da.dash_sched_deal(mask, sched, n, m, grid)
-        want = dag.deal(MASKS[mask], NAMES[sched], n, m, grid)
-        assert got == want, (mask, sched, n, m, grid)
+        m, grid = rng.randint(1, 8), rng.randint(1, 3 * n + 2)
+        hd = rng.choice([64, 128])
+        got = da.dash_sched_deal(mask, sched, n, m, grid, hd)
+        want = dag.deal(MASKS[mask], NAMES[sched], n, m, grid, head_dim=hd)
+        assert got == want, (mask, sched, n, m, grid, hd)
 
 
 def test_deal_at_the_kernel_sizes():
-    # 152 CTAs. Causal 4x16 heads of n = 16 (512 units of 17 tasks) and 1x32 heads of
-    # n = 128 (2048 units of 129) overrun whole rounds: pieces dealt longest first bring
-    # the busiest CTA to the mean (57.3 and 1738.1 tasks) instead of a whole unit above
-    # it. Full 2x16 heads of n = 64 (2048 units of 64, 72 in the last round): those 72 KV
-    # tiles are halved over 144 CTAs, so the busiest runs 13.5 units (mean 13.47).
-    for mask, sched, n, heads, rr_max, max_load, splits in [(1, 3, 16, 64, 68, 58, 0),
-                                                           (1, 3, 128, 32, 1806, 1739, 0),
-                                                           (0, 2, 64, 32, 896, 864, 72)]:
-        got = da.dash_sched_deal(mask, sched, n, heads, 152)
-        want = dag.deal(MASKS[mask], NAMES[sched], n, heads, 152)
+    # 152 CTAs. Causal 4x16 heads of n = 16 at head dim 64 (512 units of 17 tasks): every
+    # unit's pieces dealt longest first bring the busiest CTA to the mean (57.3 tasks)
+    # instead of a whole unit above it. Causal 1x32 heads of n = 128 at head dim 128 (2048
+    # units of 129): 12 round-robin rounds, then the last 224 units' pieces longest first
+    # (mean 1738.1; all pieces: 1739). Full 2x16 heads of n = 64 (2048 units of 64, 72 in
+    # the last round): those 72 KV tiles are halved over 144 CTAs, so the busiest runs 13.5
+    # units (mean 13.47).
+    for mask, sched, n, heads, hd, rr_max, max_load, splits in [
+            (1, 3, 16, 64, 64, 68, 58, 0), (1, 3, 128, 32, 128, 1806, 1757, 0),
+            (1, 3, 128, 32, 64, 1806, 1739, 0), (0, 2, 64, 32, 128, 896, 864, 72)]:
+        got = da.dash_sched_deal(mask, sched, n, heads, 152, hd)
+        want = dag.deal(MASKS[mask], NAMES[sched], n, heads, 152, head_dim=hd)
         assert got == want
         loads = [sum(len(run) for _, run, _, _ in runs) for runs in got]
         assert max(loads) == max_load
@@ -130,8 +134,9 @@ def test_simulator_matches_oracle(seed):
         m = rng.randint(1, 5)
         sms = rng.randint(1, 2 * n + 2)
         c, r = rng.choice([(3.0, 1.0), (1.0, 0.25), (2.0, 2.0), (0.5, 1.5)])
-        want = dag.simulate(MASKS[mask], NAMES[sched], n, m, sms, c, r, dealt=True)
-        mk, ends = da.dash_sched_simulate(mask, sched, n, m, sms, c, r)
+        hd = rng.choice([64, 128])
+        want = dag.simulate(MASKS[mask], NAMES[sched], n, m, sms, c, r, dealt=True, head_dim=hd)
+        mk, ends = da.dash_sched_simulate(mask, sched, n, m, sms, c, r, hd)
         if want["makespan"] is None:
             assert mk is None, (mask, sched, n, m, sms)
         else:
@@ -160,9 +165,10 @@ def test_sync_simulator_matches_oracle(seed):
         c, r = rng.choice([(3.0, 1.0), (1.0, 0.25), (2.0, 2.0), (0.5, 1.5)])
         h = rng.choice([0.0, 0.5, 2.0, 5.0])
         ovl = rng.randint(0, 1)
+        hd = rng.choice([64, 128])
         want = dag.simulate_ex(MASKS[mask], NAMES[sched], n, m, sms, c, r, h, bool(ovl),
-                               dealt=True)
-        mk, ends = da.dash_sched_simulate_ex(mask, sched, n, m, sms, c, r, h, ovl)
+                               dealt=True, head_dim=hd)
+        mk, ends = da.dash_sched_simulate_ex(mask, sched, n, m, sms, c, r, h, ovl, hd)
         if want["makespan"] is None:
             assert mk is None
         else:
@@ -179,15 +185,16 @@ def test_selector_is_the_oracle_argmin(seed):
         m, sms = rng.randint(1, 4), rng.randint(1, 3 * n)
         c, r, h = rng.choice([3.0, 1.0]), rng.choice([1.0, 2.5]), rng.choice([0.0, 1.0, 4.0])
         ovl = rng.randint(0, 1)
+        hd = rng.choice([64, 128])
         best, best_mk = None, None
         for s in (0, 1, 2, 3):
             if not _valid(mask, s, n):
                 continue
             mk = dag.simulate_ex(MASKS[mask], NAMES[s], n, m, sms, c, r, h, bool(ovl),
-                                 dealt=True)["makespan"]
+                                 dealt=True, head_dim=hd)["makespan"]
             if mk is not None and (best is None or mk < best_mk):
                 best, best_mk = s, mk
-        got, got_mk = da.dash_sched_select(mask, n, m, sms, c, r, h, ovl)
+        got, got_mk = da.dash_sched_select(mask, n, m, sms, c, r, h, ovl, hd)
         assert got == best and got_mk == pytest.approx(best_mk)
 
 
@@ -196,13 +203,13 @@ def test_selector_is_the_oracle_argmin(seed):
 GB300_COSTS = (6900.0, 5600.0, 3000.0, 1)
 
 
-@pytest.mark.parametrize("mask,n,heads,measured_best", [
-    (0, 64, 32, 2),     # full 2x16x8192x128: shift measured fastest
-    (1, 128, 32, 3),    # causal 1x32x16384x128: symmetric shift measured fastest
-    (1, 16, 64, 3),     # causal 4x16x2048x64: symmetric shift measured fastest
+@pytest.mark.parametrize("mask,n,heads,hd,measured_best", [
+    (0, 64, 32, 128, 2),     # full 2x16x8192x128: shift measured fastest
+    (1, 128, 32, 128, 3),    # causal 1x32x16384x128: symmetric shift measured fastest
+    (1, 16, 64, 64, 3),      # causal 4x16x2048x64: symmetric shift measured fastest
 ])
-def test_selector_picks_the_measured_best_on_gb300(mask, n, heads, measured_best):
-    got, _ = da.dash_sched_select(mask, n, heads, 152, *GB300_COSTS)
+def test_selector_picks_the_measured_best_on_gb300(mask, n, heads, hd, measured_best):
+    got, _ = da.dash_sched_select(mask, n, heads, 152, *GB300_COSTS, head_dim=hd)
     assert got == measured_best
 
 
@@ -215,3 +222,12 @@ def test_selector_and_simulate_ex_argument_errors():
         da.dash_sched_simulate_ex(0, 0, 8, 1, 8, 1.0, 1.0, -1.0, 0)
     with pytest.raises(da.DashError):
         da.dash_sched_simulate_ex(0, 0, 8, 1, 8, 1.0, 1.0, 0.0, 2)
+    for bad_hd in (0, 96):                              # head dims the kernels do not have
+        with pytest.raises(da.DashError):
+            da.dash_sched_select(0, 8, 1, 8, 1.0, 1.0, 0.0, 0, bad_hd)
+        with pytest.raises(da.DashError):
+            da.dash_sched_simulate_ex(0, 0, 8, 1, 8, 1.0, 1.0, 0.0, 0, bad_hd)
+        with pytest.raises(da.DashError):
+            da.dash_sched_dealt_table(0, 2, 8, 1, 4, bad_hd)
+        with pytest.raises(da.DashError):
+            da.dash_sched_deal(0, 2, 8, 1, 4, bad_hd)
