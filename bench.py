@@ -314,13 +314,15 @@ def run_gpu(args, w, rank, world, local_rank):
         selected_by = "dash_sched_select, costs " + json.dumps(SELECT_COSTS)
     sched = da.SCHEDULES[args.schedule]
     # deterministic mode: 1 = one fixed chain per dQ block (the pages' order as one serial
-    # chain), 2 = the same order as two interleaved chains. Measured on GB300 the second is
-    # faster from S = 2048 on (full 2x8192x16x128: 942 vs 811 TF/s; causal 1x16384x32x128:
-    # 933 vs 841; causal 4x4096x32x128: 769 vs 703; causal 1x16384x32x64: 460 vs 428; causal
-    # 4x2048x16x64: 325 vs 308) and slower at S = 1024 (causal 16x1024x32x128: 432 vs 459),
-    # where chains are short and zeroing and summing the second fp32 copy costs more than
-    # the shorter waits save.
-    DET = ((2 if S >= 2048 else 1) if args.dq_chains == "auto" else int(args.dq_chains))
+    # chain), 2 = the same order as two interleaved chains. Measured on GB300 (TF/s, two
+    # chains vs one) the second pays at head dimension 128 from S = 4096 on (full
+    # 2x8192x16x128: 998 vs 948; causal 4x4096x32x128: 809 vs 776; causal 1x16384x32x128:
+    # 1004 vs 940) and not below (causal 8x2048x32x128: 638 vs 645; 16x1024x32x128: 442 vs
+    # 482), nor at head dimension 64 (causal 4x4096x32x64: 499 vs 532; 1x16384x32x64: 637
+    # vs 633), where the dealing's balanced pieces already keep the waits short and zeroing
+    # and summing the second fp32 copy costs more than they save.
+    DET = ((2 if D == 128 and S >= 4096 else 1) if args.dq_chains == "auto"
+           else int(args.dq_chains))
 
     x = make_inputs(B, S, H, D, seed=rank)
     q, k, v, do = (x[nm].to(dev) for nm in ("q", "k", "v", "do"))
