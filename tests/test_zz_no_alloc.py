@@ -37,6 +37,10 @@ CASES = [
     (1, 1024, 4, 128, False, "shift", 1),
     (2, 512, 3, 64, True, "symmetric_shift", 1),
     (1, 768, 2, 128, True, "descending", 0),
+    # 160 units on a 152-SM grid: full shift splits the last round's 8 KV tiles over two
+    # CTAs each; causal symmetric shift at head dim 64 deals KV-tile pieces longest first
+    (1, 2048, 10, 128, False, "shift", 2),
+    (5, 1024, 8, 64, True, "symmetric_shift", 1),
 ]
 
 
