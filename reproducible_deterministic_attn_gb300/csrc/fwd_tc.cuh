@@ -4,12 +4,17 @@
 // One CTA per (128-row Q tile, batch * head); the longest causal rows are launched first.
 // Per KV tile j (128 keys):
 //   S_j = Q K_j^T        M = 128 q, N = 128 kv, K = D     TMEM cols [128 (j & 1), +128)
-//   running max m, P_j = exp2(S_j * scale*log2e - m)      bf16 in shared buffer j & 1
-//   O  += P_j V_j        M = 128 q, N = D, K = 128 kv     TMEM cols [256, 256 + D)
+//   running max m, P_j = exp2(S_j * scale*log2e - m)      packed bf16 over S_j's first 64
+//                                                         columns (kv 2c, 2c + 1 in col c)
+//   O  += P_j V_j        M = 128 q, N = D, K = 128 kv     TMEM cols [256, 256 + D), A = P_j
+//                                                         read from TMEM
 // S is double-buffered, so S_{j+1} runs on the tensor pipe while the softmax warps work on
-// S_j. When a row's running max grows, its O row is rescaled in TMEM (after P_{j-1} V_{j-1}
-// has landed) before P_j V_j accumulates onto it; rows whose max did not change are left
-// alone. At the end O / l goes to global memory as bf16 and LSE = (m + log2 l) * ln 2.
+// S_j; S_{j+2} reuses the buffer once P_j V_j has read P_j from it. Each softmax thread
+// reads its row's scores from TMEM twice: for the row maximum, then 64 at a time for
+// P (holding all 128 in registers at once measured ~20 % slower). When a row's running max
+// grows, its O row is rescaled in TMEM (after P_{j-1} V_{j-1} has landed) before P_j V_j
+// accumulates onto it; rows whose max did not change are left alone. At the end O / l goes
+// to global memory as bf16 and LSE = (m + log2 l) * ln 2.
 //
 // Warp roles (256 threads): 0 = TMA producer (Q once, K and V in two stages), 1 = MMA
 // issuer, 2..3 idle, 4..7 = softmax (thread = one Q row = one TMEM lane). Every wait is
@@ -27,9 +32,7 @@ struct FwdL {
   static constexpr int TILE = kTile * D * 2;                  // one 128-row bf16 tile
   static constexpr int Q_OFF = 0;
   static constexpr int KV_OFF = Q_OFF + TILE;                 // stage s: K at +2s*TILE, V next
-  static constexpr int P_OFF = KV_OFF + 4 * TILE;             // two P buffers [q][kv] bf16
-  static constexpr int P_BYTES = kTile * kTile * 2;
-  static constexpr int BAR_OFF = P_OFF + 2 * P_BYTES;
+  static constexpr int BAR_OFF = KV_OFF + 4 * TILE;
   static constexpr int TOTAL = BAR_OFF + 256;
   static constexpr int ALLOC = TOTAL + 1024;                  // slack for 1024 alignment
   static_assert(ALLOC <= 232448, "shared memory budget");
@@ -38,8 +41,7 @@ struct FwdL {
 
 enum {
   F_Q_FULL = 0, F_KV_FULL, F_KV_EMPTY = F_KV_FULL + 2, F_S_FULL = F_KV_EMPTY + 2,
-  F_S_EMPTY = F_S_FULL + 2, F_P_FULL = F_S_EMPTY + 2, F_PV_DONE = F_P_FULL + 2,
-  F_DRAIN = F_PV_DONE + 2, F_COUNT
+  F_P_FULL = F_S_FULL + 2, F_PV_DONE = F_P_FULL + 2, F_DRAIN = F_PV_DONE + 2, F_COUNT
 };
 
 constexpr int kFwdThreads = 256;
@@ -68,7 +70,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       ptx::mbar_init(bars + F_KV_FULL + s, 1);
       ptx::mbar_init(bars + F_KV_EMPTY + s, 1);
       ptx::mbar_init(bars + F_S_FULL + s, 1);
-      ptx::mbar_init(bars + F_S_EMPTY + s, 4);
       ptx::mbar_init(bars + F_P_FULL + s, 4);
       ptx::mbar_init(bars + F_PV_DONE + s, 1);
     }
@@ -112,17 +113,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // ====================================== MMA issuer ======================================
     if (lane == 0) {
       const uint32_t sQ = ptx::smem_u32(sm + L::Q_OFF), sKV = ptx::smem_u32(sm + L::KV_OFF);
-      const uint32_t sP = ptx::smem_u32(sm + L::P_OFF);
       const uint32_t dQ_k = ptx::sdesc_lo(sQ, 16);
       constexpr uint32_t ID_S = ptx::idesc_bf16(128, 128, 0, 0);   // S = Q K^T
       constexpr uint32_t ID_O = ptx::idesc_bf16(128, D, 0, 1);     // O += P V (V MN-major)
-      constexpr uint32_t TILE16 = L::TILE >> 4, P16 = L::P_BYTES >> 4;
+      constexpr uint32_t TILE16 = L::TILE >> 4;
       auto kstep = [](int ks) -> uint32_t { return ((ks >> 2) * kTile * 128 + (ks & 3) * 32) >> 4; };
       constexpr uint32_t MN_STEP = 2048 >> 4;
       auto issue_s = [&](int j) -> bool {
         const int s = j & 1;
         if (!ptx::mbar_wait(bars + F_KV_FULL + s, (j >> 1) & 1, abort_flag, tmo)) return false;
-        if (j >= 2 && !ptx::mbar_wait(bars + F_S_EMPTY + s, ((j >> 1) - 1) & 1, abort_flag, tmo))
+        // the buffer's last reader: P_{j-2} V_{j-2} (which came after the softmax's reads)
+        if (j >= 2 && !ptx::mbar_wait(bars + F_PV_DONE + s, ((j >> 1) - 1) & 1, abort_flag, tmo))
           return false;
         ptx::tc_fence_after();
         const uint32_t dK_k = ptx::sdesc_lo(sKV, 16) + 2 * s * TILE16;
@@ -138,12 +139,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (j + 1 < nt && !(ok = issue_s(j + 1))) break;
         if (!(ok = ptx::mbar_wait(bars + F_P_FULL + s, (j >> 1) & 1, abort_flag, tmo))) break;
         ptx::tc_fence_after();
-        // O += P_j V_j: A = P (K-major over kv), B = V (MN-major over d)
-        const uint32_t dP_k = ptx::sdesc_lo(sP, 16) + s * P16;
+        // O += P_j V_j: A = P_j from TMEM (16 kv = 8 packed columns per step), B = V
+        // (MN-major over d)
         const uint32_t dV_mn = ptx::sdesc_lo(sKV + (2 * s + 1) * L::TILE, kTile * 128);
 #pragma unroll
         for (int ks = 0; ks < kTile / 16; ++ks)
-          ptx::mma_lo(tmem + L::T_O, dP_k + kstep(ks), dV_mn + ks * MN_STEP, ID_O,
+          ptx::mma_ts(tmem + L::T_O, tmem + L::T_S + 128 * s + 8 * ks, dV_mn + ks * MN_STEP, ID_O,
                       (j > 0 || ks > 0) ? 1u : 0u);
         ptx::mma_commit(bars + F_PV_DONE + s);
         ptx::mma_commit(bars + F_KV_EMPTY + s);
@@ -156,7 +157,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;                 // Q row within the tile = TMEM lane
     const uint32_t lane_addr = ((uint32_t)(quarter * 32) << 16);
-    const uint32_t sP = ptx::smem_u32(sm + L::P_OFF);
     float m = -INFINITY, l = 0.f;                     // running max (log2 units) and sum
     bool ok = true;
     for (int j = 0; ok && j < nt; ++j) {
@@ -166,42 +166,43 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       ptx::tc_fence_after();
       const uint32_t t_s = tmem + lane_addr + L::T_S + 128 * s;
       const bool diag = p.causal && j == qt;           // keys after row r are masked there
-      // pass 1: the row maximum of the scaled scores
       float mx = -INFINITY;
 #pragma unroll
       for (int c0 = 0; c0 < kTile; c0 += 32) {
-        float v[32];
-        ptx::tmem_ld32(t_s + c0, v);
+        float t[32];
+        ptx::tmem_ld32(t_s + c0, t);
 #pragma unroll
         for (int c = 0; c < 32; ++c)
-          if (!diag || c0 + c <= r) mx = fmaxf(mx, v[c]);
+          if (!diag || c0 + c <= r) mx = fmaxf(mx, t[c]);
       }
       const float m_new = fmaxf(m, mx * p.scale_log2);
-      // P_j goes into buffer s once P_{j-2} V_{j-2} has read it
-      if (j >= 2) ok = ptx::warp_wait(bars + F_PV_DONE + s, ((j >> 1) - 1) & 1, abort_flag, tmo);
-      if (!ok) break;
-      // pass 2: P = exp2(S * scale*log2e - m_new), row sum, bf16 into the P buffer
       float lt = 0.f;
 #pragma unroll
-      for (int c0 = 0; c0 < kTile; c0 += 32) {
-        float v[32];
-        ptx::tmem_ld32(t_s + c0, v);
+      for (int c0 = 0; c0 < kTile; c0 += 64) {
+        float v[64];
+        {
+          float t[32];
+          ptx::tmem_ld32(t_s + c0, t);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float e = ptx::ex2(fmaf(v[c], p.scale_log2, -m_new));
-          v[c] = (!diag || c0 + c <= r) ? e : 0.f;
-          lt += v[c];
+          for (int c = 0; c < 32; ++c) v[c] = t[c];
+          ptx::tmem_ld32(t_s + c0 + 32, t);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[32 + c] = t[c];
         }
+        uint32_t u[32];
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          ptx::st_shared_v4(sP + s * L::P_BYTES + sw_chunk(r, (c0 >> 3) + k, kTile),
-                            ptx::pack_bf16(v[8 * k], v[8 * k + 1]), ptx::pack_bf16(v[8 * k + 2], v[8 * k + 3]),
-                            ptx::pack_bf16(v[8 * k + 4], v[8 * k + 5]), ptx::pack_bf16(v[8 * k + 6], v[8 * k + 7]));
+        for (int k = 0; k < 32; ++k) {
+          const int c = c0 + 2 * k;
+          float e0 = ptx::ex2(fmaf(v[2 * k], p.scale_log2, -m_new));
+          float e1 = ptx::ex2(fmaf(v[2 * k + 1], p.scale_log2, -m_new));
+          e0 = (!diag || c <= r) ? e0 : 0.f;
+          e1 = (!diag || c + 1 <= r) ? e1 : 0.f;
+          lt += e0;
+          lt += e1;
+          u[k] = ptx::pack_bf16(e0, e1);
+        }
+        ptx::tmem_st32(t_s + c0 / 2, u);
       }
-      // S_j has been read: S_{j+2} may overwrite its columns
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bars + F_S_EMPTY + s);
       const float alpha = ptx::ex2(m - m_new);        // 0 on the first tile (m = -inf)
       l = l * alpha + lt;
       m = m_new;
@@ -212,15 +213,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ptx::tc_fence_after();
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
-          float v[32];
-          ptx::tmem_ld32(tmem + lane_addr + L::T_O + c0, v);
-          uint32_t u[32];
+          float o[32];
+          ptx::tmem_ld32(tmem + lane_addr + L::T_O + c0, o);
+          uint32_t uo[32];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) u[c] = __float_as_uint(v[c] * alpha);
-          ptx::tmem_st32(tmem + lane_addr + L::T_O + c0, u);
+          for (int c = 0; c < 32; ++c) uo[c] = __float_as_uint(o[c] * alpha);
+          ptx::tmem_st32(tmem + lane_addr + L::T_O + c0, uo);
         }
       }
-      ptx::fence_proxy_async_smem();
+      ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bars + F_P_FULL + s);
