@@ -403,10 +403,20 @@ dash_status_t dash_attn_fwd_ex(const void* q, const void* k, const void* v, void
     g_last_error = "cuTensorMapEncodeTiled rejected a tensor";
     return DASH_ERR_CUDA;
   }
-  // one CTA per (128-row Q tile, batch * head); blockIdx.x counts the Q tiles from the last
-  dim3 grid(S / dash::kTile, B * H);
+  // one CTA per pair of adjacent 128-row Q tiles of one batch * head; blockIdx.x is the
+  // batch * head and blockIdx.y counts the pairs from the last tiles, so blocks are handed
+  // out pair rank by pair rank over all heads: under a causal mask, longest first
+  dim3 grid(B * H, (S / dash::kTile + 1) / 2);
   void* kfn = D == 64 ? (void*)dash::tc::fwd_tc_kernel<64> : (void*)dash::tc::fwd_tc_kernel<128>;
   const size_t smem = D == 64 ? dash::tc::FwdL<64>::ALLOC : dash::tc::FwdL<128>::ALLOC;
+  // the kernel moves registers between its warpgroups (setmaxnreg); the split adds up to
+  // exactly the per-thread count it is launched with, so any other count is refused
+  cudaFuncAttributes fa;
+  DASH_CUDA(cudaFuncGetAttributes(&fa, kfn));
+  if (fa.numRegs != dash::tc::kFwdRegsLaunch) {
+    g_last_error = "forward kernel was not built with the register count its warp roles share";
+    return DASH_ERR_CUDA;
+  }
   DASH_CUDA(cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   if (status) DASH_CUDA(cudaMemsetAsync(status, 0, sizeof(int), stream));
   void* args[] = {&p, &maps};

@@ -1,25 +1,30 @@
 // Forward pass on the 5th-generation tensor cores: O = softmax(scale * Q K^T) V and the
 // natural-log LSE per row, the inputs from which the backward recomputes P.
 //
-// One CTA per (128-row Q tile, batch * head); the longest causal rows are launched first.
-// Per KV tile j (128 keys):
-//   S_j = Q K_j^T        M = 128 q, N = 128 kv, K = D     TMEM cols [128 (j & 1), +128)
-//   running max m, P_j = exp2(S_j * scale*log2e - m)      packed bf16 over S_j's first 64
-//                                                         columns (kv 2c, 2c + 1 in col c)
-//   O  += P_j V_j        M = 128 q, N = D, K = 128 kv     TMEM cols [256, 256 + D), A = P_j
-//                                                         read from TMEM
-// S is double-buffered, so S_{j+1} runs on the tensor pipe while the softmax warps work on
-// S_j; S_{j+2} reuses the buffer once P_j V_j has read P_j from it. Each softmax thread
-// reads its row's scores from TMEM twice: for the row maximum, then 64 at a time for
-// P (holding all 128 in registers at once measured ~20 % slower). When a row's running max
-// grows, its O row is rescaled in TMEM (after P_{j-1} V_{j-1} has landed) before P_j V_j
-// accumulates onto it; rows whose max did not change are left alone. At the end O / l goes
-// to global memory as bf16 and LSE = (m + log2 l) * ln 2.
+// One CTA per pair of 128-row Q tiles (A and B, adjacent tiles of one batch * head); the
+// pairs with the longest causal rows are launched first. Each tile has its own softmax
+// warpgroup and its own TMEM, and both walk the same K/V tiles. Per KV tile j (128 keys),
+// for tile x in {A, B}:
+//   S_x = Q_x K_j^T       M = 128 q, N = 128 kv, K = D    TMEM cols [128 x, +128)
+//   running max m, P_x = exp2(S_x * scale*log2e - m)     packed bf16 over S_x's first 64
+//                                                        columns (kv 2c, 2c + 1 in col c)
+//   O_x += P_x V_j        M = 128 q, N = D, K = 128 kv    TMEM cols [256 + D x, +D), A = P_x
+//                                                        read from TMEM
+// The two tiles ping-pong on the tensor pipe: while one warpgroup turns S into P, the MMAs
+// of the other run. S_x(j+1) overwrites P_x(j) once P_x(j) V_j has read it. The MMA
+// issuer polls both tiles' barriers and issues whatever is ready next, so neither tile
+// waits behind the other. Each softmax thread reads its row's scores from TMEM twice: for
+// the row maximum, then 64 at a time for P (holding all 128 in registers at once measured
+// slower). When a row's running max grows, its O row is rescaled in TMEM (P_x(j-1) V_{j-1}
+// has landed by then: S_x(j) waited for it) before P_x(j) V_j accumulates onto it; rows
+// whose max did not change are left alone. At the end O / l goes to global memory as bf16
+// and LSE = (m + log2 l) * ln 2.
 //
-// Warp roles (256 threads): 0 = TMA producer (Q once, K and V in two stages), 1 = MMA
-// issuer, 2..3 idle, 4..7 = softmax (thread = one Q row = one TMEM lane). Every wait is
-// bounded; a CTA that gives up writes NaN into its LSE rows and, when the caller passed a
-// status word, records DASH_ERR_SYNC_TIMEOUT there, so the failure cannot pass unnoticed.
+// Warp roles (384 threads): 0 = TMA producer (both Q tiles once, K and V in two stages),
+// 1 = MMA issuer, 2..3 idle, 4..7 = softmax of tile A, 8..11 = softmax of tile B (thread =
+// one Q row = one TMEM lane). Every wait is bounded; a CTA that gives up writes NaN into
+// its LSE rows and, when the caller passed a status word, records DASH_ERR_SYNC_TIMEOUT
+// there, so the failure cannot pass unnoticed.
 #pragma once
 
 #include "tc_shared.cuh"
@@ -30,21 +35,49 @@ namespace tc {
 template <int D>
 struct FwdL {
   static constexpr int TILE = kTile * D * 2;                  // one 128-row bf16 tile
-  static constexpr int Q_OFF = 0;
-  static constexpr int KV_OFF = Q_OFF + TILE;                 // stage s: K at +2s*TILE, V next
+  static constexpr int Q_OFF = 0;                             // tile A, then tile B
+  static constexpr int KV_OFF = Q_OFF + 2 * TILE;             // stage s: K at +2s*TILE, V next
   static constexpr int BAR_OFF = KV_OFF + 4 * TILE;
   static constexpr int TOTAL = BAR_OFF + 256;
   static constexpr int ALLOC = TOTAL + 1024;                  // slack for 1024 alignment
   static_assert(ALLOC <= 232448, "shared memory budget");
-  static constexpr int T_S = 0, T_O = 256;                     // TMEM columns
+  static constexpr int T_S = 0, T_O = 256;                    // TMEM columns (+128 x, +D x)
+  static_assert(T_O + 2 * D <= 512, "TMEM columns");
 };
+
+// registers per thread: launched at 168 (384 threads), re-split so the two softmax
+// warpgroups hold a row's scores and the producer / issuer warpgroup gives them its share
+constexpr int kFwdThreads = 384;
+constexpr int kFwdRegsLaunch = 168, kFwdRegsCtrl = 88, kFwdRegsSoftmax = 208;
+static_assert(kFwdRegsCtrl + 2 * kFwdRegsSoftmax == 3 * kFwdRegsLaunch,
+              "the three warpgroups must share exactly the launch's registers");
 
 enum {
   F_Q_FULL = 0, F_KV_FULL, F_KV_EMPTY = F_KV_FULL + 2, F_S_FULL = F_KV_EMPTY + 2,
   F_P_FULL = F_S_FULL + 2, F_PV_DONE = F_P_FULL + 2, F_DRAIN = F_PV_DONE + 2, F_COUNT
 };
 
-constexpr int kFwdThreads = 256;
+// P for 32 scores of a row (columns c0 .. c0 + 31 of S): exp2(S * scale*log2e - m_new),
+// zero where the causal mask removes the key, added into the row's partial sums (column c
+// into lt4[c % 4]) and stored as 16 packed bf16 columns at t_p.
+__device__ __forceinline__ void fwd_p_chunk(const uint32_t (&t)[32], int c0, bool diag, int r,
+                                            float scale_log2, float m_new, float (&lt4)[4],
+                                            uint32_t t_p) {
+  uint32_t u[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const int c = c0 + 2 * k;
+    float e0 = ptx::ex2(fmaf(__uint_as_float(t[2 * k]), scale_log2, -m_new));
+    float e1 = ptx::ex2(fmaf(__uint_as_float(t[2 * k + 1]), scale_log2, -m_new));
+    e0 = (!diag || c <= r) ? e0 : 0.f;
+    e1 = (!diag || c + 1 <= r) ? e1 : 0.f;
+    lt4[(2 * k) & 3] += e0;
+    lt4[(2 * k + 1) & 3] += e1;
+    u[k] = ptx::pack_bf16(e0, e1);
+  }
+  ptx::tmem_st8(t_p, u);
+  ptx::tmem_st8(t_p + 8, u + 8);
+}
 
 template <int D>
 __global__ void __launch_bounds__(kFwdThreads, 1)
@@ -59,17 +92,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const long long tmo = p.timeout_ns;   // per wait: far beyond any legitimate wait
 
   const int n = p.S / kTile;
-  const int qt = n - 1 - (int)blockIdx.x;          // longest causal rows first
-  const int bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
-  const int nt = p.causal ? qt + 1 : n;            // KV tiles this Q tile sees
-  const int q0 = qt * kTile;
+  const int qa = n - 1 - 2 * (int)blockIdx.y;      // longest causal rows first
+  const int qb = qa - 1;                            // tile B (absent when qa is tile 0)
+  const bool has_b = qb >= 0;
+  const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
+  const int nt_a = p.causal ? qa + 1 : n;          // KV tiles each Q tile sees
+  const int nt_b = has_b ? (p.causal ? qb + 1 : n) : 0;
+  const int nt = nt_a;                              // KV tiles loaded (nt_b <= nt_a)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bars + F_Q_FULL, 1);
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(bars + F_KV_FULL + s, 1);
       ptx::mbar_init(bars + F_KV_EMPTY + s, 1);
-      ptx::mbar_init(bars + F_S_FULL + s, 1);
+      ptx::mbar_init(bars + F_S_FULL + s, 1);      // per Q tile from here on
       ptx::mbar_init(bars + F_P_FULL + s, 4);
       ptx::mbar_init(bars + F_PV_DONE + s, 1);
     }
@@ -83,13 +119,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ===================================== TMA producer =====================================
-    if (lane == 0) {
-      ptx::mbar_expect_tx(bars + F_Q_FULL, L::TILE);
-      for (int cb = 0; cb < D / 64; ++cb)
-        ptx::tma_load_3d(sm + L::Q_OFF + cb * kTile * 128, &maps.q, cb * 64, h, b * p.S + q0,
-                         bars + F_Q_FULL);
+  if (warp < 4) {
+    ptx::regs_dec<kFwdRegsCtrl>();
+    if (warp == 0 && lane == 0) {
+      // ===================================== TMA producer =====================================
+      ptx::mbar_expect_tx(bars + F_Q_FULL, (has_b ? 2 : 1) * L::TILE);
+      for (int x = 0; x < (has_b ? 2 : 1); ++x)
+        for (int cb = 0; cb < D / 64; ++cb)
+          ptx::tma_load_3d(sm + L::Q_OFF + x * L::TILE + cb * kTile * 128, &maps.q, cb * 64, h,
+                           b * p.S + (x ? qb : qa) * kTile, bars + F_Q_FULL);
       int j = 0;
       for (; j < (p.withhold_kv ? 0 : nt); ++j) {
         const int s = j & 1;
@@ -108,147 +146,188 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       ptx::mbar_drain(bars + F_Q_FULL, 0, 100000000ll);
       for (int k = (j > 2 ? j - 2 : 0); k < j; ++k)
         ptx::mbar_drain(bars + F_KV_FULL + (k & 1), (k >> 1) & 1, 100000000ll);
-    }
-  } else if (warp == 1) {
-    // ====================================== MMA issuer ======================================
-    if (lane == 0) {
+    } else if (warp == 1 && lane == 0) {
+      // ====================================== MMA issuer ======================================
+      // Per tile x: ns[x] = next S to issue, np[x] = next P V to issue. S_x(t) needs K_t
+      // landed and P_x(t-1) V_{t-1} done (S_x overwrites P_x), and follows P_x(t-1) V_{t-1}
+      // in issue order; P_x(t) V_t needs P_x(t) stored. A KV stage is released once both
+      // tiles have issued their P V for its tile. The loop polls and issues what is ready.
       const uint32_t sQ = ptx::smem_u32(sm + L::Q_OFF), sKV = ptx::smem_u32(sm + L::KV_OFF);
-      const uint32_t dQ_k = ptx::sdesc_lo(sQ, 16);
       constexpr uint32_t ID_S = ptx::idesc_bf16(128, 128, 0, 0);   // S = Q K^T
       constexpr uint32_t ID_O = ptx::idesc_bf16(128, D, 0, 1);     // O += P V (V MN-major)
       constexpr uint32_t TILE16 = L::TILE >> 4;
-      auto kstep = [](int ks) -> uint32_t { return ((ks >> 2) * kTile * 128 + (ks & 3) * 32) >> 4; };
       constexpr uint32_t MN_STEP = 2048 >> 4;
-      auto issue_s = [&](int j) -> bool {
-        const int s = j & 1;
-        if (!ptx::mbar_wait(bars + F_KV_FULL + s, (j >> 1) & 1, abort_flag, tmo)) return false;
-        // the buffer's last reader: P_{j-2} V_{j-2} (which came after the softmax's reads)
-        if (j >= 2 && !ptx::mbar_wait(bars + F_PV_DONE + s, ((j >> 1) - 1) & 1, abort_flag, tmo))
-          return false;
-        ptx::tc_fence_after();
-        const uint32_t dK_k = ptx::sdesc_lo(sKV, 16) + 2 * s * TILE16;
+      int ns[2] = {0, 0}, np[2] = {0, 0};
+      const int ntx[2] = {nt_a, nt_b};
+      int kv_rel = 0;
+      bool ok = ptx::mbar_wait(bars + F_Q_FULL, 0, abort_flag, tmo);
+      long long t_last = global_timer_ns();
+      while (ok && (np[0] < nt_a || np[1] < nt_b)) {
+        bool progress = false;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          ptx::mma_lo(tmem + L::T_S + 128 * s, dQ_k + kstep(ks), dK_k + kstep(ks), ID_S, ks > 0);
-        ptx::mma_commit(bars + F_S_FULL + s);
-        return true;
-      };
-      bool ok = ptx::mbar_wait(bars + F_Q_FULL, 0, abort_flag, tmo) && issue_s(0);
-      for (int j = 0; ok && j < nt; ++j) {
-        const int s = j & 1;
-        if (j + 1 < nt && !(ok = issue_s(j + 1))) break;
-        if (!(ok = ptx::mbar_wait(bars + F_P_FULL + s, (j >> 1) & 1, abort_flag, tmo))) break;
-        ptx::tc_fence_after();
-        // O += P_j V_j: A = P_j from TMEM (16 kv = 8 packed columns per step), B = V
-        // (MN-major over d)
-        const uint32_t dV_mn = ptx::sdesc_lo(sKV + (2 * s + 1) * L::TILE, kTile * 128);
+        for (int x = 0; x < 2; ++x) {
+          const int t = ns[x];
+          if (t < ntx[x] && t == np[x] &&
+              ptx::mbar_try(bars + F_KV_FULL + (t & 1), (t >> 1) & 1) &&
+              (t == 0 || ptx::mbar_try(bars + F_PV_DONE + x, (t - 1) & 1))) {
+            ptx::tc_fence_after();
+            const uint32_t dQ_k = ptx::sdesc_lo(sQ, 16) + x * TILE16;
+            const uint32_t dK_k = ptx::sdesc_lo(sKV, 16) + 2 * (t & 1) * TILE16;
 #pragma unroll
-        for (int ks = 0; ks < kTile / 16; ++ks)
-          ptx::mma_ts(tmem + L::T_O, tmem + L::T_S + 128 * s + 8 * ks, dV_mn + ks * MN_STEP, ID_O,
-                      (j > 0 || ks > 0) ? 1u : 0u);
-        ptx::mma_commit(bars + F_PV_DONE + s);
-        ptx::mma_commit(bars + F_KV_EMPTY + s);
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const uint32_t step = ((ks >> 2) * kTile * 128 + (ks & 3) * 32) >> 4;
+              ptx::mma_lo(tmem + L::T_S + 128 * x, dQ_k + step, dK_k + step, ID_S, ks > 0);
+            }
+            ptx::mma_commit(bars + F_S_FULL + x);
+            ns[x] = t + 1;
+            progress = true;
+          }
+          const int u = np[x];
+          if (u < ns[x] && ptx::mbar_try(bars + F_P_FULL + x, u & 1)) {
+            ptx::tc_fence_after();
+            // O_x += P_x V_u: A = P_x from TMEM (16 kv = 8 packed columns per step), B = V
+            // (MN-major over d)
+            const uint32_t dV_mn = ptx::sdesc_lo(sKV + (2 * (u & 1) + 1) * L::TILE, kTile * 128);
+#pragma unroll
+            for (int ks = 0; ks < kTile / 16; ++ks)
+              ptx::mma_ts(tmem + L::T_O + D * x, tmem + L::T_S + 128 * x + 8 * ks,
+                          dV_mn + ks * MN_STEP, ID_O, (u > 0 || ks > 0) ? 1u : 0u);
+            ptx::mma_commit(bars + F_PV_DONE + x);
+            np[x] = u + 1;
+            progress = true;
+          }
+        }
+        // KV stage of tile kv_rel: free once every tile that reads it has issued its P V
+        while (kv_rel < nt && (np[0] > kv_rel || nt_a <= kv_rel) &&
+               (np[1] > kv_rel || nt_b <= kv_rel)) {
+          ptx::mma_commit(bars + F_KV_EMPTY + (kv_rel & 1));
+          ++kv_rel;
+        }
+        if (progress) {
+          t_last = global_timer_ns();
+        } else if (__nanosleep(32), *abort_flag) {   // idle: leave the issue slots to softmax
+          ok = false;
+        } else if (global_timer_ns() - t_last > tmo) {
+          *abort_flag = 1;
+          ok = false;
+        }
       }
       ptx::mma_commit(bars + F_DRAIN);
       ptx::mbar_drain(bars + F_DRAIN, 0, 1000000000ll);
     }
-  } else if (warp >= 4) {
+  } else {
+    ptx::regs_inc<kFwdRegsSoftmax>();
     // ======================================= softmax ========================================
+    const int x = (warp - 4) >> 2;                   // Q tile: 0 = A, 1 = B
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;                 // Q row within the tile = TMEM lane
+    const int r = quarter * 32 + lane;               // Q row within the tile = TMEM lane
     const uint32_t lane_addr = ((uint32_t)(quarter * 32) << 16);
-    float m = -INFINITY, l = 0.f;                     // running max (log2 units) and sum
+    const int qt = x ? qb : qa, ntt = x ? nt_b : nt_a;
+    const uint32_t t_s = tmem + lane_addr + L::T_S + 128 * x;
+    const uint32_t t_o = tmem + lane_addr + L::T_O + D * x;
+    float m = -INFINITY, l = 0.f;                   // running max (log2 units) and sum
     bool ok = true;
-    for (int j = 0; ok && j < nt; ++j) {
-      const int s = j & 1;
-      ok = ptx::warp_wait(bars + F_S_FULL + s, (j >> 1) & 1, abort_flag, tmo);
+    for (int j = 0; ok && j < ntt; ++j) {
+      ok = ptx::warp_wait(bars + F_S_FULL + x, j & 1, abort_flag, tmo);
       if (!ok) break;
       ptx::tc_fence_after();
-      const uint32_t t_s = tmem + lane_addr + L::T_S + 128 * s;
-      const bool diag = p.causal && j == qt;           // keys after row r are masked there
+      const bool diag = p.causal && j == qt;         // keys after row r are masked there
+      // Both passes read S 32 columns at a time with the next 32 loading while the current
+      // ones are used (one load in flight at a time; a wait covers every earlier load).
+      // pass 1: the row maximum of the scaled scores
       float mx = -INFINITY;
+      {
+        uint32_t ta[32], tb[32];
+        ptx::tmem_ld32_issue(t_s, ta);
+        ptx::tmem_ld32_wait(ta);
 #pragma unroll
-      for (int c0 = 0; c0 < kTile; c0 += 32) {
-        float t[32];
-        ptx::tmem_ld32(t_s + c0, t);
+        for (int c0 = 0; c0 < kTile; c0 += 64) {
+          ptx::tmem_ld32_issue(t_s + c0 + 32, tb);
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if (!diag || c0 + c <= r) mx = fmaxf(mx, t[c]);
+          for (int c = 0; c < 32; ++c)
+            if (!diag || c0 + c <= r) mx = fmaxf(mx, __uint_as_float(ta[c]));
+          ptx::tmem_ld32_wait(tb);
+          if (c0 + 64 < kTile) ptx::tmem_ld32_issue(t_s + c0 + 64, ta);
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (!diag || c0 + 32 + c <= r) mx = fmaxf(mx, __uint_as_float(tb[c]));
+          if (c0 + 64 < kTile) ptx::tmem_ld32_wait(ta);
+        }
       }
       const float m_new = fmaxf(m, mx * p.scale_log2);
-      float lt = 0.f;
+      // pass 2: P = exp2(S * scale*log2e - m_new), row sum, packed bf16 over the first 64
+      // columns: columns c0 .. c0 + 31 go to packed columns c0 / 2 .. c0 / 2 + 15, which
+      // lie in scores this thread has already read and not in the 32 loading meanwhile.
+      // The row sum is four partial sums, added in a fixed order at the end.
+      float lt4[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        uint32_t ta[32], tb[32];
+        ptx::tmem_ld32_issue(t_s, ta);
+        ptx::tmem_ld32_wait(ta);
 #pragma unroll
-      for (int c0 = 0; c0 < kTile; c0 += 64) {
-        float v[64];
-        {
-          float t[32];
-          ptx::tmem_ld32(t_s + c0, t);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) v[c] = t[c];
-          ptx::tmem_ld32(t_s + c0 + 32, t);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) v[32 + c] = t[c];
+        for (int c0 = 0; c0 < kTile; c0 += 64) {
+          ptx::tmem_ld32_issue(t_s + c0 + 32, tb);
+          fwd_p_chunk(ta, c0, diag, r, p.scale_log2, m_new, lt4, t_s + c0 / 2);
+          ptx::tmem_ld32_wait(tb);
+          if (c0 + 64 < kTile) ptx::tmem_ld32_issue(t_s + c0 + 64, ta);
+          fwd_p_chunk(tb, c0 + 32, diag, r, p.scale_log2, m_new, lt4, t_s + (c0 + 32) / 2);
+          if (c0 + 64 < kTile) ptx::tmem_ld32_wait(ta);
         }
-        uint32_t u[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int c = c0 + 2 * k;
-          float e0 = ptx::ex2(fmaf(v[2 * k], p.scale_log2, -m_new));
-          float e1 = ptx::ex2(fmaf(v[2 * k + 1], p.scale_log2, -m_new));
-          e0 = (!diag || c <= r) ? e0 : 0.f;
-          e1 = (!diag || c + 1 <= r) ? e1 : 0.f;
-          lt += e0;
-          lt += e1;
-          u[k] = ptx::pack_bf16(e0, e1);
-        }
-        ptx::tmem_st32(t_s + c0 / 2, u);
       }
-      const float alpha = ptx::ex2(m - m_new);        // 0 on the first tile (m = -inf)
+      const float lt = (lt4[0] + lt4[1]) + (lt4[2] + lt4[3]);
+      const float alpha = ptx::ex2(m - m_new);      // 0 on the first tile (m = -inf)
       l = l * alpha + lt;
       m = m_new;
-      // rescale this warp's O rows when any of their maxima grew (after P_{j-1} V_{j-1})
+      // rescale this warp's O rows when any of their maxima grew (P_x(j-1) V_{j-1} is done:
+      // S_x(j) was issued after it)
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        ok = ptx::warp_wait(bars + F_PV_DONE + (s ^ 1), ((j - 1) >> 1) & 1, abort_flag, tmo);
-        if (!ok) break;
-        ptx::tc_fence_after();
+        uint32_t oa[32], ob[32];
+        ptx::tmem_ld32_issue(t_o, oa);
+        ptx::tmem_ld32_wait(oa);
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          float o[32];
-          ptx::tmem_ld32(tmem + lane_addr + L::T_O + c0, o);
-          uint32_t uo[32];
+        for (int c0 = 0; c0 < D; c0 += 64) {
+          ptx::tmem_ld32_issue(t_o + c0 + 32, ob);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) uo[c] = __float_as_uint(o[c] * alpha);
-          ptx::tmem_st32(tmem + lane_addr + L::T_O + c0, uo);
+          for (int c = 0; c < 32; ++c) oa[c] = __float_as_uint(__uint_as_float(oa[c]) * alpha);
+          ptx::tmem_st32(t_o + c0, oa);
+          ptx::tmem_ld32_wait(ob);
+          if (c0 + 64 < D) ptx::tmem_ld32_issue(t_o + c0 + 64, oa);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) ob[c] = __float_as_uint(__uint_as_float(ob[c]) * alpha);
+          ptx::tmem_st32(t_o + c0 + 32, ob);
+          if (c0 + 64 < D) ptx::tmem_ld32_wait(oa);
         }
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bars + F_P_FULL + s);
+      if (lane == 0) ptx::mbar_arrive(bars + F_P_FULL + x);
     }
     // epilogue: O / l as bf16, LSE = (m + log2 l) * ln 2
-    const int last = nt - 1;
-    if (ok) ok = ptx::warp_wait(bars + F_PV_DONE + (last & 1), (last >> 1) & 1, abort_flag, tmo);
-    const size_t row = (size_t)b * p.S + q0 + r;
-    if (ok) {
-      ptx::tc_fence_after();
-      const float inv = 1.f / l;
-      __nv_bfloat16* dst = p.o + (row * p.H + h) * D;
+    if (ntt > 0) {
+      const int last = ntt - 1;
+      if (ok) ok = ptx::warp_wait(bars + F_PV_DONE + x, last & 1, abort_flag, tmo);
+      const size_t row = (size_t)b * p.S + (size_t)qt * kTile + r;
+      if (ok) {
+        ptx::tc_fence_after();
+        const float inv = 1.f / l;
+        __nv_bfloat16* dst = p.o + (row * p.H + h) * D;
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        float v[32];
-        ptx::tmem_ld32(tmem + lane_addr + L::T_O + c0, v);
-        uint4* d4 = (uint4*)(dst + c0);
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          float v[32];
+          ptx::tmem_ld32(t_o + c0, v);
+          uint4* d4 = (uint4*)(dst + c0);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          d4[k] = make_uint4(ptx::pack_bf16(v[8 * k] * inv, v[8 * k + 1] * inv),
-                             ptx::pack_bf16(v[8 * k + 2] * inv, v[8 * k + 3] * inv),
-                             ptx::pack_bf16(v[8 * k + 4] * inv, v[8 * k + 5] * inv),
-                             ptx::pack_bf16(v[8 * k + 6] * inv, v[8 * k + 7] * inv));
+          for (int k = 0; k < 4; ++k)
+            d4[k] = make_uint4(ptx::pack_bf16(v[8 * k] * inv, v[8 * k + 1] * inv),
+                               ptx::pack_bf16(v[8 * k + 2] * inv, v[8 * k + 3] * inv),
+                               ptx::pack_bf16(v[8 * k + 4] * inv, v[8 * k + 5] * inv),
+                               ptx::pack_bf16(v[8 * k + 6] * inv, v[8 * k + 7] * inv));
+        }
+        p.lse[(size_t)bh * p.S + (size_t)qt * kTile + r] = (m + __log2f(l)) * kLn2;
+      } else {
+        p.lse[(size_t)bh * p.S + (size_t)qt * kTile + r] = __int_as_float(0x7fc00000);   // NaN
       }
-      p.lse[(size_t)bh * p.S + q0 + r] = (m + __log2f(l)) * kLn2;
-    } else {
-      p.lse[(size_t)bh * p.S + q0 + r] = __int_as_float(0x7fc00000);   // NaN: this tile failed
     }
   }
 
