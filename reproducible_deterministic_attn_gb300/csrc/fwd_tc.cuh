@@ -48,6 +48,7 @@ struct FwdL {
 // registers per thread: launched at 168 (384 threads), re-split so the two softmax
 // warpgroups hold a row's scores and the producer / issuer warpgroup gives them its share
 constexpr int kFwdThreads = 384;
+constexpr float kFwdRescaleLog2 = 8.f;   // lazy rescale threshold (log2 units): P <= 2^8
 constexpr int kFwdRegsLaunch = 168, kFwdRegsCtrl = 88, kFwdRegsSoftmax = 208;
 static_assert(kFwdRegsCtrl + 2 * kFwdRegsSoftmax == 3 * kFwdRegsLaunch,
               "the three warpgroups must share exactly the launch's registers");
@@ -56,6 +57,19 @@ enum {
   F_Q_FULL = 0, F_KV_FULL, F_KV_EMPTY = F_KV_FULL + 2, F_S_FULL = F_KV_EMPTY + 2,
   F_P_FULL = F_S_FULL + 2, F_PV_DONE = F_P_FULL + 2, F_DRAIN = F_PV_DONE + 2, F_COUNT
 };
+
+// Non-blocking test of an mbarrier phase. The issuer polls several barriers in turn, so it
+// must not use try_wait, which may suspend the thread on a phase that is not yet complete
+// while another barrier is already ready.
+__device__ __forceinline__ bool fwd_mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(done)
+      : "r"(ptx::smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
 
 // P for 32 scores of a row (columns c0 .. c0 + 31 of S): exp2(S * scale*log2e - m_new),
 // zero where the causal mask removes the key, added into the row's partial sums (column c
@@ -168,8 +182,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int x = 0; x < 2; ++x) {
           const int t = ns[x];
           if (t < ntx[x] && t == np[x] &&
-              ptx::mbar_try(bars + F_KV_FULL + (t & 1), (t >> 1) & 1) &&
-              (t == 0 || ptx::mbar_try(bars + F_PV_DONE + x, (t - 1) & 1))) {
+              fwd_mbar_test(bars + F_KV_FULL + (t & 1), (t >> 1) & 1) &&
+              (t == 0 || fwd_mbar_test(bars + F_PV_DONE + x, (t - 1) & 1))) {
             ptx::tc_fence_after();
             const uint32_t dQ_k = ptx::sdesc_lo(sQ, 16) + x * TILE16;
             const uint32_t dK_k = ptx::sdesc_lo(sKV, 16) + 2 * (t & 1) * TILE16;
@@ -183,7 +197,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             progress = true;
           }
           const int u = np[x];
-          if (u < ns[x] && ptx::mbar_try(bars + F_P_FULL + x, u & 1)) {
+          if (u < ns[x] && fwd_mbar_test(bars + F_P_FULL + x, u & 1)) {
             ptx::tc_fence_after();
             // O_x += P_x V_u: A = P_x from TMEM (16 kv = 8 packed columns per step), B = V
             // (MN-major over d)
@@ -254,7 +268,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (c0 + 64 < kTile) ptx::tmem_ld32_wait(ta);
         }
       }
-      const float m_new = fmaxf(m, mx * p.scale_log2);
+      // The exponent's reference m moves only when the row max exceeds it by more than
+      // kFwdRescaleLog2, so P is at most 2^8: far from fp32 overflow, and bf16's relative
+      // precision does not depend on magnitude. O and l share the reference, so O / l and
+      // LSE = m + log2 l are the same; O is rescaled only on tiles where a row's reference
+      // moves (the first, then rarely) instead of whenever a row's max grows.
+      const float m_row = mx * p.scale_log2;
+      const bool moved = m_row > m + kFwdRescaleLog2;
+      const float m_new = moved ? m_row : m;
       // pass 2: P = exp2(S * scale*log2e - m_new), row sum, packed bf16 over the first 64
       // columns: columns c0 .. c0 + 31 go to packed columns c0 / 2 .. c0 / 2 + 15, which
       // lie in scores this thread has already read and not in the 32 loading meanwhile.
@@ -275,12 +296,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
       }
       const float lt = (lt4[0] + lt4[1]) + (lt4[2] + lt4[3]);
-      const float alpha = ptx::ex2(m - m_new);      // 0 on the first tile (m = -inf)
+      const float alpha = moved ? ptx::ex2(m - m_new) : 1.f;   // 0 on the first tile (m = -inf)
       l = l * alpha + lt;
       m = m_new;
-      // rescale this warp's O rows when any of their maxima grew (P_x(j-1) V_{j-1} is done:
-      // S_x(j) was issued after it)
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      // rescale this warp's O rows when any of their references moved (P_x(j-1) V_{j-1} is
+      // done: S_x(j) was issued after it)
+      if (j > 0 && __any_sync(0xffffffffu, moved)) {
         uint32_t oa[32], ob[32];
         ptx::tmem_ld32_issue(t_o, oa);
         ptx::tmem_ld32_wait(oa);
