@@ -22,7 +22,12 @@ def to64(t: torch.Tensor) -> np.ndarray:
 def run_case(B, S, H, D, causal, schedule, deterministic, seed=0, device="cuda:0"):
     x = make_inputs(B, S, H, D, seed)
     q, k, v, do = (x[n].to(device) for n in ("q", "k", "v", "do"))
-    scale = 1.0 / math.sqrt(D)
+    return run_tensors(q, k, v, do, causal, schedule, deterministic)
+
+
+def run_tensors(q, k, v, do, causal, schedule, deterministic):
+    """Forward and backward on given BSHD bf16 device tensors, scale 1/sqrt(d)."""
+    scale = 1.0 / math.sqrt(q.shape[-1])
     o, lse = da.attn_forward(q, k, v, scale, causal)
     dq, dk, dv = da.attn_backward(q, k, v, o, do, lse, scale, causal, schedule, deterministic)
     torch.cuda.synchronize()

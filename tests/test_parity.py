@@ -9,7 +9,8 @@ import torch
 import reproducible_deterministic_attn_gb300 as da
 
 from tests._lib import ensure_built, has_gpu
-from tests.gpu_common import assert_within, check_against_oracle, run_case
+from reproducible_deterministic_attn_gb300.inputs import make_inputs
+from tests.gpu_common import assert_within, check_against_oracle, run_case, run_tensors
 
 pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not has_gpu(), reason="needs a CUDA GPU")]
@@ -61,6 +62,33 @@ def test_split_tiles_full_shift(D, det):
         pytest.skip("this GPU's grid splits no KV tile at this shape")
     res = run_case(B, S, H, D, False, "shift", det, seed=3)
     assert_within(check_against_oracle(res, False))
+
+
+# Row maxima that climb along the keys. The forward moves a row's exponent reference only
+# when the row max exceeds it by more than 8 (log2 units), which N(0,1) inputs reach on the
+# first KV tile alone. Here key s is scaled by 1 + 5 s / S, so the scaled scores' row max
+# grows by well over 8 log2 units across the tiles: the reference moves mid-row, O is
+# rescaled in TMEM, and P values between 1 and 2^8 occur. The test first checks on the CPU
+# that the input does that, then compares both passes with the oracle.
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("mask", ["full", "causal"])
+def test_growing_row_max(D, mask):
+    B, S, H = 1, 1024, 2
+    causal = mask == "causal"
+    x = make_inputs(B, S, H, D, 5)
+    grow = 1.0 + 5.0 * torch.arange(S, dtype=torch.float32) / S
+    k = (x["k"].float() * grow[None, :, None, None]).to(torch.bfloat16)
+    q64, k64 = x["q"].double(), k.double()
+    s2 = torch.einsum("bqhd,bkhd->bhqk", q64, k64) * (D ** -0.5) * 1.4426950408889634
+    if causal:
+        s2 = s2.masked_fill(torch.ones(S, S, dtype=torch.bool).triu(1), float("-inf"))
+    tile_max = s2.view(B, H, S, S // 128, 128).amax(-1)        # per row, per KV tile
+    prefix = torch.cummax(tile_max, dim=-1).values
+    rise = (prefix - prefix[..., :1]).amax()
+    assert rise > 16.0, float(rise)     # the reference moves at least twice in some row
+    res = run_tensors(x["q"].cuda(), k.cuda(), x["v"].cuda(), x["do"].cuda(), causal,
+                      "symmetric_shift" if causal else "shift", 1)
+    assert_within(check_against_oracle(res, causal))
 
 
 def test_config1_full_256_d64():
