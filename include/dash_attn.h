@@ -65,7 +65,8 @@ typedef enum {
   DASH_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < dash_attn_bwd_workspace_size() */
   DASH_ERR_CUDA = 4,                /* a CUDA runtime call failed; see dash_last_error() */
   DASH_ERR_SYNC_TIMEOUT = 5,        /* a wait (dQ semaphore or in-kernel pipeline) hit its limit */
-  DASH_ERR_DEADLOCK_RISK = 6        /* the schedule's waits form a cycle on this grid */
+  DASH_ERR_DEADLOCK_RISK = 6,       /* the schedule's waits form a cycle on this grid */
+  DASH_ERR_BOUNDS = 7               /* checked build: a table index failed a device-side check */
 } dash_status_t;
 
 /*
@@ -183,7 +184,10 @@ dash_status_t dash_attn_bwd_static(const void* q, const void* k, const void* v, 
  * dash_attn_bwd on it: DASH_OK, or DASH_ERR_SYNC_TIMEOUT when a wait ran out -- a dQ
  * semaphore wait, or a hand-off between the warps of one CTA -- after which the kernel
  * abandons its remaining work and the outputs are undefined (dash_last_error() says
- * which). Also returns DASH_ERR_CUDA if the stream reports an error.
+ * which). In the checked build (dash_bounds_checks_enabled() == 1) also
+ * DASH_ERR_BOUNDS: an index read from the schedule tables failed its check, the CTA
+ * stopped before using it, and dash_last_error() names the table, the head, the value
+ * and the bound. Also returns DASH_ERR_CUDA if the stream reports an error.
  */
 dash_status_t dash_attn_get_status(const void* workspace, cudaStream_t stream);
 
@@ -206,6 +210,26 @@ void dash_attn_shutdown(void);
  * and the CUDA context stays usable. Not thread-safe against concurrent calls.
  */
 void dash_debug_set_sync(long long timeout_ns, int ordinal_skew);
+
+/*
+ * Device-side bounds checks. The library is built in two forms: the product build, and a
+ * checked build (libdash_attn_checked.so, compiled with DASH_BOUNDS_CHECKS=1) whose
+ * backward checks every index it reads from its schedule tables before using it -- a
+ * CTA's range of pieces, each piece's head, task range and split tile, each task's two
+ * tile indices, each dQ ordinal -- and, on a failure, records DASH_ERR_BOUNDS in the
+ * workspace header and stops that CTA's work (no trap; the context stays usable). It
+ * stands in for a memory checker. Returns 1 in the checked build, 0 in the product build.
+ */
+int dash_bounds_checks_enabled(void);
+
+/*
+ * Testing hook of the checked build. Lowers by `tiles` the tile bound that the checks
+ * compare task indices and dQ ordinals against (0 restores it), for later dash_attn_bwd
+ * calls in this process; the kernel's own indexing is unchanged, so valid tables then
+ * fail the checks without any access going out of bounds. Returns DASH_OK,
+ * DASH_ERR_INVALID_ARG (tiles < 0), or DASH_ERR_UNSUPPORTED in the product build.
+ */
+dash_status_t dash_debug_narrow_checks(int tiles);
 
 /*
  * Tracing hook. When device_counters is not NULL, later dash_attn_bwd main kernels add,

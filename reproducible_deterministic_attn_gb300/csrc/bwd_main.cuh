@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Trace tr{(kTrace && p.trace) ? trace_s : nullptr};
       const uint8_t* qx = (const uint8_t*)p.qx;
       const uint8_t* dox = (const uint8_t*)p.dox;
-      Walk w(p);
+      Walk w(p, abort_flag);
       int it = 0, tl = 0;
       bool ok = true;
       while (ok && w.next()) {
@@ -355,12 +355,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       // them to be performed, which the read-out no longer does. E_RELD tells warp 12 the
       // hand-off is done; it grants the next turn only after that, so E_REDS never runs a
       // phase ahead of this wait.
-      Walk w(p);
+      Walk w(p, abort_flag);
       int it = 0;
       bool ok = true;
       while (ok && w.next()) {
         if (!(ok = ptx::mbar_wait(bars + E_REDS, it & 1, abort_flag, tmo))) break;
         const int ord = __ldg(p.ord + w.bh * p.ord_stride + w.i * p.n + w.j);
+#if DASH_BOUNDS_CHECKS
+        if (ord < 0 || ord >= p.check_n) {
+          report_bounds(p.ws_header, CHK_ORDINAL, w.bh, ord, p.check_n);
+          *abort_flag = 1;
+          break;
+        }
+#endif
         const int chain = ord % p.chains, o = ord / p.chains;
         st_release_gpu(p.sems + (w.bh * p.n + w.j) * kSemStride + chain, o + 1 + p.ordinal_skew);
         ptx::mbar_arrive(bars + E_RELD);
@@ -395,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t XBUF_STEP = L::EXT_BYTES >> 4;             // next Q offset block
       // The walk is stepped to the next task right after dV is issued, so that its table
       // loads overlap the wait for dS; this task's tile flags are kept in locals.
-      Walk w(p);
+      Walk w(p, abort_flag);
       int it = 0, tile = -1;
       bool ok = true;
       bool have = w.next(), s_done = false;   // s_done: S(it) was issued ahead
@@ -495,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = ((uint32_t)(quarter * 32) << 16);
     const uint32_t sDS = ptx::smem_u32(sm + L::DS_OFF);
     SegTraceShared trs((kTrace && p.trace && warp == 4 && lane == 0) ? trace_s : nullptr);
-    Walk w(p);
+    Walk w(p, abort_flag);
     int it = 0;
     bool ok = true;
     while (ok && w.next()) {
@@ -580,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = quarter * 32 + lane;       // d column of dQ^T; kv row of dK/dV
     const uint32_t lane_addr = ((uint32_t)(quarter * 32) << 16);
     const Trace trq{(kTrace && p.trace && warp == 12 && lane == 0) ? trace_s : nullptr};
-    Walk w(p);
+    Walk w(p, abort_flag);
     int it = 0, tl = 0;
     bool ok = true;
     while (ok && w.next()) {
@@ -609,6 +616,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The block's fixed order runs as p.chains interleaved chains: contribution o waits
       // for o - chains, in chain o % chains, adding into accumulator copy o % chains.
       const int ord = __ldg(p.ord + w.bh * p.ord_stride + w.i * p.n + w.j);
+#if DASH_BOUNDS_CHECKS
+      if (ord < 0 || ord >= p.check_n) {
+        report_bounds(p.ws_header, CHK_ORDINAL, w.bh, ord, p.check_n);
+        *abort_flag = 1;
+        break;
+      }
+#endif
       const int chain = ord % p.chains, o = ord / p.chains;
       const int sem_idx = (w.bh * p.n + w.j) * kSemStride + chain;
       if (p.deterministic) {

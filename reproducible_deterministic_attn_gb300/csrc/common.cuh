@@ -10,16 +10,28 @@ constexpr int kTile = 128;             // KV tile rows = Q tile rows (square tas
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// Device-side bounds checks (the checked build, -DDASH_BOUNDS_CHECKS=1): every index the
+// backward reads from its schedule tables (a CTA's piece range, a piece's fields, a task's
+// tile indices, a dQ ordinal) is checked before it is used. A failed check records
+// DASH_ERR_BOUNDS in the workspace header and stops the CTA's work; it never traps. The
+// product build compiles none of it.
+#ifndef DASH_BOUNDS_CHECKS
+#define DASH_BOUNDS_CHECKS 0
+#endif
+
 // Workspace header (int32 words). The header occupies the first 256 bytes.
 enum : int {
-  WS_STATUS = 0,      // 0 = ok, DASH_ERR_SYNC_TIMEOUT on a timed-out wait
-  WS_BH = 1,          // (batch * H + head) of the first failing wait
-  WS_QTILE = 2,       // dQ block of the first failing wait
-  WS_EXPECT = 3,      // ordinal it waited for
-  WS_SEEN = 4,        // semaphore value it last saw
+  WS_STATUS = 0,      // 0 = ok, DASH_ERR_SYNC_TIMEOUT on a timed-out wait, DASH_ERR_BOUNDS
+  WS_BH = 1,          // (batch * H + head) of the first failing wait or check
+  WS_QTILE = 2,       // dQ block of the first failing wait; the site of a failed check
+  WS_EXPECT = 3,      // ordinal it waited for; the value that failed a check
+  WS_SEEN = 4,        // semaphore value it last saw; the bound the value failed
 };
 constexpr size_t kWsHeaderBytes = 256;
 constexpr int kStatusSyncTimeout = 5;
+constexpr int kStatusBounds = 7;
+// Sites of a failed bounds check (WS_QTILE)
+enum : int { CHK_CTA_RANGE = 1, CHK_PIECE = 2, CHK_TASK = 3, CHK_ORDINAL = 4 };
 // The fixed dQ order of a block runs as k = deterministic interleaved chains (1 <= k <=
 // kDqChains): contribution o adds, in order, into accumulator copy o % k after
 // contribution o - k, so k = 1 is one serial chain; the convert adds the copies in index
@@ -93,6 +105,9 @@ struct BwdParams {
   long long timeout_ns;      // bound on one semaphore wait
   int ordinal_skew;          // testing hook: added to every awaited ordinal
   unsigned long long* trace; // optional per-CTA wait-cycle counters (null: off)
+  // read by the bounds checks only: the tables' lengths and the tile bound (n, or less
+  // under the testing hook that narrows the checks)
+  int num_pieces, num_tasks, check_n;
 };
 
 // Wait sites of the optional trace (cycles spent waiting, per CTA).
@@ -129,6 +144,19 @@ __device__ __forceinline__ void st_release_gpu(int* p, int v) {
 __device__ __forceinline__ void red_release_add_gpu(int* p, int v) {
   asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+
+#if DASH_BOUNDS_CHECKS
+// Records the first failed bounds check of a launch (any thread; the first one wins).
+__device__ __noinline__ void report_bounds(int* ws, int site, int bh, int value, int bound) {
+  if (atomicCAS(ws + WS_STATUS, 0, kStatusBounds) == 0) {
+    ws[WS_BH] = bh;
+    ws[WS_QTILE] = site;
+    ws[WS_EXPECT] = value;
+    ws[WS_SEEN] = bound;
+    __threadfence();
+  }
+}
+#endif
 
 // Spin (one thread) until *sem == target. Gives up when another CTA has already
 // reported a failure, or after timeout_ns, recording the first failure in the

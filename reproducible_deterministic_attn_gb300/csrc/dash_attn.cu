@@ -23,6 +23,9 @@
 #include "gemm_splitk.cuh"
 #include "sched.h"
 
+static_assert(dash::kStatusBounds == DASH_ERR_BOUNDS, "bounds status: one code");
+static_assert(dash::kStatusSyncTimeout == DASH_ERR_SYNC_TIMEOUT, "timeout status: one code");
+
 namespace {
 
 thread_local std::string g_last_error;
@@ -32,6 +35,7 @@ thread_local std::string g_last_error;
 long long g_timeout_ns = 10ll * 1000 * 1000 * 1000;
 int g_ordinal_skew = 0;
 unsigned long long* g_trace = nullptr;   // dash_debug_set_trace
+int g_check_narrow = 0;                  // dash_debug_narrow_checks (checked build only)
 
 dash_status_t cuda_fail(cudaError_t e, const char* what) {
   g_last_error = std::string(what) + ": " + cudaGetErrorString(e);
@@ -49,6 +53,7 @@ struct DeviceTables {
   int32_t* ord = nullptr;
   int32_t* cnt = nullptr;
   int num_slots = 0;
+  int num_tasks = 0;
 };
 
 std::mutex g_mu;
@@ -62,6 +67,7 @@ struct DealtTables {
   int32_t* ord = nullptr;       // [heads][n][n]; null: the schedule's own order
   int32_t* cta_off = nullptr;   // [grid + 1]
   int32_t* pieces = nullptr;    // [pieces][4]: head, first task, end task, split/part
+  int num_pieces = 0;
 };
 std::map<std::tuple<int, int, int, int, int, int, int>, DealtTables> g_dealt;
 
@@ -106,6 +112,7 @@ dash_status_t get_tables(int dev, int mask, int sched, int n, DeviceTables* out)
   if (rc) return (dash_status_t)rc;
   DeviceTables t;
   t.num_slots = sc.num_slots;
+  t.num_tasks = (int)sc.tasks.size();
   auto upload = [](const std::vector<int32_t>& v, int32_t** dst) -> cudaError_t {
     cudaError_t e = cudaMalloc(dst, v.size() * sizeof(int32_t));
     if (e != cudaSuccess) return e;
@@ -147,6 +154,7 @@ dash_status_t set_dealing(int dev, int mask, int sched, int n, int heads, int gr
     dash::Dealing dl;
     dash::deal(sc, heads, grid, head_dim, &dl);
     DealtTables d;
+    d.num_pieces = (int)dl.pieces.size();
     cudaError_t e = upload_new(dl.cta_off, &d.cta_off);
     if (e == cudaSuccess) e = upload_new(piece_words(dl), &d.pieces);
     if (e == cudaSuccess && dash::arrival_ordered(sc))
@@ -163,6 +171,7 @@ dash_status_t set_dealing(int dev, int mask, int sched, int n, int heads, int gr
   p->ord_stride = it->second.ord ? (long long)n * n : 0;
   p->cta_off = it->second.cta_off;
   p->pieces = it->second.pieces;
+  p->num_pieces = it->second.num_pieces;
   return DASH_OK;
 }
 
@@ -338,6 +347,7 @@ const char* dash_status_string(int status) {
     case DASH_ERR_CUDA: return "DASH_ERR_CUDA";
     case DASH_ERR_SYNC_TIMEOUT: return "DASH_ERR_SYNC_TIMEOUT";
     case DASH_ERR_DEADLOCK_RISK: return "DASH_ERR_DEADLOCK_RISK";
+    case DASH_ERR_BOUNDS: return "DASH_ERR_BOUNDS";
     default: return "DASH_ERR_UNKNOWN";
   }
 }
@@ -499,6 +509,8 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
   p.timeout_ns = g_timeout_ns;
   p.ordinal_skew = g_ordinal_skew;
   p.trace = g_trace;
+  p.num_tasks = tb.num_tasks;
+  p.check_n = n - g_check_narrow;
 
   p.num_sems = B * H * n * dash::kSemStride;
 
@@ -572,6 +584,17 @@ dash_status_t dash_attn_get_status(const void* workspace, cudaStream_t stream) {
     g_last_error = buf;
     return DASH_ERR_SYNC_TIMEOUT;
   }
+  if (words[dash::WS_STATUS] == dash::kStatusBounds) {
+    static const char* const sites[] = {"?", "a CTA's piece range", "a piece", "a task",
+                                         "a dQ ordinal"};
+    const int site = words[dash::WS_QTILE];
+    char buf[200];
+    snprintf(buf, sizeof(buf), "bounds check failed on %s: bh/cta=%d value=%d bound=%d",
+             sites[site >= 1 && site <= 4 ? site : 0], words[dash::WS_BH],
+             words[dash::WS_EXPECT], words[dash::WS_SEEN]);
+    g_last_error = buf;
+    return DASH_ERR_BOUNDS;
+  }
   if (words[dash::WS_STATUS] == dash::kStatusSyncTimeout) {
     char buf[160];
     snprintf(buf, sizeof(buf), "dQ reduction wait timed out: bh=%d q_tile=%d expected=%d seen=%d",
@@ -580,6 +603,18 @@ dash_status_t dash_attn_get_status(const void* workspace, cudaStream_t stream) {
     g_last_error = buf;
     return DASH_ERR_SYNC_TIMEOUT;
   }
+  return DASH_OK;
+}
+
+int dash_bounds_checks_enabled(void) { return DASH_BOUNDS_CHECKS; }
+
+dash_status_t dash_debug_narrow_checks(int tiles) {
+  if (!DASH_BOUNDS_CHECKS) {
+    g_last_error = "this build has no bounds checks (build with checks=True)";
+    return DASH_ERR_UNSUPPORTED;
+  }
+  if (tiles < 0) return DASH_ERR_INVALID_ARG;
+  g_check_narrow = tiles;
   return DASH_OK;
 }
 
@@ -839,6 +874,7 @@ struct StaticTables {
   std::vector<int32_t> image;
   // byte offsets of the piece, task, order and count tables (the CTA offsets come first)
   size_t piece_off, task_off, ord_off, cnt_off;
+  int num_pieces, num_tasks;
 };
 std::map<std::tuple<int, int, int, int, int, int>, std::shared_ptr<const StaticTables>>
     g_static_tables;
@@ -859,6 +895,8 @@ dash_status_t static_tables(int mask, int schedule, int n, int heads, int grid, 
     dash::deal(sc, heads, grid, head_dim, &dl);
     const std::vector<int32_t> words = piece_words(dl);
     auto t = std::make_shared<StaticTables>();
+    t->num_pieces = (int)dl.pieces.size();
+    t->num_tasks = (int)sc.tasks.size();
     t->piece_off = round_up(dl.cta_off.size() * 4, 256);
     t->task_off = round_up(t->piece_off + words.size() * 4, 256);
     t->ord_off = round_up(t->task_off + sc.tasks.size() * 4, 256);
@@ -974,6 +1012,9 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
   p.timeout_ns = g_timeout_ns;
   p.ordinal_skew = g_ordinal_skew;
   p.trace = nullptr;
+  p.num_pieces = tb->num_pieces;
+  p.num_tasks = tb->num_tasks;
+  p.check_n = n - g_check_narrow;
   p.num_sems = B * H * n * dash::kSemStride;
 
   // Every refusal comes before the first queued operation: a refused call leaves the

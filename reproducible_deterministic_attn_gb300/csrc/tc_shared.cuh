@@ -32,12 +32,40 @@ struct Walk {
   int tag;                    // this piece's (split tile << 2) | part
   int32_t prev_tk, cur_tk, nxt_tk, nxt2_tk;
   bool first_of_tile, last_of_tile;
-  __device__ Walk(const BwdParams& pp)
+#if DASH_BOUNDS_CHECKS
+  volatile int* abort_flag;   // the CTA's: raised on a failed check so no role waits on
+                              // work the others will not do
+#endif
+  __device__ Walk(const BwdParams& pp, volatile int* cta_abort)
       : p(pp), k(__ldg(pp.cta_off + blockIdx.x) - 1), k_end(__ldg(pp.cta_off + blockIdx.x + 1)),
-        t(0), t_end(0) {}
+        t(0), t_end(0) {
+#if DASH_BOUNDS_CHECKS
+    abort_flag = cta_abort;
+    if (k < -1 || k_end < k + 1 || k_end > p.num_pieces) {
+      report_bounds(p.ws_header, CHK_CTA_RANGE, (int)blockIdx.x, k_end, p.num_pieces);
+      *abort_flag = 1;
+      k_end = k + 1;   // no pieces: next() returns false at once
+    }
+#else
+    (void)cta_abort;
+#endif
+  }
   __device__ __forceinline__ int32_t task_at(int k) const {
     return k < t_end ? __ldg(p.tasks + k) : -1;
   }
+#if DASH_BOUNDS_CHECKS
+  // A task read from the table (index < t_end) must name two tiles below the bound.
+  __device__ bool task_ok(int idx, int32_t tk) const {
+    return idx >= t_end || (tk >= 0 && (tk >> 16) < p.check_n && (tk & 0xffff) < p.check_n);
+  }
+  __device__ bool fail(int site, int value, int bound) {
+    report_bounds(p.ws_header, site, bh, value, bound);
+    *abort_flag = 1;
+    k_end = k;
+    t = t_end = 0;
+    return false;
+  }
+#endif
   __device__ bool next() {
     ++t;
     if (t >= t_end) {
@@ -48,16 +76,30 @@ struct Walk {
         t = pc.y;
         t_end = pc.z;
         tag = pc.w;
+#if DASH_BOUNDS_CHECKS
+        const int part = tag & 3, split = tag >> 2;
+        if (bh < 0 || bh >= p.B * p.H) return fail(CHK_PIECE, bh, p.B * p.H);
+        if (t < 0 || t > t_end || t_end > p.num_tasks) return fail(CHK_PIECE, t_end, p.num_tasks);
+        if (part > 2 || (part != 0 && (split < 0 || split >= kSplitTiles)))
+          return fail(CHK_PIECE, tag, kSplitTiles);
+#endif
       } while (t >= t_end);
       prev_tk = -1;
       cur_tk = task_at(t);
       nxt_tk = task_at(t + 1);
+#if DASH_BOUNDS_CHECKS
+      if (!task_ok(t, cur_tk)) return fail(CHK_TASK, cur_tk, p.check_n);
+      if (!task_ok(t + 1, nxt_tk)) return fail(CHK_TASK, nxt_tk, p.check_n);
+#endif
     } else {
       prev_tk = cur_tk;
       cur_tk = nxt_tk;
       nxt_tk = nxt2_tk;
     }
     nxt2_tk = task_at(t + 2);
+#if DASH_BOUNDS_CHECKS
+    if (!task_ok(t + 2, nxt2_tk)) return fail(CHK_TASK, nxt2_tk, p.check_n);
+#endif
     i = cur_tk >> 16;
     j = cur_tk & 0xffff;
     first_of_tile = prev_tk < 0 || (prev_tk >> 16) != i;

@@ -26,8 +26,13 @@ DASH_ERR_WORKSPACE_TOO_SMALL = 3
 DASH_ERR_CUDA = 4
 DASH_ERR_SYNC_TIMEOUT = 5
 DASH_ERR_DEADLOCK_RISK = 6
+DASH_ERR_BOUNDS = 7
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdash_attn.so")
+# DASH_ATTN_BOUNDS_CHECKS=1 selects the checked build (device-side bounds checks on every
+# schedule-table index the backward reads; build it with build(checks=True)).
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                        "libdash_attn_checked.so" if os.environ.get("DASH_ATTN_BOUNDS_CHECKS") == "1"
+                        else "libdash_attn.so")
 
 _lib = None
 
@@ -53,6 +58,8 @@ _SIGNATURES = {
     "dash_last_error": (ctypes.c_char_p, []),
     "dash_attn_shutdown": (None, []),
     "dash_debug_set_sync": (None, [ctypes.c_longlong, _c_int]),
+    "dash_bounds_checks_enabled": (_c_int, []),
+    "dash_debug_narrow_checks": (_c_int, [_c_int]),
     "dash_debug_set_trace": (None, [_vp]),
     "dash_profile_enable": (_c_int, [_c_int]),
     "dash_profile_read": (_c_int, [_dblp, ctypes.POINTER(_c_int)]),
@@ -182,6 +189,16 @@ def dash_attn_shutdown() -> None:
 
 def dash_debug_set_sync(timeout_ns: int, ordinal_skew: int) -> None:
     load().dash_debug_set_sync(int(timeout_ns), int(ordinal_skew))
+
+
+def dash_bounds_checks_enabled() -> bool:
+    """True when the loaded library is the checked build."""
+    return bool(load().dash_bounds_checks_enabled())
+
+
+def dash_debug_narrow_checks(tiles: int) -> int:
+    """Checked build's testing hook: lower the checks' tile bound by `tiles` (0 restores it)."""
+    return int(load().dash_debug_narrow_checks(int(tiles)))
 
 
 # dash_debug_set_trace sites with a fixed meaning (include/dash_attn.h)

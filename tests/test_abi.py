@@ -2,8 +2,11 @@
 arguments synchronously (no GPU needed: nothing reaches the device)."""
 import ctypes
 import glob
+import json
 import os
 import re
+import subprocess
+import sys
 
 import pytest
 
@@ -40,6 +43,7 @@ def test_status_strings(lib):
     assert da.dash_status_string(0) == "DASH_OK"
     assert da.dash_status_string(5) == "DASH_ERR_SYNC_TIMEOUT"
     assert da.dash_status_string(6) == "DASH_ERR_DEADLOCK_RISK"
+    assert da.dash_status_string(7) == "DASH_ERR_BOUNDS"
     assert da.dash_status_string(99) == "DASH_ERR_UNKNOWN"
 
 
@@ -107,3 +111,36 @@ def test_gemm_splitk_rejects_bad_arguments_without_touching_the_device(lib):
     assert call(K=500) == da.DASH_ERR_UNSUPPORTED                   # K not 64 * splits aligned
     assert call(wsb=16) == da.DASH_ERR_WORKSPACE_TOO_SMALL
     assert da.dash_gemm_splitk_workspace_size(100, 128) == 0
+
+
+def test_product_build_has_no_bounds_checks(lib):
+    assert da.dash_bounds_checks_enabled() is False
+    assert da.dash_debug_narrow_checks(1) == da.DASH_ERR_UNSUPPORTED
+
+
+def test_checked_build_loads_and_exports_every_symbol():
+    """The checked variant (compiled with DASH_BOUNDS_CHECKS=1) is selected by
+    DASH_ATTN_BOUNDS_CHECKS=1, exports the same functions, reports itself and takes the
+    narrowing hook; run in a child process because a process loads one library."""
+    from reproducible_deterministic_attn_gb300 import build as _build
+
+    _build.build(checks=True)
+    script = (
+        "import ctypes, json, sys; sys.path.insert(0, %r)\n"
+        "import reproducible_deterministic_attn_gb300 as da\n"
+        "from tests.test_abi import _declared\n"
+        "raw = ctypes.CDLL(da.dash_attn.LIB_PATH)\n"
+        "print(json.dumps({'path': da.dash_attn.LIB_PATH,\n"
+        "  'missing': [n for n in _declared() if not hasattr(raw, n)],\n"
+        "  'enabled': da.dash_bounds_checks_enabled(),\n"
+        "  'neg': da.dash_debug_narrow_checks(-1), 'one': da.dash_debug_narrow_checks(1),\n"
+        "  'zero': da.dash_debug_narrow_checks(0)}))\n" % ROOT)
+    env = dict(os.environ, DASH_ATTN_BOUNDS_CHECKS="1")
+    out = subprocess.run([sys.executable, "-c", script], env=env, cwd=ROOT,
+                         capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr
+    got = json.loads(out.stdout.strip().splitlines()[-1])
+    assert got["path"].endswith("libdash_attn_checked.so")
+    assert got["missing"] == []
+    assert got["enabled"] is True
+    assert (got["neg"], got["one"], got["zero"]) == (da.DASH_ERR_INVALID_ARG, da.DASH_OK, da.DASH_OK)
