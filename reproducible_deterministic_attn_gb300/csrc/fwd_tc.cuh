@@ -71,10 +71,23 @@ __device__ __forceinline__ bool fwd_mbar_test(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
+// The running max folded with 32 scores of a row (columns c0 .. c0 + 31 of S). kDiag: the
+// causal diagonal tile, where keys after row r are left out; every other tile has no
+// masked key, so its version carries no per-score test.
+template <bool kDiag>
+__device__ __forceinline__ float fwd_chunk_max(const uint32_t (&t)[32], int c0, int r, float mx) {
+#pragma unroll
+  for (int c = 0; c < 32; ++c)
+    if (!kDiag || c0 + c <= r) mx = fmaxf(mx, __uint_as_float(t[c]));
+  return mx;
+}
+
 // P for 32 scores of a row (columns c0 .. c0 + 31 of S): exp2(S * scale*log2e - m_new),
-// zero where the causal mask removes the key, added into the row's partial sums (column c
-// into lt4[c % 4]) and stored as 16 packed bf16 columns at t_p.
-__device__ __forceinline__ void fwd_p_chunk(const uint32_t (&t)[32], int c0, bool diag, int r,
+// on the diagonal tile (kDiag) zero where the causal mask removes the key, added into the
+// row's partial sums (column c into lt4[c % 4]) and stored as 16 packed bf16 columns at
+// t_p.
+template <bool kDiag>
+__device__ __forceinline__ void fwd_p_chunk(const uint32_t (&t)[32], int c0, int r,
                                             float scale_log2, float m_new, float (&lt4)[4],
                                             uint32_t t_p) {
   uint32_t u[16];
@@ -83,8 +96,10 @@ __device__ __forceinline__ void fwd_p_chunk(const uint32_t (&t)[32], int c0, boo
     const int c = c0 + 2 * k;
     float e0 = ptx::ex2(fmaf(__uint_as_float(t[2 * k]), scale_log2, -m_new));
     float e1 = ptx::ex2(fmaf(__uint_as_float(t[2 * k + 1]), scale_log2, -m_new));
-    e0 = (!diag || c <= r) ? e0 : 0.f;
-    e1 = (!diag || c + 1 <= r) ? e1 : 0.f;
+    if (kDiag) {
+      e0 = c <= r ? e0 : 0.f;
+      e1 = c + 1 <= r ? e1 : 0.f;
+    }
     lt4[(2 * k) & 3] += e0;
     lt4[(2 * k + 1) & 3] += e1;
     u[k] = ptx::pack_bf16(e0, e1);
@@ -257,14 +272,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
         for (int c0 = 0; c0 < kTile; c0 += 64) {
           ptx::tmem_ld32_issue(t_s + c0 + 32, tb);
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (!diag || c0 + c <= r) mx = fmaxf(mx, __uint_as_float(ta[c]));
+          mx = diag ? fwd_chunk_max<true>(ta, c0, r, mx) : fwd_chunk_max<false>(ta, c0, r, mx);
           ptx::tmem_ld32_wait(tb);
           if (c0 + 64 < kTile) ptx::tmem_ld32_issue(t_s + c0 + 64, ta);
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (!diag || c0 + 32 + c <= r) mx = fmaxf(mx, __uint_as_float(tb[c]));
+          mx = diag ? fwd_chunk_max<true>(tb, c0 + 32, r, mx)
+                    : fwd_chunk_max<false>(tb, c0 + 32, r, mx);
           if (c0 + 64 < kTile) ptx::tmem_ld32_wait(ta);
         }
       }
@@ -288,10 +300,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
         for (int c0 = 0; c0 < kTile; c0 += 64) {
           ptx::tmem_ld32_issue(t_s + c0 + 32, tb);
-          fwd_p_chunk(ta, c0, diag, r, p.scale_log2, m_new, lt4, t_s + c0 / 2);
+          if (diag) fwd_p_chunk<true>(ta, c0, r, p.scale_log2, m_new, lt4, t_s + c0 / 2);
+          else fwd_p_chunk<false>(ta, c0, r, p.scale_log2, m_new, lt4, t_s + c0 / 2);
           ptx::tmem_ld32_wait(tb);
           if (c0 + 64 < kTile) ptx::tmem_ld32_issue(t_s + c0 + 64, ta);
-          fwd_p_chunk(tb, c0 + 32, diag, r, p.scale_log2, m_new, lt4, t_s + (c0 + 32) / 2);
+          if (diag)
+            fwd_p_chunk<true>(tb, c0 + 32, r, p.scale_log2, m_new, lt4, t_s + (c0 + 32) / 2);
+          else
+            fwd_p_chunk<false>(tb, c0 + 32, r, p.scale_log2, m_new, lt4, t_s + (c0 + 32) / 2);
           if (c0 + 64 < kTile) ptx::tmem_ld32_wait(ta);
         }
       }
