@@ -55,7 +55,8 @@ static_assert(kFwdRegsCtrl + 2 * kFwdRegsSoftmax == 3 * kFwdRegsLaunch,
 
 enum {
   F_Q_FULL = 0, F_KV_FULL, F_KV_EMPTY = F_KV_FULL + 2, F_S_FULL = F_KV_EMPTY + 2,
-  F_P_FULL = F_S_FULL + 2, F_PV_DONE = F_P_FULL + 2, F_DRAIN = F_PV_DONE + 2, F_COUNT
+  F_P_FULL = F_S_FULL + 2, F_PV_DONE = F_P_FULL + 2, F_VERDICT = F_PV_DONE + 2,
+  F_DRAIN = F_VERDICT + 2, F_COUNT
 };
 
 // Non-blocking test of an mbarrier phase. The issuer polls several barriers in turn, so it
@@ -108,6 +109,27 @@ __device__ __forceinline__ void fwd_p_chunk(const uint32_t (&t)[32], int c0, int
   ptx::tmem_st8(t_p + 8, u + 8);
 }
 
+// P for 32 scores of a row of a tile that is neither the first nor the causal diagonal,
+// against the current reference m (the same P and partial sums as fwd_p_chunk<false> with
+// m_new = m), folding the scores into the row max mx as it goes.
+__device__ __forceinline__ void fwd_p_chunk_spec(const uint32_t (&t)[32], float scale_log2,
+                                                 float m, float (&lt4)[4], uint32_t t_p,
+                                                 float& mx) {
+  uint32_t u[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const float s0 = __uint_as_float(t[2 * k]), s1 = __uint_as_float(t[2 * k + 1]);
+    mx = fmaxf(mx, fmaxf(s0, s1));
+    const float e0 = ptx::ex2(fmaf(s0, scale_log2, -m));
+    const float e1 = ptx::ex2(fmaf(s1, scale_log2, -m));
+    lt4[(2 * k) & 3] += e0;
+    lt4[(2 * k + 1) & 3] += e1;
+    u[k] = ptx::pack_bf16(e0, e1);
+  }
+  ptx::tmem_st8(t_p, u);
+  ptx::tmem_st8(t_p + 8, u + 8);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_tc_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ TmaMaps maps) {
@@ -117,6 +139,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   uint64_t* bars = (uint64_t*)(sm + L::BAR_OFF);
   uint32_t* tmem_slot = (uint32_t*)(sm + L::BAR_OFF + 8 * F_COUNT);
   volatile int* abort_flag = (volatile int*)(sm + L::BAR_OFF + 8 * F_COUNT + 4);
+  // per Q tile: set by a softmax warp whose rows need the exact path on a speculative tile;
+  // the issuer's verdict for the tile (1 = S is issued again)
+  volatile int* redo_flag = (volatile int*)(sm + L::BAR_OFF + 8 * F_COUNT + 8);
+  volatile int* verdict = (volatile int*)(sm + L::BAR_OFF + 8 * F_COUNT + 16);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long tmo = p.timeout_ns;   // per wait: far beyond any legitimate wait
 
@@ -137,6 +163,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       ptx::mbar_init(bars + F_S_FULL + s, 1);      // per Q tile from here on
       ptx::mbar_init(bars + F_P_FULL + s, 4);
       ptx::mbar_init(bars + F_PV_DONE + s, 1);
+      ptx::mbar_init(bars + F_VERDICT + s, 1);
+      redo_flag[s] = 0;
     }
     ptx::mbar_init(bars + F_DRAIN, 1);
     *abort_flag = 0;
@@ -181,13 +209,30 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // landed and P_x(t-1) V_{t-1} done (S_x overwrites P_x), and follows P_x(t-1) V_{t-1}
       // in issue order; P_x(t) V_t needs P_x(t) stored. A KV stage is released once both
       // tiles have issued their P V for its tile. The loop polls and issues what is ready.
+      // On a speculative tile (neither the first nor the last of its Q tile) the softmax
+      // computes P against the current reference without the max pass; if a row's max
+      // exceeded it by more than the threshold, the issuer issues S_x(t) again (K_t is still
+      // resident: its stage is released only after both P V) instead of P_x(t) V_t, and the
+      // softmax takes the exact path.
       const uint32_t sQ = ptx::smem_u32(sm + L::Q_OFF), sKV = ptx::smem_u32(sm + L::KV_OFF);
       constexpr uint32_t ID_S = ptx::idesc_bf16(128, 128, 0, 0);   // S = Q K^T
       constexpr uint32_t ID_O = ptx::idesc_bf16(128, D, 0, 1);     // O += P V (V MN-major)
       constexpr uint32_t TILE16 = L::TILE >> 4;
       constexpr uint32_t MN_STEP = 2048 >> 4;
       int ns[2] = {0, 0}, np[2] = {0, 0};
+      int pf_par[2] = {0, 0};             // P_FULL phases (a redone tile completes it twice)
+      bool redone[2] = {false, false};    // S_x(np[x]) was issued again: its P is exact
       const int ntx[2] = {nt_a, nt_b};
+      auto issue_s = [&](int x, int t) {
+        const uint32_t dQ_k = ptx::sdesc_lo(sQ, 16) + x * TILE16;
+        const uint32_t dK_k = ptx::sdesc_lo(sKV, 16) + 2 * (t & 1) * TILE16;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t step = ((ks >> 2) * kTile * 128 + (ks & 3) * 32) >> 4;
+          ptx::mma_lo(tmem + L::T_S + 128 * x, dQ_k + step, dK_k + step, ID_S, ks > 0);
+        }
+        ptx::mma_commit(bars + F_S_FULL + x);
+      };
       int kv_rel = 0;
       bool ok = ptx::mbar_wait(bars + F_Q_FULL, 0, abort_flag, tmo);
       long long t_last = global_timer_ns();
@@ -200,20 +245,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               fwd_mbar_test(bars + F_KV_FULL + (t & 1), (t >> 1) & 1) &&
               (t == 0 || fwd_mbar_test(bars + F_PV_DONE + x, (t - 1) & 1))) {
             ptx::tc_fence_after();
-            const uint32_t dQ_k = ptx::sdesc_lo(sQ, 16) + x * TILE16;
-            const uint32_t dK_k = ptx::sdesc_lo(sKV, 16) + 2 * (t & 1) * TILE16;
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-              const uint32_t step = ((ks >> 2) * kTile * 128 + (ks & 3) * 32) >> 4;
-              ptx::mma_lo(tmem + L::T_S + 128 * x, dQ_k + step, dK_k + step, ID_S, ks > 0);
-            }
-            ptx::mma_commit(bars + F_S_FULL + x);
+            issue_s(x, t);
             ns[x] = t + 1;
             progress = true;
           }
           const int u = np[x];
-          if (u < ns[x] && fwd_mbar_test(bars + F_P_FULL + x, u & 1)) {
+          if (u < ns[x] && fwd_mbar_test(bars + F_P_FULL + x, pf_par[x])) {
+            pf_par[x] ^= 1;
             ptx::tc_fence_after();
+            if (u > 0 && u < ntx[x] - 1 && !redone[x]) {   // speculative P: give the verdict
+              const int redo = redo_flag[x];
+              redo_flag[x] = 0;
+              verdict[x] = redo;
+              ptx::mbar_arrive(bars + F_VERDICT + x);
+              if (redo) {
+                issue_s(x, u);
+                redone[x] = true;
+                progress = true;
+                continue;
+              }
+            }
+            redone[x] = false;
             // O_x += P_x V_u: A = P_x from TMEM (16 kv = 8 packed columns per step), B = V
             // (MN-major over d)
             const uint32_t dV_mn = ptx::sdesc_lo(sKV + (2 * (u & 1) + 1) * L::TILE, kTile * 128);
@@ -256,10 +308,52 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t t_o = tmem + lane_addr + L::T_O + D * x;
     float m = -INFINITY, l = 0.f;                   // running max (log2 units) and sum
     bool ok = true;
+    int s_par = 0, v_par = 0;                       // S_FULL / VERDICT phases
     for (int j = 0; ok && j < ntt; ++j) {
-      ok = ptx::warp_wait(bars + F_S_FULL + x, j & 1, abort_flag, tmo);
+      ok = ptx::warp_wait(bars + F_S_FULL + x, s_par, abort_flag, tmo);
+      s_par ^= 1;
       if (!ok) break;
       ptx::tc_fence_after();
+      if (j > 0 && j < ntt - 1) {
+        // Speculative tile: P against the current reference m in one pass, the row max
+        // alongside. That P is the exact path's unless some row's max exceeds m by more
+        // than kFwdRescaleLog2; then this warpgroup asks for S again (the issuer's verdict)
+        // and takes the exact path on it.
+        float mx = -INFINITY;
+        float lt4[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+          uint32_t ta[32], tb[32];
+          ptx::tmem_ld32_issue(t_s, ta);
+          ptx::tmem_ld32_wait(ta);
+#pragma unroll
+          for (int c0 = 0; c0 < kTile; c0 += 64) {
+            ptx::tmem_ld32_issue(t_s + c0 + 32, tb);
+            fwd_p_chunk_spec(ta, p.scale_log2, m, lt4, t_s + c0 / 2, mx);
+            ptx::tmem_ld32_wait(tb);
+            if (c0 + 64 < kTile) ptx::tmem_ld32_issue(t_s + c0 + 64, ta);
+            fwd_p_chunk_spec(tb, p.scale_log2, m, lt4, t_s + (c0 + 32) / 2, mx);
+            if (c0 + 64 < kTile) ptx::tmem_ld32_wait(ta);
+          }
+        }
+        if (__any_sync(0xffffffffu, mx * p.scale_log2 > m + kFwdRescaleLog2) && lane == 0)
+          redo_flag[x] = 1;
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bars + F_P_FULL + x);
+        ok = ptx::warp_wait(bars + F_VERDICT + x, v_par, abort_flag, tmo);
+        v_par ^= 1;
+        if (!ok) break;
+        if (!verdict[x]) {                          // P_x(j) V_j is issued; m stays
+          const float lt = (lt4[0] + lt4[1]) + (lt4[2] + lt4[3]);
+          l = l * 1.f + lt;
+          continue;
+        }
+        ok = ptx::warp_wait(bars + F_S_FULL + x, s_par, abort_flag, tmo);   // S_x(j) again
+        s_par ^= 1;
+        if (!ok) break;
+        ptx::tc_fence_after();
+      }
       const bool diag = p.causal && j == qt;         // keys after row r are masked there
       // Both passes read S 32 columns at a time with the next 32 loading while the current
       // ones are used (one load in flight at a time; a wait covers every earlier load).
