@@ -213,7 +213,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // computes P against the current reference without the max pass; if a row's max
       // exceeded it by more than the threshold, the issuer issues S_x(t) again (K_t is still
       // resident: its stage is released only after both P V) instead of P_x(t) V_t, and the
-      // softmax takes the exact path.
+      // softmax takes the exact path. Each round checks both tiles' P V before either S:
+      // the tensor pipe runs MMAs in issue order, and a P V issued first completes first,
+      // which is what its tile's next S and the K/V stage release wait for (measured 10 %
+      // faster than checking S first).
       const uint32_t sQ = ptx::smem_u32(sm + L::Q_OFF), sKV = ptx::smem_u32(sm + L::KV_OFF);
       constexpr uint32_t ID_S = ptx::idesc_bf16(128, 128, 0, 0);   // S = Q K^T
       constexpr uint32_t ID_O = ptx::idesc_bf16(128, D, 0, 1);     // O += P V (V MN-major)
@@ -240,15 +243,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         bool progress = false;
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
-          const int t = ns[x];
-          if (t < ntx[x] && t == np[x] &&
-              fwd_mbar_test(bars + F_KV_FULL + (t & 1), (t >> 1) & 1) &&
-              (t == 0 || fwd_mbar_test(bars + F_PV_DONE + x, (t - 1) & 1))) {
-            ptx::tc_fence_after();
-            issue_s(x, t);
-            ns[x] = t + 1;
-            progress = true;
-          }
           const int u = np[x];
           if (u < ns[x] && fwd_mbar_test(bars + F_P_FULL + x, pf_par[x])) {
             pf_par[x] ^= 1;
@@ -275,6 +269,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                           dV_mn + ks * MN_STEP, ID_O, (u > 0 || ks > 0) ? 1u : 0u);
             ptx::mma_commit(bars + F_PV_DONE + x);
             np[x] = u + 1;
+            progress = true;
+          }
+        }
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          const int t = ns[x];
+          if (t < ntx[x] && t == np[x] &&
+              fwd_mbar_test(bars + F_KV_FULL + (t & 1), (t >> 1) & 1) &&
+              (t == 0 || fwd_mbar_test(bars + F_PV_DONE + x, (t - 1) & 1))) {
+            ptx::tc_fence_after();
+            issue_s(x, t);
+            ns[x] = t + 1;
             progress = true;
           }
         }
