@@ -70,8 +70,6 @@ struct LTc {
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = K_OFF + TILE_BYTES;
   static constexpr int NQ = D == 64 ? 3 : 2;                  // Q buffers (task t: t % NQ)
-  // issue S(t+1) between dK(t) and dQ^T(t) (measured faster at D = 64 only)
-  static constexpr bool kEarlyS = D == 64;
   static constexpr int Q_OFF = V_OFF + TILE_BYTES;
   static constexpr int DO_OFF = Q_OFF + NQ * TILE_BYTES;      // one dO buffer
   static constexpr int DS_OFF = DO_OFF + TILE_BYTES;          // dS^T [kv][q]
@@ -169,6 +167,17 @@ __device__ __forceinline__ void issue_ss(uint32_t d, uint32_t a, uint32_t b, uin
     }
   }
 }
+// dQ^T's K steps K0 .. K1 - 1 (A and B MN-major), leaving a and b at step K1: dQ^T issued
+// in two parts around another product, in the same step order as issue_ss<true, true>
+template <int K0, int K1>
+__device__ __forceinline__ void issue_ss_mn_part(uint32_t d, uint32_t& a, uint32_t& b, uint32_t id) {
+#pragma unroll
+  for (int ks = K0; ks < K1; ++ks) {
+    ptx::mma_lo(d, a, b, id, ks > 0 ? 1u : 0u);
+    a = ptx::step_add<kMnStep>(a);
+    b = ptx::step_add<kMnStep>(b);
+  }
+}
 __device__ __forceinline__ void issue_ts(uint32_t d, uint32_t a_tmem, uint32_t b_mn, uint32_t id,
                                          uint32_t acc0) {
 #pragma unroll
@@ -224,8 +233,9 @@ __device__ __forceinline__ void store_chunk8(uint32_t sTile, int r, int chunk, c
 // kTrace: compiled with the optional wait-cycle trace (launched only while a trace buffer
 // is set); without it the trace code and its registers are absent. kSplit: compiled with
 // the epilogue of KV tiles split over two CTAs (launched only for a dealing that splits
-// one); without it the epilogue is the whole-tile one alone.
-template <int D, bool kTrace, bool kSplit>
+// one); without it the epilogue is the whole-tile one alone. kEarly (D = 128; launched for
+// shift's order in two chains): S(t+1) is issued between the two halves of dQ^T(t).
+template <int D, bool kTrace, bool kSplit, bool kEarly>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ TmaMaps maps) {
   using L = LTc<D>;
@@ -465,10 +475,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mma_commit(bars + E_Q_EMPTY + qb);          // Q(it)'s last reader
         ptx::mma_commit(bars + E_SP_FREE);               // P^T and dS^T have been read
         tr.mark(X_ISSUE_DKDQ);
-        // ---- D = 64: S''^T(it+1) ahead of dQ^T(it) when task it+1 uses the same K, once
-        // dK(it) has completed (S overwrites the dS^T it reads), so the softmax-gradient
-        // warps get it a whole product earlier
-        s_done = L::kEarlyS && have && !w.first_of_tile;
+        // ---- S''^T(it+1) ahead of dQ^T(it) when task it+1 uses the same K, once dK(it) has
+        // completed (S overwrites the dS^T it reads), so the softmax-gradient warps get it
+        // earlier. D = 64: always, ahead of the whole dQ^T. D = 128: only in the kEarly
+        // instance, between dQ^T's two halves, which keep the pipe busy while dK(it)
+        // completes. The host picks it where it measured faster (shift's order in two
+        // chains: +2 %); with unordered adds their burst then meets the earlier S load.
+        s_done = (D == 64 || kEarly) && have && !w.first_of_tile;
+        uint32_t dq_a = dKt_mn, dq_b = dDS_mn;
+        if (D == 128 && s_done) issue_ss_mn_part<0, 4>(tmem + L::T_DPQ, dq_a, dq_b, ID_DQ);
         if (s_done) {
           const int qn = (it + 1) % L::NQ;
           ok = ptx::mbar_wait(bars + E_Q_FULL + qn, ((it + 1) / L::NQ) & 1, abort_flag, tmo);
@@ -480,7 +495,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_s_mmas<D>(tmem, dK_k, dQ_k0 + qn * BUF_STEP, dOnes, dQx0 + qn * XBUF_STEP, bars + E_S_FULL);
           tr.mark(X_ISSUE_S);
         }
-        issue_ss<true, true>(tmem + L::T_DPQ, dKt_mn, dDS_mn, ID_DQ, 0u);
+        if (D == 128 && s_done) issue_ss_mn_part<4, 8>(tmem + L::T_DPQ, dq_a, dq_b, ID_DQ);
+        else issue_ss<true, true>(tmem + L::T_DPQ, dKt_mn, dDS_mn, ID_DQ, 0u);
         ptx::mma_commit(bars + E_DQ_FULL);
         if (last) {
           ptx::mma_commit(bars + E_ACC_FULL);

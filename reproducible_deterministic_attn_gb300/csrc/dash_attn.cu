@@ -186,17 +186,30 @@ struct MainKernel {
 // wait-cycle trace; the traced build is launched only while a trace buffer is set.
 // `split`: the dealing splits a KV tile over two CTAs (its epilogue is compiled only into
 // those instances; the traced build always has it).
-MainKernel main_kernel(int D, bool traced, bool split) {
+// `early` (D = 128): the instances that issue S(t+1) between the two halves of dQ^T(t).
+// Measured on full 2x8192x16x128: faster only for shift's order in two interleaved chains
+// (991 -> 1011 TFLOP/s); slower with unordered adds (1128 -> 1072), one chain (948 -> 939)
+// and the ascending and descending orders (876 -> 855); about even for symmetric shift.
+bool early_s(int schedule, int deterministic) {
+  return schedule == DASH_SCHED_SHIFT && deterministic == 2;
+}
+MainKernel main_kernel(int D, bool traced, bool split, bool early) {
   using namespace dash::tc;
   if (D == 64)
-    return {traced  ? (void*)bwd_main_kernel<64, true, true>
-            : split ? (void*)bwd_main_kernel<64, false, true>
-                    : (void*)bwd_main_kernel<64, false, false>,
+    return {traced  ? (void*)bwd_main_kernel<64, true, true, false>
+            : split ? (void*)bwd_main_kernel<64, false, true, false>
+                    : (void*)bwd_main_kernel<64, false, false, false>,
             (size_t)LTc<64>::ALLOC, dash::kTile};
-  return {traced  ? (void*)bwd_main_kernel<128, true, true>
-          : split ? (void*)bwd_main_kernel<128, false, true>
-                  : (void*)bwd_main_kernel<128, false, false>,
-          (size_t)LTc<128>::ALLOC, dash::kTile};
+  void* fn;
+  if (early)
+    fn = traced  ? (void*)bwd_main_kernel<128, true, true, true>
+         : split ? (void*)bwd_main_kernel<128, false, true, true>
+                 : (void*)bwd_main_kernel<128, false, false, true>;
+  else
+    fn = traced  ? (void*)bwd_main_kernel<128, true, true, false>
+         : split ? (void*)bwd_main_kernel<128, false, true, false>
+                 : (void*)bwd_main_kernel<128, false, false, false>;
+  return {fn, (size_t)LTc<128>::ALLOC, dash::kTile};
 }
 
 // The main kernel moves registers between warpgroups (setmaxnreg); its split adds up to
@@ -526,7 +539,8 @@ dash_status_t dash_attn_bwd(const void* q, const void* k, const void* v, const v
   int grid = sms;                      // one CTA per SM (512 TMEM columns each)
   if (grid > units) grid = units;
   const MainKernel mk =
-      main_kernel(D, g_trace != nullptr, dash::split_tiles(schedule, n, units, grid) > 0);
+      main_kernel(D, g_trace != nullptr, dash::split_tiles(schedule, n, units, grid) > 0,
+                  early_s(schedule, deterministic));
   const int br = mk.br;
   if (!map_bshd(&maps.q, q, B, S, H, D, br) || !map_bshd(&maps.dO, dO, B, S, H, D, br) ||
       !map_bshd(&maps.k, k, B, S, H, D, dash::kTile) ||
@@ -1024,7 +1038,9 @@ extern "C" dash_status_t dash_attn_bwd_static(const void* q, const void* k, cons
     return DASH_ERR_CUDA;
   }
   dash::tc::TmaMaps maps;
-  const MainKernel mk = main_kernel(D, false, dash::split_tiles(schedule, n, units, grid) > 0);
+  const MainKernel mk =
+      main_kernel(D, false, dash::split_tiles(schedule, n, units, grid) > 0,
+                  early_s(schedule, deterministic));
   const int br = mk.br;
   if (!map_bshd(&maps.q, q, B, S, H, D, br) || !map_bshd(&maps.dO, dO, B, S, H, D, br) ||
       !map_bshd(&maps.k, k, B, S, H, D, dash::kTile) ||
