@@ -43,6 +43,11 @@ struct FwdL {
   static_assert(ALLOC <= 232448, "shared memory budget");
   static constexpr int T_S = 0, T_O = 256;                    // TMEM columns (+128 x, +D x)
   static_assert(T_O + 2 * D <= 512, "TMEM columns");
+  // D = 64 leaves 128 columns free: P gets its own 64 packed columns per Q tile there, so
+  // S_x(j+1) need not wait for P_x(j) V_j to complete. D = 128: P over S's first 64.
+  static constexpr bool kSepP = T_O + 2 * D + 2 * 64 <= 512;
+  static constexpr int T_P = kSepP ? T_O + 2 * D : T_S;       // + (kSepP ? 64 : 128) x
+  static constexpr int P_STRIDE = kSepP ? 64 : 128;
 };
 
 // registers per thread: launched at 168 (384 threads), re-split so the two softmax
@@ -265,7 +270,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const uint32_t dV_mn = ptx::sdesc_lo(sKV + (2 * (u & 1) + 1) * L::TILE, kTile * 128);
 #pragma unroll
             for (int ks = 0; ks < kTile / 16; ++ks)
-              ptx::mma_ts(tmem + L::T_O + D * x, tmem + L::T_S + 128 * x + 8 * ks,
+              ptx::mma_ts(tmem + L::T_O + D * x, tmem + L::T_P + L::P_STRIDE * x + 8 * ks,
                           dV_mn + ks * MN_STEP, ID_O, (u > 0 || ks > 0) ? 1u : 0u);
             ptx::mma_commit(bars + F_PV_DONE + x);
             np[x] = u + 1;
@@ -275,9 +280,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
           const int t = ns[x];
+          // With P in its own columns (kSepP), S_x(t) only has to follow P_x(t-1) V_{t-1} in
+          // issue order (t == np[x]); its commit then also covers that P V, which the
+          // softmax's next P stores need complete.
           if (t < ntx[x] && t == np[x] &&
               fwd_mbar_test(bars + F_KV_FULL + (t & 1), (t >> 1) & 1) &&
-              (t == 0 || fwd_mbar_test(bars + F_PV_DONE + x, (t - 1) & 1))) {
+              (t == 0 || L::kSepP || fwd_mbar_test(bars + F_PV_DONE + x, (t - 1) & 1))) {
             ptx::tc_fence_after();
             issue_s(x, t);
             ns[x] = t + 1;
@@ -311,6 +319,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t lane_addr = ((uint32_t)(quarter * 32) << 16);
     const int qt = x ? qb : qa, ntt = x ? nt_b : nt_a;
     const uint32_t t_s = tmem + lane_addr + L::T_S + 128 * x;
+    const uint32_t t_pp = tmem + lane_addr + L::T_P + L::P_STRIDE * x;   // P's packed columns
     const uint32_t t_o = tmem + lane_addr + L::T_O + D * x;
     float m = -INFINITY, l = 0.f;                   // running max (log2 units) and sum
     bool ok = true;
@@ -334,10 +343,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
           for (int c0 = 0; c0 < kTile; c0 += 64) {
             ptx::tmem_ld32_issue(t_s + c0 + 32, tb);
-            fwd_p_chunk_spec(ta, p.scale_log2, m, lt4, t_s + c0 / 2, mx);
+            fwd_p_chunk_spec(ta, p.scale_log2, m, lt4, t_pp + c0 / 2, mx);
             ptx::tmem_ld32_wait(tb);
             if (c0 + 64 < kTile) ptx::tmem_ld32_issue(t_s + c0 + 64, ta);
-            fwd_p_chunk_spec(tb, p.scale_log2, m, lt4, t_s + (c0 + 32) / 2, mx);
+            fwd_p_chunk_spec(tb, p.scale_log2, m, lt4, t_pp + (c0 + 32) / 2, mx);
             if (c0 + 64 < kTile) ptx::tmem_ld32_wait(ta);
           }
         }
@@ -388,9 +397,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const float m_row = mx * p.scale_log2;
       const bool moved = m_row > m + kFwdRescaleLog2;
       const float m_new = moved ? m_row : m;
-      // pass 2: P = exp2(S * scale*log2e - m_new), row sum, packed bf16 over the first 64
-      // columns: columns c0 .. c0 + 31 go to packed columns c0 / 2 .. c0 / 2 + 15, which
-      // lie in scores this thread has already read and not in the 32 loading meanwhile.
+      // pass 2: P = exp2(S * scale*log2e - m_new), row sum, packed bf16 into P's columns
+      // (D = 128: over S's first 64: columns c0 .. c0 + 31 go to packed columns c0 / 2 ..
+      // c0 / 2 + 15, which lie in scores this thread has already read and not in the 32
+      // loading meanwhile).
       // The row sum is four partial sums, added in a fixed order at the end.
       float lt4[4] = {0.f, 0.f, 0.f, 0.f};
       {
@@ -400,14 +410,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
         for (int c0 = 0; c0 < kTile; c0 += 64) {
           ptx::tmem_ld32_issue(t_s + c0 + 32, tb);
-          if (diag) fwd_p_chunk<true>(ta, c0, r, p.scale_log2, m_new, lt4, t_s + c0 / 2);
-          else fwd_p_chunk<false>(ta, c0, r, p.scale_log2, m_new, lt4, t_s + c0 / 2);
+          if (diag) fwd_p_chunk<true>(ta, c0, r, p.scale_log2, m_new, lt4, t_pp + c0 / 2);
+          else fwd_p_chunk<false>(ta, c0, r, p.scale_log2, m_new, lt4, t_pp + c0 / 2);
           ptx::tmem_ld32_wait(tb);
           if (c0 + 64 < kTile) ptx::tmem_ld32_issue(t_s + c0 + 64, ta);
           if (diag)
-            fwd_p_chunk<true>(tb, c0 + 32, r, p.scale_log2, m_new, lt4, t_s + (c0 + 32) / 2);
+            fwd_p_chunk<true>(tb, c0 + 32, r, p.scale_log2, m_new, lt4, t_pp + (c0 + 32) / 2);
           else
-            fwd_p_chunk<false>(tb, c0 + 32, r, p.scale_log2, m_new, lt4, t_s + (c0 + 32) / 2);
+            fwd_p_chunk<false>(tb, c0 + 32, r, p.scale_log2, m_new, lt4, t_pp + (c0 + 32) / 2);
           if (c0 + 64 < kTile) ptx::tmem_ld32_wait(ta);
         }
       }
