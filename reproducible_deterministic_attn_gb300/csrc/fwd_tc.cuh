@@ -6,19 +6,24 @@
 // warpgroup and its own TMEM, and both walk the same K/V tiles. Per KV tile j (128 keys),
 // for tile x in {A, B}:
 //   S_x = Q_x K_j^T       M = 128 q, N = 128 kv, K = D    TMEM cols [128 x, +128)
-//   running max m, P_x = exp2(S_x * scale*log2e - m)     packed bf16 over S_x's first 64
-//                                                        columns (kv 2c, 2c + 1 in col c)
+//   P_x = exp2(S_x * scale*log2e - m)                    packed bf16 (kv 2c, 2c + 1 in col
+//                                                        c): over S_x's first 64 columns
+//                                                        at D = 128, in 64 columns of its
+//                                                        own at D = 64
 //   O_x += P_x V_j        M = 128 q, N = D, K = 128 kv    TMEM cols [256 + D x, +D), A = P_x
 //                                                        read from TMEM
 // The two tiles ping-pong on the tensor pipe: while one warpgroup turns S into P, the MMAs
-// of the other run. S_x(j+1) overwrites P_x(j) once P_x(j) V_j has read it. The MMA
-// issuer polls both tiles' barriers and issues whatever is ready next, so neither tile
-// waits behind the other. Each softmax thread reads its row's scores from TMEM twice: for
-// the row maximum, then 64 at a time for P (holding all 128 in registers at once measured
-// slower). When a row's running max grows, its O row is rescaled in TMEM (P_x(j-1) V_{j-1}
-// has landed by then: S_x(j) waited for it) before P_x(j) V_j accumulates onto it; rows
-// whose max did not change are left alone. At the end O / l goes to global memory as bf16
-// and LSE = (m + log2 l) * ln 2.
+// of the other run. The MMA issuer polls both tiles' barriers and issues what is ready,
+// each tile's P V before either S (the pipe runs MMAs in issue order, and a P V gates its
+// tile's next S and the K/V stage's release). At D = 128, S_x(j+1) overwrites P_x(j) once
+// P_x(j) V_j has completed; at D = 64 it only follows that P V in issue order.
+// The exponent's reference m of a row moves only when the row max exceeds it by more than
+// 2^8 (lazy rescaling; O and l share the reference, so O / l and LSE are unchanged), and O
+// is rescaled in TMEM only on those tiles. On the first and last KV tile of a Q tile a
+// softmax thread reads its scores twice (row max, then P); on the others once, computing P
+// against the current reference and the row max alongside. If some row's max crossed the
+// threshold there, the issuer issues S_x(j) again and the softmax takes the two-pass path.
+// At the end O / l goes to global memory as bf16 and LSE = (m + log2 l) * ln 2.
 //
 // Warp roles (384 threads): 0 = TMA producer (both Q tiles once, K and V in two stages),
 // 1 = MMA issuer, 2..3 idle, 4..7 = softmax of tile A, 8..11 = softmax of tile B (thread =
