@@ -18,11 +18,12 @@
 // tile's next S and the K/V stage's release). At D = 128, S_x(j+1) overwrites P_x(j) once
 // P_x(j) V_j has completed; at D = 64 it only follows that P V in issue order.
 // The exponent's reference m of a row moves only when the row max exceeds it by more than
-// 2^8 (lazy rescaling; O and l share the reference, so O / l and LSE are unchanged), and O
-// is rescaled in TMEM only on those tiles. On the first and last KV tile of a Q tile a
-// softmax thread reads its scores twice (row max, then P); on the others once, computing P
-// against the current reference and the row max alongside. If some row's max crossed the
-// threshold there, the issuer issues S_x(j) again and the softmax takes the two-pass path.
+// 8 in log2 units, so P <= 2^8 (lazy rescaling; O and l share the reference, so O / l and
+// LSE are unchanged), and O is rescaled in TMEM only on those tiles. On the first and last
+// KV tile of a Q tile a softmax thread reads its scores twice (row max, then P); on the
+// others once, computing P against the current reference and the row max alongside. If
+// some row's max crossed the threshold there, the issuer issues S_x(j) again and the
+// softmax takes the two-pass path.
 // At the end O / l goes to global memory as bf16 and LSE = (m + log2 l) * ln 2.
 //
 // Warp roles (384 threads): 0 = TMA producer (both Q tiles once, K and V in two stages),
