@@ -66,8 +66,8 @@ static_assert(kFwdRegsCtrl + 2 * kFwdRegsSoftmax == 3 * kFwdRegsLaunch,
 
 enum {
   F_Q_FULL = 0, F_KV_FULL, F_KV_EMPTY = F_KV_FULL + 2, F_S_FULL = F_KV_EMPTY + 2,
-  F_P_FULL = F_S_FULL + 2, F_PV_DONE = F_P_FULL + 2, F_VERDICT = F_PV_DONE + 2,
-  F_DRAIN = F_VERDICT + 2, F_COUNT
+  F_P_FULL = F_S_FULL + 2, F_PV_DONE = F_P_FULL + 2, F_DECIDED = F_PV_DONE + 2,
+  F_DRAIN = F_DECIDED + 2, F_COUNT
 };
 
 // Non-blocking test of an mbarrier phase. The issuer polls several barriers in turn, so it
@@ -151,9 +151,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   uint32_t* tmem_slot = (uint32_t*)(sm + L::BAR_OFF + 8 * F_COUNT);
   volatile int* abort_flag = (volatile int*)(sm + L::BAR_OFF + 8 * F_COUNT + 4);
   // per Q tile: set by a softmax warp whose rows need the exact path on a speculative tile;
-  // the issuer's verdict for the tile (1 = S is issued again)
+  // the issuer's decision for the tile (1 = S is issued again)
   volatile int* redo_flag = (volatile int*)(sm + L::BAR_OFF + 8 * F_COUNT + 8);
-  volatile int* verdict = (volatile int*)(sm + L::BAR_OFF + 8 * F_COUNT + 16);
+  volatile int* decision = (volatile int*)(sm + L::BAR_OFF + 8 * F_COUNT + 16);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long tmo = p.timeout_ns;   // per wait: far beyond any legitimate wait
 
@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       ptx::mbar_init(bars + F_S_FULL + s, 1);      // per Q tile from here on
       ptx::mbar_init(bars + F_P_FULL + s, 4);
       ptx::mbar_init(bars + F_PV_DONE + s, 1);
-      ptx::mbar_init(bars + F_VERDICT + s, 1);
+      ptx::mbar_init(bars + F_DECIDED + s, 1);
       redo_flag[s] = 0;
     }
     ptx::mbar_init(bars + F_DRAIN, 1);
@@ -258,11 +258,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (u < ns[x] && fwd_mbar_test(bars + F_P_FULL + x, pf_par[x])) {
             pf_par[x] ^= 1;
             ptx::tc_fence_after();
-            if (u > 0 && u < ntx[x] - 1 && !redone[x]) {   // speculative P: give the verdict
+            if (u > 0 && u < ntx[x] - 1 && !redone[x]) {   // speculative P: post the decision
               const int redo = redo_flag[x];
               redo_flag[x] = 0;
-              verdict[x] = redo;
-              ptx::mbar_arrive(bars + F_VERDICT + x);
+              decision[x] = redo;
+              ptx::mbar_arrive(bars + F_DECIDED + x);
               if (redo) {
                 issue_s(x, u);
                 redone[x] = true;
@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t t_o = tmem + lane_addr + L::T_O + D * x;
     float m = -INFINITY, l = 0.f;                   // running max (log2 units) and sum
     bool ok = true;
-    int s_par = 0, v_par = 0;                       // S_FULL / VERDICT phases
+    int s_par = 0, v_par = 0;                       // S_FULL / DECIDED phases
     for (int j = 0; ok && j < ntt; ++j) {
       ok = ptx::warp_wait(bars + F_S_FULL + x, s_par, abort_flag, tmo);
       s_par ^= 1;
@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (j > 0 && j < ntt - 1) {
         // Speculative tile: P against the current reference m in one pass, the row max
         // alongside. That P is the exact path's unless some row's max exceeds m by more
-        // than kFwdRescaleLog2; then this warpgroup asks for S again (the issuer's verdict)
+        // than kFwdRescaleLog2; then this warpgroup asks for S again (the issuer's decision)
         // and takes the exact path on it.
         float mx = -INFINITY;
         float lt4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -362,10 +362,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bars + F_P_FULL + x);
-        ok = ptx::warp_wait(bars + F_VERDICT + x, v_par, abort_flag, tmo);
+        ok = ptx::warp_wait(bars + F_DECIDED + x, v_par, abort_flag, tmo);
         v_par ^= 1;
         if (!ok) break;
-        if (!verdict[x]) {                          // P_x(j) V_j is issued; m stays
+        if (!decision[x]) {                          // P_x(j) V_j is issued; m stays
           const float lt = (lt4[0] + lt4[1]) + (lt4[2] + lt4[3]);
           l = l * 1.f + lt;
           continue;
