@@ -91,20 +91,20 @@ def test_growing_row_max(D, mask):
     assert_within(check_against_oracle(res, causal))
 
 
-def test_config1_full_256_d64():
+def test_full_1x256x1x64():
     res = run_case(1, 256, 1, 64, False, "shift", 1)
     assert_within(check_against_oracle(res, False))
 
 
 @pytest.mark.parametrize("sched", ["ascending", "descending", "symmetric_shift"])
-def test_config2_causal_4x2048x16x64(sched):
+def test_causal_4x2048x16x64(sched):
     res = run_case(4, 2048, 16, 64, True, sched, 1)
     assert_within(check_against_oracle(res, True, heads=[(0, 0), (1, 7), (3, 15)]))
 
 
 @pytest.mark.parametrize("sched,det", [("ascending", 1), ("shift", 1), ("ascending", 0),
                                        ("shift", 2)])
-def test_config3_full_2x8192x16x128_sampled(sched, det):
+def test_full_2x8192x16x128_sampled(sched, det):
     res = run_case(2, 8192, 16, 128, False, sched, det)
     assert_within(check_against_oracle(res, False, heads=[(0, 3), (1, 15)]))
     del res
@@ -112,7 +112,7 @@ def test_config3_full_2x8192x16x128_sampled(sched, det):
 
 
 @pytest.mark.parametrize("sched", ["descending", "symmetric_shift"])
-def test_config4_causal_1x16384x32x128_sampled(sched):
+def test_causal_1x16384x32x128_sampled(sched):
     res = run_case(1, 16384, 32, 128, True, sched, 1)
     assert_within(check_against_oracle(res, True, heads=[(0, 31)]))
     del res
@@ -126,7 +126,7 @@ SWEEP = [(S, D) for D in (64, 128) for S in (1024, 2048, 4096, 8192, 16384)]
 
 
 @pytest.mark.parametrize("S,D", SWEEP, ids=lambda v: str(v))
-def test_config5_token_sweep_sampled(S, D):
+def test_causal_16384_token_sweep_sampled(S, D):
     B = 16384 // S
     res = run_case(B, S, 32, D, True, "symmetric_shift", 2 if D == 128 else 1)
     heads = [(B - 1, 31)] if S >= 8192 else [(0, 0), (B - 1, 31)]
