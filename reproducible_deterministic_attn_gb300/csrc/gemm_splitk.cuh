@@ -58,6 +58,22 @@ struct GemmL {
 enum { G_FULL = 0, G_EMPTY = G_FULL + kGemmStages, G_ACC_FULL = G_EMPTY + kGemmStages,
        G_ACC_EMPTY = G_ACC_FULL + 2, G_DRAIN = G_ACC_EMPTY + 2, G_COUNT };
 
+// Output tile `tile` -> its (m, n) tile indices, in groups of kGemmGroupM m-tiles: within a
+// group consecutive tiles step through the group's m-tiles first, then n. The grid's
+// concurrent units then share a few A and B panels (8 A + 19 B at one chunk per tile on
+// 152 CTAs) that stay in L2, instead of sweeping all of B for each row of A. A bijection
+// onto [0, tiles_m) x [0, tiles_n); a tile's arithmetic and reduction order do not depend
+// on it.
+constexpr int kGemmGroupM = 8;
+__device__ __forceinline__ void gemm_tile_mn(int tile, int tiles_m, int tiles_n, int& mi, int& ni) {
+  const int per_group = kGemmGroupM * tiles_n;
+  const int first_m = (tile / per_group) * kGemmGroupM;
+  const int gm = min(kGemmGroupM, tiles_m - first_m);
+  const int r = tile % per_group;
+  mi = first_m + r % gm;
+  ni = r / gm;
+}
+
 template <int TM>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_splitk_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ GemmMaps maps) {
@@ -99,7 +115,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool ok = true;
       for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
         const int tile = u / p.splits, split = u % p.splits;
-        const int m0 = (tile / tiles_n) * TM, n0 = (tile % tiles_n) * 128;
+        int mi, ni;
+        gemm_tile_mn(tile, p.M / TM, tiles_n, mi, ni);
+        const int m0 = mi * TM, n0 = ni * 128;
         for (int k = 0; k < ksteps; ++k, ++kb) {
           const int s = (int)(kb % kGemmStages);
           if (kb >= kGemmStages &&
@@ -156,7 +174,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++it) {
       const int acc = it & 1;
       const int tile = u / p.splits, split = u % p.splits;
-      const int m0 = (tile / tiles_n) * TM, n0 = (tile % tiles_n) * 128;
+      int mi, ni;
+      gemm_tile_mn(tile, p.M / TM, tiles_n, mi, ni);
+      const int m0 = mi * TM, n0 = ni * 128;
       ok = ptx::warp_wait(bars + G_ACC_FULL + acc, (it >> 1) & 1, abort_flag, tmo);
       if (!ok) break;
       ptx::tc_fence_after();
