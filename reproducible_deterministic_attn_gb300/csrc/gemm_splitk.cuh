@@ -6,7 +6,9 @@
 //
 // A unit is one (TM x 128 output tile, K chunk), TM = 256 rows of C when M allows it, else
 // 128; units are dealt tile-major, round robin, to a persistent grid (cooperative launch in
-// deterministic mode), so a tile's chunks run side by side on neighbouring SMs. Per unit:
+// deterministic mode), so a tile's chunks run side by side on neighbouring SMs. Tiles are
+// numbered in groups of 8 m-tiles (gemm_tile_mn), so that concurrent units share their A
+// and B panels in L2. Per unit:
 //   C^T tile partial = B_tile A_tile^T    M = 128 (n), N = TM (m), K = chunk   -> TMEM
 // (TMEM lane = n, so one warp's red.global covers 32 consecutive n of one row of C: a full
 // 128-byte line). The MMA is TM columns wide: at TM = 256 it runs at the tensor core's full
